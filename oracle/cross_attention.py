@@ -1,0 +1,169 @@
+"""fp64 CPU oracle for encoder-decoder cross-attention: populate and decode.
+
+TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import or run this module. The product path
+(the CUDA library and its Python binding) never imports it and shares no code
+with it: this file uses numpy only.
+
+What it computes, and where the pages define it:
+
+* ``populate`` -- each decoder layer l re-projects the encoder memory E with its
+  own weights, ``K_l = E x WK_l`` and ``V_l = E x WV_l`` ("Whisper: Trace One
+  Encoder Tensor into Every Decoder Layer", "The concept: one tensor, many
+  consumers"), plus a value bias bV_l and no key bias (the key bias is
+  redundant under softmax shift invariance: "Caso de estudio: WhisperKit", §2).
+  The token-major GEMM rows are re-laid out head-major ("Deliberate failure:
+  token-major K meets a head-major consumer": a bit-exact copy) into a
+  layer-major, head-major slab per layer (the circuit's
+  ``projection_cache.storage``, "The concept"; layer-5 slab offset in "View 2").
+* ``decode`` -- one query row per (slot, layer, head) attends non-causally
+  ("The concept", ``"causal": false``) over the valid encoder keys, with the
+  call's scale 0.125 = 1/sqrt(64) applied to q.k ("View 2 -- expand one
+  cross-attention operation"); padded keys are excluded, which is the exact
+  limit of the additive key-padding mask, and an empty key set gives 0 by the
+  clamped softmax denominator (WhisperKit case study §2 and §4).
+* ``full_window`` -- the "whole window" formula kept as a check beside one-query
+  decode ("Recurrence as feeds", "What it opened").
+
+Readings where the pages are silent (each one is pinned by a test):
+  WK_l is ``[d_in, d_out]`` ("E x WK_l"); head h owns columns h*dh .. h*dh+dh-1;
+  a layer slab is ``[H][T][dh]``; key_len is clamped to [0, T].
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against brute
+force, closed forms and the invariants the pages fix; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# Clamp of the softmax denominator for an empty key set (WhisperKit case study
+# §2 clamps the lazy-softmax denominator; with no keys the numerator is 0 too).
+DENOM_FLOOR = 1e-300
+
+
+def _f64(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64)
+
+
+def check_geometry(T: int, d: int, H: int, dh: int) -> None:
+    """Fail closed on the geometry the compiler rejects ("View 3 -- prefill vs
+    decode": a positive encoder_memory_length and num_heads * head_dim ==
+    embed_dim are hard errors)."""
+    if T <= 0:
+        raise ValueError("encoder memory length must be positive")
+    if H * dh != d:
+        raise ValueError("num_heads * head_dim must equal embed_dim")
+
+
+def head_major(X: np.ndarray, H: int) -> np.ndarray:
+    """Token-major ``[T, d]`` rows -> head-major ``[H, T, dh]``; column j of X is
+    (head j // dh, channel j % dh). A pure copy: no value changes."""
+    T, d = X.shape
+    dh = d // H
+    out = np.empty((H, T, dh), dtype=X.dtype)
+    for h in range(H):
+        out[h] = X[:, h * dh:(h + 1) * dh]
+    return out
+
+
+def populate(E, WK, WV, bV, H: int, bK=None):
+    """Project every slot's encoder memory with every layer's WK/WV.
+
+    E: ``[B, T, d]``; WK, WV: ``[L, d, d]`` indexed (d_in, d_out); bV: ``[L, d]``;
+    bK: optional ``[L, d]`` key bias, only used by the invariance pin.
+    Returns Kc, Vc as fp64 ``[B, L, H, T, dh]`` (slot, layer-major, head-major).
+    """
+    E, WK, WV, bV = _f64(E), _f64(WK), _f64(WV), _f64(bV)
+    B, T, d = E.shape
+    L = WK.shape[0]
+    dh = d // H
+    check_geometry(T, d, H, dh)
+    Kc = np.empty((B, L, H, T, dh))
+    Vc = np.empty((B, L, H, T, dh))
+    for b in range(B):
+        for l in range(L):
+            K = E[b] @ WK[l]                 # K_l = E x WK_l        [T, d]
+            V = E[b] @ WV[l] + bV[l]         # V_l = E x WV_l + bV_l [T, d]
+            if bK is not None:
+                K = K + _f64(bK)[l]
+            Kc[b, l] = head_major(K, H)
+            Vc[b, l] = head_major(V, H)
+    return Kc, Vc
+
+
+def populate_head(E_b, WK_l, WV_l, bV_l, h: int, dh: int = 64):
+    """K and V ``[T, dh]`` of one (slot, layer, head): the same projection as
+    ``populate`` restricted to head h's column block, for sampled checks at
+    sizes where projecting every head in fp64 would take too long."""
+    E_b = _f64(E_b)
+    cols = slice(h * dh, (h + 1) * dh)
+    K = E_b @ _f64(WK_l)[:, cols]
+    V = E_b @ _f64(WV_l)[:, cols] + _f64(bV_l)[cols]
+    return K, V
+
+
+def clamp_key_len(key_len, T: int) -> np.ndarray:
+    return np.clip(np.asarray(key_len, dtype=np.int64), 0, T)
+
+
+def attend_row(q, K, V, n: int, scale: float) -> np.ndarray:
+    """One query row against the first n keys: softmax(scale * q.K^T) V.
+
+    The max-subtraction is the usual overflow guard; it leaves the result
+    unchanged (shift invariance, WhisperKit case study §2)."""
+    q, K, V = _f64(q), _f64(K), _f64(V)
+    dh = q.shape[0]
+    if n <= 0:
+        return np.zeros(dh)
+    s = scale * (K[:n] @ q)
+    w = np.exp(s - s.max())
+    return (w @ V[:n]) / max(w.sum(), DENOM_FLOOR)
+
+
+def decode(Q, Kc, Vc, key_len, scale: float | None = None) -> np.ndarray:
+    """One decode step over all slots, layers and heads.
+
+    Q: ``[B, L, H, dh]``; Kc, Vc: ``[B, L, H, T, dh]``; key_len: ``[B]``.
+    Returns out ``[B, L, H, dh]`` (one query token, head-major)."""
+    Q = _f64(Q)
+    B, L, H, T, dh = np.shape(Kc)
+    if scale is None:
+        scale = 1.0 / np.sqrt(dh)
+    n = clamp_key_len(key_len, T)
+    out = np.zeros((B, L, H, dh))
+    for b in range(B):
+        for l in range(L):
+            for h in range(H):
+                out[b, l, h] = attend_row(Q[b, l, h], Kc[b, l, h], Vc[b, l, h], int(n[b]), scale)
+    return out
+
+
+def decode_rows(Q, Kc, Vc, key_len, rows, scale: float | None = None) -> np.ndarray:
+    """Decode only the listed (b, l, h) rows; returns ``[len(rows), dh]``."""
+    B, L, H, T, dh = np.shape(Kc)
+    if scale is None:
+        scale = 1.0 / np.sqrt(dh)
+    n = clamp_key_len(key_len, T)
+    return np.stack([attend_row(np.asarray(Q)[b, l, h], Kc[b, l, h], Vc[b, l, h], int(n[b]), scale)
+                     for (b, l, h) in rows])
+
+
+def full_window(Qblock, K, V, n: int, scale: float) -> np.ndarray:
+    """All query rows at once as one matrix-softmax-matrix: ``[nq, dh]``."""
+    Qblock, K, V = _f64(Qblock), _f64(K), _f64(V)
+    S = scale * (Qblock @ K[:n].T)
+    S = S - S.max(axis=1, keepdims=True)
+    P = np.exp(S)
+    P = P / P.sum(axis=1, keepdims=True)
+    return P @ V[:n]
+
+
+def cross_attention_from_memory(Q, E, WK, WV, bV, key_len, H: int, scale: float | None = None):
+    """Decode computed by re-projecting E (no cache), for the cache-reuse pin."""
+    Kc, Vc = populate(E, WK, WV, bV, H)
+    return decode(Q, Kc, Vc, key_len, scale)
+
+
+def rel_frobenius(x, ref) -> float:
+    x, ref = _f64(x), _f64(ref)
+    return float(np.linalg.norm((x - ref).ravel()) / max(np.linalg.norm(ref.ravel()), 1e-300))

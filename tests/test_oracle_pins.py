@@ -1,0 +1,362 @@
+"""Pins for the fp64 oracle: brute force, closed forms, the invariants the pages
+fix, and the printed Whisper-Base layout facts. Each pin is also run against
+deliberately broken copies of the oracle (planted on the CPU) to show that a
+plausible mistake -- a transposed operand, a wrong sign, a dropped term, an
+off-by-one mask, a wrong layout -- makes at least one pin fail.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from encoder_decoder_speech_gb300 import workloads as W
+from oracle import cross_attention as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "whisper_base_decode_call.json")
+
+
+def _rand(shape, seed, std=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * std
+
+
+# ---------------------------------------------------------------------------
+# independent pure-Python restatements (no numpy arithmetic, fsum sums)
+# ---------------------------------------------------------------------------
+def bf_populate(E, WK, WV, bV, H):
+    """K[b][l][h][t][c] = sum_i E[b][t][i] * WK[l][i][h*dh+c]; V adds bV[l][h*dh+c]."""
+    E, WK, WV, bV = E.tolist(), WK.tolist(), WV.tolist(), bV.tolist()
+    B, T, d, L = len(E), len(E[0]), len(E[0][0]), len(WK)
+    dh = d // H
+    K = [[[[[0.0] * dh for _ in range(T)] for _ in range(H)] for _ in range(L)] for _ in range(B)]
+    V = [[[[[0.0] * dh for _ in range(T)] for _ in range(H)] for _ in range(L)] for _ in range(B)]
+    for b in range(B):
+        for l in range(L):
+            for h in range(H):
+                for t in range(T):
+                    for c in range(dh):
+                        j = h * dh + c
+                        K[b][l][h][t][c] = math.fsum(E[b][t][i] * WK[l][i][j] for i in range(d))
+                        V[b][l][h][t][c] = math.fsum([E[b][t][i] * WV[l][i][j] for i in range(d)]
+                                                     + [bV[l][j]])
+    return np.array(K), np.array(V)
+
+
+def bf_attend(q, K, V, n, scale):
+    """softmax without the max shift: w_t = exp(s_t) / sum_u exp(s_u)."""
+    q, K, V = list(q), [list(r) for r in K], [list(r) for r in V]
+    dh = len(q)
+    if n <= 0:
+        return [0.0] * dh
+    e = [math.exp(scale * math.fsum(q[c] * K[t][c] for c in range(dh))) for t in range(n)]
+    z = math.fsum(e)
+    return [math.fsum(e[t] * V[t][c] for t in range(n)) / z for c in range(dh)]
+
+
+# ---------------------------------------------------------------------------
+# pin checks, each returning an error measure (0 == exact agreement)
+# ---------------------------------------------------------------------------
+def pin_populate_bruteforce():
+    err = 0.0
+    for (B, T, d, L, H) in [(2, 1, 4, 2, 2), (1, 2, 4, 2, 2), (2, 3, 4, 1, 2), (1, 3, 6, 2, 3)]:
+        E, WK, WV = _rand((B, T, d), 1), _rand((L, d, d), 2), _rand((L, d, d), 3)
+        bV = _rand((L, d), 4)
+        Kc, Vc = O.populate(E, WK, WV, bV, H)
+        Kb, Vb = bf_populate(E, WK, WV, bV, H)
+        err = max(err, np.abs(Kc - Kb).max(), np.abs(Vc - Vb).max())
+    return err
+
+
+def pin_decode_bruteforce():
+    err = 0.0
+    cases = [(1, 2, 2, 1), (2, 2, 2, 2), (3, 2, 2, 3), (3, 2, 2, 2), (5, 64, 1, 5), (5, 64, 1, 3), (4, 2, 2, 0)]
+    for i, (T, dh, H, n) in enumerate(cases):
+        B, L = 2, 2
+        Q = _rand((B, L, H, dh), 10 + i)
+        Kc = _rand((B, L, H, T, dh), 20 + i)
+        Vc = _rand((B, L, H, T, dh), 30 + i)
+        kl = np.array([n, T])
+        scale = 1.0 / math.sqrt(dh)
+        out = O.decode(Q, Kc, Vc, kl, scale)
+        for b in range(B):
+            for l in range(L):
+                for h in range(H):
+                    ref = bf_attend(Q[b, l, h], Kc[b, l, h], Vc[b, l, h], int(kl[b]), scale)
+                    err = max(err, float(np.abs(out[b, l, h] - np.array(ref)).max()))
+    return err
+
+
+def pin_closed_forms():
+    """Returns the largest deviation from the closed forms."""
+    errs = []
+    B, L, H, T, dh = 2, 2, 2, 9, 64
+    Q = _rand((B, L, H, dh), 40)
+    Kc, Vc = _rand((B, L, H, T, dh), 41), _rand((B, L, H, T, dh), 42)
+    # key_len = 1 (or T = 1): the output is V row 0
+    out = O.decode(Q, Kc, Vc, [1, 1])
+    errs.append(np.abs(out - Vc[:, :, :, 0]).max())
+    out = O.decode(Q, Kc[:, :, :, :1], Vc[:, :, :, :1], [1, 1])
+    errs.append(np.abs(out - Vc[:, :, :, 0]).max())
+    # q = 0: uniform weights -> mean of the first n V rows
+    out = O.decode(np.zeros_like(Q), Kc, Vc, [5, 9])
+    errs.append(np.abs(out[0] - Vc[0, :, :, :5].mean(axis=2)).max())
+    errs.append(np.abs(out[1] - Vc[1].mean(axis=2)).max())
+    # V rows all equal to one vector -> that vector
+    vconst = _rand((dh,), 43)
+    out = O.decode(Q, Kc, np.broadcast_to(vconst, Vc.shape), [9, 4])
+    errs.append(np.abs(out - vconst).max())
+    # one key aligned with q by a huge margin, another anti-aligned: the output is
+    # the aligned key's V row (a flipped softmax sign would pick the other one)
+    K2 = Kc * 1e-3
+    for b in range(B):
+        for l in range(L):
+            for h in range(H):
+                qn = Q[b, l, h] / np.linalg.norm(Q[b, l, h])
+                K2[b, l, h, 3] = 60.0 * qn
+                K2[b, l, h, 6] = -60.0 * qn
+    out = O.decode(Q, K2, Vc, [9, 9], scale=1.0)
+    errs.append(np.abs(out - Vc[:, :, :, 3]).max())
+    # key_len = 0 -> zeros; key_len beyond T clamps to T; negative clamps to 0
+    out = O.decode(Q, Kc, Vc, [0, 100])
+    errs.append(np.abs(out[0]).max())
+    errs.append(np.abs(out[1] - O.decode(Q, Kc, Vc, [T, T])[1]).max())
+    errs.append(np.abs(O.decode(Q, Kc, Vc, [-3, 0])).max())
+    return float(max(errs))
+
+
+def pin_key_bias_invariance():
+    """Adding a key bias bK leaves decode unchanged (WhisperKit case study §2)."""
+    B, T, d, L, H = 2, 11, 128, 2, 2
+    E, WK, WV, bV = _rand((B, T, d), 50), _rand((L, d, d), 51, d ** -0.5), _rand((L, d, d), 52, d ** -0.5), _rand((L, d), 53, 0.02)
+    bK = _rand((L, d), 54)
+    Q = _rand((B, L, H, 64), 55)
+    Kc, Vc = O.populate(E, WK, WV, bV, H)
+    Kb, Vb = O.populate(E, WK, WV, bV, H, bK=bK)
+    assert np.abs(Kb - Kc).max() > 0.1            # the bias really changed the keys
+    a = O.decode(Q, Kc, Vc, [11, 7])
+    c = O.decode(Q, Kb, Vb, [11, 7])
+    return float(np.abs(a - c).max() / np.abs(a).max())
+
+
+def pin_full_window():
+    """One-query decode == the matching row of the full-window formula
+    ("Recurrence as feeds": the whole-window formula kept as a check)."""
+    B, T, L, H, dh = 1, 13, 1, 1, 64
+    Kc, Vc = _rand((B, L, H, T, dh), 60), _rand((B, L, H, T, dh), 61)
+    Qblock = _rand((7, dh), 62)
+    err = 0.0
+    for n in (13, 8):
+        full = O.full_window(Qblock, Kc[0, 0, 0], Vc[0, 0, 0], n, 0.125)
+        for r in range(7):
+            one = O.decode(Qblock[r].reshape(1, 1, 1, dh), Kc, Vc, [n])[0, 0, 0]
+            err = max(err, float(np.abs(one - full[r]).max() / np.abs(full[r]).max()))
+    return err
+
+
+def pin_cache_reuse():
+    """4 decode steps on one populated cache == re-projecting E every step
+    ("View 3 -- prefill vs decode": projected once, reused per step)."""
+    w = W.custom("reuse", B=2, T=17, d=128, L=2, H=2, ragged=True, steps=4)
+    E, (WK, WV, bV), kl = W.make_E_all(w), W.make_weights(w), W.make_key_len(w)
+    Kc, Vc = O.populate(E, WK, WV, bV, w.H)
+    err = 0.0
+    for s in range(4):
+        Q = W.make_Q(w, s)
+        err = max(err, float(np.abs(O.decode(Q, Kc, Vc, kl)
+                                    - O.cross_attention_from_memory(Q, E, WK, WV, bV, kl, w.H)).max()))
+    return err
+
+
+def pin_layout_offset():
+    """Whisper-Base dims: the layer-5 K slab starts 15,360,000 bytes into an fp32
+    cache, and element (l, h, t, c) sits at ((l*H + h)*T + t)*dh + c."""
+    g = json.load(open(GOLDEN))
+    T, d = g["encoder_memory_shape"]
+    L, H, dh = g["decoder_layers"], g["num_heads"], g["head_dim"]
+    E = _rand((1, T, d), 70)
+    WK, WV = _rand((L, d, d), 71, d ** -0.5), _rand((L, d, d), 72, d ** -0.5)
+    Kc, _ = O.populate(E, WK, WV, np.zeros((L, d)), H)
+    flat = Kc.reshape(-1)
+    bad = 0
+    idx = g["layer5_k_cache_offset_bytes"] // 4
+    if not np.isclose(flat[idx], E[0, 0] @ WK[5][:, 0], rtol=1e-12, atol=1e-12):
+        bad += 1
+    for (l, h, t, c) in [(5, 0, 0, 0), (5, 3, 7, 11), (2, 7, 1499, 63), (0, 1, 1, 0)]:
+        if not np.isclose(flat[((l * H + h) * T + t) * dh + c], E[0, t] @ WK[l][:, h * dh + c],
+                          rtol=1e-12, atol=1e-12):
+            bad += 1
+    return bad
+
+
+def pin_token_major_rejected():
+    """A token-major cache has the same element count but must not decode to the
+    same result ("Deliberate failure": shape equality is not compatibility)."""
+    w = W.custom("tm", B=1, T=12, d=128, L=2, H=2)
+    E, (WK, WV, bV) = W.make_E_all(w), W.make_weights(w)
+    Kc, Vc = O.populate(E, WK, WV, bV, w.H)
+    tok_K = np.stack([E[0] @ WK[l] for l in range(w.L)]).reshape(Kc.shape)
+    tok_V = np.stack([E[0] @ WV[l] + bV[l] for l in range(w.L)]).reshape(Vc.shape)
+    Q = W.make_Q(w, 0)
+    good = O.decode(Q, Kc, Vc, [12])
+    wrong = O.decode(Q, tok_K, tok_V, [12])
+    return float(np.abs(good - wrong).max())
+
+
+def pin_scale_on_scores():
+    """scale multiplies q.k: decode(Q, scale=s) == decode(s*Q, scale=1); default 1/sqrt(dh)."""
+    B, L, H, T, dh = 1, 2, 2, 10, 64
+    Q, Kc, Vc = _rand((B, L, H, dh), 80), _rand((B, L, H, T, dh), 81), _rand((B, L, H, T, dh), 82)
+    a = O.decode(Q, Kc, Vc, [10], scale=0.37)
+    b = O.decode(0.37 * Q, Kc, Vc, [10], scale=1.0)
+    c = O.decode(Q, Kc, Vc, [10])
+    d = O.decode(Q, Kc, Vc, [10], scale=json.load(open(GOLDEN))["scale"])
+    return float(max(np.abs(a - b).max(), np.abs(c - d).max()))
+
+
+# ---------------------------------------------------------------------------
+# the pins on the real oracle
+# ---------------------------------------------------------------------------
+def test_populate_matches_bruteforce():
+    assert pin_populate_bruteforce() < 1e-12
+
+
+def test_decode_matches_bruteforce():
+    assert pin_decode_bruteforce() < 1e-12
+
+
+def test_closed_forms():
+    assert pin_closed_forms() < 1e-12
+
+
+def test_key_bias_invariance():
+    assert pin_key_bias_invariance() < 1e-12
+
+
+def test_full_window_row():
+    assert pin_full_window() < 1e-13
+
+
+def test_cache_reuse_equals_reprojection():
+    assert pin_cache_reuse() == 0.0
+
+
+def test_layout_offset_whisper_base():
+    assert pin_layout_offset() == 0
+
+
+def test_token_major_cache_gives_a_different_answer():
+    assert pin_token_major_rejected() > 1e-3
+
+
+def test_scale_applies_to_scores():
+    assert pin_scale_on_scores() < 1e-13
+
+
+def test_geometry_fails_closed():
+    with pytest.raises(ValueError):
+        O.populate(np.zeros((1, 0, 128)), np.zeros((1, 128, 128)), np.zeros((1, 128, 128)), np.zeros((1, 128)), 2)
+    with pytest.raises(ValueError):
+        O.check_geometry(10, 128, 3, 64)
+
+
+def test_golden_call_arguments():
+    g = json.load(open(GOLDEN))
+    assert g["num_heads"] * g["head_dim"] == g["encoder_memory_shape"][1]
+    assert g["scale"] == 1.0 / math.sqrt(g["head_dim"])
+    assert g["key_tokens"] == g["encoder_memory_shape"][0]
+    assert g["layer5_k_cache_offset_bytes"] == 5 * g["key_tokens"] * g["encoder_memory_shape"][1] * 4
+
+
+def test_padding_rows_never_reach_the_output():
+    B, L, H, T, dh = 2, 1, 2, 8, 64
+    Q, Kc, Vc = _rand((B, L, H, dh), 90), _rand((B, L, H, T, dh), 91), _rand((B, L, H, T, dh), 92)
+    ref = O.decode(Q, Kc, Vc, [5, 3])
+    Kp, Vp = Kc.copy(), Vc.copy()
+    Kp[0, :, :, 5:] = np.nan
+    Vp[0, :, :, 5:] = np.inf
+    Kp[1, :, :, 3:] = np.inf
+    Vp[1, :, :, 3:] = np.nan
+    assert np.array_equal(O.decode(Q, Kp, Vp, [5, 3]), ref)
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: each must make some pin fail
+# ---------------------------------------------------------------------------
+def _mut_transposed_w(monkeypatch):
+    orig = O.populate
+
+    def populate(E, WK, WV, bV, H, bK=None):
+        return orig(E, np.swapaxes(np.asarray(WK, float), 1, 2), np.swapaxes(np.asarray(WV, float), 1, 2), bV, H, bK)
+    monkeypatch.setattr(O, "populate", populate)
+
+
+def _mut_interleaved_heads(monkeypatch):
+    def head_major(X, H):
+        T, d = X.shape
+        return X.reshape(T, d // H, H).transpose(2, 0, 1).copy()
+    monkeypatch.setattr(O, "head_major", head_major)
+
+
+def _mut_token_major_slab(monkeypatch):
+    def head_major(X, H):
+        T, d = X.shape
+        return X.reshape(H, T, d // H).copy()
+    monkeypatch.setattr(O, "head_major", head_major)
+
+
+def _mut_bias_on_keys(monkeypatch):
+    orig = O.populate
+
+    def populate(E, WK, WV, bV, H, bK=None):
+        K, V = orig(E, WK, WV, np.zeros_like(np.asarray(bV, float)), H, bK)
+        K2, _ = orig(E, WK, WV, np.zeros_like(np.asarray(bV, float)), H, bV)
+        return K2, V
+    monkeypatch.setattr(O, "populate", populate)
+
+
+def _mut_sign_flip(monkeypatch):
+    def attend_row(q, K, V, n, scale):
+        return O.__dict__["_orig_attend"](q, K, V, n, -scale)
+    monkeypatch.setitem(O.__dict__, "_orig_attend", O.attend_row)
+    monkeypatch.setattr(O, "attend_row", attend_row)
+
+
+def _mut_mask_off_by_one(monkeypatch):
+    def attend_row(q, K, V, n, scale):
+        return O.__dict__["_orig_attend"](q, K, V, n - 1, scale)
+    monkeypatch.setitem(O.__dict__, "_orig_attend", O.attend_row)
+    monkeypatch.setattr(O, "attend_row", attend_row)
+
+
+def _mut_no_normalisation(monkeypatch):
+    def attend_row(q, K, V, n, scale):
+        q, K, V = np.asarray(q, float), np.asarray(K, float), np.asarray(V, float)
+        if n <= 0:
+            return np.zeros(q.shape[0])
+        s = scale * (K[:n] @ q)
+        w = np.exp(s - s.max())
+        return w @ V[:n]
+    monkeypatch.setattr(O, "attend_row", attend_row)
+
+
+def _mut_missing_scale(monkeypatch):
+    def attend_row(q, K, V, n, scale):
+        return O.__dict__["_orig_attend"](q, K, V, n, 1.0)
+    monkeypatch.setitem(O.__dict__, "_orig_attend", O.attend_row)
+    monkeypatch.setattr(O, "attend_row", attend_row)
+
+
+def _all_pins_pass():
+    return (pin_populate_bruteforce() < 1e-12 and pin_decode_bruteforce() < 1e-12
+            and pin_closed_forms() < 1e-12 and pin_full_window() < 1e-13
+            and pin_layout_offset() == 0 and pin_scale_on_scores() < 1e-13)
+
+
+@pytest.mark.parametrize("mutation", [
+    _mut_transposed_w, _mut_interleaved_heads, _mut_token_major_slab, _mut_bias_on_keys,
+    _mut_sign_flip, _mut_mask_off_by_one, _mut_no_normalisation, _mut_missing_scale,
+])
+def test_planted_mistake_is_caught(monkeypatch, mutation):
+    mutation(monkeypatch)
+    assert not _all_pins_pass()
