@@ -1,0 +1,477 @@
+#!/usr/bin/env python
+"""Benchmark of the cross-attention hot path on batched Whisper-Base windows.
+
+One step = one window of the workload: populate the K/V projection cache of
+B = 16 encoder memories (E_b [1500, 512], 6 layers, 8 heads x 64, ragged
+key_len ~ U{500..1500}), then 128 decode steps, each one query row per (slot,
+layer, head) over the cache. Throughput is decode tokens/s over the whole
+window (a token = one query row per slot through all 6 layers' cross-attention),
+populate included. Inputs are seeded synthetic tensors resident in HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cxa|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores (a bounded sample
+of the same workload per step). Under torchrun each rank runs its own replica of
+the workload on its own GPU (weak scaling, no data-path collective); rank 0
+prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "batched_base"
+NOMINAL_HBM_GBS = 7900.0
+TF32_OVER_BF16 = 1.1 / 2.25          # nominal dense TF32 / bf16 tensor rates
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_DECODE = os.path.join(ROOT, "profiles", "decode_split_batched_base.md")
+
+
+# ---------------------------------------------------------------- host helpers
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["cxa", "reference"], default="cxa")
+    p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    p.add_argument("--no-variants", action="store_true", help="skip the bf16-cache variant")
+    p.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
+    p.add_argument("--budget-s", type=float, default=12.0, help=argparse.SUPPRESS)
+    p.add_argument("--max-slots", type=int, default=16, help=argparse.SUPPRESS)
+    a = p.parse_args(argv)
+    if a.warmup < 3 and not a.oracle_sample:
+        p.error("--warmup must be >= 3")
+    return a
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def rank_slots(rank: int, B: int):
+    """Seed indices of the encoder memories a rank owns: each rank runs its own
+    B windows (weak scaling), distinct across ranks."""
+    return list(range(rank * B, rank * B + B))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        pk["source"] = "measured"
+        return pk
+    except (OSError, ValueError):
+        pk = dict(FALLBACK_PEAKS)
+        pk["source"] = "fallback"
+        return pk
+
+
+def decode_bytes(L, H, dh, cache_esz, key_len, B):
+    """Algorithmic bytes of one decode launch: K and V rows of the valid keys,
+    the query rows read and the output rows written."""
+    return 2 * L * H * dh * cache_esz * int(sum(int(k) for k in key_len)) + 2 * B * L * H * dh * 4
+
+
+def populate_flops(L, d, B, T):
+    """K and V projections of every row of every memory: 2 * (2*L*d) * d * B*T."""
+    return 4 * L * d * d * B * T
+
+
+def source_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic():
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary,
+    valid only while the kernel source is the one that was profiled."""
+    try:
+        text = open(PROFILE_DECODE).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"decode_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not s:
+        return None
+    src = os.path.join(ROOT, "encoder_decoder_speech_gb300", "csrc", "decode.cu")
+    if source_sha(src) != s.group(1):
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="clk", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm = []
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+            except ValueError:
+                pass
+            for i, n in enumerate(names):
+                if r[5 + i].lower() == "active":
+                    reasons.add(n)
+        sm.sort()
+        try:
+            smax = float(rows[-1][2])
+        except ValueError:
+            smax = None
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- oracle legs
+def oracle_sample(budget_s: float, max_slots: int, warmup_slots: int = 0):
+    """Time the fp64 oracle on whole windows of the workload (one memory: its
+    populate, then its 128 decode steps), one memory after another, until
+    max_slots windows are timed or the time budget is spent. warmup_slots
+    windows run first, untimed. Returns tokens, seconds, slots."""
+    from encoder_decoder_speech_gb300 import workloads as W
+    from oracle import cross_attention as O
+    w = W.WORKLOADS[WORKLOAD]
+    WK, WV, bV = W.make_weights(w)
+    kl_all = W.make_key_len(w)
+    Qs = [W.make_Q(w, s) for s in range(w.steps)]
+
+    def window(b):
+        E = W.make_E(w, b, kl_all)[None]
+        t0 = time.perf_counter()
+        Kc, Vc = O.populate(E, WK, WV, bV, w.H)
+        for s in range(w.steps):
+            O.decode(Qs[s][b:b + 1], Kc, Vc, kl_all[b:b + 1])
+        return time.perf_counter() - t0
+
+    for i in range(warmup_slots):
+        window(i % w.B)
+    tokens, slots, spent = 0, 0, 0.0
+    for i in range(max_slots):
+        spent += window(i % w.B)
+        tokens += w.steps
+        slots += 1
+        if spent >= budget_s:
+            break
+    return {"tokens": tokens, "seconds": spent, "slots": slots}
+
+
+def run_oracle_subprocess(budget_s: float, max_slots: int, warmup_slots: int = 0):
+    """The oracle timed in a fresh single-threaded process (BLAS pinned to one thread)."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", "--budget-s", str(budget_s),
+                        "--max-slots", str(max_slots), "--warmup", str(warmup_slots)],
+                       capture_output=True, text=True, env=env, timeout=3600)
+    if r.returncode != 0:
+        raise RuntimeError("oracle sample failed: " + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline_obj(res):
+    return {"value": res["tokens"] / res["seconds"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{res['slots']} whole window(s) of the workload (one memory each: fp64 populate + "
+                      f"128 decode steps), {res['tokens']} tokens in {res['seconds']:.1f} s, single thread"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is one whole window of one
+    memory (populate + 128 decode steps), W untimed then K timed."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from encoder_decoder_speech_gb300 import workloads as W
+    w = W.WORKLOADS[WORKLOAD]
+    res = run_oracle_subprocess(budget_s=float("inf"), max_slots=args.steps, warmup_slots=args.warmup)
+    value = res["tokens"] / res["seconds"]
+    line = {
+        "impl": "reference",
+        "metric": "cross-attn decode tokens/s (batched Whisper-Base window: populate + 128 decode steps)",
+        "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * res["seconds"] / max(res["slots"], 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy, Whisper-Base shapes)",
+        "config": workload_config(w, "f64 (oracle)"),
+        "cpu_baseline": cpu_baseline_obj(res),
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(w, cache_dtype):
+    return {"workload": "batched-whisper-base", "B": w.B, "T_enc": w.T, "d": w.d, "L": w.L, "H": w.H, "dh": w.dh,
+            "decode_steps_per_window": w.steps, "key_len": "U{500..1500} per memory, padded rows zeroed",
+            "cache_dtype": cache_dtype, "populate_inputs": "fp32 (TF32 tensor-core operands)",
+            "l2": "inputs larger than L2: each decode step reads the valid K/V rows of a 590 MB fp32 cache "
+                  "(394 MB), each populate writes 590 MB; no flush needed"}
+
+
+# ---------------------------------------------------------------- GPU arm
+def measure(torch, cxa, W, w, dev_inputs, cache_dtype, K, Wu, rank, world, dist, timed_clocks: bool):
+    """Times K windows; returns a dict of timings (max over ranks)."""
+    E, WK, WV, bV, kl, Qs, key_len_host = dev_inputs
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+    cache = cxa.CrossAttentionCache(w.B, w.T, w.L, w.H, w.dh, cache_dtype)
+    out = torch.empty((w.B, w.L, w.H, w.dh), dtype=torch.float32, device="cuda")
+    ws = cache.populate_workspace(cxa.CXA_F32)
+    h = cache.handle
+
+    def populate():
+        cxa.check(cxa.cxa_populate(h, 0, w.B, E, WK, WV, bV, w.T, w.d, w.L, w.H, cxa.CXA_F32, ws, ws.numel(), sptr),
+                  "cxa_populate")
+
+    def decode(s):
+        cxa.check(cxa.cxa_decode(h, Qs[s], kl, out, 0.0, cache.decode_ws, cache.decode_ws_bytes, sptr), "cxa_decode")
+
+    for _ in range(Wu):
+        populate()
+        for s in range(w.steps):
+            decode(s)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk = ClockSampler(torch.cuda.current_device()) if timed_clocks else None
+    if clk:
+        clk.start()
+    launches0 = cxa.cxa_launch_count()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        populate()
+        ev[k][1].record(stream)
+        for s in range(w.steps):
+            decode(s)
+        ev[k][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = cxa.cxa_launch_count() - launches0
+    clocks = clk.stop() if clk else None
+    if dist is not None:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    pop_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    if dist is not None:
+        t = torch.tensor([total_ms, pop_ms, dec_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, pop_ms, dec_ms = (float(x) for x in t.tolist())
+    assert cxa.cxa_device_status(1) == cxa.CXA_OK, "a kernel reported a bounded-wait timeout"
+    res = {"total_ms": total_ms, "populate_ms": pop_ms, "decode_window_ms": dec_ms,
+           "decode_launch_us": 1000.0 * dec_ms / w.steps, "launches": launches, "clocks": clocks}
+    cache.close()
+    return res
+
+
+def measure_e2e(torch, cxa, w, host_inputs, dev_static, K, Wu, dist):
+    """Same windows through the public API with inputs in pinned host memory:
+    E, key_len and every step's Q are copied in, every step's output copied out."""
+    E_h, kl_h, Q_h = host_inputs
+    WK, WV, bV = dev_static
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+    E_pin = torch.from_numpy(E_h).pin_memory()
+    kl_pin = torch.from_numpy(kl_h).pin_memory()
+    Q_pin = torch.from_numpy(Q_h).pin_memory()
+    out_pin = torch.empty((w.steps, w.B, w.L, w.H, w.dh), dtype=torch.float32).pin_memory()
+    E_d = torch.empty(E_pin.shape, dtype=torch.float32, device="cuda")
+    kl_d = torch.empty(kl_pin.shape, dtype=torch.int32, device="cuda")
+    Q_d = torch.empty((w.B, w.L, w.H, w.dh), dtype=torch.float32, device="cuda")
+    out_d = torch.empty_like(Q_d)
+    cache = cxa.CrossAttentionCache(w.B, w.T, w.L, w.H, w.dh, "f32")
+    ws = cache.populate_workspace(cxa.CXA_F32)
+    h = cache.handle
+
+    def window():
+        E_d.copy_(E_pin, non_blocking=True)
+        kl_d.copy_(kl_pin, non_blocking=True)
+        cxa.check(cxa.cxa_populate(h, 0, w.B, E_d, WK, WV, bV, w.T, w.d, w.L, w.H, cxa.CXA_F32, ws, ws.numel(),
+                                   sptr), "cxa_populate")
+        for s in range(w.steps):
+            Q_d.copy_(Q_pin[s], non_blocking=True)
+            cxa.check(cxa.cxa_decode(h, Q_d, kl_d, out_d, 0.0, cache.decode_ws, cache.decode_ws_bytes, sptr),
+                      "cxa_decode")
+            out_pin[s].copy_(out_d, non_blocking=True)
+
+    for _ in range(Wu):
+        window()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        window()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    h2d = E_pin.numel() * 4 + kl_pin.numel() * 4 + w.steps * Q_d.numel() * 4
+    d2h = w.steps * out_d.numel() * 4
+    cache.close()
+    return ms, h2d, d2h
+
+
+def run_cxa(args):
+    rank, world, local = dist_env()
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # the oracle leg runs first, in its own process, before any GPU work
+        cpu_base = cpu_baseline_obj(run_oracle_subprocess(args.budget_s, args.max_slots))
+
+    import numpy as np
+    import torch
+    from encoder_decoder_speech_gb300 import _build, cxa
+    from encoder_decoder_speech_gb300 import workloads as W
+
+    _build.build_library()
+    cxa.load()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = tdist
+    w = W.WORKLOADS[WORKLOAD]
+    kl = W.make_key_len(w)
+    slots = rank_slots(rank, w.B)
+    E = np.stack([W.make_E(W.replace(w, ragged=False), s) for s in slots])
+    for i in range(w.B):                      # pad rows of each memory are zero
+        E[i, int(kl[i]):] = 0.0
+    WK, WV, bV = W.make_weights(w)
+    Q = np.stack([W.make_Q(w, s) for s in range(w.steps)])
+
+    def d(x, dt=torch.float32):
+        return torch.from_numpy(np.ascontiguousarray(x)).to("cuda", dt)
+
+    dev_inputs = (d(E), d(WK), d(WV), d(bV), d(kl, torch.int32), d(Q), kl)
+    K, Wu = args.steps, args.warmup
+    main = measure(torch, cxa, W, w, dev_inputs, "f32", K, Wu, rank, world, dist, timed_clocks=(rank == 0))
+    variants = {}
+    if not args.no_variants:
+        v = measure(torch, cxa, W, w, dev_inputs, "bf16", K, Wu, rank, world, dist, timed_clocks=False)
+        vb = decode_bytes(w.L, w.H, w.dh, 2, kl, w.B)
+        variants["bf16_cache"] = {
+            "value": world * K * w.B * w.steps / (v["total_ms"] / 1000.0), "unit": "tokens/s",
+            "ms_per_step": v["total_ms"] / K,
+            "decode_GBps": vb / (v["decode_launch_us"] * 1e-6) / 1e9,
+            "decode_launch_us": v["decode_launch_us"], "populate_ms": v["populate_ms"]}
+    e2e_ms, h2d, d2h = measure_e2e(torch, cxa, w, (E, kl.astype(np.int32), Q), dev_inputs[1:4], K, Wu, dist)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+    peaks = load_peaks()
+    props = torch.cuda.get_device_properties(local)
+    tokens = world * K * w.B * w.steps
+    value = tokens / (main["total_ms"] / 1000.0)
+    dbytes = decode_bytes(w.L, w.H, w.dh, 4, kl, w.B)
+    achieved = dbytes / (main["decode_launch_us"] * 1e-6) / 1e9
+    pflops = populate_flops(w.L, w.d, w.B, w.T)
+    tf32_peak = peaks["bf16_tflops"] * TF32_OVER_BF16
+    pop_tflops = pflops / (main["populate_ms"] * 1e-3) / 1e12
+    traffic = recorded_traffic()
+    line = {
+        "metric": "cross-attn decode tokens/s (batched Whisper-Base window: populate + 128 decode steps)",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wu,
+        "ms_per_step": main["total_ms"] / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded numpy, Whisper-Base shapes)",
+        "config": dict(workload_config(w, "f32"), parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel<f32> (+ fused combine)",
+                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dbytes, "launch_us": main["decode_launch_us"],
+                     "peak_source": peaks["source"], "frac_of_nominal_7900": achieved / NOMINAL_HBM_GBS},
+        "populate": {"bound": "tensor", "kernel": "populate_gemm_kernel<tf32> + pack_weights",
+                     "achieved": pop_tflops, "unit": "TFLOP/s", "peak": tf32_peak,
+                     "peak_note": f"{peaks['source']} bf16 burst x nominal TF32/bf16 ratio 1.1/2.25",
+                     "frac": pop_tflops / tf32_peak, "flops_per_call": pflops, "ms": main["populate_ms"]},
+        "clocks": main["clocks"],
+        "e2e": {"value": tokens / (e2e_ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "note": "E, key_len and 128 Q copied in, 128 outputs copied out per "
+                                                     "window; weights resident"},
+        "gpu_launches": main["launches"],
+        "variants": variants,
+        "device": {"name": props.name, "sms": props.multi_processor_count,
+                   "lib_sha": source_sha(os.path.join(ROOT, "encoder_decoder_speech_gb300", "_lib", "libcxa.so"))},
+    }
+    if cpu_base is not None:
+        line["cpu_baseline"] = cpu_base
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.oracle_sample:
+        print(json.dumps(oracle_sample(args.budget_s, args.max_slots, args.warmup)))
+        return 0
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_cxa(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

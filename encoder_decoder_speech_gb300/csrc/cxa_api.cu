@@ -1,0 +1,282 @@
+// The C ABI of libcxa (declared in include/cxa.h): the cache descriptor with its
+// per-slot ready flags, argument validation, and dispatch to the kernel files.
+// Every check runs before any device work is enqueued.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "cxa.h"
+#include "internal.h"
+
+// Device-side status word: kernels OR in 1 when a bounded wait expires.
+static __device__ unsigned int g_cxa_status_word = 0;
+
+struct cxa_cache {
+  void* Kc;
+  void* Vc;
+  int B, T, L, H, dh;
+  int dtype;
+  std::vector<uint8_t> ready;   // populate sets, invalidate clears ("encoder_kv_ready")
+};
+
+namespace {
+
+thread_local std::string g_last_msg;
+std::atomic<unsigned long long> g_launches{0};
+
+int fail(int code, const std::string& msg) {
+  g_last_msg = msg;
+  return code;
+}
+
+int fail_cuda(cudaError_t e, const std::string& what) {
+  g_last_msg = what + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  return CXA_ECUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_dtype(int t) { return t == CXA_F32 || t == CXA_BF16; }
+
+}  // namespace
+
+namespace cxa {
+
+void count_launches(unsigned long long n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+cudaError_t current_device_info(DeviceInfo* info, std::string* msg) {
+  static std::mutex mu;
+  static DeviceInfo cache[128];
+  static bool have[128] = {};
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    *msg = "cudaGetDevice";
+    return e;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 128 && have[dev]) {
+    *info = cache[dev];
+    return cudaSuccess;
+  }
+  DeviceInfo d{};
+  d.device = dev;
+  if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) {
+    *msg = "cudaDeviceGetAttribute";
+    return e;
+  }
+  if (d.cc_major != 10 || d.cc_minor != 3) {
+    *msg = "libcxa is built for sm_103a (GB300); device " + std::to_string(dev) + " is sm_" +
+           std::to_string(d.cc_major) + std::to_string(d.cc_minor);
+    return cudaErrorNoKernelImageForDevice;
+  }
+  void* sym = nullptr;
+  if ((e = cudaGetSymbolAddress(&sym, g_cxa_status_word)) != cudaSuccess) {
+    *msg = "cudaGetSymbolAddress(status word)";
+    return e;
+  }
+  d.status_word = static_cast<unsigned int*>(sym);
+  if (dev >= 0 && dev < 128) {
+    cache[dev] = d;
+    have[dev] = true;
+  }
+  *info = d;
+  return cudaSuccess;
+}
+
+}  // namespace cxa
+
+extern "C" {
+
+int cxa_cache_create(cxa_cache** out, void* Kc, void* Vc, int B, int T, int L, int H, int dh,
+                     int cache_dtype) {
+  if (out == nullptr) return fail(CXA_EINVAL, "cxa_cache_create: out is NULL");
+  *out = nullptr;
+  if (Kc == nullptr || Vc == nullptr) return fail(CXA_EINVAL, "cxa_cache_create: Kc or Vc is NULL");
+  if (!aligned(Kc, 16) || !aligned(Vc, 16))
+    return fail(CXA_EINVAL, "cxa_cache_create: Kc and Vc must be 16-byte aligned");
+  if (T <= 0) return fail(CXA_EINVAL, "cxa_cache_create: the encoder memory length T must be positive");
+  if (B <= 0 || L <= 0 || H <= 0) return fail(CXA_EINVAL, "cxa_cache_create: B, L and H must be positive");
+  if (dh != 64) return fail(CXA_EINVAL, "cxa_cache_create: this build supports head_dim 64 only");
+  if (!valid_dtype(cache_dtype)) return fail(CXA_EINVAL, "cxa_cache_create: cache_dtype must be CXA_F32 or CXA_BF16");
+  if (static_cast<long long>(B) * L * H > 65535LL * 65535LL)
+    return fail(CXA_EINVAL, "cxa_cache_create: too many (slot, layer, head) rows");
+  if (L * H > 65535 || B > 65535) return fail(CXA_EINVAL, "cxa_cache_create: L*H and B must be <= 65535");
+  cxa_cache* c = new (std::nothrow) cxa_cache;
+  if (c == nullptr) return fail(CXA_EINVAL, "cxa_cache_create: out of host memory");
+  c->Kc = Kc;
+  c->Vc = Vc;
+  c->B = B;
+  c->T = T;
+  c->L = L;
+  c->H = H;
+  c->dh = dh;
+  c->dtype = cache_dtype;
+  c->ready.assign(static_cast<size_t>(B), 0);
+  *out = c;
+  return CXA_OK;
+}
+
+void cxa_cache_destroy(cxa_cache* c) { delete c; }
+
+size_t cxa_populate_workspace_bytes(int d, int L, int in_dtype) {
+  if (d <= 0 || L <= 0 || !valid_dtype(in_dtype)) return 0;
+  return cxa::populate_workspace_bytes(d, L, in_dtype == CXA_BF16);
+}
+
+size_t cxa_decode_workspace_bytes(int B, int T, int L, int H, int dh) {
+  if (B <= 0 || T <= 0 || L <= 0 || H <= 0 || dh != 64) return 0;
+  return cxa::decode_workspace_bytes(B, T, L, H);
+}
+
+int cxa_populate(cxa_cache* c, int b0, int nb, const void* E, const void* WK, const void* WV,
+                 const float* bV, int T, int d, int L, int H, int in_dtype, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  if (c == nullptr) return fail(CXA_EINVAL, "cxa_populate: cache descriptor is NULL");
+  if (T <= 0) return fail(CXA_EINVAL, "cxa_populate: the encoder memory length T must be positive");
+  if (H <= 0 || H * c->dh != d)
+    return fail(CXA_EINVAL, "cxa_populate: num_heads * head_dim must equal the model width d");
+  if (T != c->T || L != c->L || H != c->H)
+    return fail(CXA_EINVAL, "cxa_populate: T, L, H do not match the cache descriptor");
+  if (nb <= 0 || b0 < 0 || b0 + nb > c->B)
+    return fail(CXA_EINVAL, "cxa_populate: slots [b0, b0+nb) out of range");
+  if (!valid_dtype(in_dtype)) return fail(CXA_EINVAL, "cxa_populate: in_dtype must be CXA_F32 or CXA_BF16");
+  if (E == nullptr || WK == nullptr || WV == nullptr || bV == nullptr || workspace == nullptr)
+    return fail(CXA_EINVAL, "cxa_populate: a pointer argument is NULL");
+  if (!aligned(E, 16) || !aligned(bV, 16) || !aligned(workspace, 256))
+    return fail(CXA_EINVAL, "cxa_populate: E and bV must be 16-byte aligned, the workspace 256-byte aligned");
+  const int esz = in_dtype == CXA_BF16 ? 2 : 4;
+  if (!aligned(WK, esz) || !aligned(WV, esz))
+    return fail(CXA_EINVAL, "cxa_populate: WK and WV must be aligned to their element size");
+  if (workspace_bytes < cxa::populate_workspace_bytes(d, L, in_dtype == CXA_BF16))
+    return fail(CXA_EINVAL, "cxa_populate: workspace smaller than cxa_populate_workspace_bytes()");
+
+  // New encoder memory: these slots are stale until the kernels are enqueued.
+  for (int b = b0; b < b0 + nb; ++b) c->ready[static_cast<size_t>(b)] = 0;
+
+  std::string msg;
+  cxa::DeviceInfo dev;
+  cudaError_t e = cxa::current_device_info(&dev, &msg);
+  if (e != cudaSuccess) return fail_cuda(e, "cxa_populate: " + msg);
+
+  cxa::PopulateLaunch a;
+  a.Kc = c->Kc;
+  a.Vc = c->Vc;
+  a.E = E;
+  a.WK = WK;
+  a.WV = WV;
+  a.bV = bV;
+  a.wpack = workspace;
+  a.b0 = b0;
+  a.nb = nb;
+  a.T = T;
+  a.d = d;
+  a.L = L;
+  a.H = H;
+  a.in_bf16 = in_dtype == CXA_BF16;
+  a.cache_bf16 = c->dtype == CXA_BF16;
+  e = cxa::launch_populate(a, dev, static_cast<cudaStream_t>(stream), &msg);
+  if (e != cudaSuccess) {
+    if (!msg.empty()) return fail(CXA_EINVAL, "cxa_populate: " + msg);
+    return fail_cuda(e, "cxa_populate: launch");
+  }
+  for (int b = b0; b < b0 + nb; ++b) c->ready[static_cast<size_t>(b)] = 1;
+  return CXA_OK;
+}
+
+int cxa_decode(const cxa_cache* c, const float* Q, const int* key_len, float* out, float scale,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  if (c == nullptr) return fail(CXA_EINVAL, "cxa_decode: cache descriptor is NULL");
+  if (Q == nullptr || key_len == nullptr || out == nullptr || workspace == nullptr)
+    return fail(CXA_EINVAL, "cxa_decode: a pointer argument is NULL");
+  if (!aligned(Q, 16) || !aligned(out, 16) || !aligned(key_len, 4) || !aligned(workspace, 256))
+    return fail(CXA_EINVAL, "cxa_decode: Q and out must be 16-byte aligned, the workspace 256-byte aligned");
+  if (static_cast<const void*>(Q) == static_cast<const void*>(out))
+    return fail(CXA_EINVAL, "cxa_decode: out must not alias Q");
+  if (!std::isfinite(scale)) return fail(CXA_EINVAL, "cxa_decode: scale must be finite");
+  if (workspace_bytes < cxa::decode_workspace_bytes(c->B, c->T, c->L, c->H))
+    return fail(CXA_EINVAL, "cxa_decode: workspace smaller than cxa_decode_workspace_bytes()");
+  for (int b = 0; b < c->B; ++b)
+    if (!c->ready[static_cast<size_t>(b)])
+      return fail(CXA_ENOTREADY, "cxa_decode: slot " + std::to_string(b) +
+                                     " is not populated (invalidated or never populated)");
+
+  std::string msg;
+  cxa::DeviceInfo dev;
+  cudaError_t e = cxa::current_device_info(&dev, &msg);
+  if (e != cudaSuccess) return fail_cuda(e, "cxa_decode: " + msg);
+
+  cxa::DecodeLaunch a;
+  a.Kc = c->Kc;
+  a.Vc = c->Vc;
+  a.Q = Q;
+  a.key_len = key_len;
+  a.out = out;
+  a.workspace = workspace;
+  a.B = c->B;
+  a.T = c->T;
+  a.L = c->L;
+  a.H = c->H;
+  a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(c->dh));
+  a.cache_bf16 = c->dtype == CXA_BF16;
+  e = cxa::launch_decode(a, dev, static_cast<cudaStream_t>(stream), &msg);
+  if (e != cudaSuccess) return fail_cuda(e, "cxa_decode: launch");
+  return CXA_OK;
+}
+
+int cxa_invalidate(cxa_cache* c, int b) {
+  if (c == nullptr) return fail(CXA_EINVAL, "cxa_invalidate: cache descriptor is NULL");
+  if (b == -1) {
+    for (auto& r : c->ready) r = 0;
+    return CXA_OK;
+  }
+  if (b < 0 || b >= c->B) return fail(CXA_EINVAL, "cxa_invalidate: slot out of range");
+  c->ready[static_cast<size_t>(b)] = 0;
+  return CXA_OK;
+}
+
+int cxa_is_ready(const cxa_cache* c, int b) {
+  if (c == nullptr || b < 0 || b >= c->B) return CXA_EINVAL;
+  return c->ready[static_cast<size_t>(b)] ? 1 : 0;
+}
+
+const char* cxa_strerror(int code) {
+  switch (code) {
+    case CXA_OK: return "CXA_OK";
+    case CXA_EINVAL: return "CXA_EINVAL: invalid argument or geometry";
+    case CXA_ENOTREADY: return "CXA_ENOTREADY: projection cache not populated";
+    case CXA_ECUDA: return "CXA_ECUDA: CUDA runtime error";
+    case CXA_ETIMEOUT: return "CXA_ETIMEOUT: a kernel's bounded wait expired";
+    default: return "unknown cxa status";
+  }
+}
+
+const char* cxa_last_error_message(void) { return g_last_msg.c_str(); }
+
+unsigned long long cxa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int cxa_device_status(int clear) {
+  std::string msg;
+  cxa::DeviceInfo dev;
+  cudaError_t e = cxa::current_device_info(&dev, &msg);
+  if (e != cudaSuccess) return fail_cuda(e, "cxa_device_status: " + msg);
+  unsigned int word = 0;
+  if ((e = cudaMemcpy(&word, dev.status_word, sizeof(word), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return fail_cuda(e, "cxa_device_status: read");
+  if (clear) {
+    const unsigned int zero = 0;
+    if ((e = cudaMemcpy(dev.status_word, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess)
+      return fail_cuda(e, "cxa_device_status: clear");
+  }
+  return word ? CXA_ETIMEOUT : CXA_OK;
+}
+
+}  // extern "C"

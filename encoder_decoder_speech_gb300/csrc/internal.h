@@ -1,0 +1,64 @@
+// Internal interface between the C-ABI layer (cxa_api.cu) and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <string>
+
+#include <cuda_runtime.h>
+
+namespace cxa {
+
+// Everything a populate launch needs; pointers are device pointers already
+// validated by the C-ABI layer.
+struct PopulateLaunch {
+  void* Kc;            // cache bases (slot 0)
+  void* Vc;
+  const void* E;       // [nb][T][d]
+  const void* WK;      // [L][d][d] (d_in, d_out)
+  const void* WV;
+  const float* bV;     // [L][d]
+  void* wpack;         // workspace: [2*L*d][d] K-major packed weights
+  int b0, nb, T, d, L, H;
+  bool in_bf16;
+  bool cache_bf16;
+};
+
+struct DecodeLaunch {
+  const void* Kc;
+  const void* Vc;
+  const float* Q;      // [B][L][H][64]
+  const int* key_len;  // [B]
+  float* out;          // [B][L][H][64]
+  void* workspace;
+  int B, T, L, H;
+  float scale;         // > 0
+  bool cache_bf16;
+};
+
+// Device facts of the current device, queried once per device.
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  int cc_major, cc_minor;
+  unsigned int* status_word;   // device address of the library's status word
+};
+
+// Fills *info for the current device; returns a CUDA error and a message on failure.
+cudaError_t current_device_info(DeviceInfo* info, std::string* msg);
+
+// Workspace layout helpers shared by the size query and the launchers.
+size_t populate_workspace_bytes(int d, int L, bool in_bf16);
+size_t decode_workspace_bytes(int B, int T, int L, int H);
+
+// Launchers: enqueue on `stream`, return cudaSuccess or the first error; on a
+// non-CUDA failure (e.g. tensor-map encoding) they return cudaErrorInvalidValue
+// and describe it in *msg.
+cudaError_t launch_populate(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t stream,
+                            std::string* msg);
+cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStream_t stream,
+                          std::string* msg);
+
+// Counts every kernel launch the library makes.
+void count_launches(unsigned long long n);
+
+}  // namespace cxa

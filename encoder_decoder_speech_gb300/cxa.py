@@ -1,0 +1,222 @@
+"""Python binding of libcxa (include/cxa.h): argument marshalling only.
+
+The C-named functions (``cxa_populate``, ``cxa_decode``, ``cxa_invalidate``, ...)
+take raw device pointers or torch tensors (their ``data_ptr()`` is passed) and
+return the C status code. ``CrossAttentionCache`` is a convenience owner of the
+cache, workspaces and descriptor that raises ``CxaError`` on a non-zero status.
+PyTorch is used for device memory and streams only; every step of populate and
+decode runs in libcxa's CUDA kernels. There is no fallback: if the library is
+not built, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+CXA_OK, CXA_EINVAL, CXA_ENOTREADY, CXA_ECUDA, CXA_ETIMEOUT = 0, -1, -2, -3, -4
+CXA_F32, CXA_BF16 = 0, 1
+
+# every symbol include/cxa.h declares: name -> (restype, argtypes)
+_c_void_pp = ctypes.POINTER(ctypes.c_void_p)
+SIGNATURES = {
+    "cxa_cache_create": (ctypes.c_int, [_c_void_pp, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "cxa_cache_destroy": (None, [ctypes.c_void_p]),
+    "cxa_populate_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "cxa_decode_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 5),
+    "cxa_populate": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "cxa_decode": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
+                                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "cxa_invalidate": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    "cxa_is_ready": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    "cxa_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "cxa_last_error_message": (ctypes.c_char_p, []),
+    "cxa_launch_count": (ctypes.c_ulonglong, []),
+    "cxa_device_status": (ctypes.c_int, [ctypes.c_int]),
+}
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load libcxa.so (once) and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"libcxa is not built ({path} is missing); build it with "
+                           "encoder_decoder_speech_gb300._build.build_library()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+class CxaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        lib = load()
+        self.code = code
+        super().__init__(f"{where}: {lib.cxa_strerror(code).decode()}: {lib.cxa_last_error_message().decode()}")
+
+
+def check(code: int, where: str = "cxa") -> None:
+    if code != CXA_OK:
+        raise CxaError(code, where)
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream
+    return int(s)
+
+
+# ---------------------------------------------------------------- C-named calls
+def cxa_cache_create(Kc, Vc, B, T, L, H, dh, cache_dtype):
+    """Returns (status, handle); handle is None unless status == CXA_OK."""
+    h = ctypes.c_void_p()
+    rc = load().cxa_cache_create(ctypes.byref(h), _ptr(Kc), _ptr(Vc), B, T, L, H, dh, cache_dtype)
+    return rc, (h.value if rc == CXA_OK else None)
+
+
+def cxa_cache_destroy(handle) -> None:
+    load().cxa_cache_destroy(handle)
+
+
+def cxa_populate_workspace_bytes(d, L, in_dtype) -> int:
+    return load().cxa_populate_workspace_bytes(d, L, in_dtype)
+
+
+def cxa_decode_workspace_bytes(B, T, L, H, dh=64) -> int:
+    return load().cxa_decode_workspace_bytes(B, T, L, H, dh)
+
+
+def cxa_populate(handle, b0, nb, E, WK, WV, bV, T, d, L, H, in_dtype, workspace, workspace_bytes, stream=None) -> int:
+    return load().cxa_populate(handle, b0, nb, _ptr(E), _ptr(WK), _ptr(WV), _ptr(bV), T, d, L, H, in_dtype,
+                               _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def cxa_decode(handle, Q, key_len, out, scale, workspace, workspace_bytes, stream=None) -> int:
+    return load().cxa_decode(handle, _ptr(Q), _ptr(key_len), _ptr(out), float(scale), _ptr(workspace),
+                             workspace_bytes, _stream(stream))
+
+
+def cxa_invalidate(handle, b=-1) -> int:
+    return load().cxa_invalidate(handle, b)
+
+
+def cxa_is_ready(handle, b) -> int:
+    return load().cxa_is_ready(handle, b)
+
+
+def cxa_strerror(code) -> str:
+    return load().cxa_strerror(code).decode()
+
+
+def cxa_last_error_message() -> str:
+    return load().cxa_last_error_message().decode()
+
+
+def cxa_launch_count() -> int:
+    return load().cxa_launch_count()
+
+
+def cxa_device_status(clear=0) -> int:
+    return load().cxa_device_status(clear)
+
+
+# ---------------------------------------------------------------- owner object
+_DTYPES = {"f32": CXA_F32, "bf16": CXA_BF16}
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t == torch.float32:
+        return CXA_F32
+    if t == torch.bfloat16:
+        return CXA_BF16
+    raise TypeError(f"unsupported dtype {t}; expected float32 or bfloat16")
+
+
+class CrossAttentionCache:
+    """Owns a [B][L][H][T][64] K/V projection cache, its decode workspace and
+    the libcxa descriptor; allocation goes through torch on ``device``."""
+
+    def __init__(self, B: int, T: int, L: int, H: int, dh: int = 64, cache_dtype: str = "f32", device="cuda"):
+        import torch
+        self.B, self.T, self.L, self.H, self.dh = B, T, L, H, dh
+        self.d = H * dh
+        self.cache_dtype = cache_dtype
+        tdt = torch.float32 if cache_dtype == "f32" else torch.bfloat16
+        self.Kc = torch.empty((B, L, H, T, dh), dtype=tdt, device=device)
+        self.Vc = torch.empty((B, L, H, T, dh), dtype=tdt, device=device)
+        self.decode_ws_bytes = cxa_decode_workspace_bytes(B, T, L, H, dh)
+        self.decode_ws = torch.zeros(max(self.decode_ws_bytes, 256), dtype=torch.uint8, device=device)
+        self._pop_ws = {}
+        rc, h = cxa_cache_create(self.Kc, self.Vc, B, T, L, H, dh, _DTYPES[cache_dtype])
+        check(rc, "cxa_cache_create")
+        self.handle = h
+
+    def populate_workspace(self, in_dtype: int):
+        import torch
+        if in_dtype not in self._pop_ws:
+            n = cxa_populate_workspace_bytes(self.d, self.L, in_dtype)
+            self._pop_ws[in_dtype] = torch.empty(n, dtype=torch.uint8, device=self.Kc.device)
+        return self._pop_ws[in_dtype]
+
+    def populate(self, E, WK, WV, bV, b0: int = 0, stream=None) -> None:
+        """E [nb, T, d]; WK, WV [L, d, d] (d_in, d_out), same dtype as E; bV [L, d] fp32."""
+        in_dtype = _dtype_code(E.dtype)
+        for name, t in (("E", E), ("WK", WK), ("WV", WV), ("bV", bV)):
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous")
+        if WK.dtype != E.dtype or WV.dtype != E.dtype:
+            raise TypeError("WK and WV must have E's dtype")
+        nb = E.shape[0] if E.dim() == 3 else 1
+        ws = self.populate_workspace(in_dtype)
+        check(cxa_populate(self.handle, b0, nb, E, WK, WV, bV, E.shape[-2], E.shape[-1], WK.shape[0],
+                           self.H, in_dtype, ws, ws.numel(), stream), "cxa_populate")
+
+    def decode(self, Q, key_len, out=None, scale: float = 0.0, stream=None):
+        """Q [B, L, H, 64] fp32, key_len [B] int32 (device). Returns out [B, L, H, 64] fp32."""
+        import torch
+        if out is None:
+            out = torch.empty_like(Q)
+        check(cxa_decode(self.handle, Q, key_len, out, scale, self.decode_ws, self.decode_ws_bytes, stream),
+              "cxa_decode")
+        return out
+
+    def invalidate(self, b: int = -1) -> None:
+        check(cxa_invalidate(self.handle, b), "cxa_invalidate")
+
+    def is_ready(self, b: int) -> bool:
+        return cxa_is_ready(self.handle, b) == 1
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            cxa_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

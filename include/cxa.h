@@ -1,0 +1,183 @@
+/*
+ * cxa.h -- C ABI of libcxa: encoder-decoder cross-attention on one GB300 (sm_103a).
+ *
+ * Two operations make up the path:
+ *
+ *   populate  K_l = E x WK_l and V_l = E x WV_l + bV_l for every decoder layer l,
+ *             written straight into a layer-major, head-major K/V projection cache
+ *             ("Whisper: Trace One Encoder Tensor into Every Decoder Layer",
+ *             "The concept: one tensor, many consumers" for the formulas and the
+ *             cache policy; "View 2 -- expand one cross-attention operation" for
+ *             the per-layer slab; "Deliberate failure: token-major K meets a
+ *             head-major consumer" for the token-major -> head-major re-layout).
+ *   decode    one query row per (slot, layer, head) attends non-causally over all
+ *             valid encoder keys: out = softmax(scale * q.K^T) V ("View 2": the
+ *             decode call with num_heads, query_tokens = 1, key_tokens, head_dim
+ *             and scale = 0.125 = 1/sqrt(64)).
+ *
+ * The cache is caller-owned explicit I/O ("Recurrence as feeds", "What it
+ * opened": a cache is an extra input that one run writes and the next reads).
+ * The library allocates no device memory: every device buffer below (E, weights,
+ * biases, cache, queries, key lengths, outputs, workspaces) belongs to the caller
+ * and must stay alive until the work enqueued on the stream has finished.
+ * The descriptor (cxa_cache) is a small host object: geometry, dtype and the
+ * per-slot ready flags.
+ *
+ * All calls that take a stream are asynchronous: they validate their arguments
+ * on the host, enqueue kernels on `stream` (a cudaStream_t; NULL = legacy default
+ * stream) and return. Every check happens before any device work is enqueued,
+ * so a call that returns an error has launched nothing.
+ *
+ * Status codes (int): CXA_OK on success, otherwise one of the negative codes
+ * below; cxa_strerror() names a code and cxa_last_error_message() gives the
+ * detail of the calling thread's last failure.
+ */
+#ifndef CXA_H_
+#define CXA_H_
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define CXA_API __attribute__((visibility("default")))
+#else
+#define CXA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------- */
+#define CXA_OK          0
+#define CXA_EINVAL     (-1)  /* bad geometry, null or misaligned pointer, short workspace */
+#define CXA_ENOTREADY  (-2)  /* a slot of the cache is not populated: decode refuses
+                                ("View 3 -- prefill vs decode": decode refuses (-2)
+                                until prefill repopulates the cache) */
+#define CXA_ECUDA      (-3)  /* a CUDA runtime error (launch failure, wrong device) */
+#define CXA_ETIMEOUT   (-4)  /* a kernel's bounded wait expired (see cxa_device_status) */
+
+/* ---- element types ------------------------------------------------------- */
+#define CXA_F32   0   /* IEEE fp32 */
+#define CXA_BF16  1   /* bfloat16, stored as 16-bit words */
+
+typedef struct cxa_cache cxa_cache;
+
+/*
+ * Create a cache descriptor over caller-owned K/V cache buffers.
+ *
+ *   Kc, Vc  device pointers, each B*L*H*T*dh elements of cache_dtype, laid out
+ *           [B][L][H][T][dh] (slot, layer-major, head-major: element (b,l,h,t,c)
+ *           at (((b*L + l)*H + h)*T + t)*dh + c; for one Whisper-Base slot in fp32
+ *           the layer-5 K slab starts 15,360,000 bytes in, as "View 2" prints).
+ *           16-byte aligned.
+ *   B       batch slots (independent encoder memories), >= 1.
+ *   T       encoder length T_enc, > 0 ("View 3": a positive encoder memory
+ *           length is required).
+ *   L, H    decoder layers and heads, >= 1.
+ *   dh      head dimension; this build supports dh == 64 only.
+ *   cache_dtype  CXA_F32 or CXA_BF16 (bf16 stores round to nearest even).
+ *
+ * Every slot starts not ready. Returns CXA_EINVAL on bad arguments (and leaves
+ * *out NULL). Performs no CUDA call.
+ */
+CXA_API int cxa_cache_create(cxa_cache** out, void* Kc, void* Vc, int B, int T, int L, int H,
+                     int dh, int cache_dtype);
+
+/* Free the descriptor (not the caller's buffers). NULL is ignored. */
+CXA_API void cxa_cache_destroy(cxa_cache* c);
+
+/*
+ * Bytes of device workspace cxa_populate needs for width d, L layers and input
+ * type in_dtype: the layer weights repacked once per call into the K-major
+ * operand layout of the tensor-core GEMM (2*L*d*d elements of in_dtype).
+ */
+CXA_API size_t cxa_populate_workspace_bytes(int d, int L, int in_dtype);
+
+/*
+ * Bytes of device workspace cxa_decode needs for a cache of this geometry: one
+ * partial softmax state (running max, running sum, dh accumulators) per
+ * (slot, layer, head, key chunk), plus per-row arrival counters.
+ */
+CXA_API size_t cxa_decode_workspace_bytes(int B, int T, int L, int H, int dh);
+
+/*
+ * Populate slots [b0, b0+nb) of the cache from nb encoder memories.
+ *
+ *   E       device, [nb][T][d] of in_dtype, token-major (row t = one encoder
+ *           frame), 16-byte aligned.
+ *   WK, WV  device, [L][d][d] of in_dtype, each layer indexed (d_in, d_out) so
+ *           that K_l = E x WK_l; head h owns output columns h*dh .. h*dh+dh-1.
+ *   bV      device, [L][d] fp32 value bias, 16-byte aligned, added to V only. There is no key
+ *           bias: it cannot change the softmax ("Caso de estudio: WhisperKit",
+ *           §2: the key-projection bias is dropped as redundant).
+ *   T, d, L, H   must match the descriptor, with H*dh == d ("View 3": num_heads *
+ *           head_dim == embed_dim is a hard error).
+ *   in_dtype CXA_F32 (tensor cores read the fp32 operands as TF32) or CXA_BF16.
+ *   workspace, workspace_bytes  device scratch of at least
+ *           cxa_populate_workspace_bytes(d, L, in_dtype) bytes, 256-byte aligned.
+ *
+ * The slots are marked not ready first and ready again once both kernels are
+ * enqueued without error, so a failed call leaves them not ready. Readiness is
+ * stream-ordered: decode on the same stream (or after an event) sees the data.
+ */
+CXA_API int cxa_populate(cxa_cache* c, int b0, int nb, const void* E, const void* WK,
+                 const void* WV, const float* bV, int T, int d, int L, int H,
+                 int in_dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * One decode step for every slot, layer and head.
+ *
+ *   Q        device fp32 [B][L][H][dh], one query row per (slot, layer, head);
+ *            16-byte aligned.
+ *   key_len  device int32 [B], valid encoder keys per slot; keys t >= key_len[b]
+ *            are excluded exactly (the limit of the additive key-padding mask,
+ *            "Caso de estudio: WhisperKit", §4). Values are clamped to [0, T];
+ *            a slot with no valid key gets a zero output (the clamped softmax
+ *            denominator of §2). Padded cache rows are never read.
+ *   out      device fp32 [B][L][H][dh], 16-byte aligned; may not alias Q.
+ *   scale    multiplies q.k; a value <= 0 selects 1/sqrt(dh).
+ *   workspace, workspace_bytes  device scratch of at least
+ *            cxa_decode_workspace_bytes(B, T, L, H, dh) bytes, 256-byte aligned;
+ *            its counters must be zero before the first call on a new buffer
+ *            (cudaMemset) and the kernels leave them zero afterwards. Calls that
+ *            share a workspace must be ordered on one stream.
+ *
+ * Returns CXA_ENOTREADY, launching nothing, unless every slot is ready.
+ */
+CXA_API int cxa_decode(const cxa_cache* c, const float* Q, const int* key_len, float* out,
+               float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Mark slot b (or every slot when b == -1) not ready: installing new encoder
+ * memory invalidates the projection cache by flag ("View 3": encoder_kv_ready = 0;
+ * the circuit's invalidation trigger is an encoder memory update). Host only,
+ * no device work. Returns CXA_EINVAL for a slot out of range.
+ */
+CXA_API int cxa_invalidate(cxa_cache* c, int b);
+
+/* 1 if slot b is ready, 0 if not, CXA_EINVAL for a bad slot or descriptor. */
+CXA_API int cxa_is_ready(const cxa_cache* c, int b);
+
+/* Static name of a status code. */
+CXA_API const char* cxa_strerror(int code);
+
+/* Detail of the calling thread's last failed call ("" if none). */
+CXA_API const char* cxa_last_error_message(void);
+
+/* Number of kernels this library has launched in this process. */
+CXA_API unsigned long long cxa_launch_count(void);
+
+/*
+ * Read the device-side status word of the current device: 0, or CXA_ETIMEOUT
+ * when a kernel's bounded wait expired since the word was last cleared (the
+ * kernel then skipped its remaining work). Synchronises the device. clear != 0
+ * resets the word. Returns CXA_ECUDA if the word cannot be read. After a
+ * timeout, the decode workspace's counters must be zeroed again before reuse.
+ */
+CXA_API int cxa_device_status(int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CXA_H_ */

@@ -1,0 +1,285 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Populate is compared element by element with the oracle's projection of the
+same inputs (relative Frobenius, TF32 / bf16 tensor-core inputs). Decode is
+compared kernel-isolated -- the oracle decodes the very cache the GPU holds,
+upcast to fp64 -- element by element (max-abs). Sizes span several tiles and
+ragged tails; the full-size workloads are checked on sampled heads and rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+from _gpu_common import (DECODE_BF16_MAX_ABS, DECODE_F32_MAX_ABS, POPULATE_REL_FROB, cache_for, dev, host,
+                         inputs_on_device)
+from encoder_decoder_speech_gb300 import cxa
+from encoder_decoder_speech_gb300 import workloads as W
+from oracle import cross_attention as O
+
+pytestmark = pytest.mark.gpu
+
+DECODE_TOL = {"f32": DECODE_F32_MAX_ABS, "bf16": DECODE_BF16_MAX_ABS}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cxa_lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    yield
+    torch.cuda.synchronize()
+    assert cxa.cxa_device_status(1) == cxa.CXA_OK
+
+
+def _populate(w, cache_dtype):
+    d, h = inputs_on_device(w)
+    c = cache_for(w, cache_dtype)
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    torch.cuda.synchronize()
+    return c, d, h
+
+
+SMALL = [
+    # name, B, T, d, L, H: tiles of 128 rows x 256 columns, ragged in both
+    ("one_row", 1, 1, 64, 1, 1),
+    ("two_mtiles_ragged", 2, 200, 128, 2, 2),
+    ("three_ntiles", 3, 129, 384, 1, 6),
+    ("odd_heads_straddle", 2, 300, 192, 3, 3),
+    ("exact_tiles", 1, 256, 256, 2, 4),
+]
+
+
+@pytest.mark.parametrize("in_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", SMALL, ids=[s[0] for s in SMALL])
+def test_populate_small(shape, in_dtype, cache_dtype):
+    name, B, T, d, L, H = shape
+    w = W.custom(name, B=B, T=T, d=d, L=L, H=H, in_dtype=in_dtype, index=910)
+    c, _, h = _populate(w, cache_dtype)
+    Kr, Vr = O.populate(h["E"], h["WK"], h["WV"], h["bV"], H)
+    assert O.rel_frobenius(host(c.Kc), Kr) <= POPULATE_REL_FROB
+    assert O.rel_frobenius(host(c.Vc), Vr) <= POPULATE_REL_FROB
+    assert np.isfinite(host(c.Kc)).all() and np.isfinite(host(c.Vc)).all()
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+def test_populate_tiny_config(cache_dtype):
+    w = W.WORKLOADS["tiny"]
+    c, _, h = _populate(w, cache_dtype)
+    Kr, Vr = O.populate(h["E"], h["WK"], h["WV"], h["bV"], w.H)
+    ek, ev = O.rel_frobenius(host(c.Kc), Kr), O.rel_frobenius(host(c.Vc), Vr)
+    print(f"tiny populate rel-frob K {ek:.3e} V {ev:.3e} ({cache_dtype} cache)")
+    assert ek <= POPULATE_REL_FROB and ev <= POPULATE_REL_FROB
+
+
+def test_populate_partial_slots_leave_others_untouched():
+    w = W.custom("partial", B=4, T=150, d=128, L=2, H=2, index=911)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, "f32")
+    c.Kc.fill_(7.0)
+    c.Vc.fill_(7.0)
+    c.populate(d["E"][1:3].contiguous(), d["WK"], d["WV"], d["bV"], b0=1)
+    torch.cuda.synchronize()
+    assert [c.is_ready(b) for b in range(4)] == [False, True, True, False]
+    assert torch.all(c.Kc[0] == 7.0) and torch.all(c.Kc[3] == 7.0) and torch.all(c.Vc[3] == 7.0)
+    Kr, Vr = O.populate(h["E"][1:3], h["WK"], h["WV"], h["bV"], w.H)
+    assert O.rel_frobenius(host(c.Kc[1:3]), Kr) <= POPULATE_REL_FROB
+    assert O.rel_frobenius(host(c.Vc[1:3]), Vr) <= POPULATE_REL_FROB
+
+
+def _fill_cache(c, seed):
+    """Overwrite a populated cache with seeded N(0,1) values (bf16-exact for a bf16 cache)."""
+    rng = np.random.default_rng(seed)
+    K = rng.standard_normal(tuple(c.Kc.shape), dtype=np.float32)
+    V = rng.standard_normal(tuple(c.Vc.shape), dtype=np.float32)
+    if c.cache_dtype == "bf16":
+        K, V = W.bf16_round(K), W.bf16_round(V)
+    c.Kc.copy_(dev(K, c.Kc.dtype))
+    c.Vc.copy_(dev(V, c.Vc.dtype))
+    return K.astype(np.float64), V.astype(np.float64)
+
+
+def _decode_case(T, key_len, cache_dtype, L=2, H=3, seed=0, scale=0.0):
+    B = len(key_len)
+    w = W.custom(f"dec{T}", B=B, T=T, d=64 * H, L=L, H=H, index=920)
+    c, d, _ = _populate(w, cache_dtype)
+    K, V = _fill_cache(c, 100 + seed)
+    Q = np.random.default_rng(200 + seed).standard_normal((B, L, H, 64)).astype(np.float32)
+    kl = np.array(key_len, dtype=np.int32)
+    out = c.decode(dev(Q), dev(kl, torch.int32), scale=scale)
+    torch.cuda.synchronize()
+    ref = O.decode(Q, K, V, kl, scale if scale > 0 else None)
+    return host(out), ref
+
+
+DECODE_CASES = [
+    (1, [1, 0]),
+    (2, [2, 1, 0]),
+    (3, [3, 2, 5, -4]),
+    (63, [63, 1, 62]),
+    (64, [64, 63, 1]),
+    (65, [65, 64, 33]),
+    (127, [127, 64, 65, 0]),
+    (129, [129, 128, 100]),
+    (1500, [1500, 500, 1, 1499, 2000]),
+]
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T,key_len", DECODE_CASES, ids=[f"T{c[0]}" for c in DECODE_CASES])
+def test_decode_kernel_isolated(T, key_len, cache_dtype):
+    got, ref = _decode_case(T, key_len, cache_dtype, seed=T)
+    err = np.abs(got - ref).max()
+    assert err <= DECODE_TOL[cache_dtype], err
+    for b, n in enumerate(key_len):
+        if n <= 0:
+            assert np.all(got[b] == 0.0)
+
+
+def test_decode_scale_override():
+    got, ref = _decode_case(300, [300, 150], "f32", scale=0.37, seed=3)
+    assert np.abs(got - ref).max() <= DECODE_F32_MAX_ABS
+
+
+def test_decode_repeated_calls_share_the_workspace():
+    """The arrival counters are reset by each call: consecutive steps stay exact."""
+    w = W.custom("rep", B=3, T=700, d=256, L=2, H=4, ragged=True, index=921)
+    c, d, _ = _populate(w, "f32")
+    K, V = host(c.Kc), host(c.Vc)
+    kl = W.make_key_len(w)
+    for s in range(4):
+        Q = W.make_Q(w, s)
+        out = host(c.decode(dev(Q), d["key_len"]))
+        assert np.abs(out - O.decode(Q, K, V, kl)).max() <= DECODE_F32_MAX_ABS
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+def test_padding_rows_are_never_read(cache_dtype):
+    """NaN / Inf in cache rows t >= key_len[b] must not reach the output."""
+    w = W.custom("poison", B=3, T=500, d=128, L=2, H=2, ragged=True, index=922)
+    c, d, _ = _populate(w, cache_dtype)
+    Q = dev(W.make_Q(w, 0))
+    clean = c.decode(Q, d["key_len"]).clone()
+    kl = W.make_key_len(w)
+    for b in range(w.B):
+        c.Kc[b, :, :, int(kl[b]):] = float("nan")
+        c.Vc[b, :, :, int(kl[b]):] = float("inf")
+    poisoned = c.decode(Q, d["key_len"])
+    torch.cuda.synchronize()
+    assert torch.equal(clean, poisoned)
+
+
+def test_workspace_poison_does_not_leak():
+    """Partials are fully rewritten each call: NaN-filled partial storage is harmless."""
+    w = W.custom("wspoison", B=2, T=400, d=128, L=1, H=2, index=923)
+    c, d, h = _populate(w, "f32")
+    nctr = ((w.B * w.L * w.H * 4 + 255) // 256) * 256
+    c.decode_ws[nctr:c.decode_ws_bytes].view(torch.float32).fill_(float("nan"))
+    Q = W.make_Q(w, 0)
+    out = host(c.decode(dev(Q), d["key_len"]))
+    assert np.abs(out - O.decode(Q, host(c.Kc), host(c.Vc), h["key_len"])).max() <= DECODE_F32_MAX_ABS
+
+
+def test_invalidate_refuses_then_repopulate():
+    w = W.custom("inval", B=3, T=260, d=128, L=2, H=2, index=924)
+    c, d, h = _populate(w, "f32")
+    Q = dev(W.make_Q(w, 0))
+    ref = c.decode(Q, d["key_len"]).clone()
+    c.invalidate(1)
+    out = torch.full_like(ref, 123.0)
+    launches = cxa.cxa_launch_count()
+    rc = cxa.cxa_decode(c.handle, Q, d["key_len"], out, 0.0, c.decode_ws, c.decode_ws_bytes)
+    assert rc == cxa.CXA_ENOTREADY
+    assert cxa.cxa_launch_count() == launches
+    torch.cuda.synchronize()
+    assert torch.all(out == 123.0)
+    c.populate(d["E"][1:2].contiguous(), d["WK"], d["WV"], d["bV"], b0=1)
+    again = c.decode(Q, d["key_len"])
+    torch.cuda.synchronize()
+    assert torch.allclose(again, ref, atol=1e-6, rtol=0)
+
+
+def test_key_bias_folded_into_the_cache_leaves_decode_unchanged():
+    """A key bias adds q.bK to every score of a row: softmax ignores it."""
+    w = W.custom("kbias", B=2, T=333, d=256, L=2, H=4, index=925)
+    c, d, _ = _populate(w, "f32")
+    Q = dev(W.make_Q(w, 1))
+    ref = c.decode(Q, d["key_len"]).clone()
+    bK = dev(np.random.default_rng(5).standard_normal((w.L, w.H, 64)).astype(np.float32))
+    c.Kc += bK[None, :, :, None, :]
+    got = c.decode(Q, d["key_len"])
+    torch.cuda.synchronize()
+    assert (got - ref).abs().max().item() <= DECODE_F32_MAX_ABS
+
+
+def test_whisper_base_layer5_slab_offset():
+    """Whisper-Base dims, fp32 cache: the layer-5 K slab starts 15,360,000 bytes
+    into slot 0 and holds K_5 = E x WK_5 head-major."""
+    w = W.WORKLOADS["base"]
+    c, _, h = _populate(w, "f32")
+    flat = c.Kc.view(-1)
+    off = 15360000 // 4
+    got = host(flat[off:off + 64])
+    ref = h["E"][0, 0].astype(np.float64) @ h["WK"][5][:, :64].astype(np.float64)
+    assert np.abs(got - ref).max() <= 2e-3 * np.abs(ref).max()
+    # token-major placement would put E[0, 1] x WK_5[:, 0] at offset + 512 instead
+    ref_t1 = h["E"][0, 1].astype(np.float64) @ h["WK"][5][:, 0].astype(np.float64)
+    assert abs(host(flat[off + 64:off + 65])[0] - ref_t1) <= 2e-3 * abs(ref_t1) + 1e-3
+
+
+@pytest.mark.parametrize("name", ["tiny", "base"])
+def test_config_end_to_end(name):
+    """Full Tiny / Base workloads: populate parity, then every decode step
+    kernel-isolated and end to end against the oracle from E."""
+    w = W.WORKLOADS[name]
+    c, d, h = _populate(w, "f32")
+    Kr, Vr = O.populate(h["E"], h["WK"], h["WV"], h["bV"], w.H)
+    assert O.rel_frobenius(host(c.Kc), Kr) <= POPULATE_REL_FROB
+    assert O.rel_frobenius(host(c.Vc), Vr) <= POPULATE_REL_FROB
+    Kg, Vg = host(c.Kc), host(c.Vc)
+    worst_iso = worst_e2e = 0.0
+    for s in range(w.steps):
+        Q = W.make_Q(w, s)
+        out = host(c.decode(dev(Q), d["key_len"]))
+        worst_iso = max(worst_iso, np.abs(out - O.decode(Q, Kg, Vg, h["key_len"])).max())
+        if s < 4:
+            worst_e2e = max(worst_e2e, np.abs(out - O.decode(Q, Kr, Vr, h["key_len"])).max())
+    print(f"{name}: decode max-abs kernel-isolated {worst_iso:.2e}, end-to-end {worst_e2e:.2e}")
+    assert worst_iso <= DECODE_F32_MAX_ABS
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+def test_batched_base(cache_dtype):
+    """Batched Whisper-Base (16 memories, ragged key_len): populate parity on two
+    slots, every row of four decode steps kernel-isolated."""
+    w = W.WORKLOADS["batched_base"]
+    c, d, h = _populate(w, cache_dtype)
+    for b in (0, 11):
+        Kr, Vr = O.populate(h["E"][b:b + 1], h["WK"], h["WV"], h["bV"], w.H)
+        assert O.rel_frobenius(host(c.Kc[b:b + 1]), Kr) <= POPULATE_REL_FROB
+        assert O.rel_frobenius(host(c.Vc[b:b + 1]), Vr) <= POPULATE_REL_FROB
+    Kg, Vg = host(c.Kc), host(c.Vc)
+    for s in (0, 1, 64, 127):
+        Q = W.make_Q(w, s)
+        out = host(c.decode(dev(Q), d["key_len"]))
+        assert np.abs(out - O.decode(Q, Kg, Vg, h["key_len"])).max() <= DECODE_TOL[cache_dtype]
+
+
+def test_large_sampled_heads():
+    """Whisper-large dims, bf16 inputs and cache, 8 memories: sampled (slot,
+    layer, head) K/V blocks against the oracle, sampled decode rows both
+    kernel-isolated and end to end."""
+    w = W.WORKLOADS["large"]
+    c, d, h = _populate(w, "bf16")
+    rng = np.random.default_rng(77)
+    heads = [(int(rng.integers(w.B)), int(rng.integers(w.L)), int(rng.integers(w.H))) for _ in range(10)]
+    heads += [(0, 0, 0), (w.B - 1, w.L - 1, w.H - 1)]
+    Q = W.make_Q(w, 0)
+    out = host(c.decode(dev(Q), d["key_len"]))
+    for (b, l, hh) in heads:
+        Kr, Vr = O.populate_head(h["E"][b], h["WK"][l], h["WV"][l], h["bV"][l], hh)
+        Kg, Vg = host(c.Kc[b, l, hh]), host(c.Vc[b, l, hh])
+        assert O.rel_frobenius(Kg, Kr) <= POPULATE_REL_FROB
+        assert O.rel_frobenius(Vg, Vr) <= POPULATE_REL_FROB
+        iso = O.attend_row(Q[b, l, hh], Kg, Vg, w.T, w.scale)
+        e2e = O.attend_row(Q[b, l, hh], Kr, Vr, w.T, w.scale)
+        assert np.abs(out[b, l, hh] - iso).max() <= DECODE_BF16_MAX_ABS
+        assert np.abs(out[b, l, hh] - e2e).max() <= DECODE_BF16_MAX_ABS
