@@ -92,6 +92,18 @@ cudaError_t current_device_info(DeviceInfo* info, std::string* msg) {
   return cudaSuccess;
 }
 
+void set_last_error(const std::string& msg) { g_last_msg = msg; }
+
+bool cache_geometry(const cxa_cache* c, int* B, int* T, int* L, int* H, int* dh) {
+  if (c == nullptr) return false;
+  *B = c->B;
+  *T = c->T;
+  *L = c->L;
+  *H = c->H;
+  *dh = c->dh;
+  return true;
+}
+
 }  // namespace cxa
 
 extern "C" {

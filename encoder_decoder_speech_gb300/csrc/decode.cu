@@ -234,6 +234,8 @@ size_t decode_workspace_bytes(int B, int T, int L, int H) {
   return counters_bytes(B, L, H) + static_cast<size_t>(B) * L * H * nchunk * kPartFloats * sizeof(float);
 }
 
+size_t decode_counter_bytes(int B, int L, int H) { return counters_bytes(B, L, H); }
+
 cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStream_t stream,
                           std::string* msg) {
   (void)msg;

@@ -6,6 +6,8 @@
 
 #include <cuda_runtime.h>
 
+struct cxa_cache;   // the C ABI's opaque descriptor (cxa_api.cu)
+
 namespace cxa {
 
 // Everything a populate launch needs; pointers are device pointers already
@@ -57,6 +59,16 @@ cudaError_t launch_populate(const PopulateLaunch& a, const DeviceInfo& dev, cuda
                             std::string* msg);
 cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStream_t stream,
                           std::string* msg);
+
+// Bytes at the start of a decode workspace that hold the per-row arrival
+// counters (the part that must be zero before a decode kernel starts).
+size_t decode_counter_bytes(int B, int L, int H);
+
+// Geometry of a cache descriptor (false for a NULL descriptor).
+bool cache_geometry(const cxa_cache* c, int* B, int* T, int* L, int* H, int* dh);
+
+// Records the calling thread's last failure text (cxa_last_error_message).
+void set_last_error(const std::string& msg);
 
 // Counts every kernel launch the library makes.
 void count_launches(unsigned long long n);

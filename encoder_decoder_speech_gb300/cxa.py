@@ -37,7 +37,12 @@ SIGNATURES = {
     "cxa_last_error_message": (ctypes.c_char_p, []),
     "cxa_launch_count": (ctypes.c_ulonglong, []),
     "cxa_device_status": (ctypes.c_int, [ctypes.c_int]),
+    "cxa_decode_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_float, ctypes.c_void_p]),
 }
+
+# bytes of the fixed device scratch behind cxa_decode_noalloc (CXA_NOALLOC_SCRATCH_BYTES)
+CXA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _lib = None
 
@@ -117,6 +122,12 @@ def cxa_populate(handle, b0, nb, E, WK, WV, bV, T, d, L, H, in_dtype, workspace,
 def cxa_decode(handle, Q, key_len, out, scale, workspace, workspace_bytes, stream=None) -> int:
     return load().cxa_decode(handle, _ptr(Q), _ptr(key_len), _ptr(out), float(scale), _ptr(workspace),
                              workspace_bytes, _stream(stream))
+
+
+def cxa_decode_noalloc(handle, Q, key_len, out, scale, stream=None) -> int:
+    """cxa_decode with its scratch in libcxa's fixed device array: for callers
+    that cannot allocate device memory. Calls must be ordered on one stream."""
+    return load().cxa_decode_noalloc(handle, _ptr(Q), _ptr(key_len), _ptr(out), float(scale), _stream(stream))
 
 
 def cxa_invalidate(handle, b=-1) -> int:

@@ -176,6 +176,37 @@ CXA_API unsigned long long cxa_launch_count(void);
  */
 CXA_API int cxa_device_status(int clear);
 
+/*
+ * Allocation-free decode (no counterpart in the source pages: an addition of
+ * this library for callers that cannot allocate device memory).
+ *
+ * Some callers cannot call cudaMalloc or any allocating routine: a host
+ * framework that has handed all device memory to its own pool allocator, or a
+ * serving loop that must not take the device-wide synchronisation and latency
+ * a fresh allocation can bring. They still own Q, key_len, out and the cache,
+ * but have nowhere to put the decode scratch. cxa_decode_noalloc runs the same
+ * kernel as cxa_decode with its scratch (split-T partials and per-row arrival
+ * counters) in a fixed array that lives in libcxa's device module: every GPU
+ * that loads the library holds CXA_NOALLOC_SCRATCH_BYTES of it until the
+ * process exits.
+ *
+ * Arguments and results are those of cxa_decode without the workspace. The
+ * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine. Geometry whose scratch, cxa_decode_workspace_bytes(B, T, L, H, dh),
+ * exceeds CXA_NOALLOC_SCRATCH_BYTES is rejected with CXA_EINVAL. Each call
+ * clears the arrival counters (cudaMemsetAsync on `stream`) before its kernel.
+ * All calls share the one array and it keeps the last call's contents, so
+ * calls that may overlap on the GPU (different streams without ordering, or
+ * several host threads) race and produce wrong results: order them on one
+ * stream. The first call on a device looks up the array's device address with
+ * that device current (cudaGetSymbolAddress); make that first call before any
+ * stream capture begins.
+ */
+#define CXA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+CXA_API int cxa_decode_noalloc(const cxa_cache* c, const float* Q, const int* key_len, float* out,
+                               float scale, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
