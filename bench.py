@@ -46,6 +46,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["cxa", "reference"], default="cxa")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     p.add_argument("--no-variants", action="store_true", help="skip the bf16-cache variant")
+    p.add_argument("--profile", choices=["decode", "decode_bf16", "populate"], default=None,
+                   help="run a few launches of one kernel on the workload's inputs (for ncu), print nothing else")
     p.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--budget-s", type=float, default=12.0, help=argparse.SUPPRESS)
     p.add_argument("--max-slots", type=int, default=16, help=argparse.SUPPRESS)
@@ -66,6 +68,14 @@ def rank_slots(rank: int, B: int):
     """Seed indices of the encoder memories a rank owns: each rank runs its own
     B windows (weak scaling), distinct across ranks."""
     return list(range(rank * B, rank * B + B))
+
+
+def max_over_ranks(dist, values, device):
+    """Element-wise max of per-rank timings (the slowest rank sets the job time)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
 
 
 def load_peaks():
@@ -309,9 +319,7 @@ def measure(torch, cxa, W, w, dev_inputs, cache_dtype, K, Wu, rank, world, dist,
     pop_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
     dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
     if dist is not None:
-        t = torch.tensor([total_ms, pop_ms, dec_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, pop_ms, dec_ms = (float(x) for x in t.tolist())
+        total_ms, pop_ms, dec_ms = max_over_ranks(dist, [total_ms, pop_ms, dec_ms], "cuda")
     assert cxa.cxa_device_status(1) == cxa.CXA_OK, "a kernel reported a bounded-wait timeout"
     res = {"total_ms": total_ms, "populate_ms": pop_ms, "decode_window_ms": dec_ms,
            "decode_launch_us": 1000.0 * dec_ms / w.steps, "launches": launches, "clocks": clocks}
@@ -362,13 +370,52 @@ def measure_e2e(torch, cxa, w, host_inputs, dev_static, K, Wu, dist):
     torch.cuda.synchronize()
     ms = a.elapsed_time(b)
     if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(dist, [ms], "cuda")[0]
     h2d = E_pin.numel() * 4 + kl_pin.numel() * 4 + w.steps * Q_d.numel() * 4
     d2h = w.steps * out_d.numel() * 4
     cache.close()
     return ms, h2d, d2h
+
+
+def device_inputs(torch, W, w, rank):
+    """Seeded inputs of the workload for this rank, uploaded to the current GPU."""
+    import numpy as np
+    kl = W.make_key_len(w)
+    E = np.stack([W.make_E(W.replace(w, ragged=False), s) for s in rank_slots(rank, w.B)])
+    for i in range(w.B):                      # pad rows of each memory are zero
+        E[i, int(kl[i]):] = 0.0
+    WK, WV, bV = W.make_weights(w)
+    Q = np.stack([W.make_Q(w, s) for s in range(w.steps)])
+
+    def d(x, dt=torch.float32):
+        return torch.from_numpy(np.ascontiguousarray(x)).to("cuda", dt)
+
+    return (d(E), d(WK), d(WV), d(bV), d(kl, torch.int32), d(Q), kl), (E, kl.astype(np.int32), Q)
+
+
+def run_profile(args):
+    """A handful of launches of one kernel on the bench workload's inputs, for
+    Nsight Compute: one populate (weight repack + GEMM), then two more populate
+    calls or three decode steps."""
+    import torch
+    from encoder_decoder_speech_gb300 import _build, cxa
+    from encoder_decoder_speech_gb300 import workloads as W
+    _build.build_library()
+    cxa.load()
+    torch.cuda.set_device(0)
+    w = W.WORKLOADS[WORKLOAD]
+    (E, WK, WV, bV, kl, Q, _), _ = device_inputs(torch, W, w, 0)
+    cache = cxa.CrossAttentionCache(w.B, w.T, w.L, w.H, w.dh, "bf16" if args.profile == "decode_bf16" else "f32")
+    cache.populate(E, WK, WV, bV)
+    if args.profile == "populate":
+        for _ in range(2):
+            cache.populate(E, WK, WV, bV)
+    else:
+        for s in range(3):
+            cache.decode(Q[s], kl)
+    torch.cuda.synchronize()
+    assert cxa.cxa_device_status(1) == cxa.CXA_OK
+    return 0
 
 
 def run_cxa(args):
@@ -378,7 +425,6 @@ def run_cxa(args):
         # the oracle leg runs first, in its own process, before any GPU work
         cpu_base = cpu_baseline_obj(run_oracle_subprocess(args.budget_s, args.max_slots))
 
-    import numpy as np
     import torch
     from encoder_decoder_speech_gb300 import _build, cxa
     from encoder_decoder_speech_gb300 import workloads as W
@@ -392,18 +438,8 @@ def run_cxa(args):
         tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
         dist = tdist
     w = W.WORKLOADS[WORKLOAD]
-    kl = W.make_key_len(w)
-    slots = rank_slots(rank, w.B)
-    E = np.stack([W.make_E(W.replace(w, ragged=False), s) for s in slots])
-    for i in range(w.B):                      # pad rows of each memory are zero
-        E[i, int(kl[i]):] = 0.0
-    WK, WV, bV = W.make_weights(w)
-    Q = np.stack([W.make_Q(w, s) for s in range(w.steps)])
-
-    def d(x, dt=torch.float32):
-        return torch.from_numpy(np.ascontiguousarray(x)).to("cuda", dt)
-
-    dev_inputs = (d(E), d(WK), d(WV), d(bV), d(kl, torch.int32), d(Q), kl)
+    dev_inputs, host_inputs = device_inputs(torch, W, w, rank)
+    kl = host_inputs[1]
     K, Wu = args.steps, args.warmup
     main = measure(torch, cxa, W, w, dev_inputs, "f32", K, Wu, rank, world, dist, timed_clocks=(rank == 0))
     variants = {}
@@ -415,7 +451,7 @@ def run_cxa(args):
             "ms_per_step": v["total_ms"] / K,
             "decode_GBps": vb / (v["decode_launch_us"] * 1e-6) / 1e9,
             "decode_launch_us": v["decode_launch_us"], "populate_ms": v["populate_ms"]}
-    e2e_ms, h2d, d2h = measure_e2e(torch, cxa, w, (E, kl.astype(np.int32), Q), dev_inputs[1:4], K, Wu, dist)
+    e2e_ms, h2d, d2h = measure_e2e(torch, cxa, w, host_inputs, dev_inputs[1:4], K, Wu, dist)
 
     if rank != 0:
         if dist is not None:
@@ -468,6 +504,8 @@ def main(argv=None):
     if args.oracle_sample:
         print(json.dumps(oracle_sample(args.budget_s, args.max_slots, args.warmup)))
         return 0
+    if args.profile:
+        return run_profile(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_cxa(args)
