@@ -473,7 +473,7 @@ def run_cxa(args):
         "ms_per_step": main["total_ms"] / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded numpy, Whisper-Base shapes)",
         "config": dict(workload_config(w, "f32"), parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
-        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel<f32> (+ fused combine)",
+        "roofline": {"bound": "hbm", "kernel": "decode_stream_kernel<f32> (persistent, last-arriver merge)",
                      "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "algorithmic_bytes_per_launch": dbytes, "launch_us": main["decode_launch_us"],

@@ -4,25 +4,37 @@
 // expand one cross-attention operation": one query token, all key tokens,
 // head_dim 64, scale 0.125).
 //
-// Split-T flash decoding with the lazy (online) softmax of SplitKV ("Caso de
-// estudio: WhisperKit", §3): the keys of a row are cut into chunks of kChunk;
-// each chunk is one CTA that
-//   1. bulk-copies its K rows and V rows (contiguous in the head-major cache)
-//      into shared memory with two cp.async.bulk copies,
-//   2. computes the chunk's scores in fp32 (16 or 8 lanes per key row, warp
-//      shuffle reduction), its max m and sum s of 2^(score - m),
-//   3. accumulates sum_t 2^(score_t - m) V_t,
-//   4. stores the partial (m, s, acc[64]) and counts itself done on the row's
-//      arrival counter; the CTA that arrives last merges the row's partials
-//      (M = max m_i, S = sum s_i 2^(m_i - M), out = sum acc_i 2^(m_i - M) / S),
-//      writes out and resets the counter. No CTA ever waits for another.
-// Scores are kept in base 2: q is pre-multiplied by scale * log2(e).
-// Keys t >= key_len[b] are never copied and never enter the arithmetic; a row
-// with no valid key gets out = 0.
+// Split-T decoding with the lazy (online) softmax of SplitKV ("Caso de estudio:
+// WhisperKit", §3), laid out for an HBM-bound GPU:
+//
+//  * Work = every valid key of every row, cut into chunks of kChunkKeys keys
+//    (16 KB of K and 16 KB of V). The chunks of all rows are numbered densely,
+//    slot-major then (layer, head) then key order, and the persistent grid
+//    gives each CTA one contiguous, equal-sized range of chunk numbers, so every
+//    CTA streams the same number of bytes whatever the key lengths are.
+//  * In each CTA a producer warp keeps a kStages-deep ring of shared-memory
+//    stages full with three cp.async.bulk copies per chunk (K rows, V rows and
+//    the row's query, all contiguous in the head-major cache) completing on a
+//    "full" mbarrier; four consumer warps read a stage and release it on its
+//    "empty" mbarrier.
+//  * Each consumer lane group (16 lanes per fp32 key row, 8 per bf16 row) runs
+//    its own online softmax (running max m, sum s, accumulators) over the keys
+//    it is given, in fp32 and base 2 (q is pre-multiplied by scale * log2(e)).
+//  * When a row's run of chunks in this CTA ends, the groups' states are merged
+//    (warp shuffles, then shared memory). A CTA that owned the whole row writes
+//    out directly; otherwise it stores its partial (m, s, acc[64]) and counts
+//    itself on the row's arrival counter, and the CTA that arrives last merges
+//    the row's partials (M = max m_i, S = sum s_i 2^(m_i - M),
+//    out = sum acc_i 2^(m_i - M) / S) and resets the counter. No CTA ever waits
+//    for another CTA.
+//  * Keys t >= key_len[b] are never copied and never enter the arithmetic; a
+//    row with no valid key gets out = 0 (the clamped softmax denominator,
+//    WhisperKit case study §2).
 #include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 #include <string>
 
 #include "internal.h"
@@ -31,18 +43,40 @@
 namespace cxa {
 namespace {
 
-constexpr int kChunk = 64;          // keys per CTA
-constexpr int kThreads = 128;       // 4 warps x 16 keys
-constexpr int kPartFloats = 68;     // m, s, 2 pad, acc[64]
 constexpr int kDh = 64;
+constexpr int kPartFloats = 68;        // m, s, 2 pad, acc[64]
+constexpr int kPartChunk = 64;         // partial-slot granularity of the workspace layout
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 3;
+constexpr int kQBytes = kDh * 4;
 
 template <bool kBF16>
-struct RowTraits {
+struct Traits {
   static constexpr int kElemBytes = kBF16 ? 2 : 4;
-  static constexpr int kRowBytes = kDh * kElemBytes;     // 256 / 128
-  static constexpr int kLanesPerRow = kRowBytes / 16;    // 16 / 8
-  static constexpr int kRowsPerPass = 32 / kLanesPerRow; // 2 / 4
-  static constexpr int kElemsPerLane = 16 / kElemBytes;  // 4 / 8
+  static constexpr int kRowBytes = kDh * kElemBytes;        // 256 / 128
+  static constexpr int kLanesPerRow = kRowBytes / 16;       // 16 / 8 lanes share a key row
+  static constexpr int kRowsPerPass = 32 / kLanesPerRow;    // 2 / 4 keys per warp pass
+  static constexpr int kElemsPerLane = 16 / kElemBytes;     // 4 / 8 channels per lane
+  static constexpr int kChunkKeys = kBF16 ? 128 : 64;       // 16 KB of K per chunk
+  static constexpr int kKVBytes = kChunkKeys * kRowBytes;
+  static constexpr int kStageBytes = 2 * kKVBytes + kQBytes;
+  static constexpr int kKeysPerWarp = kChunkKeys / kConsumerWarps;
+  static constexpr int kPasses = kKeysPerWarp / kRowsPerPass;   // 8 / 8
+};
+
+struct DecodeParams {
+  const float* Q;
+  const uint8_t* Kc;
+  const uint8_t* Vc;
+  const int* key_len;
+  float* out;
+  float* part;
+  unsigned int* counters;
+  unsigned int* status;
+  int B, T, LH;
+  int part_stride;     // partial slots per row (ceil(T / 64))
+  float qscale;        // scale * log2(e)
 };
 
 // 16 bytes of a cache row -> fp32 values
@@ -63,163 +97,321 @@ __device__ __forceinline__ void unpack16(const uint4 u, float* f) {
   }
 }
 
+// Weight of a softmax state with running max m against a merged max M (0 for an
+// empty state, m == -inf).
+__device__ __forceinline__ float rescale(float m, float M) { return m == -INFINITY ? 0.f : exp2f(m - M); }
+
+__device__ __forceinline__ void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Position in the dense chunk numbering: slot b, row-in-slot lh, chunk c.
+struct Cursor {
+  int b, lh, c;
+};
+
+// The chunk numbering lives in shared memory: s_nch[b] = chunks per row of
+// slot b, s_first[b] = number of the first chunk of slot b (s_first[B] = total).
+__device__ __forceinline__ Cursor locate(long long g, const long long* s_first, const int* s_nch, int B, int LH) {
+  int lo = 0, hi = B - 1;   // last b with s_first[b] <= g
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_first[mid] <= g) lo = mid; else hi = mid - 1;
+  }
+  const long long local = g - s_first[lo];
+  Cursor cur;
+  cur.b = lo;
+  cur.lh = static_cast<int>(local / s_nch[lo]);
+  cur.c = static_cast<int>(local - static_cast<long long>(cur.lh) * s_nch[lo]);
+  return cur;
+}
+
+__device__ __forceinline__ void advance(Cursor& cur, const int* s_nch, int B, int LH) {
+  if (++cur.c < s_nch[cur.b]) return;
+  cur.c = 0;
+  if (++cur.lh < LH) return;
+  cur.lh = 0;
+  do {
+    ++cur.b;
+  } while (cur.b < B && s_nch[cur.b] == 0);
+}
+
+// The CTA that owns dense chunk g when total chunks are split into `ranges`
+// equal ranges [j*total/ranges, (j+1)*total/ranges).
+__device__ __forceinline__ long long owner_of(long long g, long long total, long long ranges) {
+  return ((g + 1) * ranges + total - 1) / total - 1;
+}
+
 template <bool kBF16>
 __global__ void __launch_bounds__(kThreads)
-    decode_split_kernel(const float* __restrict__ Q, const uint8_t* __restrict__ Kc,
-                        const uint8_t* __restrict__ Vc, const int* __restrict__ key_len,
-                        float* __restrict__ out, float* __restrict__ part,
-                        unsigned int* __restrict__ counters, int T, int LH, int nchunk_max,
-                        float qscale, unsigned int* status) {
-  using R = RowTraits<kBF16>;
-  constexpr int kRowsPerWarp = kChunk / (kThreads / 32);   // 16
-  constexpr int kPasses = kRowsPerWarp / R::kRowsPerPass;  // 8 / 4
+    decode_stream_kernel(const DecodeParams p) {
+  using R = Traits<kBF16>;
+  constexpr int LPR = R::kLanesPerRow;
+  constexpr int EPL = R::kElemsPerLane;
 
-  __shared__ __align__(128) uint8_t sK[kChunk * R::kRowBytes];
-  __shared__ __align__(128) uint8_t sV[kChunk * R::kRowBytes];
-  __shared__ float s_score[kChunk];
-  __shared__ float s_red[kThreads / 32][kDh];
-  __shared__ __align__(8) uint64_t s_bar[2];
-  __shared__ int s_last;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* stages = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * R::kStageBytes);   // full[S], empty[S]
+  long long* s_first = reinterpret_cast<long long*>(bars + 2 * kStages);
+  int* s_nch = reinterpret_cast<int*>(s_first + p.B + 1);
+  float* s_red = reinterpret_cast<float*>(s_nch + p.B + (p.B & 1));   // [4][64] acc, then m[4], s[4]
+  float* s_redm = s_red + kConsumerWarps * kDh;
+  float* s_reds = s_redm + kConsumerWarps;
+  volatile int* s_flags = reinterpret_cast<volatile int*>(s_reds + kConsumerWarps);   // [0] abort, [1] last
 
-  const int chunk = blockIdx.x;
-  const int lh = blockIdx.y;
-  const int b = blockIdx.z;
-  const int row = b * LH + lh;
-  const int kl = min(max(__ldg(key_len + b), 0), T);
-  const int t0 = chunk * kChunk;
-  if (kl == 0) {
-    if (chunk == 0 && threadIdx.x < kDh) out[static_cast<size_t>(row) * kDh + threadIdx.x] = 0.f;
-    return;
-  }
-  if (t0 >= kl) return;
-  const int n = min(kChunk, kl - t0);
-  const int nch = (kl + kChunk - 1) / kChunk;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t barK = smem_u32(&s_bar[0]);
-  const uint32_t barV = smem_u32(&s_bar[1]);
+  const int LH = p.LH;
 
+  // ---- chunk numbering (every CTA computes the same prefix from key_len)
+  if (warp == 0) {
+    long long run = 0;
+    for (int base = 0; base < p.B; base += 32) {
+      const int b = base + lane;
+      int nch = 0;
+      if (b < p.B) {
+        const int kl = min(max(__ldg(p.key_len + b), 0), p.T);
+        nch = (kl + R::kChunkKeys - 1) / R::kChunkKeys;
+        s_nch[b] = nch;
+      }
+      long long v = static_cast<long long>(nch) * LH;   // inclusive warp scan
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const long long o = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += o;
+      }
+      if (b < p.B) s_first[b] = run + v - static_cast<long long>(nch) * LH;
+      run += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) {
+      s_first[p.B] = run;
+      s_flags[0] = 0;
+      s_flags[1] = 0;
+    }
+  }
   if (threadIdx.x == 0) {
-    mbar_init(barK, 1);
-    mbar_init(barV, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bars[s]), 1);
+      mbar_init(smem_u32(&bars[kStages + s]), kConsumerWarps);
+    }
     fence_mbar_init();
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    const size_t off = (static_cast<size_t>(row) * T + t0) * R::kRowBytes;
-    const uint32_t bytes = static_cast<uint32_t>(n) * R::kRowBytes;
-    const uint64_t pol = policy_evict_first();
-    mbar_arrive_expect_tx(barK, bytes);
-    bulk_g2s_hint(smem_u32(sK), Kc + off, bytes, barK, pol);
-    mbar_arrive_expect_tx(barV, bytes);
-    bulk_g2s_hint(smem_u32(sV), Vc + off, bytes, barV, pol);
-  }
 
-  // this lane's slice of the query, pre-scaled into base-2 logits
-  const int sub = lane % R::kLanesPerRow;
-  const int rsub = lane / R::kLanesPerRow;
-  float q[R::kElemsPerLane];
-  {
-    const float4* q4 = reinterpret_cast<const float4*>(Q + static_cast<size_t>(row) * kDh + sub * R::kElemsPerLane);
+  const long long total = s_first[p.B];
+  // rows of slots without any valid key: out = 0
+  for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
+       i < static_cast<long long>(p.B) * LH * (kDh / 4); i += static_cast<long long>(gridDim.x) * kThreads) {
+    const int b = static_cast<int>(i / (static_cast<long long>(LH) * (kDh / 4)));
+    if (s_nch[b] == 0) reinterpret_cast<float4*>(p.out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (total == 0) return;
+  const long long ranges = total < gridDim.x ? total : static_cast<long long>(gridDim.x);
+  if (blockIdx.x >= ranges) return;
+  const long long g0 = blockIdx.x * total / ranges;
+  const long long g1 = (blockIdx.x + 1) * total / ranges;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      Cursor cur = locate(g0, s_first, s_nch, p.B, LH);
+      uint32_t armed = 0, armed_parity = 0;
+      bool ok = true;
+      for (long long g = g0, i = 0; g < g1; ++g, ++i) {
+        const int s = static_cast<int>(i % kStages);
+        const uint32_t parity = static_cast<uint32_t>((i / kStages) & 1);
+        if (!mbar_wait(smem_u32(&bars[kStages + s]), parity ^ 1u, s_flags)) {
+          ok = false;
+          break;
+        }
+        const int kl = min(max(__ldg(p.key_len + cur.b), 0), p.T);
+        const int t0 = cur.c * R::kChunkKeys;
+        const int n = min(R::kChunkKeys, kl - t0);
+        const long long row = static_cast<long long>(cur.b) * LH + cur.lh;
+        const size_t off = (static_cast<size_t>(row) * p.T + t0) * R::kRowBytes;
+        const uint32_t kv_bytes = static_cast<uint32_t>(n) * R::kRowBytes;
+        const uint32_t full = smem_u32(&bars[s]);
+        const uint32_t dst = smem_u32(stages + s * R::kStageBytes);
+        mbar_arrive_expect_tx(full, 2 * kv_bytes + kQBytes);
+        bulk_g2s_hint(dst, p.Kc + off, kv_bytes, full, pol);
+        bulk_g2s_hint(dst + R::kKVBytes, p.Vc + off, kv_bytes, full, pol);
+        bulk_g2s(dst + 2 * R::kKVBytes, p.Q + row * kDh, kQBytes, full);
+        armed |= 1u << s;
+        armed_parity = (armed_parity & ~(1u << s)) | (parity << s);
+        advance(cur, s_nch, p.B, LH);
+      }
+      if (!ok) {
+        s_flags[0] = 1;
+        atomicOr(p.status, 1u);
+        for (int s = 0; s < kStages; ++s)   // let issued copies land before exiting
+          if (armed & (1u << s)) mbar_wait(smem_u32(&bars[s]), (armed_parity >> s) & 1u);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int sub = lane % LPR;          // 16-byte slice of a key row this lane reads
+    const int grp = lane / LPR;          // lane group = independent softmax stream
+    const int tid = threadIdx.x;         // 0..127
+    Cursor cur = locate(g0, s_first, s_nch, p.B, LH);
+    int seg_c0 = cur.c;                  // first chunk of the current row in this CTA
+    float m = -INFINITY, ssum = 0.f;
+    float acc[EPL];
 #pragma unroll
-    for (int i = 0; i < R::kElemsPerLane / 4; ++i) {
-      const float4 v = __ldg(q4 + i);
-      q[4 * i + 0] = v.x * qscale;
-      q[4 * i + 1] = v.y * qscale;
-      q[4 * i + 2] = v.z * qscale;
-      q[4 * i + 3] = v.w * qscale;
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    bool ok = true;
+
+    for (long long g = g0, i = 0; g < g1; ++g, ++i) {
+      const int s = static_cast<int>(i % kStages);
+      const uint32_t parity = static_cast<uint32_t>((i / kStages) & 1);
+      if (ok && !mbar_wait(smem_u32(&bars[s]), parity, s_flags)) {
+        ok = false;
+        s_flags[0] = 1;
+        atomicOr(p.status, 1u);
+      }
+      const int kl = min(max(__ldg(p.key_len + cur.b), 0), p.T);
+      const int nch = s_nch[cur.b];
+      const int n = min(R::kChunkKeys, kl - cur.c * R::kChunkKeys);
+      if (ok) {
+        const uint8_t* sK = stages + s * R::kStageBytes;
+        const uint8_t* sV = sK + R::kKVBytes;
+        const float* sQ = reinterpret_cast<const float*>(sK + 2 * R::kKVBytes);
+        float q[EPL];
+#pragma unroll
+        for (int e4 = 0; e4 < EPL / 4; ++e4) {
+          const float4 v = *reinterpret_cast<const float4*>(sQ + sub * EPL + 4 * e4);
+          q[4 * e4 + 0] = v.x * p.qscale;
+          q[4 * e4 + 1] = v.y * p.qscale;
+          q[4 * e4 + 2] = v.z * p.qscale;
+          q[4 * e4 + 3] = v.w * p.qscale;
+        }
+        float sc[R::kPasses];
+        float mloc = -INFINITY;
+#pragma unroll
+        for (int it = 0; it < R::kPasses; ++it) {
+          const int r = warp * R::kKeysPerWarp + it * R::kRowsPerPass + grp;
+          float f[EPL];
+          unpack16<kBF16>(*reinterpret_cast<const uint4*>(sK + r * R::kRowBytes + sub * 16), f);
+          float dot = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) dot = fmaf(q[e], f[e], dot);
+#pragma unroll
+          for (int off = LPR / 2; off >= 1; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+          sc[it] = r < n ? dot : -INFINITY;
+          mloc = fmaxf(mloc, sc[it]);
+        }
+        const float mnew = fmaxf(m, mloc);
+        if (mnew != -INFINITY) {
+          const float corr = rescale(m, mnew);
+          ssum *= corr;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) acc[e] *= corr;
+#pragma unroll
+          for (int it = 0; it < R::kPasses; ++it) {
+            const int r = warp * R::kKeysPerWarp + it * R::kRowsPerPass + grp;
+            if (r < n) {
+              const float pw = exp2f(sc[it] - mnew);
+              float f[EPL];
+              unpack16<kBF16>(*reinterpret_cast<const uint4*>(sV + r * R::kRowBytes + sub * 16), f);
+              ssum += pw;
+#pragma unroll
+              for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pw, f[e], acc[e]);
+            }
+          }
+          m = mnew;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
+
+      const bool row_ends = (cur.c == nch - 1) || (g + 1 == g1);
+      if (row_ends) {
+        // ---- merge the lane groups of this warp, then the four warps
+#pragma unroll
+        for (int off = LPR; off < 32; off <<= 1) {
+          const float mo = __shfl_xor_sync(0xffffffffu, m, off);
+          const float so = __shfl_xor_sync(0xffffffffu, ssum, off);
+          const float M = fmaxf(m, mo);
+          const float f0 = rescale(m, M), f1 = rescale(mo, M);
+          ssum = ssum * f0 + so * f1;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) {
+            const float ao = __shfl_xor_sync(0xffffffffu, acc[e], off);
+            acc[e] = acc[e] * f0 + ao * f1;
+          }
+          m = M;
+        }
+        if (lane < LPR) {
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) s_red[warp * kDh + sub * EPL + e] = acc[e];
+        }
+        if (lane == 0) {
+          s_redm[warp] = m;
+          s_reds[warp] = ssum;
+        }
+        named_barrier(1, kConsumerWarps * 32);
+        const long long row = static_cast<long long>(cur.b) * LH + cur.lh;
+        const bool whole_row = seg_c0 == 0 && cur.c == nch - 1;
+        if (tid < kDh) {
+          float M = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s_redm[w]);
+          float S = 0.f, A = 0.f;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float f = rescale(s_redm[w], M);
+            S = fmaf(s_reds[w], f, S);
+            A = fmaf(s_red[w * kDh + tid], f, A);
+          }
+          if (whole_row) {
+            if (ok) p.out[row * kDh + tid] = S > 0.f ? A / S : 0.f;
+          } else {
+            const long long grow = s_first[cur.b] + static_cast<long long>(cur.lh) * nch;   // chunk 0 of row
+            const long long first_owner = owner_of(grow, total, ranges);
+            const int nseg = static_cast<int>(owner_of(grow + nch - 1, total, ranges) - first_owner + 1);
+            const int seg = static_cast<int>(blockIdx.x - first_owner);
+            float* P = p.part + (row * p.part_stride + seg) * kPartFloats;
+            P[4 + tid] = ok ? A : 0.f;
+            if (tid == 0) {
+              P[0] = ok ? M : -INFINITY;
+              P[1] = ok ? S : 0.f;
+            }
+            named_barrier(2, kDh);
+            if (tid == 0) {
+              __threadfence();
+              const unsigned int prev = atomicAdd(p.counters + row, 1u);
+              s_flags[1] = (prev == static_cast<unsigned int>(nseg - 1)) ? 1 : 0;
+            }
+            named_barrier(2, kDh);
+            if (s_flags[1]) {
+              __threadfence();
+              const float* P0 = p.part + row * p.part_stride * kPartFloats;
+              float MM = -INFINITY;
+              for (int k = 0; k < nseg; ++k) MM = fmaxf(MM, __ldcg(P0 + k * kPartFloats));
+              float SS = 0.f, AA = 0.f;
+              for (int k = 0; k < nseg; ++k) {
+                const float f = rescale(__ldcg(P0 + k * kPartFloats), MM);
+                SS = fmaf(f, __ldcg(P0 + k * kPartFloats + 1), SS);
+                AA = fmaf(f, __ldcg(P0 + k * kPartFloats + 4 + tid), AA);
+              }
+              p.out[row * kDh + tid] = SS > 0.f ? AA / SS : 0.f;
+              if (tid == 0) p.counters[row] = 0u;
+            }
+          }
+        }
+        named_barrier(1, kConsumerWarps * 32);
+        m = -INFINITY;
+        ssum = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+      }
+      const int prev_b = cur.b, prev_lh = cur.lh;
+      advance(cur, s_nch, p.B, LH);
+      if (cur.b != prev_b || cur.lh != prev_lh) seg_c0 = cur.c;
     }
   }
-
-  bool ok = mbar_wait(barK, 0);
-  // ---- scores
-#pragma unroll
-  for (int it = 0; it < kPasses; ++it) {
-    const int r = warp * kRowsPerWarp + it * R::kRowsPerPass + rsub;
-    float f[R::kElemsPerLane];
-    unpack16<kBF16>(*reinterpret_cast<const uint4*>(sK + r * R::kRowBytes + sub * 16), f);
-    float dot = 0.f;
-#pragma unroll
-    for (int e = 0; e < R::kElemsPerLane; ++e) dot = fmaf(q[e], f[e], dot);
-#pragma unroll
-    for (int off = R::kLanesPerRow / 2; off >= 1; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-    if (sub == 0) s_score[r] = (r < n && ok) ? dot : -INFINITY;
-  }
   __syncthreads();
-
-  // ---- chunk max and sum (every warp computes them from shared memory)
-  const float sa = s_score[lane];
-  const float sb = s_score[lane + 32];
-  float m = fmaxf(sa, sb);
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  float ssum = (lane < n ? exp2f(sa - m) : 0.f) + (lane + 32 < n ? exp2f(sb - m) : 0.f);
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, off);
-
-  // ---- weighted V rows
-  ok = mbar_wait(barV, 0) && ok;
-  float acc[R::kElemsPerLane];
-#pragma unroll
-  for (int e = 0; e < R::kElemsPerLane; ++e) acc[e] = 0.f;
-#pragma unroll
-  for (int it = 0; it < kPasses; ++it) {
-    const int r = warp * kRowsPerWarp + it * R::kRowsPerPass + rsub;
-    if (r < n && ok) {
-      const float pr = exp2f(s_score[r] - m);
-      float f[R::kElemsPerLane];
-      unpack16<kBF16>(*reinterpret_cast<const uint4*>(sV + r * R::kRowBytes + sub * 16), f);
-#pragma unroll
-      for (int e = 0; e < R::kElemsPerLane; ++e) acc[e] = fmaf(pr, f[e], acc[e]);
-    }
-  }
-#pragma unroll
-  for (int off = R::kLanesPerRow; off < 32; off <<= 1)
-#pragma unroll
-    for (int e = 0; e < R::kElemsPerLane; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
-  if (lane < R::kLanesPerRow) {
-#pragma unroll
-    for (int e = 0; e < R::kElemsPerLane; ++e) s_red[warp][sub * R::kElemsPerLane + e] = acc[e];
-  }
-  if (!ok && threadIdx.x == 0) atomicOr(status, 1u);
-  __syncthreads();
-
-  float* P = part + (static_cast<size_t>(row) * nchunk_max + chunk) * kPartFloats;
-  if (threadIdx.x < kDh) {
-    float a = 0.f;
-#pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) a += s_red[w][threadIdx.x];
-    P[4 + threadIdx.x] = a;
-    if (threadIdx.x == 0) {
-      P[0] = ok ? m : -INFINITY;
-      P[1] = ok ? ssum : 0.f;
-    }
-    __threadfence();
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned int prev = atomicAdd(counters + row, 1u);
-    s_last = (prev == static_cast<unsigned int>(nch - 1)) ? 1 : 0;
-  }
-  __syncthreads();
-  if (!s_last) return;
-
-  // ---- last CTA of this row: merge the partials
-  __threadfence();
-  if (threadIdx.x < kDh) {
-    const float* P0 = part + static_cast<size_t>(row) * nchunk_max * kPartFloats;
-    float M = -INFINITY;
-    for (int i = 0; i < nch; ++i) M = fmaxf(M, __ldcg(P0 + i * kPartFloats));
-    float S = 0.f, A = 0.f;
-    for (int i = 0; i < nch; ++i) {
-      const float mi = __ldcg(P0 + i * kPartFloats);
-      const float w = mi == -INFINITY ? 0.f : exp2f(mi - M);
-      S = fmaf(w, __ldcg(P0 + i * kPartFloats + 1), S);
-      A = fmaf(w, __ldcg(P0 + i * kPartFloats + 4 + threadIdx.x), A);
-    }
-    out[static_cast<size_t>(row) * kDh + threadIdx.x] = S > 0.f ? A / S : 0.f;
-  }
-  if (threadIdx.x == 0) counters[row] = 0u;
 }
 
 size_t counters_bytes(int B, int L, int H) {
@@ -227,11 +419,47 @@ size_t counters_bytes(int B, int L, int H) {
   return (n + 255) & ~static_cast<size_t>(255);
 }
 
+template <bool kBF16>
+size_t dynamic_smem_bytes(int B) {
+  using R = Traits<kBF16>;
+  size_t n = static_cast<size_t>(kStages) * R::kStageBytes;
+  n += 2 * kStages * sizeof(uint64_t);
+  n += static_cast<size_t>(B + 1) * sizeof(long long);
+  n += static_cast<size_t>(B + (B & 1)) * sizeof(int);
+  n += (kConsumerWarps * kDh + 2 * kConsumerWarps) * sizeof(float) + 4 * sizeof(int);
+  return n;
+}
+
+template <bool kBF16>
+cudaError_t launch(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t stream) {
+  static std::mutex mu;
+  static size_t attr_bytes[128] = {};
+  const size_t smem = dynamic_smem_bytes<kBF16>(prm.B);
+  cudaError_t e;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const int d = dev.device >= 0 && dev.device < 128 ? dev.device : 0;
+    if (attr_bytes[d] < smem) {
+      e = cudaFuncSetAttribute(decode_stream_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      attr_bytes[d] = smem;
+    }
+  }
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<kBF16>, kThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int grid = dev.num_sms * (per_sm < 2 ? per_sm : 2);
+  decode_stream_kernel<kBF16><<<grid, kThreads, smem, stream>>>(prm);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t decode_workspace_bytes(int B, int T, int L, int H) {
-  const size_t nchunk = static_cast<size_t>((T + kChunk - 1) / kChunk);
-  return counters_bytes(B, L, H) + static_cast<size_t>(B) * L * H * nchunk * kPartFloats * sizeof(float);
+  const size_t nslot = static_cast<size_t>((T + kPartChunk - 1) / kPartChunk);
+  return counters_bytes(B, L, H) + static_cast<size_t>(B) * L * H * nslot * kPartFloats * sizeof(float);
 }
 
 size_t decode_counter_bytes(int B, int L, int H) { return counters_bytes(B, L, H); }
@@ -239,21 +467,21 @@ size_t decode_counter_bytes(int B, int L, int H) { return counters_bytes(B, L, H
 cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStream_t stream,
                           std::string* msg) {
   (void)msg;
-  const int LH = a.L * a.H;
-  const int nchunk_max = (a.T + kChunk - 1) / kChunk;
-  unsigned int* counters = static_cast<unsigned int*>(a.workspace);
-  float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + counters_bytes(a.B, a.L, a.H));
-  const float qscale = a.scale * 1.4426950408889634f;   // scale * log2(e)
-  dim3 grid(nchunk_max, LH, a.B);
-  if (a.cache_bf16)
-    decode_split_kernel<true><<<grid, kThreads, 0, stream>>>(
-        a.Q, static_cast<const uint8_t*>(a.Kc), static_cast<const uint8_t*>(a.Vc), a.key_len, a.out, part,
-        counters, a.T, LH, nchunk_max, qscale, dev.status_word);
-  else
-    decode_split_kernel<false><<<grid, kThreads, 0, stream>>>(
-        a.Q, static_cast<const uint8_t*>(a.Kc), static_cast<const uint8_t*>(a.Vc), a.key_len, a.out, part,
-        counters, a.T, LH, nchunk_max, qscale, dev.status_word);
-  cudaError_t e = cudaGetLastError();
+  DecodeParams prm;
+  prm.Q = a.Q;
+  prm.Kc = static_cast<const uint8_t*>(a.Kc);
+  prm.Vc = static_cast<const uint8_t*>(a.Vc);
+  prm.key_len = a.key_len;
+  prm.out = a.out;
+  prm.counters = static_cast<unsigned int*>(a.workspace);
+  prm.part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + counters_bytes(a.B, a.L, a.H));
+  prm.status = dev.status_word;
+  prm.B = a.B;
+  prm.T = a.T;
+  prm.LH = a.L * a.H;
+  prm.part_stride = (a.T + kPartChunk - 1) / kPartChunk;
+  prm.qscale = a.scale * 1.4426950408889634f;   // scale * log2(e)
+  cudaError_t e = a.cache_bf16 ? launch<true>(prm, dev, stream) : launch<false>(prm, dev, stream);
   if (e == cudaSuccess) count_launches(1);
   return e;
 }
