@@ -46,10 +46,30 @@ namespace {
 constexpr int kDh = 64;
 constexpr int kPartFloats = 68;        // m, s, 2 pad, acc[64]
 constexpr int kPartChunk = 64;         // partial-slot granularity of the workspace layout
-constexpr int kConsumerWarps = 4;
+// Launch shape (compile-time; the defaults were chosen by timing on GB300).
+#ifndef CXA_DECODE_CONSUMER_WARPS
+#define CXA_DECODE_CONSUMER_WARPS 4
+#endif
+#ifndef CXA_DECODE_STAGES
+#define CXA_DECODE_STAGES 2
+#endif
+#ifndef CXA_DECODE_CHUNK_F32
+#define CXA_DECODE_CHUNK_F32 64
+#endif
+#ifndef CXA_DECODE_CHUNK_BF16
+#define CXA_DECODE_CHUNK_BF16 128
+#endif
+#ifndef CXA_DECODE_CTAS_PER_SM
+#define CXA_DECODE_CTAS_PER_SM 3
+#endif
+#ifndef CXA_DECODE_PDL
+#define CXA_DECODE_PDL 1
+#endif
+constexpr int kConsumerWarps = CXA_DECODE_CONSUMER_WARPS;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 3;
+constexpr int kStages = CXA_DECODE_STAGES;
 constexpr int kQBytes = kDh * 4;
+static_assert(kConsumerWarps >= 2, "the row merge uses the first 64 consumer threads");
 
 template <bool kBF16>
 struct Traits {
@@ -58,11 +78,13 @@ struct Traits {
   static constexpr int kLanesPerRow = kRowBytes / 16;       // 16 / 8 lanes share a key row
   static constexpr int kRowsPerPass = 32 / kLanesPerRow;    // 2 / 4 keys per warp pass
   static constexpr int kElemsPerLane = 16 / kElemBytes;     // 4 / 8 channels per lane
-  static constexpr int kChunkKeys = kBF16 ? 128 : 64;       // 16 KB of K per chunk
+  static constexpr int kChunkKeys = kBF16 ? CXA_DECODE_CHUNK_BF16 : CXA_DECODE_CHUNK_F32;   // 16 KB of K
   static constexpr int kKVBytes = kChunkKeys * kRowBytes;
   static constexpr int kStageBytes = 2 * kKVBytes + kQBytes;
   static constexpr int kKeysPerWarp = kChunkKeys / kConsumerWarps;
   static constexpr int kPasses = kKeysPerWarp / kRowsPerPass;   // 8 / 8
+  static_assert(kPasses >= 1 && kKeysPerWarp % kRowsPerPass == 0, "chunk must split evenly over warps");
+  static_assert(kChunkKeys >= kPartChunk, "a row then has at most ceil(T / 64) segments: one partial slot each");
 };
 
 struct DecodeParams {
@@ -100,6 +122,12 @@ __device__ __forceinline__ void unpack16(const uint4 u, float* f) {
 // Weight of a softmax state with running max m against a merged max M (0 for an
 // empty state, m == -inf).
 __device__ __forceinline__ float rescale(float m, float M) { return m == -INFINITY ? 0.f : exp2f(m - M); }
+
+// Programmatic dependent launch: let the next grid on the stream be scheduled
+// as this grid's CTAs retire, and wait for the previous grid to complete (and
+// its memory to be visible) before touching anything it may have written.
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -143,7 +171,7 @@ __device__ __forceinline__ long long owner_of(long long g, long long total, long
 }
 
 template <bool kBF16>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, CXA_DECODE_CTAS_PER_SM)
     decode_stream_kernel(const DecodeParams p) {
   using R = Traits<kBF16>;
   constexpr int LPR = R::kLanesPerRow;
@@ -162,6 +190,7 @@ __global__ void __launch_bounds__(kThreads)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int LH = p.LH;
+  allow_dependent_launch();
 
   // ---- chunk numbering (every CTA computes the same prefix from key_len)
   if (warp == 0) {
@@ -199,26 +228,58 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
 
   const long long total = s_first[p.B];
+  const long long ranges = total < gridDim.x ? total : static_cast<long long>(gridDim.x);
+  const bool active = total > 0 && blockIdx.x < ranges;
+  const long long g0 = active ? blockIdx.x * total / ranges : 0;
+  const long long g1 = active ? (blockIdx.x + 1) * total / ranges : 0;
+  const bool producer = warp == kConsumerWarps && lane == 0;
+
+  // The cache and key_len are inputs no decode writes: the producer starts
+  // streaming the first stages' K and V rows before the previous grid is done.
+  const uint64_t pol = policy_evict_first();
+  Cursor pcur{0, 0, 0};
+  long long npre = 0;
+  if (active && producer) {
+    pcur = locate(g0, s_first, s_nch, p.B, LH);
+    Cursor c = pcur;
+    npre = (g1 - g0) < kStages ? (g1 - g0) : kStages;
+    for (long long i = 0; i < npre; ++i) {
+      const int kl = min(max(__ldg(p.key_len + c.b), 0), p.T);
+      const int n = min(R::kChunkKeys, kl - c.c * R::kChunkKeys);
+      const long long row = static_cast<long long>(c.b) * LH + c.lh;
+      const size_t off = (static_cast<size_t>(row) * p.T + static_cast<size_t>(c.c) * R::kChunkKeys) * R::kRowBytes;
+      const uint32_t kv_bytes = static_cast<uint32_t>(n) * R::kRowBytes;
+      const uint32_t full = smem_u32(&bars[i]);
+      const uint32_t dst = smem_u32(stages + i * R::kStageBytes);
+      mbar_arrive_expect_tx(full, 2 * kv_bytes + kQBytes);
+      bulk_g2s_hint(dst, p.Kc + off, kv_bytes, full, pol);
+      bulk_g2s_hint(dst + R::kKVBytes, p.Vc + off, kv_bytes, full, pol);
+      advance(c, s_nch, p.B, LH);
+    }
+  }
+  // Q, out and the workspace may belong to the previous grid: wait for it.
+  wait_prior_grid();
   // rows of slots without any valid key: out = 0
   for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
        i < static_cast<long long>(p.B) * LH * (kDh / 4); i += static_cast<long long>(gridDim.x) * kThreads) {
     const int b = static_cast<int>(i / (static_cast<long long>(LH) * (kDh / 4)));
     if (s_nch[b] == 0) reinterpret_cast<float4*>(p.out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  if (total == 0) return;
-  const long long ranges = total < gridDim.x ? total : static_cast<long long>(gridDim.x);
-  if (blockIdx.x >= ranges) return;
-  const long long g0 = blockIdx.x * total / ranges;
-  const long long g1 = (blockIdx.x + 1) * total / ranges;
+  if (!active) return;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      Cursor cur = locate(g0, s_first, s_nch, p.B, LH);
-      uint32_t armed = 0, armed_parity = 0;
+      Cursor cur = pcur;
+      for (long long i = 0; i < npre; ++i) {   // the queries of the pre-issued stages
+        const long long row = static_cast<long long>(cur.b) * LH + cur.lh;
+        bulk_g2s(smem_u32(stages + i * R::kStageBytes) + 2 * R::kKVBytes, p.Q + row * kDh, kQBytes,
+                 smem_u32(&bars[i]));
+        advance(cur, s_nch, p.B, LH);
+      }
+      uint32_t armed = static_cast<uint32_t>((1u << npre) - 1u), armed_parity = 0;
       bool ok = true;
-      for (long long g = g0, i = 0; g < g1; ++g, ++i) {
+      for (long long g = g0 + npre, i = npre; g < g1; ++g, ++i) {
         const int s = static_cast<int>(i % kStages);
         const uint32_t parity = static_cast<uint32_t>((i / kStages) & 1);
         if (!mbar_wait(smem_u32(&bars[kStages + s]), parity ^ 1u, s_flags)) {
@@ -450,9 +511,18 @@ cudaError_t launch(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t 
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<kBF16>, kThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  const int grid = dev.num_sms * (per_sm < 2 ? per_sm : 2);
-  decode_stream_kernel<kBF16><<<grid, kThreads, smem, stream>>>(prm);
-  return cudaGetLastError();
+  const int grid = dev.num_sms * (per_sm < CXA_DECODE_CTAS_PER_SM ? per_sm : CXA_DECODE_CTAS_PER_SM);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = CXA_DECODE_PDL;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_stream_kernel<kBF16>, prm);
 }
 
 }  // namespace

@@ -283,3 +283,61 @@ def test_large_sampled_heads():
         e2e = O.attend_row(Q[b, l, hh], Kr, Vr, w.T, w.scale)
         assert np.abs(out[b, l, hh] - iso).max() <= DECODE_BF16_MAX_ABS
         assert np.abs(out[b, l, hh] - e2e).max() <= DECODE_BF16_MAX_ABS
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+def test_back_to_back_steps_without_sync(cache_dtype):
+    """Consecutive decode launches on one stream overlap (the next grid starts
+    streaming the cache while the previous one finishes); every step's output
+    must still be exact."""
+    w = W.custom("b2b", B=5, T=900, d=384, L=2, H=6, ragged=True, index=926)
+    c, d, h = _populate(w, cache_dtype)
+    Kg, Vg = host(c.Kc), host(c.Vc)
+    Qs = [W.make_Q(w, s) for s in range(12)]
+    Qd = [dev(q) for q in Qs]
+    outs = [torch.empty_like(Qd[0]) for _ in Qs]
+    torch.cuda.synchronize()
+    for q, o in zip(Qd, outs):
+        c.decode(q, d["key_len"], out=o)
+    torch.cuda.synchronize()
+    for q, o in zip(Qs, outs):
+        assert np.abs(host(o) - O.decode(q, Kg, Vg, h["key_len"])).max() <= DECODE_TOL[cache_dtype]
+
+
+def test_chained_queries_read_after_the_previous_step():
+    """Step k+1's query buffer is step k's output buffer: the next launch must
+    not read Q before the previous grid has written it."""
+    w = W.custom("chain", B=3, T=1100, d=256, L=2, H=4, ragged=True, index=927)
+    c, d, h = _populate(w, "f32")
+    Kg, Vg = host(c.Kc), host(c.Vc)
+    q0 = W.make_Q(w, 0)
+    bufs = [dev(q0), torch.empty_like(dev(q0))]
+    torch.cuda.synchronize()
+    for k in range(10):
+        c.decode(bufs[k % 2], d["key_len"], out=bufs[(k + 1) % 2])
+    torch.cuda.synchronize()
+    ref = q0.astype(np.float64)
+    for k in range(10):
+        ref = O.decode(ref, Kg, Vg, h["key_len"])
+    assert np.abs(host(bufs[10 % 2]) - ref).max() <= DECODE_F32_MAX_ABS
+
+
+def test_two_caches_interleaved_back_to_back():
+    """Decodes of two caches (own workspaces) alternate on one stream without syncs."""
+    w1 = W.custom("il1", B=2, T=640, d=128, L=3, H=2, ragged=True, index=928)
+    w2 = W.custom("il2", B=4, T=333, d=256, L=1, H=4, index=929)
+    c1, d1, h1 = _populate(w1, "f32")
+    c2, d2, h2 = _populate(w2, "bf16")
+    Q1 = [W.make_Q(w1, s) for s in range(6)]
+    Q2 = [W.make_Q(w2, s) for s in range(6)]
+    o1 = [torch.empty(q.shape, device="cuda") for q in Q1]
+    o2 = [torch.empty(q.shape, device="cuda") for q in Q2]
+    q1d, q2d = [dev(q) for q in Q1], [dev(q) for q in Q2]
+    torch.cuda.synchronize()
+    for s in range(6):
+        c1.decode(q1d[s], d1["key_len"], out=o1[s])
+        c2.decode(q2d[s], d2["key_len"], out=o2[s])
+    torch.cuda.synchronize()
+    for s in range(6):
+        assert np.abs(host(o1[s]) - O.decode(Q1[s], host(c1.Kc), host(c1.Vc), h1["key_len"])).max() <= DECODE_F32_MAX_ABS
+        assert np.abs(host(o2[s]) - O.decode(Q2[s], host(c2.Kc), host(c2.Vc), h2["key_len"])).max() <= DECODE_BF16_MAX_ABS
