@@ -34,7 +34,7 @@ WORKLOAD = "batched_base"
 NOMINAL_HBM_GBS = 7900.0
 TF32_OVER_BF16 = 1.1 / 2.25          # nominal dense TF32 / bf16 tensor rates
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-PROFILE_DECODE = os.path.join(ROOT, "profiles", "decode_split_batched_base.md")
+PROFILE_DECODE = os.path.join(ROOT, "profiles", "decode_stream_batched_base.md")
 
 
 # ---------------------------------------------------------------- host helpers
@@ -393,6 +393,31 @@ def device_inputs(torch, W, w, rank):
     return (d(E), d(WK), d(WV), d(bV), d(kl, torch.int32), d(Q), kl), (E, kl.astype(np.int32), Q)
 
 
+def measure_populate_large(torch, cxa, W, Wu, reps=10):
+    """Whisper-large dims (8 memories [1500, 1280], 32 layers, 20 heads): bf16
+    inputs and cache, the populate the bf16 tensor-core roofline is quoted on."""
+    import numpy as np
+    w = W.WORKLOADS["large"]
+    E = torch.from_numpy(W.make_E_all(w)).to("cuda", torch.bfloat16)
+    WK, WV, bV = W.make_weights(w)
+    WK = torch.from_numpy(WK).to("cuda", torch.bfloat16)
+    WV = torch.from_numpy(WV).to("cuda", torch.bfloat16)
+    bV = torch.from_numpy(np.ascontiguousarray(bV)).to("cuda")
+    cache = cxa.CrossAttentionCache(w.B, w.T, w.L, w.H, w.dh, "bf16")
+    for _ in range(Wu):
+        cache.populate(E, WK, WV, bV)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        cache.populate(E, WK, WV, bV)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    cache.close()
+    return {"ms": ms, "flops_per_call": populate_flops(w.L, w.d, w.B, w.T)}
+
+
 def run_profile(args):
     """A handful of launches of one kernel on the bench workload's inputs, for
     Nsight Compute: one populate (weight repack + GEMM), then two more populate
@@ -452,6 +477,7 @@ def run_cxa(args):
             "decode_GBps": vb / (v["decode_launch_us"] * 1e-6) / 1e9,
             "decode_launch_us": v["decode_launch_us"], "populate_ms": v["populate_ms"]}
     e2e_ms, h2d, d2h = measure_e2e(torch, cxa, w, host_inputs, dev_inputs[1:4], K, Wu, dist)
+    large = None if args.no_variants else measure_populate_large(torch, cxa, W, Wu)
 
     if rank != 0:
         if dist is not None:
@@ -482,6 +508,13 @@ def run_cxa(args):
                      "achieved": pop_tflops, "unit": "TFLOP/s", "peak": tf32_peak,
                      "peak_note": f"{peaks['source']} bf16 burst x nominal TF32/bf16 ratio 1.1/2.25",
                      "frac": pop_tflops / tf32_peak, "flops_per_call": pflops, "ms": main["populate_ms"]},
+        "populate_large_bf16": None if large is None else {
+            "bound": "tensor", "kernel": "populate_gemm_kernel<bf16> + pack_weights",
+            "workload": "whisper-large dims: 8 x E [1500,1280] bf16, 32 layers, 20x64 heads, bf16 cache",
+            "achieved": large["flops_per_call"] / (large["ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "peak": peaks["bf16_tflops"], "peak_note": f"{peaks['source']} bf16 burst",
+            "frac": large["flops_per_call"] / (large["ms"] * 1e-3) / 1e12 / peaks["bf16_tflops"],
+            "ms": large["ms"]},
         "clocks": main["clocks"],
         "e2e": {"value": tokens / (e2e_ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "note": "E, key_len and 128 Q copied in, 128 outputs copied out per "
