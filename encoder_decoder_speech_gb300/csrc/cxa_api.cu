@@ -189,6 +189,7 @@ int cxa_populate(cxa_cache* c, int b0, int nb, const void* E, const void* WK, co
   a.wpack = workspace;
   a.b0 = b0;
   a.nb = nb;
+  a.B = c->B;
   a.T = T;
   a.d = d;
   a.L = L;

@@ -21,6 +21,7 @@ struct PopulateLaunch {
   const float* bV;     // [L][d]
   void* wpack;         // workspace: [2*L*d][d] K-major packed weights
   int b0, nb, T, d, L, H;
+  int B;               // slots of the cache (for the cache tensor maps)
   bool in_bf16;
   bool cache_bf16;
 };

@@ -46,8 +46,12 @@ constexpr uint32_t kBBytes = kBN * kRowBytes;  // 32 KB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kTmemCols = 2 * kBN;        // two accumulators
 constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr uint32_t kBoxBytes = 32 * 128;       // one store box: 32 rows x 128 bytes
+constexpr uint32_t kStagingBytes = kEpiWarps * 2 * kBoxBytes;   // double-buffered per warp
 constexpr int kNumBarriers = 2 * kStages + 4 + 1;
-constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + 8 * kNumBarriers + 16;
+constexpr size_t kSmemBytes =
+    1024 + size_t(kStages) * kStageBytes + kStagingBytes + 8 * kNumBarriers + 16;
 
 struct GemmParams {
   void* Kc;
@@ -71,7 +75,9 @@ __device__ __forceinline__ void report_timeout(unsigned int* status, volatile in
 template <bool kBF16In>
 __global__ void __launch_bounds__(kThreads, 1)
     populate_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                         const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+                         const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const GemmParams p) {
   constexpr int kKElems = kBF16In ? 64 : 32;   // elements per 128-byte k-block row
   constexpr int kKStep = kBF16In ? 16 : 8;     // K of one MMA instruction
   constexpr int kMmasPerBlock = kKElems / kKStep;
@@ -83,13 +89,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* base_ptr = smem_raw + (base - raw);
   const uint32_t sA = base;
   const uint32_t sB = base + kStages * kABytes;
-  const uint32_t bars = base + kStages * kStageBytes;
+  const uint32_t staging = base + kStages * kStageBytes;   // 1024-byte aligned
+  const uint32_t bars = staging + kStagingBytes;
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
   auto tfull_bar = [&](int a) { return bars + 8u * (2 * kStages + a); };
   auto tempty_bar = [&](int a) { return bars + 8u * (2 * kStages + 2 + a); };
   const uint32_t drain_bar = bars + 8u * (2 * kStages + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + kStages * kStageBytes + 8 * kNumBarriers);
+  uint32_t* tmem_slot =
+      reinterpret_cast<uint32_t*>(base_ptr + kStages * kStageBytes + kStagingBytes + 8 * kNumBarriers);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -109,6 +117,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -208,10 +218,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quad = warp & 3;   // TMEM lanes 32*quad .. 32*quad+31 belong to this warp
+    // Each warp owns TMEM lanes 32*quad .. 32*quad+31 = 32 consecutive tokens t of
+    // one memory. For every 64-column head block it reads the accumulator rows,
+    // adds bV on V columns, writes them into a 128-byte-swizzled staging box in
+    // shared memory (conflict-free: the 16-byte chunk j of row r lands at slot
+    // j ^ (r & 7)) and one lane TMA-stores the box into the head-major cache,
+    // viewed as (c, t, slot*L*H + l*H + h): the 32 rows are contiguous there, and
+    // rows t >= T fall outside the tensor and are not written.
+    const int quad = warp & 3;
+    const int ew = warp - 2;                    // staging owner 0..3
+    const uint32_t my_staging = staging + static_cast<uint32_t>(ew) * 2u * kBoxBytes;
     const int LH = p.L * p.H;
+    const uint32_t swz = static_cast<uint32_t>(lane & 7);
     int acc = 0;
     uint32_t acc_phase = 0;
+    int sbuf = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) {
         report_timeout(p.status, abort_flag);
@@ -222,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nt = tile / p.num_m_tiles;
       const int slot = mtg / p.mt_per_slot;
       const int mt = mtg - slot * p.mt_per_slot;
-      const int t = mt * kBM + quad * 32 + lane;
-      const bool row_ok = t < p.T;
+      const int t0w = mt * kBM + quad * 32;     // first token of this warp's rows
+      const bool any_row = t0w < p.T;
       const int b = p.b0 + slot;
 #pragma unroll 1
       for (int g = 0; g < kBN / 64; ++g) {
@@ -233,49 +254,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lh = head - kv * LH;
         const int l = lh / p.H;
         const int h = lh - l * p.H;
-        const size_t row_elem = ((static_cast<size_t>(b) * LH + lh) * p.T + t) * 64;
-        void* dst_base = kv ? p.Vc : p.Kc;
+        const CUtensorMap* tm = kv ? &tmV : &tmK;
+        const int row3 = b * LH + lh;
+        uint32_t r[2][32];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          uint32_t r[32];
           const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                  static_cast<uint32_t>(acc * kBN + g * 64 + half * 32);
-          tmem_ld_32x32b_x32(taddr, r);
-          tmem_ld_wait();
-          if (row_ok) {
-            float v[32];
+          tmem_ld_32x32b_x32(taddr, r[half]);
+        }
+        tmem_ld_wait();
+        if (kv) {
+          const float4* bv4 = reinterpret_cast<const float4*>(p.bV + static_cast<size_t>(l) * p.d + h * 64);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-            if (kv) {
-              const float4* bv4 =
-                  reinterpret_cast<const float4*>(p.bV + static_cast<size_t>(l) * p.d + h * 64 + half * 32);
+          for (int half = 0; half < 2; ++half)
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float4 bb = __ldg(bv4 + i);
-                v[4 * i + 0] += bb.x;
-                v[4 * i + 1] += bb.y;
-                v[4 * i + 2] += bb.z;
-                v[4 * i + 3] += bb.w;
-              }
+            for (int i = 0; i < 8; ++i) {
+              const float4 bb = __ldg(bv4 + half * 8 + i);
+              r[half][4 * i + 0] = __float_as_uint(__uint_as_float(r[half][4 * i + 0]) + bb.x);
+              r[half][4 * i + 1] = __float_as_uint(__uint_as_float(r[half][4 * i + 1]) + bb.y);
+              r[half][4 * i + 2] = __float_as_uint(__uint_as_float(r[half][4 * i + 2]) + bb.z);
+              r[half][4 * i + 3] = __float_as_uint(__uint_as_float(r[half][4 * i + 3]) + bb.w);
             }
-            if (p.cache_bf16) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst_base) + row_elem + half * 32);
+        }
+        if (!any_row) continue;                 // warp-uniform: every row of this warp is past T
+        if (p.cache_bf16) {
+          // one box: 64 bf16 channels = 128 bytes per row
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+          const uint32_t box = my_staging + static_cast<uint32_t>(sbuf) * kBoxBytes + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                uint32_t w[4];
+          for (int j = 0; j < 8; ++j) {
+            uint32_t w[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  __nv_bfloat162 pr = __floats2bfloat162_rn(v[8 * i + 2 * j], v[8 * i + 2 * j + 1]);
-                  w[j] = *reinterpret_cast<uint32_t*>(&pr);
-                }
-                dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            } else {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(dst_base) + row_elem + half * 32);
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            for (int k = 0; k < 4; ++k) {
+              const int c = 8 * j + 2 * k;      // channels c, c+1
+              const float lo = __uint_as_float(r[c >> 5][c & 31]);
+              const float hi = __uint_as_float(r[(c + 1) >> 5][(c + 1) & 31]);
+              __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
+              w[k] = *reinterpret_cast<uint32_t*>(&pr);
             }
+            st_shared_v4(box + ((static_cast<uint32_t>(j) ^ swz) << 4), w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(tm, my_staging + static_cast<uint32_t>(sbuf) * kBoxBytes, 0, t0w, row3);
+            bulk_commit_group();
+          }
+          sbuf ^= 1;
+        } else {
+          // two boxes: channels 0-31 and 32-63, 128 bytes of fp32 per row each
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            const uint32_t box = my_staging + static_cast<uint32_t>(sbuf) * kBoxBytes + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              st_shared_v4(box + ((static_cast<uint32_t>(j) ^ swz) << 4), r[half][4 * j], r[half][4 * j + 1],
+                           r[half][4 * j + 2], r[half][4 * j + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(tm, my_staging + static_cast<uint32_t>(sbuf) * kBoxBytes, half * 32, t0w, row3);
+              bulk_commit_group();
+            }
+            sbuf ^= 1;
           }
         }
       }
@@ -285,6 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (lane == 0) bulk_wait_group_all();   // every store done before the CTA exits
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -393,6 +440,26 @@ cudaError_t run(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t str
     }
   }
 
+  // the cache as (c, t, slot*L*H + l*H + h): boxes of 32 tokens x 128 bytes
+  CUtensorMap tmK, tmV;
+  {
+    const int cesz = a.cache_bf16 ? 2 : 4;
+    const CUtensorMapDataType cdt = a.cache_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(a.T), static_cast<cuuint64_t>(a.B) * a.L * a.H};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(64) * cesz, static_cast<cuuint64_t>(a.T) * 64 * cesz};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / cesz), 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    for (int kv = 0; kv < 2; ++kv) {
+      CUresult r = encode(kv ? &tmV : &tmK, cdt, 3, kv ? a.Vc : a.Kc, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) {
+        *msg = "cuTensorMapEncodeTiled failed for the cache (code " + std::to_string(static_cast<int>(r)) + ")";
+        return cudaErrorInvalidValue;
+      }
+    }
+  }
+
   cudaError_t e = set_smem_attr_once<kBF16In>(dev.device);
   if (e != cudaSuccess) return e;
 
@@ -425,7 +492,7 @@ cudaError_t run(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t str
   p.cache_bf16 = a.cache_bf16 ? 1 : 0;
 
   const int grid = p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms;
-  populate_gemm_kernel<kBF16In><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, p);
+  populate_gemm_kernel<kBF16In><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, tmK, tmV, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   count_launches(1);
