@@ -344,30 +344,53 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // WK/WV [L][d_in][d_out] -> Wp[(kv*L + l)*d + j][i] (K-major). fp32 weights are
 // rounded to TF32 (round to nearest, ties away from zero: cvt.rna.tf32.f32).
+// One 64 x 64 tile per CTA: 16-byte global loads along d_out, a transposed
+// shared-memory tile whose 16-byte chunks are XOR-swizzled so that neither the
+// scattered writes nor the row reads conflict on banks, 16-byte global stores
+// along d_in.
+constexpr int kPackTile = 64;
+constexpr int kPackThreads = 256;
+
 template <bool kBF16In>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kPackThreads)
     pack_weights_kernel(const void* __restrict__ WK, const void* __restrict__ WV,
                         void* __restrict__ Wp, int d, int L) {
   using Elem = typename std::conditional<kBF16In, uint16_t, uint32_t>::type;
-  __shared__ Elem tile[32][33];
+  constexpr int V = 16 / sizeof(Elem);              // elements per 16-byte chunk
+  constexpr int kChunks = kPackTile / V;            // chunks per tile row
+  __shared__ __align__(16) Elem tile[kPackTile][kPackTile];   // tile[j][i], chunk-swizzled
+
   const int kvl = blockIdx.z;
   const int kv = kvl / L;
   const int l = kvl - kv * L;
   const Elem* W = static_cast<const Elem*>(kv ? WV : WK) + static_cast<size_t>(l) * d * d;
   Elem* out = static_cast<Elem*>(Wp);
-  const int i0 = blockIdx.y * 32;
-  const int j0 = blockIdx.x * 32;
-  for (int r = threadIdx.y; r < 32; r += 8)
-    tile[r][threadIdx.x] = W[static_cast<size_t>(i0 + r) * d + j0 + threadIdx.x];
-  __syncthreads();
-  for (int r = threadIdx.y; r < 32; r += 8) {
-    Elem v = tile[threadIdx.x][r];   // W[i0 + threadIdx.x][j0 + r]
-    if constexpr (!kBF16In) {
-      uint32_t u;
-      asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(u) : "f"(__uint_as_float(v)));
-      v = u;
+  const int i0 = blockIdx.y * kPackTile;            // d_in
+  const int j0 = blockIdx.x * kPackTile;            // d_out
+
+  for (int idx = threadIdx.x; idx < kPackTile * kChunks; idx += kPackThreads) {
+    const int r = idx / kChunks;                    // d_in row of the source tile
+    const int cv = idx - r * kChunks;               // 16-byte chunk along d_out
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(W + static_cast<size_t>(i0 + r) * d + j0 + cv * V));
+    const Elem* e = reinterpret_cast<const Elem*>(&u);
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const int j = cv * V + k;                     // transposed row
+      const int chunk = (r / V) ^ ((j / V) & 7);
+      tile[j][chunk * V + (r % V)] = e[k];
     }
-    out[(static_cast<size_t>(kvl) * d + j0 + r) * d + i0 + threadIdx.x] = v;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < kPackTile * kChunks; idx += kPackThreads) {
+    const int j = idx / kChunks;                    // d_out row of the packed tile
+    const int q = idx - j * kChunks;                // 16-byte chunk along d_in
+    uint4 u = *reinterpret_cast<const uint4*>(&tile[j][(q ^ ((j / V) & 7)) * V]);
+    if constexpr (!kBF16In) {
+      uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(w[k]) : "f"(__uint_as_float(w[k])));
+    }
+    *reinterpret_cast<uint4*>(out + (static_cast<size_t>(kvl) * d + j0 + j) * d + i0 + q * V) = u;
   }
 }
 
@@ -465,8 +488,8 @@ cudaError_t run(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t str
 
   // 2. repack the weights (K-major) into the workspace
   {
-    dim3 grid(a.d / 32, a.d / 32, 2 * a.L), block(32, 8);
-    pack_weights_kernel<kBF16In><<<grid, block, 0, stream>>>(a.WK, a.WV, a.wpack, a.d, a.L);
+    dim3 grid(a.d / kPackTile, a.d / kPackTile, 2 * a.L);
+    pack_weights_kernel<kBF16In><<<grid, kPackThreads, 0, stream>>>(a.WK, a.WV, a.wpack, a.d, a.L);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_launches(1);
