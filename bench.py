@@ -48,6 +48,9 @@ def parse_args(argv=None):
     p.add_argument("--no-variants", action="store_true", help="skip the bf16-cache variant")
     p.add_argument("--profile", choices=["decode", "decode_bf16", "populate"], default=None,
                    help="run a few launches of one kernel on the workload's inputs (for ncu), print nothing else")
+    p.add_argument("--sweep", action="store_true",
+                   help="time decode and populate at every point of the decode bandwidth sweep "
+                        "(T_enc x batch, d=512, 6 layers, 8x64 heads); one JSON line per point")
     p.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--budget-s", type=float, default=12.0, help=argparse.SUPPRESS)
     p.add_argument("--max-slots", type=int, default=16, help=argparse.SUPPRESS)
@@ -418,6 +421,64 @@ def measure_populate_large(torch, cxa, W, Wu, reps=10):
     return {"ms": ms, "flops_per_call": populate_flops(w.L, w.d, w.B, w.T)}
 
 
+def run_sweep(args):
+    """Decode bandwidth sweep: every (T_enc, batch) point, fp32 and bf16 caches,
+    `--steps` timed decode steps after `--warmup` (CUDA events around the step
+    loop, programmatic launch overlap included) and one timed populate."""
+    import numpy as np
+    import torch
+    from encoder_decoder_speech_gb300 import _build, cxa
+    from encoder_decoder_speech_gb300 import workloads as W
+    _build.build_library()
+    cxa.load()
+    torch.cuda.set_device(0)
+    peaks = load_peaks()
+    for T in W.SWEEP_T:
+        for B in W.SWEEP_B:
+            w = W.sweep_workload(T, B)
+            WK, WV, bV = (torch.from_numpy(np.ascontiguousarray(x)).to("cuda") for x in W.make_weights(w))
+            kl_h = W.make_key_len(w)
+            kl = torch.from_numpy(kl_h).to("cuda")
+            E = torch.empty((B, T, w.d), dtype=torch.float32, device="cuda")
+            for b in range(B):
+                E[b].copy_(torch.from_numpy(W.make_E(w, b, kl_h)))
+            Q = torch.from_numpy(W.make_Q(w, 0)).to("cuda")
+            line = {"sweep_point": {"T_enc": T, "B": B, "d": w.d, "L": w.L, "H": w.H}}
+            for cd, esz in (("f32", 4), ("bf16", 2)):
+                cache = cxa.CrossAttentionCache(B, T, w.L, w.H, 64, cd)
+                out = torch.empty_like(Q)
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                cache.populate(E, WK, WV, bV)
+                torch.cuda.synchronize()
+                a.record()
+                cache.populate(E, WK, WV, bV)
+                b_.record()
+                torch.cuda.synchronize()
+                pop_ms = a.elapsed_time(b_)
+                for _ in range(args.warmup):
+                    cache.decode(Q, kl, out=out)
+                torch.cuda.synchronize()
+                a.record()
+                for _ in range(args.steps):
+                    cache.decode(Q, kl, out=out)
+                b_.record()
+                torch.cuda.synchronize()
+                us = a.elapsed_time(b_) * 1000.0 / args.steps
+                gbs = decode_bytes(w.L, w.H, w.dh, esz, kl_h, B) / (us * 1e-6) / 1e9
+                line[cd] = {"decode_us": round(us, 2), "decode_GBps": round(gbs, 1),
+                            "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 3),
+                            "tokens_per_s": round(B / (us * 1e-6), 1), "populate_ms": round(pop_ms, 4),
+                            "populate_TFLOPs": round(populate_flops(w.L, w.d, B, T) / (pop_ms * 1e-3) / 1e12, 1)}
+                cache.close()
+                del cache
+                torch.cuda.empty_cache()
+            assert cxa.cxa_device_status(1) == cxa.CXA_OK
+            print(json.dumps(line), flush=True)
+            del E
+            torch.cuda.empty_cache()
+    return 0
+
+
 def run_profile(args):
     """A handful of launches of one kernel on the bench workload's inputs, for
     Nsight Compute: one populate (weight repack + GEMM), then two more populate
@@ -539,6 +600,8 @@ def main(argv=None):
         return 0
     if args.profile:
         return run_profile(args)
+    if args.sweep:
+        return run_sweep(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_cxa(args)
