@@ -51,6 +51,9 @@ def parse_args(argv=None):
     p.add_argument("--sweep", action="store_true",
                    help="time decode and populate at every point of the decode bandwidth sweep "
                         "(T_enc x batch, d=512, 6 layers, 8x64 heads); one JSON line per point")
+    p.add_argument("--shared", action="store_true",
+                   help="time shared-cache decode (nq hypotheses per memory) on the batched Whisper-Base "
+                        "workload for nq = 1, 2, 4, 5, 8; one JSON line per (nq, cache dtype)")
     p.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--budget-s", type=float, default=12.0, help=argparse.SUPPRESS)
     p.add_argument("--max-slots", type=int, default=16, help=argparse.SUPPRESS)
@@ -479,6 +482,48 @@ def run_sweep(args):
     return 0
 
 
+def run_shared(args):
+    """Shared-cache decode on batched Whisper-Base: nq hypothesis rows per memory
+    read the memory's K/V once. A token here is one query row of one hypothesis
+    through all layers; bytes = valid K/V rows + nq x (Q + out) rows."""
+    import numpy as np
+    import torch
+    from encoder_decoder_speech_gb300 import _build, cxa
+    from encoder_decoder_speech_gb300 import workloads as W
+    _build.build_library()
+    cxa.load()
+    torch.cuda.set_device(0)
+    peaks = load_peaks()
+    w = W.WORKLOADS[WORKLOAD]
+    (E, WK, WV, bV, kl, _, kl_h), _ = device_inputs(torch, W, w, 0)
+    for cd, esz in (("f32", 4), ("bf16", 2)):
+        cache = cxa.CrossAttentionCache(w.B, w.T, w.L, w.H, w.dh, cd)
+        cache.populate(E, WK, WV, bV)
+        for nq in (1, 2, 4, 5, 8):
+            Q = torch.from_numpy(np.random.default_rng(nq).standard_normal(
+                (w.B, nq, w.L, w.H, w.dh)).astype(np.float32)).to("cuda")
+            out = torch.empty_like(Q)
+            for _ in range(args.warmup):
+                cache.decode_shared(Q, kl, out=out)
+            torch.cuda.synchronize()
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(args.steps):
+                cache.decode_shared(Q, kl, out=out)
+            b_.record()
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b_) * 1000.0 / args.steps
+            byts = decode_bytes(w.L, w.H, w.dh, esz, kl_h, w.B) + (nq - 1) * 2 * w.B * w.L * w.H * w.dh * 4
+            print(json.dumps({"shared_decode": {"workload": "batched-whisper-base", "nq": nq, "cache_dtype": cd},
+                              "us_per_step": round(us, 2), "tokens_per_s": round(w.B * nq / (us * 1e-6), 1),
+                              "GBps": round(byts / (us * 1e-6) / 1e9, 1),
+                              "frac_of_measured_hbm": round(byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 3)}),
+                  flush=True)
+        cache.close()
+    assert cxa.cxa_device_status(1) == cxa.CXA_OK
+    return 0
+
+
 def run_profile(args):
     """A handful of launches of one kernel on the bench workload's inputs, for
     Nsight Compute: one populate (weight repack + GEMM), then two more populate
@@ -602,6 +647,8 @@ def main(argv=None):
         return run_profile(args)
     if args.sweep:
         return run_sweep(args)
+    if args.shared:
+        return run_shared(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_cxa(args)

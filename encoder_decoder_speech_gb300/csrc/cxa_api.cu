@@ -146,7 +146,12 @@ size_t cxa_populate_workspace_bytes(int d, int L, int in_dtype) {
 
 size_t cxa_decode_workspace_bytes(int B, int T, int L, int H, int dh) {
   if (B <= 0 || T <= 0 || L <= 0 || H <= 0 || dh != 64) return 0;
-  return cxa::decode_workspace_bytes(B, T, L, H);
+  return cxa::decode_workspace_bytes(B, T, L, H, 1);
+}
+
+size_t cxa_decode_shared_workspace_bytes(int B, int T, int L, int H, int dh, int nq) {
+  if (B <= 0 || T <= 0 || L <= 0 || H <= 0 || dh != 64 || nq < 1 || nq > CXA_MAX_SHARED_QUERIES) return 0;
+  return cxa::decode_workspace_bytes(B, T, L, H, nq);
 }
 
 int cxa_populate(cxa_cache* c, int b0, int nb, const void* E, const void* WK, const void* WV,
@@ -205,27 +210,30 @@ int cxa_populate(cxa_cache* c, int b0, int nb, const void* E, const void* WK, co
   return CXA_OK;
 }
 
-int cxa_decode(const cxa_cache* c, const float* Q, const int* key_len, float* out, float scale,
-               void* workspace, size_t workspace_bytes, void* stream) {
-  if (c == nullptr) return fail(CXA_EINVAL, "cxa_decode: cache descriptor is NULL");
+static int decode_common(const char* who, const cxa_cache* c, int nq, const float* Q, const int* key_len,
+                         float* out, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  const std::string w(who);
+  if (c == nullptr) return fail(CXA_EINVAL, w + ": cache descriptor is NULL");
+  if (nq < 1 || nq > CXA_MAX_SHARED_QUERIES)
+    return fail(CXA_EINVAL, w + ": nq must be in [1, " + std::to_string(CXA_MAX_SHARED_QUERIES) + "]");
   if (Q == nullptr || key_len == nullptr || out == nullptr || workspace == nullptr)
-    return fail(CXA_EINVAL, "cxa_decode: a pointer argument is NULL");
+    return fail(CXA_EINVAL, w + ": a pointer argument is NULL");
   if (!aligned(Q, 16) || !aligned(out, 16) || !aligned(key_len, 4) || !aligned(workspace, 256))
-    return fail(CXA_EINVAL, "cxa_decode: Q and out must be 16-byte aligned, the workspace 256-byte aligned");
+    return fail(CXA_EINVAL, w + ": Q and out must be 16-byte aligned, the workspace 256-byte aligned");
   if (static_cast<const void*>(Q) == static_cast<const void*>(out))
-    return fail(CXA_EINVAL, "cxa_decode: out must not alias Q");
-  if (!std::isfinite(scale)) return fail(CXA_EINVAL, "cxa_decode: scale must be finite");
-  if (workspace_bytes < cxa::decode_workspace_bytes(c->B, c->T, c->L, c->H))
-    return fail(CXA_EINVAL, "cxa_decode: workspace smaller than cxa_decode_workspace_bytes()");
+    return fail(CXA_EINVAL, w + ": out must not alias Q");
+  if (!std::isfinite(scale)) return fail(CXA_EINVAL, w + ": scale must be finite");
+  if (workspace_bytes < cxa::decode_workspace_bytes(c->B, c->T, c->L, c->H, nq))
+    return fail(CXA_EINVAL, w + ": workspace smaller than the decode workspace size query");
   for (int b = 0; b < c->B; ++b)
     if (!c->ready[static_cast<size_t>(b)])
-      return fail(CXA_ENOTREADY, "cxa_decode: slot " + std::to_string(b) +
+      return fail(CXA_ENOTREADY, w + ": slot " + std::to_string(b) +
                                      " is not populated (invalidated or never populated)");
 
   std::string msg;
   cxa::DeviceInfo dev;
   cudaError_t e = cxa::current_device_info(&dev, &msg);
-  if (e != cudaSuccess) return fail_cuda(e, "cxa_decode: " + msg);
+  if (e != cudaSuccess) return fail_cuda(e, w + ": " + msg);
 
   cxa::DecodeLaunch a;
   a.Kc = c->Kc;
@@ -233,6 +241,7 @@ int cxa_decode(const cxa_cache* c, const float* Q, const int* key_len, float* ou
   a.Q = Q;
   a.key_len = key_len;
   a.out = out;
+  a.nq = nq;
   a.workspace = workspace;
   a.B = c->B;
   a.T = c->T;
@@ -241,8 +250,18 @@ int cxa_decode(const cxa_cache* c, const float* Q, const int* key_len, float* ou
   a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(c->dh));
   a.cache_bf16 = c->dtype == CXA_BF16;
   e = cxa::launch_decode(a, dev, static_cast<cudaStream_t>(stream), &msg);
-  if (e != cudaSuccess) return fail_cuda(e, "cxa_decode: launch");
+  if (e != cudaSuccess) return fail_cuda(e, w + ": launch");
   return CXA_OK;
+}
+
+int cxa_decode(const cxa_cache* c, const float* Q, const int* key_len, float* out, float scale,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_common("cxa_decode", c, 1, Q, key_len, out, scale, workspace, workspace_bytes, stream);
+}
+
+int cxa_decode_shared(const cxa_cache* c, int nq, const float* Q, const int* key_len, float* out,
+                      float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_common("cxa_decode_shared", c, nq, Q, key_len, out, scale, workspace, workspace_bytes, stream);
 }
 
 int cxa_invalidate(cxa_cache* c, int b) {

@@ -1,35 +1,42 @@
-// Decode: one query row per (slot, layer, head) attends non-causally over the
-// valid encoder keys of the projection cache, out = softmax(scale * q.K^T) V
-// ("Whisper: Trace One Encoder Tensor into Every Decoder Layer", "View 2 --
-// expand one cross-attention operation": one query token, all key tokens,
-// head_dim 64, scale 0.125).
+// Decode: query rows attend non-causally over the valid encoder keys of the
+// projection cache, out = softmax(scale * q.K^T) V ("Whisper: Trace One Encoder
+// Tensor into Every Decoder Layer", "View 2 -- expand one cross-attention
+// operation": one query token, all key tokens, head_dim 64, scale 0.125).
+// cxa_decode has one query row per (slot, layer, head); cxa_decode_shared has nq
+// query rows (beam or speculative hypotheses) per (slot, layer, head) that all
+// attend the same cache slot, the batch-N-queries-over-one-shared-cache case of
+// SharedSplitKVCached ("Caso de estudio: WhisperKit", §3): each K/V row is read
+// from HBM once and used for all nq queries.
 //
-// Split-T decoding with the lazy (online) softmax of SplitKV ("Caso de estudio:
-// WhisperKit", §3), laid out for an HBM-bound GPU:
+// Split-T decoding with the lazy (online) softmax of SplitKV (same page, §3),
+// laid out for an HBM-bound GPU:
 //
-//  * Work = every valid key of every row, cut into chunks of kChunkKeys keys
-//    (16 KB of K and 16 KB of V). The chunks of all rows are numbered densely,
-//    slot-major then (layer, head) then key order, and the persistent grid
-//    gives each CTA one contiguous, equal-sized range of chunk numbers, so every
-//    CTA streams the same number of bytes whatever the key lengths are.
+//  * Work = every valid key of every cache row, cut into chunks of kChunkKeys
+//    keys (16 KB of K and 16 KB of V). The chunks of all rows are numbered
+//    densely, slot-major then (layer, head) then key order, and the persistent
+//    grid gives each CTA one contiguous, equal-sized range of chunk numbers, so
+//    every CTA streams the same number of bytes whatever the key lengths are.
 //  * In each CTA a producer warp keeps a kStages-deep ring of shared-memory
-//    stages full with three cp.async.bulk copies per chunk (K rows, V rows and
-//    the row's query, all contiguous in the head-major cache) completing on a
-//    "full" mbarrier; four consumer warps read a stage and release it on its
-//    "empty" mbarrier.
-//  * Each consumer lane group (16 lanes per fp32 key row, 8 per bf16 row) runs
-//    its own online softmax (running max m, sum s, accumulators) over the keys
-//    it is given, in fp32 and base 2 (q is pre-multiplied by scale * log2(e)).
+//    stages full with cp.async.bulk copies per chunk (K rows, V rows and the
+//    row's query rows, all contiguous) completing on a "full" mbarrier; the
+//    consumer warps read a stage and release it on its "empty" mbarrier.
+//  * Each consumer lane group (16 lanes per fp32 key row, 8 or 16 per bf16 row)
+//    runs its own online softmax per query (running max m, sum s, accumulators)
+//    over the keys it is given, in fp32 and base 2 (q is pre-multiplied by
+//    scale * log2(e)).
 //  * When a row's run of chunks in this CTA ends, the groups' states are merged
 //    (warp shuffles, then shared memory). A CTA that owned the whole row writes
-//    out directly; otherwise it stores its partial (m, s, acc[64]) and counts
-//    itself on the row's arrival counter, and the CTA that arrives last merges
-//    the row's partials (M = max m_i, S = sum s_i 2^(m_i - M),
+//    out directly; otherwise it stores its partials (m, s, acc[64]), one per
+//    query, and counts itself on the row's arrival counter, and the CTA that
+//    arrives last merges the row's partials (M = max m_i, S = sum s_i 2^(m_i - M),
 //    out = sum acc_i 2^(m_i - M) / S) and resets the counter. No CTA ever waits
 //    for another CTA.
 //  * Keys t >= key_len[b] are never copied and never enter the arithmetic; a
 //    row with no valid key gets out = 0 (the clamped softmax denominator,
 //    WhisperKit case study §2).
+//  * Programmatic dependent launch: the next decode grid on the stream starts
+//    streaming K/V while this one drains; it waits for this grid before
+//    reading queries or writing anything.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -68,22 +75,28 @@ constexpr int kPartChunk = 64;         // partial-slot granularity of the worksp
 constexpr int kConsumerWarps = CXA_DECODE_CONSUMER_WARPS;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = CXA_DECODE_STAGES;
-constexpr int kQBytes = kDh * 4;
+constexpr int kQRowBytes = kDh * 4;
 static_assert(kConsumerWarps >= 2, "the row merge uses the first 64 consumer threads");
 
-template <bool kBF16>
+template <bool kBF16, int kNQ>
 struct Traits {
   static constexpr int kElemBytes = kBF16 ? 2 : 4;
-  static constexpr int kRowBytes = kDh * kElemBytes;        // 256 / 128
-  static constexpr int kLanesPerRow = kRowBytes / 16;       // 16 / 8 lanes share a key row
-  static constexpr int kRowsPerPass = 32 / kLanesPerRow;    // 2 / 4 keys per warp pass
-  static constexpr int kElemsPerLane = 16 / kElemBytes;     // 4 / 8 channels per lane
+  static constexpr int kRowBytes = kDh * kElemBytes;                 // 256 / 128
+  // One query: 8 lanes per bf16 row (16-byte slices). Several queries: 16 lanes
+  // per row for both dtypes, halving the per-lane query and accumulator registers.
+  static constexpr int kLanesPerRow = (kBF16 && kNQ == 1) ? 8 : 16;
+  static constexpr int kSliceBytes = kRowBytes / kLanesPerRow;       // 16 or 8
+  static constexpr int kRowsPerPass = 32 / kLanesPerRow;             // keys per warp pass
+  static constexpr int kElemsPerLane = kSliceBytes / kElemBytes;     // channels per lane
   static constexpr int kChunkKeys = kBF16 ? CXA_DECODE_CHUNK_BF16 : CXA_DECODE_CHUNK_F32;   // 16 KB of K
   static constexpr int kKVBytes = kChunkKeys * kRowBytes;
-  static constexpr int kStageBytes = 2 * kKVBytes + kQBytes;
+  static constexpr int kStageBytes = 2 * kKVBytes + kNQ * kQRowBytes;
   static constexpr int kKeysPerWarp = kChunkKeys / kConsumerWarps;
-  static constexpr int kPasses = kKeysPerWarp / kRowsPerPass;   // 8 / 8
+  static constexpr int kPasses = kKeysPerWarp / kRowsPerPass;
+  // passes whose scores are held at once (bounds the score registers to 16)
+  static constexpr int kPassBlock = kPasses < 16 / kNQ ? kPasses : 16 / kNQ;
   static_assert(kPasses >= 1 && kKeysPerWarp % kRowsPerPass == 0, "chunk must split evenly over warps");
+  static_assert(kPasses % kPassBlock == 0, "pass blocks must tile the passes");
   static_assert(kChunkKeys >= kPartChunk, "a row then has at most ceil(T / 64) segments: one partial slot each");
 };
 
@@ -97,25 +110,35 @@ struct DecodeParams {
   unsigned int* counters;
   unsigned int* status;
   int B, T, LH;
-  int part_stride;     // partial slots per row (ceil(T / 64))
+  int nq;              // query rows per cache row (<= kNQ)
+  int part_stride;     // partial slots per (row, query) (ceil(T / 64))
   float qscale;        // scale * log2(e)
 };
 
-// 16 bytes of a cache row -> fp32 values
-template <bool kBF16>
-__device__ __forceinline__ void unpack16(const uint4 u, float* f) {
-  if constexpr (kBF16) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+// One lane's slice of a cache row -> fp32 values
+template <bool kBF16, int kSlice>
+__device__ __forceinline__ void load_slice(const uint8_t* p, float* f) {
+  if constexpr (kSlice == 16) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    if constexpr (kBF16) {
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      f[2 * i] = __uint_as_float(w[i] << 16);
-      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    } else {
+      f[0] = __uint_as_float(u.x);
+      f[1] = __uint_as_float(u.y);
+      f[2] = __uint_as_float(u.z);
+      f[3] = __uint_as_float(u.w);
     }
-  } else {
-    f[0] = __uint_as_float(u.x);
-    f[1] = __uint_as_float(u.y);
-    f[2] = __uint_as_float(u.z);
-    f[3] = __uint_as_float(u.w);
+  } else {   // 8-byte bf16 slice
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    f[0] = __uint_as_float(u.x << 16);
+    f[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(u.y << 16);
+    f[3] = __uint_as_float(u.y & 0xFFFF0000u);
   }
 }
 
@@ -170,10 +193,15 @@ __device__ __forceinline__ long long owner_of(long long g, long long total, long
   return ((g + 1) * ranges + total - 1) / total - 1;
 }
 
-template <bool kBF16>
-__global__ void __launch_bounds__(kThreads, CXA_DECODE_CTAS_PER_SM)
+template <bool kBF16, int kNQ>
+constexpr int min_ctas_per_sm() {
+  return kNQ >= 4 ? 2 : CXA_DECODE_CTAS_PER_SM;
+}
+
+template <bool kBF16, int kNQ>
+__global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
     decode_stream_kernel(const DecodeParams p) {
-  using R = Traits<kBF16>;
+  using R = Traits<kBF16, kNQ>;
   constexpr int LPR = R::kLanesPerRow;
   constexpr int EPL = R::kElemsPerLane;
 
@@ -182,14 +210,15 @@ __global__ void __launch_bounds__(kThreads, CXA_DECODE_CTAS_PER_SM)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * R::kStageBytes);   // full[S], empty[S]
   long long* s_first = reinterpret_cast<long long*>(bars + 2 * kStages);
   int* s_nch = reinterpret_cast<int*>(s_first + p.B + 1);
-  float* s_red = reinterpret_cast<float*>(s_nch + p.B + (p.B & 1));   // [4][64] acc, then m[4], s[4]
-  float* s_redm = s_red + kConsumerWarps * kDh;
-  float* s_reds = s_redm + kConsumerWarps;
-  volatile int* s_flags = reinterpret_cast<volatile int*>(s_reds + kConsumerWarps);   // [0] abort, [1] last
+  float* s_red = reinterpret_cast<float*>(s_nch + p.B + (p.B & 1));   // [kNQ][warps][64] acc
+  float* s_redm = s_red + kNQ * kConsumerWarps * kDh;                // [kNQ][warps] m
+  float* s_reds = s_redm + kNQ * kConsumerWarps;                     // [kNQ][warps] s
+  volatile int* s_flags = reinterpret_cast<volatile int*>(s_reds + kNQ * kConsumerWarps);   // [0] abort, [1] last
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int LH = p.LH;
+  const int nq = p.nq;
   allow_dependent_launch();
 
   // ---- chunk numbering (every CTA computes the same prefix from key_len)
@@ -251,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, CXA_DECODE_CTAS_PER_SM)
       const uint32_t kv_bytes = static_cast<uint32_t>(n) * R::kRowBytes;
       const uint32_t full = smem_u32(&bars[i]);
       const uint32_t dst = smem_u32(stages + i * R::kStageBytes);
-      mbar_arrive_expect_tx(full, 2 * kv_bytes + kQBytes);
+      mbar_arrive_expect_tx(full, 2 * kv_bytes + static_cast<uint32_t>(nq) * kQRowBytes);
       bulk_g2s_hint(dst, p.Kc + off, kv_bytes, full, pol);
       bulk_g2s_hint(dst + R::kKVBytes, p.Vc + off, kv_bytes, full, pol);
       advance(c, s_nch, p.B, LH);
@@ -260,21 +289,27 @@ __global__ void __launch_bounds__(kThreads, CXA_DECODE_CTAS_PER_SM)
   // Q, out and the workspace may belong to the previous grid: wait for it.
   wait_prior_grid();
   // rows of slots without any valid key: out = 0
-  for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
-       i < static_cast<long long>(p.B) * LH * (kDh / 4); i += static_cast<long long>(gridDim.x) * kThreads) {
-    const int b = static_cast<int>(i / (static_cast<long long>(LH) * (kDh / 4)));
-    if (s_nch[b] == 0) reinterpret_cast<float4*>(p.out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  {
+    const long long per_slot = static_cast<long long>(nq) * LH * (kDh / 4);
+    for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < p.B * per_slot;
+         i += static_cast<long long>(gridDim.x) * kThreads) {
+      if (s_nch[static_cast<int>(i / per_slot)] == 0)
+        reinterpret_cast<float4*>(p.out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
   if (!active) return;
+
+  // query row n of cache row (b, lh): Q[b][n][lh][:]
+  auto qrow = [&](int b, int lh, int n) { return (static_cast<long long>(b) * nq + n) * LH + lh; };
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       Cursor cur = pcur;
       for (long long i = 0; i < npre; ++i) {   // the queries of the pre-issued stages
-        const long long row = static_cast<long long>(cur.b) * LH + cur.lh;
-        bulk_g2s(smem_u32(stages + i * R::kStageBytes) + 2 * R::kKVBytes, p.Q + row * kDh, kQBytes,
-                 smem_u32(&bars[i]));
+        const uint32_t qdst = smem_u32(stages + i * R::kStageBytes) + 2 * R::kKVBytes;
+        for (int n = 0; n < nq; ++n)
+          bulk_g2s(qdst + n * kQRowBytes, p.Q + qrow(cur.b, cur.lh, n) * kDh, kQRowBytes, smem_u32(&bars[i]));
         advance(cur, s_nch, p.B, LH);
       }
       uint32_t armed = static_cast<uint32_t>((1u << npre) - 1u), armed_parity = 0;
@@ -294,10 +329,11 @@ __global__ void __launch_bounds__(kThreads, CXA_DECODE_CTAS_PER_SM)
         const uint32_t kv_bytes = static_cast<uint32_t>(n) * R::kRowBytes;
         const uint32_t full = smem_u32(&bars[s]);
         const uint32_t dst = smem_u32(stages + s * R::kStageBytes);
-        mbar_arrive_expect_tx(full, 2 * kv_bytes + kQBytes);
+        mbar_arrive_expect_tx(full, 2 * kv_bytes + static_cast<uint32_t>(nq) * kQRowBytes);
         bulk_g2s_hint(dst, p.Kc + off, kv_bytes, full, pol);
         bulk_g2s_hint(dst + R::kKVBytes, p.Vc + off, kv_bytes, full, pol);
-        bulk_g2s(dst + 2 * R::kKVBytes, p.Q + row * kDh, kQBytes, full);
+        for (int qn = 0; qn < nq; ++qn)
+          bulk_g2s(dst + 2 * R::kKVBytes + qn * kQRowBytes, p.Q + qrow(cur.b, cur.lh, qn) * kDh, kQRowBytes, full);
         armed |= 1u << s;
         armed_parity = (armed_parity & ~(1u << s)) | (parity << s);
         advance(cur, s_nch, p.B, LH);
@@ -312,15 +348,19 @@ __global__ void __launch_bounds__(kThreads, CXA_DECODE_CTAS_PER_SM)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ consumers
-    const int sub = lane % LPR;          // 16-byte slice of a key row this lane reads
+    const int sub = lane % LPR;          // slice of a key row this lane reads
     const int grp = lane / LPR;          // lane group = independent softmax stream
     const int tid = threadIdx.x;         // 0..127
     Cursor cur = locate(g0, s_first, s_nch, p.B, LH);
     int seg_c0 = cur.c;                  // first chunk of the current row in this CTA
-    float m = -INFINITY, ssum = 0.f;
-    float acc[EPL];
+    float m[kNQ], ssum[kNQ], acc[kNQ][EPL];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    for (int q = 0; q < kNQ; ++q) {
+      m[q] = -INFINITY;
+      ssum[q] = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[q][e] = 0.f;
+    }
     bool ok = true;
 
     for (long long g = g0, i = 0; g < g1; ++g, ++i) {
@@ -338,49 +378,72 @@ __global__ void __launch_bounds__(kThreads, CXA_DECODE_CTAS_PER_SM)
         const uint8_t* sK = stages + s * R::kStageBytes;
         const uint8_t* sV = sK + R::kKVBytes;
         const float* sQ = reinterpret_cast<const float*>(sK + 2 * R::kKVBytes);
-        float q[EPL];
+        float qv[kNQ][EPL];
 #pragma unroll
-        for (int e4 = 0; e4 < EPL / 4; ++e4) {
-          const float4 v = *reinterpret_cast<const float4*>(sQ + sub * EPL + 4 * e4);
-          q[4 * e4 + 0] = v.x * p.qscale;
-          q[4 * e4 + 1] = v.y * p.qscale;
-          q[4 * e4 + 2] = v.z * p.qscale;
-          q[4 * e4 + 3] = v.w * p.qscale;
+        for (int q = 0; q < kNQ; ++q) {
+          if (q < nq) {
+#pragma unroll
+            for (int e4 = 0; e4 < EPL / 4; ++e4) {
+              const float4 v = *reinterpret_cast<const float4*>(sQ + q * kDh + sub * EPL + 4 * e4);
+              qv[q][4 * e4 + 0] = v.x * p.qscale;
+              qv[q][4 * e4 + 1] = v.y * p.qscale;
+              qv[q][4 * e4 + 2] = v.z * p.qscale;
+              qv[q][4 * e4 + 3] = v.w * p.qscale;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) qv[q][e] = 0.f;
+          }
         }
-        float sc[R::kPasses];
-        float mloc = -INFINITY;
 #pragma unroll
-        for (int it = 0; it < R::kPasses; ++it) {
-          const int r = warp * R::kKeysPerWarp + it * R::kRowsPerPass + grp;
-          float f[EPL];
-          unpack16<kBF16>(*reinterpret_cast<const uint4*>(sK + r * R::kRowBytes + sub * 16), f);
-          float dot = 0.f;
+        for (int blk = 0; blk < R::kPasses / R::kPassBlock; ++blk) {
+          float sc[R::kPassBlock][kNQ];
+          float mloc[kNQ];
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) dot = fmaf(q[e], f[e], dot);
+          for (int q = 0; q < kNQ; ++q) mloc[q] = -INFINITY;
 #pragma unroll
-          for (int off = LPR / 2; off >= 1; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-          sc[it] = r < n ? dot : -INFINITY;
-          mloc = fmaxf(mloc, sc[it]);
-        }
-        const float mnew = fmaxf(m, mloc);
-        if (mnew != -INFINITY) {
-          const float corr = rescale(m, mnew);
-          ssum *= corr;
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) acc[e] *= corr;
-#pragma unroll
-          for (int it = 0; it < R::kPasses; ++it) {
+          for (int pb = 0; pb < R::kPassBlock; ++pb) {
+            const int it = blk * R::kPassBlock + pb;
             const int r = warp * R::kKeysPerWarp + it * R::kRowsPerPass + grp;
-            if (r < n) {
-              const float pw = exp2f(sc[it] - mnew);
-              float f[EPL];
-              unpack16<kBF16>(*reinterpret_cast<const uint4*>(sV + r * R::kRowBytes + sub * 16), f);
-              ssum += pw;
+            float f[EPL];
+            load_slice<kBF16, R::kSliceBytes>(sK + r * R::kRowBytes + sub * R::kSliceBytes, f);
 #pragma unroll
-              for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pw, f[e], acc[e]);
+            for (int q = 0; q < kNQ; ++q) {
+              float dot = 0.f;
+#pragma unroll
+              for (int e = 0; e < EPL; ++e) dot = fmaf(qv[q][e], f[e], dot);
+#pragma unroll
+              for (int off = LPR / 2; off >= 1; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+              sc[pb][q] = r < n ? dot : -INFINITY;
+              mloc[q] = fmaxf(mloc[q], sc[pb][q]);
             }
           }
-          m = mnew;
+          float mnew[kNQ];
+#pragma unroll
+          for (int q = 0; q < kNQ; ++q) {
+            mnew[q] = fmaxf(m[q], mloc[q]);
+            const float corr = mnew[q] == -INFINITY ? 1.f : rescale(m[q], mnew[q]);
+            ssum[q] *= corr;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[q][e] *= corr;
+            m[q] = mnew[q];
+          }
+#pragma unroll
+          for (int pb = 0; pb < R::kPassBlock; ++pb) {
+            const int it = blk * R::kPassBlock + pb;
+            const int r = warp * R::kKeysPerWarp + it * R::kRowsPerPass + grp;
+            if (r < n) {
+              float f[EPL];
+              load_slice<kBF16, R::kSliceBytes>(sV + r * R::kRowBytes + sub * R::kSliceBytes, f);
+#pragma unroll
+              for (int q = 0; q < kNQ; ++q) {
+                const float pw = exp2f(sc[pb][q] - m[q]);
+                ssum[q] += pw;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[q][e] = fmaf(pw, f[e], acc[q][e]);
+              }
+            }
+          }
         }
       }
       __syncwarp();
@@ -388,56 +451,67 @@ __global__ void __launch_bounds__(kThreads, CXA_DECODE_CTAS_PER_SM)
 
       const bool row_ends = (cur.c == nch - 1) || (g + 1 == g1);
       if (row_ends) {
-        // ---- merge the lane groups of this warp, then the four warps
+        // ---- merge the lane groups of this warp, then the warps, per query
 #pragma unroll
-        for (int off = LPR; off < 32; off <<= 1) {
-          const float mo = __shfl_xor_sync(0xffffffffu, m, off);
-          const float so = __shfl_xor_sync(0xffffffffu, ssum, off);
-          const float M = fmaxf(m, mo);
-          const float f0 = rescale(m, M), f1 = rescale(mo, M);
-          ssum = ssum * f0 + so * f1;
+        for (int q = 0; q < kNQ; ++q) {
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) {
-            const float ao = __shfl_xor_sync(0xffffffffu, acc[e], off);
-            acc[e] = acc[e] * f0 + ao * f1;
+          for (int off = LPR; off < 32; off <<= 1) {
+            const float mo = __shfl_xor_sync(0xffffffffu, m[q], off);
+            const float so = __shfl_xor_sync(0xffffffffu, ssum[q], off);
+            const float M = fmaxf(m[q], mo);
+            const float f0 = rescale(m[q], M), f1 = rescale(mo, M);
+            ssum[q] = ssum[q] * f0 + so * f1;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+              const float ao = __shfl_xor_sync(0xffffffffu, acc[q][e], off);
+              acc[q][e] = acc[q][e] * f0 + ao * f1;
+            }
+            m[q] = M;
           }
-          m = M;
-        }
-        if (lane < LPR) {
+          if (lane < LPR) {
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) s_red[warp * kDh + sub * EPL + e] = acc[e];
-        }
-        if (lane == 0) {
-          s_redm[warp] = m;
-          s_reds[warp] = ssum;
+            for (int e = 0; e < EPL; ++e) s_red[(q * kConsumerWarps + warp) * kDh + sub * EPL + e] = acc[q][e];
+          }
+          if (lane == 0) {
+            s_redm[q * kConsumerWarps + warp] = m[q];
+            s_reds[q * kConsumerWarps + warp] = ssum[q];
+          }
         }
         named_barrier(1, kConsumerWarps * 32);
         const long long row = static_cast<long long>(cur.b) * LH + cur.lh;
         const bool whole_row = seg_c0 == 0 && cur.c == nch - 1;
         if (tid < kDh) {
-          float M = -INFINITY;
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s_redm[w]);
-          float S = 0.f, A = 0.f;
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            const float f = rescale(s_redm[w], M);
-            S = fmaf(s_reds[w], f, S);
-            A = fmaf(s_red[w * kDh + tid], f, A);
-          }
-          if (whole_row) {
-            if (ok) p.out[row * kDh + tid] = S > 0.f ? A / S : 0.f;
-          } else {
+          long long first_owner = 0;
+          int nseg = 1, seg = 0;
+          if (!whole_row) {
             const long long grow = s_first[cur.b] + static_cast<long long>(cur.lh) * nch;   // chunk 0 of row
-            const long long first_owner = owner_of(grow, total, ranges);
-            const int nseg = static_cast<int>(owner_of(grow + nch - 1, total, ranges) - first_owner + 1);
-            const int seg = static_cast<int>(blockIdx.x - first_owner);
-            float* P = p.part + (row * p.part_stride + seg) * kPartFloats;
-            P[4 + tid] = ok ? A : 0.f;
-            if (tid == 0) {
-              P[0] = ok ? M : -INFINITY;
-              P[1] = ok ? S : 0.f;
+            first_owner = owner_of(grow, total, ranges);
+            nseg = static_cast<int>(owner_of(grow + nch - 1, total, ranges) - first_owner + 1);
+            seg = static_cast<int>(blockIdx.x - first_owner);
+          }
+          for (int q = 0; q < nq; ++q) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s_redm[q * kConsumerWarps + w]);
+            float S = 0.f, A = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+              const float f = rescale(s_redm[q * kConsumerWarps + w], M);
+              S = fmaf(s_reds[q * kConsumerWarps + w], f, S);
+              A = fmaf(s_red[(q * kConsumerWarps + w) * kDh + tid], f, A);
             }
+            if (whole_row) {
+              if (ok) p.out[qrow(cur.b, cur.lh, q) * kDh + tid] = S > 0.f ? A / S : 0.f;
+            } else {
+              float* P = p.part + ((row * nq + q) * p.part_stride + seg) * kPartFloats;
+              P[4 + tid] = ok ? A : 0.f;
+              if (tid == 0) {
+                P[0] = ok ? M : -INFINITY;
+                P[1] = ok ? S : 0.f;
+              }
+            }
+          }
+          if (!whole_row) {
             named_barrier(2, kDh);
             if (tid == 0) {
               __threadfence();
@@ -447,25 +521,30 @@ __global__ void __launch_bounds__(kThreads, CXA_DECODE_CTAS_PER_SM)
             named_barrier(2, kDh);
             if (s_flags[1]) {
               __threadfence();
-              const float* P0 = p.part + row * p.part_stride * kPartFloats;
-              float MM = -INFINITY;
-              for (int k = 0; k < nseg; ++k) MM = fmaxf(MM, __ldcg(P0 + k * kPartFloats));
-              float SS = 0.f, AA = 0.f;
-              for (int k = 0; k < nseg; ++k) {
-                const float f = rescale(__ldcg(P0 + k * kPartFloats), MM);
-                SS = fmaf(f, __ldcg(P0 + k * kPartFloats + 1), SS);
-                AA = fmaf(f, __ldcg(P0 + k * kPartFloats + 4 + tid), AA);
+              for (int q = 0; q < nq; ++q) {
+                const float* P0 = p.part + (row * nq + q) * p.part_stride * kPartFloats;
+                float MM = -INFINITY;
+                for (int k = 0; k < nseg; ++k) MM = fmaxf(MM, __ldcg(P0 + k * kPartFloats));
+                float SS = 0.f, AA = 0.f;
+                for (int k = 0; k < nseg; ++k) {
+                  const float f = rescale(__ldcg(P0 + k * kPartFloats), MM);
+                  SS = fmaf(f, __ldcg(P0 + k * kPartFloats + 1), SS);
+                  AA = fmaf(f, __ldcg(P0 + k * kPartFloats + 4 + tid), AA);
+                }
+                p.out[qrow(cur.b, cur.lh, q) * kDh + tid] = SS > 0.f ? AA / SS : 0.f;
               }
-              p.out[row * kDh + tid] = SS > 0.f ? AA / SS : 0.f;
               if (tid == 0) p.counters[row] = 0u;
             }
           }
         }
         named_barrier(1, kConsumerWarps * 32);
-        m = -INFINITY;
-        ssum = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+        for (int q = 0; q < kNQ; ++q) {
+          m[q] = -INFINITY;
+          ssum[q] = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) acc[q][e] = 0.f;
+        }
       }
       const int prev_b = cur.b, prev_lh = cur.lh;
       advance(cur, s_nch, p.B, LH);
@@ -480,35 +559,35 @@ size_t counters_bytes(int B, int L, int H) {
   return (n + 255) & ~static_cast<size_t>(255);
 }
 
-template <bool kBF16>
+template <bool kBF16, int kNQ>
 size_t dynamic_smem_bytes(int B) {
-  using R = Traits<kBF16>;
+  using R = Traits<kBF16, kNQ>;
   size_t n = static_cast<size_t>(kStages) * R::kStageBytes;
   n += 2 * kStages * sizeof(uint64_t);
   n += static_cast<size_t>(B + 1) * sizeof(long long);
   n += static_cast<size_t>(B + (B & 1)) * sizeof(int);
-  n += (kConsumerWarps * kDh + 2 * kConsumerWarps) * sizeof(float) + 4 * sizeof(int);
+  n += static_cast<size_t>(kNQ) * kConsumerWarps * (kDh + 2) * sizeof(float) + 4 * sizeof(int);
   return n;
 }
 
-template <bool kBF16>
+template <bool kBF16, int kNQ>
 cudaError_t launch(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t stream) {
   static std::mutex mu;
   static size_t attr_bytes[128] = {};
-  const size_t smem = dynamic_smem_bytes<kBF16>(prm.B);
+  const size_t smem = dynamic_smem_bytes<kBF16, kNQ>(prm.B);
   cudaError_t e;
   {
     std::lock_guard<std::mutex> lock(mu);
     const int d = dev.device >= 0 && dev.device < 128 ? dev.device : 0;
     if (attr_bytes[d] < smem) {
-      e = cudaFuncSetAttribute(decode_stream_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      e = cudaFuncSetAttribute(decode_stream_kernel<kBF16, kNQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem));
       if (e != cudaSuccess) return e;
       attr_bytes[d] = smem;
     }
   }
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<kBF16>, kThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<kBF16, kNQ>, kThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int grid = dev.num_sms * (per_sm < CXA_DECODE_CTAS_PER_SM ? per_sm : CXA_DECODE_CTAS_PER_SM);
@@ -522,14 +601,22 @@ cudaError_t launch(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t 
   attr[0].val.programmaticStreamSerializationAllowed = CXA_DECODE_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_stream_kernel<kBF16>, prm);
+  return cudaLaunchKernelEx(&cfg, decode_stream_kernel<kBF16, kNQ>, prm);
+}
+
+template <bool kBF16>
+cudaError_t launch_nq(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t stream) {
+  if (prm.nq == 1) return launch<kBF16, 1>(prm, dev, stream);
+  if (prm.nq == 2) return launch<kBF16, 2>(prm, dev, stream);
+  if (prm.nq <= 4) return launch<kBF16, 4>(prm, dev, stream);
+  return launch<kBF16, 8>(prm, dev, stream);
 }
 
 }  // namespace
 
-size_t decode_workspace_bytes(int B, int T, int L, int H) {
+size_t decode_workspace_bytes(int B, int T, int L, int H, int nq) {
   const size_t nslot = static_cast<size_t>((T + kPartChunk - 1) / kPartChunk);
-  return counters_bytes(B, L, H) + static_cast<size_t>(B) * L * H * nslot * kPartFloats * sizeof(float);
+  return counters_bytes(B, L, H) + static_cast<size_t>(B) * L * H * nq * nslot * kPartFloats * sizeof(float);
 }
 
 size_t decode_counter_bytes(int B, int L, int H) { return counters_bytes(B, L, H); }
@@ -549,9 +636,10 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStre
   prm.B = a.B;
   prm.T = a.T;
   prm.LH = a.L * a.H;
+  prm.nq = a.nq;
   prm.part_stride = (a.T + kPartChunk - 1) / kPartChunk;
   prm.qscale = a.scale * 1.4426950408889634f;   // scale * log2(e)
-  cudaError_t e = a.cache_bf16 ? launch<true>(prm, dev, stream) : launch<false>(prm, dev, stream);
+  cudaError_t e = a.cache_bf16 ? launch_nq<true>(prm, dev, stream) : launch_nq<false>(prm, dev, stream);
   if (e == cudaSuccess) count_launches(1);
   return e;
 }

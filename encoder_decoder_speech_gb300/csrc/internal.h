@@ -29,9 +29,10 @@ struct PopulateLaunch {
 struct DecodeLaunch {
   const void* Kc;
   const void* Vc;
-  const float* Q;      // [B][L][H][64]
+  const float* Q;      // [B][nq][L][H][64]
   const int* key_len;  // [B]
-  float* out;          // [B][L][H][64]
+  float* out;          // [B][nq][L][H][64]
+  int nq;              // query rows per cache row (1..8)
   void* workspace;
   int B, T, L, H;
   float scale;         // > 0
@@ -51,7 +52,7 @@ cudaError_t current_device_info(DeviceInfo* info, std::string* msg);
 
 // Workspace layout helpers shared by the size query and the launchers.
 size_t populate_workspace_bytes(int d, int L, bool in_bf16);
-size_t decode_workspace_bytes(int B, int T, int L, int H);
+size_t decode_workspace_bytes(int B, int T, int L, int H, int nq);
 
 // Launchers: enqueue on `stream`, return cudaSuccess or the first error; on a
 // non-CUDA failure (e.g. tensor-map encoding) they return cudaErrorInvalidValue

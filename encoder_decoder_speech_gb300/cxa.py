@@ -39,7 +39,14 @@ SIGNATURES = {
     "cxa_device_status": (ctypes.c_int, [ctypes.c_int]),
     "cxa_decode_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                           ctypes.c_float, ctypes.c_void_p]),
+    "cxa_decode_shared_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 6),
+    "cxa_decode_shared": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t,
+                                         ctypes.c_void_p]),
 }
+
+# most query rows cxa_decode_shared takes per cache row (CXA_MAX_SHARED_QUERIES)
+CXA_MAX_SHARED_QUERIES = 8
 
 # bytes of the fixed device scratch behind cxa_decode_noalloc (CXA_NOALLOC_SCRATCH_BYTES)
 CXA_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -124,6 +131,15 @@ def cxa_decode(handle, Q, key_len, out, scale, workspace, workspace_bytes, strea
                              workspace_bytes, _stream(stream))
 
 
+def cxa_decode_shared_workspace_bytes(B, T, L, H, dh=64, nq=1) -> int:
+    return load().cxa_decode_shared_workspace_bytes(B, T, L, H, dh, nq)
+
+
+def cxa_decode_shared(handle, nq, Q, key_len, out, scale, workspace, workspace_bytes, stream=None) -> int:
+    return load().cxa_decode_shared(handle, nq, _ptr(Q), _ptr(key_len), _ptr(out), float(scale), _ptr(workspace),
+                                    workspace_bytes, _stream(stream))
+
+
 def cxa_decode_noalloc(handle, Q, key_len, out, scale, stream=None) -> int:
     """cxa_decode with its scratch in libcxa's fixed device array: for callers
     that cannot allocate device memory. Calls must be ordered on one stream."""
@@ -182,6 +198,7 @@ class CrossAttentionCache:
         self.decode_ws_bytes = cxa_decode_workspace_bytes(B, T, L, H, dh)
         self.decode_ws = torch.zeros(max(self.decode_ws_bytes, 256), dtype=torch.uint8, device=device)
         self._pop_ws = {}
+        self._shared_ws = None
         rc, h = cxa_cache_create(self.Kc, self.Vc, B, T, L, H, dh, _DTYPES[cache_dtype])
         check(rc, "cxa_cache_create")
         self.handle = h
@@ -213,6 +230,20 @@ class CrossAttentionCache:
             out = torch.empty_like(Q)
         check(cxa_decode(self.handle, Q, key_len, out, scale, self.decode_ws, self.decode_ws_bytes, stream),
               "cxa_decode")
+        return out
+
+    def decode_shared(self, Q, key_len, out=None, scale: float = 0.0, stream=None):
+        """Q [B, nq, L, H, 64] fp32: nq hypotheses per slot sharing the slot's cache.
+        Returns out [B, nq, L, H, 64] fp32."""
+        import torch
+        nq = Q.shape[1]
+        need = cxa_decode_shared_workspace_bytes(self.B, self.T, self.L, self.H, self.dh, nq)
+        if self._shared_ws is None or self._shared_ws.numel() < need:
+            self._shared_ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=self.Kc.device)
+        if out is None:
+            out = torch.empty_like(Q)
+        check(cxa_decode_shared(self.handle, nq, Q, key_len, out, scale, self._shared_ws, self._shared_ws.numel(),
+                                stream), "cxa_decode_shared")
         return out
 
     def invalidate(self, b: int = -1) -> None:

@@ -148,6 +148,32 @@ CXA_API int cxa_decode(const cxa_cache* c, const float* Q, const int* key_len, f
                float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Shared-cache decode: nq query rows per (slot, layer, head), all attending the
+ * same cache slot -- the beam or speculative hypotheses of one audio window
+ * share its encoder memory ("Caso de estudio: WhisperKit", §3: SharedSplitKVCached
+ * attends one shared batch-1 cache from a batch-N query). Each K/V row is read
+ * once per step for all nq queries.
+ *
+ *   nq       query rows per cache row, 1 .. CXA_MAX_SHARED_QUERIES.
+ *   Q, out   device fp32 [B][nq][L][H][dh]: row (b, n, l, h) is hypothesis n of
+ *            slot b; out row (b, n, l, h) = softmax(scale * q.K[b,l,h]^T) V[b,l,h].
+ *   key_len, scale  as for cxa_decode (key_len is per slot, shared by its rows).
+ *   workspace, workspace_bytes  at least cxa_decode_shared_workspace_bytes(B, T,
+ *            L, H, dh, nq) bytes, 256-byte aligned, with the same counter rules
+ *            as cxa_decode's workspace.
+ *
+ * With nq = 1 this is exactly cxa_decode. Errors as for cxa_decode, and
+ * CXA_EINVAL for nq outside [1, CXA_MAX_SHARED_QUERIES].
+ */
+#define CXA_MAX_SHARED_QUERIES 8
+
+CXA_API size_t cxa_decode_shared_workspace_bytes(int B, int T, int L, int H, int dh, int nq);
+
+CXA_API int cxa_decode_shared(const cxa_cache* c, int nq, const float* Q, const int* key_len,
+                              float* out, float scale, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
  * Mark slot b (or every slot when b == -1) not ready: installing new encoder
  * memory invalidates the projection cache by flag ("View 3": encoder_kv_ready = 0;
  * the circuit's invalidation trigger is an encoder memory update). Host only,

@@ -22,6 +22,8 @@ What it computes, and where the pages define it:
   cross-attention operation"); padded keys are excluded, which is the exact
   limit of the additive key-padding mask, and an empty key set gives 0 by the
   clamped softmax denominator (WhisperKit case study §2 and §4).
+* ``decode_shared`` -- several query rows (hypotheses) per (slot, layer, head)
+  over the slot's one cache (WhisperKit case study §3, SharedSplitKVCached).
 * ``full_window`` -- the "whole window" formula kept as a check beside one-query
   decode ("Recurrence as feeds", "What it opened").
 
@@ -146,6 +148,19 @@ def decode_rows(Q, Kc, Vc, key_len, rows, scale: float | None = None) -> np.ndar
     n = clamp_key_len(key_len, T)
     return np.stack([attend_row(np.asarray(Q)[b, l, h], Kc[b, l, h], Vc[b, l, h], int(n[b]), scale)
                      for (b, l, h) in rows])
+
+
+def decode_shared(Q, Kc, Vc, key_len, scale: float | None = None) -> np.ndarray:
+    """nq query rows per (slot, layer, head) over the slot's one cache: the
+    beam / speculative hypotheses of one window sharing its encoder memory
+    ("Caso de estudio: WhisperKit", §3, SharedSplitKVCached: a batch-N query
+    attending a shared batch-1 cache).
+
+    Q: ``[B, nq, L, H, dh]``; returns out ``[B, nq, L, H, dh]``, hypothesis n of
+    slot b decoded exactly as ``decode`` decodes a single query row."""
+    Q = _f64(Q)
+    nq = Q.shape[1]
+    return np.stack([decode(Q[:, n], Kc, Vc, key_len, scale) for n in range(nq)], axis=1)
 
 
 def full_window(Qblock, K, V, n: int, scale: float) -> np.ndarray:

@@ -1,0 +1,87 @@
+"""Parity of cxa_decode_shared (nq hypotheses per slot attending the slot's one
+cache) with the oracle's decode_shared, kernel-isolated: the oracle decodes the
+very cache the GPU holds."""
+import numpy as np
+import pytest
+import torch
+
+from _gpu_common import DECODE_BF16_MAX_ABS, DECODE_F32_MAX_ABS, cache_for, dev, host, inputs_on_device
+from encoder_decoder_speech_gb300 import cxa
+from encoder_decoder_speech_gb300 import workloads as W
+from oracle import cross_attention as O
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": DECODE_F32_MAX_ABS, "bf16": DECODE_BF16_MAX_ABS}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cxa_lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    yield
+    torch.cuda.synchronize()
+    assert cxa.cxa_device_status(1) == cxa.CXA_OK
+
+
+def _queries(w, nq, seed):
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((w.B, nq, w.L, w.H, 64)).astype(np.float32)
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("nq", [1, 2, 3, 4, 5, 7, 8])
+def test_shared_decode_matches_oracle(nq, cache_dtype):
+    w = W.custom("shared", B=4, T=700, d=256, L=2, H=4, ragged=True, index=940)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, cache_dtype)
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    kl = h["key_len"].copy()
+    kl[2] = 0                                   # an empty slot gets zeros
+    Q = _queries(w, nq, nq)
+    out = host(c.decode_shared(dev(Q), dev(kl, torch.int32)))
+    ref = O.decode_shared(Q, host(c.Kc), host(c.Vc), kl)
+    assert np.abs(out - ref).max() <= TOL[cache_dtype]
+    assert np.all(out[2] == 0.0)
+
+
+def test_shared_decode_with_one_query_is_decode():
+    w = W.custom("shared1", B=3, T=500, d=128, L=3, H=2, ragged=True, index=941)
+    d, _ = inputs_on_device(w)
+    c = cache_for(w, "f32")
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    Q = dev(W.make_Q(w, 0))
+    a = c.decode(Q, d["key_len"])
+    b = c.decode_shared(Q[:, None].contiguous(), d["key_len"])[:, 0]
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_shared_decode_back_to_back_and_invalid_nq():
+    w = W.custom("shared_b2b", B=2, T=1300, d=512, L=2, H=8, ragged=True, index=942)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, "bf16")
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    Qs = [_queries(w, 5, 50 + s) for s in range(6)]
+    outs = [c.decode_shared(dev(q), d["key_len"]) for q in Qs]
+    torch.cuda.synchronize()
+    K, V = host(c.Kc), host(c.Vc)
+    for q, o in zip(Qs, outs):
+        assert np.abs(host(o) - O.decode_shared(q, K, V, h["key_len"])).max() <= DECODE_BF16_MAX_ABS
+    Q9 = dev(_queries(w, 9, 1))
+    out = torch.empty_like(Q9)
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    assert cxa.cxa_decode_shared(c.handle, 9, Q9, d["key_len"], out, 0.0, ws, ws.numel()) == cxa.CXA_EINVAL
+    assert cxa.cxa_decode_shared(c.handle, 0, Q9, d["key_len"], out, 0.0, ws, ws.numel()) == cxa.CXA_EINVAL
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+def test_batched_base_beam5(cache_dtype):
+    """Batched Whisper-Base with 5 hypotheses per memory (a beam of 5), all rows."""
+    w = W.WORKLOADS["batched_base"]
+    d, h = inputs_on_device(w)
+    c = cache_for(w, cache_dtype)
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    Q = _queries(w, 5, 7)
+    out = host(c.decode_shared(dev(Q), d["key_len"]))
+    ref = O.decode_shared(Q, host(c.Kc), host(c.Vc), h["key_len"])
+    assert np.abs(out - ref).max() <= TOL[cache_dtype]

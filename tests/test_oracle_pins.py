@@ -214,6 +214,28 @@ def pin_scale_on_scores():
     return float(max(np.abs(a - b).max(), np.abs(c - d).max()))
 
 
+def pin_shared_decode():
+    """Shared-cache decode: the nq rows of each (slot, layer, head) equal the
+    full-window matrix formula on that block of queries, and brute force."""
+    B, nq, L, H, T, dh = 2, 5, 2, 2, 9, 64
+    Q = _rand((B, nq, L, H, dh), 100)
+    Kc, Vc = _rand((B, L, H, T, dh), 101), _rand((B, L, H, T, dh), 102)
+    kl = np.array([9, 4])
+    out = O.decode_shared(Q, Kc, Vc, kl)
+    err = 0.0
+    for b in range(B):
+        for l in range(L):
+            for h in range(H):
+                full = O.full_window(Q[b, :, l, h], Kc[b, l, h], Vc[b, l, h], int(kl[b]), 0.125)
+                err = max(err, float(np.abs(out[b, :, l, h] - full).max()))
+                for n in (0, nq - 1):
+                    bf = bf_attend(Q[b, n, l, h], Kc[b, l, h], Vc[b, l, h], int(kl[b]), 0.125)
+                    err = max(err, float(np.abs(out[b, n, l, h] - np.array(bf)).max()))
+    one = O.decode_shared(Q[:, :1], Kc, Vc, kl)[:, 0]
+    err = max(err, float(np.abs(one - O.decode(Q[:, 0], Kc, Vc, kl)).max()))
+    return err
+
+
 # ---------------------------------------------------------------------------
 # the pins on the real oracle
 # ---------------------------------------------------------------------------
@@ -251,6 +273,10 @@ def test_token_major_cache_gives_a_different_answer():
 
 def test_scale_applies_to_scores():
     assert pin_scale_on_scores() < 1e-13
+
+
+def test_shared_decode_matches_full_window_and_bruteforce():
+    assert pin_shared_decode() < 1e-12
 
 
 def test_geometry_fails_closed():
@@ -349,7 +375,7 @@ def _mut_missing_scale(monkeypatch):
 
 def _all_pins_pass():
     return (pin_populate_bruteforce() < 1e-12 and pin_decode_bruteforce() < 1e-12
-            and pin_closed_forms() < 1e-12 and pin_full_window() < 1e-13
+            and pin_closed_forms() < 1e-12 and pin_full_window() < 1e-13 and pin_shared_decode() < 1e-12
             and pin_layout_offset() == 0 and pin_scale_on_scores() < 1e-13)
 
 
