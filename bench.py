@@ -54,6 +54,9 @@ def parse_args(argv=None):
     p.add_argument("--shared", action="store_true",
                    help="time shared-cache decode (nq hypotheses per memory) on the batched Whisper-Base "
                         "workload for nq = 1, 2, 4, 5, 8; one JSON line per (nq, cache dtype)")
+    p.add_argument("--block", action="store_true",
+                   help="time the per-layer cross-attention block (LayerNorm, Q projection, attention, out "
+                        "projection + residual) for all 6 layers of a batched Whisper-Base decode step")
     p.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--budget-s", type=float, default=12.0, help=argparse.SUPPRESS)
     p.add_argument("--max-slots", type=int, default=16, help=argparse.SUPPRESS)
@@ -524,6 +527,75 @@ def run_shared(args):
     return 0
 
 
+def run_block(args):
+    """One decoder step of batched Whisper-Base through the per-layer entry point:
+    for l = 0..5, x = x + CrossAttn_l(LayerNorm(x)) (cxa_cross_block), fp32 weights."""
+    import numpy as np
+    import torch
+    from encoder_decoder_speech_gb300 import _build, cxa
+    from encoder_decoder_speech_gb300 import workloads as W
+    _build.build_library()
+    cxa.load()
+    torch.cuda.set_device(0)
+    peaks = load_peaks()
+    w = W.WORKLOADS[WORKLOAD]
+    (E, WK, WV, bV, kl, _, kl_h), _ = device_inputs(torch, W, w, 0)
+    rng = np.random.default_rng(5)
+
+    def t(shape, std):
+        return torch.from_numpy((rng.standard_normal(shape) * std).astype(np.float32)).to("cuda")
+
+    prm = [dict(WQ=t((w.d, w.d), w.d ** -0.5), WO=t((w.d, w.d), w.d ** -0.5), g=1 + t((w.d,), 0.1),
+                b=t((w.d,), 0.1), bQ=t((w.d,), 0.02), bO=t((w.d,), 0.02)) for _ in range(w.L)]
+    for cd, esz in (("f32", 4), ("bf16", 2)):
+        cache = cxa.CrossAttentionCache(w.B, w.T, w.L, w.H, w.dh, cd)
+        cache.populate(E, WK, WV, bV)
+        x = t((w.B, w.d), 1.0)
+
+        def step():
+            for l in range(w.L):
+                p = prm[l]
+                cache.cross_block(l, x, p["WQ"], p["WO"], kl, ln_gamma=p["g"], ln_beta=p["b"], bQ=p["bQ"], bO=p["bO"])
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        byts = decode_bytes(w.L, w.H, w.dh, esz, kl_h, w.B) + w.L * 2 * w.d * w.d * 4 + w.L * 3 * w.B * w.d * 4
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # launched one call at a time from Python, then replayed as one captured CUDA graph per step
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
+        for mode in ("eager", "graph"):
+            run = step if mode == "eager" else graph.replay
+            for _ in range(args.warmup):
+                run()
+            torch.cuda.synchronize()
+            a.record()
+            for _ in range(args.steps):
+                run()
+            b_.record()
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b_) * 1000.0 / args.steps
+            print(json.dumps({"cross_block_step": {"workload": "batched-whisper-base", "layers": w.L,
+                                                   "cache_dtype": cd, "launch": mode},
+                              "us_per_step": round(us, 2), "tokens_per_s": round(w.B / (us * 1e-6), 1),
+                              "GBps": round(byts / (us * 1e-6) / 1e9, 1),
+                              "frac_of_measured_hbm": round(byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 3),
+                              "kernels_per_step": 3 * w.L}), flush=True)
+        del graph
+        cache.close()
+    assert cxa.cxa_device_status(1) == cxa.CXA_OK
+    return 0
+
+
 def run_profile(args):
     """A handful of launches of one kernel on the bench workload's inputs, for
     Nsight Compute: one populate (weight repack + GEMM), then two more populate
@@ -649,6 +721,8 @@ def main(argv=None):
         return run_sweep(args)
     if args.shared:
         return run_shared(args)
+    if args.block:
+        return run_block(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_cxa(args)

@@ -210,10 +210,13 @@ int cxa_populate(cxa_cache* c, int b0, int nb, const void* E, const void* WK, co
   return CXA_OK;
 }
 
-static int decode_common(const char* who, const cxa_cache* c, int nq, const float* Q, const int* key_len,
-                         float* out, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+static int decode_common(const char* who, const cxa_cache* c, int l0, int nl, int nq, const float* Q,
+                         const int* key_len, float* out, float scale, void* workspace, size_t workspace_bytes,
+                         void* stream) {
   const std::string w(who);
   if (c == nullptr) return fail(CXA_EINVAL, w + ": cache descriptor is NULL");
+  if (nl == -1) nl = c->L;
+  if (l0 < 0 || nl < 1 || l0 + nl > c->L) return fail(CXA_EINVAL, w + ": layers [l0, l0+nl) out of range");
   if (nq < 1 || nq > CXA_MAX_SHARED_QUERIES)
     return fail(CXA_EINVAL, w + ": nq must be in [1, " + std::to_string(CXA_MAX_SHARED_QUERIES) + "]");
   if (Q == nullptr || key_len == nullptr || out == nullptr || workspace == nullptr)
@@ -223,7 +226,7 @@ static int decode_common(const char* who, const cxa_cache* c, int nq, const floa
   if (static_cast<const void*>(Q) == static_cast<const void*>(out))
     return fail(CXA_EINVAL, w + ": out must not alias Q");
   if (!std::isfinite(scale)) return fail(CXA_EINVAL, w + ": scale must be finite");
-  if (workspace_bytes < cxa::decode_workspace_bytes(c->B, c->T, c->L, c->H, nq))
+  if (workspace_bytes < cxa::decode_workspace_bytes(c->B, c->T, nl, c->H, nq))
     return fail(CXA_EINVAL, w + ": workspace smaller than the decode workspace size query");
   for (int b = 0; b < c->B; ++b)
     if (!c->ready[static_cast<size_t>(b)])
@@ -242,6 +245,8 @@ static int decode_common(const char* who, const cxa_cache* c, int nq, const floa
   a.key_len = key_len;
   a.out = out;
   a.nq = nq;
+  a.l0 = l0;
+  a.nl = nl;
   a.workspace = workspace;
   a.B = c->B;
   a.T = c->T;
@@ -256,12 +261,73 @@ static int decode_common(const char* who, const cxa_cache* c, int nq, const floa
 
 int cxa_decode(const cxa_cache* c, const float* Q, const int* key_len, float* out, float scale,
                void* workspace, size_t workspace_bytes, void* stream) {
-  return decode_common("cxa_decode", c, 1, Q, key_len, out, scale, workspace, workspace_bytes, stream);
+  return decode_common("cxa_decode", c, 0, -1, 1, Q, key_len, out, scale, workspace, workspace_bytes, stream);
+}
+
+int cxa_decode_layers(const cxa_cache* c, int l0, int nl, const float* Q, const int* key_len, float* out,
+                      float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (nl < 1) return fail(CXA_EINVAL, "cxa_decode_layers: nl must be >= 1");
+  return decode_common("cxa_decode_layers", c, l0, nl, 1, Q, key_len, out, scale, workspace, workspace_bytes,
+                       stream);
 }
 
 int cxa_decode_shared(const cxa_cache* c, int nq, const float* Q, const int* key_len, float* out,
                       float scale, void* workspace, size_t workspace_bytes, void* stream) {
-  return decode_common("cxa_decode_shared", c, nq, Q, key_len, out, scale, workspace, workspace_bytes, stream);
+  return decode_common("cxa_decode_shared", c, 0, -1, nq, Q, key_len, out, scale, workspace, workspace_bytes,
+                       stream);
+}
+
+size_t cxa_cross_block_workspace_bytes(int B, int T, int L, int H, int dh) {
+  if (B <= 0 || T <= 0 || L <= 0 || H <= 0 || dh != 64) return 0;
+  return cxa::block_workspace_bytes(B, T, H);
+}
+
+int cxa_cross_block(const cxa_cache* c, int layer, float* x, const float* ln_gamma, const float* ln_beta,
+                    float ln_eps, const float* WQ, const float* bQ, const float* WO, const float* bO,
+                    const int* key_len, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (c == nullptr) return fail(CXA_EINVAL, "cxa_cross_block: cache descriptor is NULL");
+  if (layer < 0 || layer >= c->L) return fail(CXA_EINVAL, "cxa_cross_block: layer out of range");
+  if (x == nullptr || WQ == nullptr || WO == nullptr || key_len == nullptr || workspace == nullptr)
+    return fail(CXA_EINVAL, "cxa_cross_block: a required pointer argument is NULL");
+  if (!aligned(x, 16) || !aligned(WQ, 16) || !aligned(WO, 16) || !aligned(workspace, 256) || !aligned(key_len, 4))
+    return fail(CXA_EINVAL, "cxa_cross_block: x, WQ and WO must be 16-byte aligned, the workspace 256-byte aligned");
+  if (!std::isfinite(scale) || !std::isfinite(ln_eps) || ln_eps < 0.f)
+    return fail(CXA_EINVAL, "cxa_cross_block: scale and ln_eps must be finite, ln_eps >= 0");
+  if (workspace_bytes < cxa::block_workspace_bytes(c->B, c->T, c->H))
+    return fail(CXA_EINVAL, "cxa_cross_block: workspace smaller than cxa_cross_block_workspace_bytes()");
+  for (int b = 0; b < c->B; ++b)
+    if (!c->ready[static_cast<size_t>(b)])
+      return fail(CXA_ENOTREADY, "cxa_cross_block: slot " + std::to_string(b) + " is not populated");
+  std::string msg;
+  cxa::DeviceInfo dev;
+  cudaError_t e = cxa::current_device_info(&dev, &msg);
+  if (e != cudaSuccess) return fail_cuda(e, "cxa_cross_block: " + msg);
+  cxa::BlockLaunch a;
+  a.Kc = c->Kc;
+  a.Vc = c->Vc;
+  a.x = x;
+  a.gamma = ln_gamma;
+  a.beta = ln_beta;
+  a.eps = ln_eps;
+  a.WQ = WQ;
+  a.bQ = bQ;
+  a.WO = WO;
+  a.bO = bO;
+  a.key_len = key_len;
+  a.workspace = workspace;
+  a.B = c->B;
+  a.T = c->T;
+  a.L = c->L;
+  a.H = c->H;
+  a.layer = layer;
+  a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(c->dh));
+  a.cache_bf16 = c->dtype == CXA_BF16;
+  e = cxa::launch_block(a, dev, static_cast<cudaStream_t>(stream), &msg);
+  if (e != cudaSuccess) {
+    if (!msg.empty()) return fail(CXA_EINVAL, "cxa_cross_block: " + msg);
+    return fail_cuda(e, "cxa_cross_block: launch");
+  }
+  return CXA_OK;
 }
 
 int cxa_invalidate(cxa_cache* c, int b) {

@@ -109,7 +109,9 @@ struct DecodeParams {
   float* part;
   unsigned int* counters;
   unsigned int* status;
-  int B, T, LH;
+  int B, T, LH;        // LH = rows per slot in this call (layers [l0, l0+nl) x H)
+  int LHc;             // rows per slot in the cache (L x H)
+  int lh0;             // first cache row of the call within a slot (l0 x H)
   int nq;              // query rows per cache row (<= kNQ)
   int part_stride;     // partial slots per (row, query) (ceil(T / 64))
   float qscale;        // scale * log2(e)
@@ -275,8 +277,8 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
     for (long long i = 0; i < npre; ++i) {
       const int kl = min(max(__ldg(p.key_len + c.b), 0), p.T);
       const int n = min(R::kChunkKeys, kl - c.c * R::kChunkKeys);
-      const long long row = static_cast<long long>(c.b) * LH + c.lh;
-      const size_t off = (static_cast<size_t>(row) * p.T + static_cast<size_t>(c.c) * R::kChunkKeys) * R::kRowBytes;
+      const long long crow = static_cast<long long>(c.b) * p.LHc + p.lh0 + c.lh;   // cache row
+      const size_t off = (static_cast<size_t>(crow) * p.T + static_cast<size_t>(c.c) * R::kChunkKeys) * R::kRowBytes;
       const uint32_t kv_bytes = static_cast<uint32_t>(n) * R::kRowBytes;
       const uint32_t full = smem_u32(&bars[i]);
       const uint32_t dst = smem_u32(stages + i * R::kStageBytes);
@@ -324,8 +326,8 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
         const int kl = min(max(__ldg(p.key_len + cur.b), 0), p.T);
         const int t0 = cur.c * R::kChunkKeys;
         const int n = min(R::kChunkKeys, kl - t0);
-        const long long row = static_cast<long long>(cur.b) * LH + cur.lh;
-        const size_t off = (static_cast<size_t>(row) * p.T + t0) * R::kRowBytes;
+        const long long crow = static_cast<long long>(cur.b) * p.LHc + p.lh0 + cur.lh;   // cache row
+        const size_t off = (static_cast<size_t>(crow) * p.T + t0) * R::kRowBytes;
         const uint32_t kv_bytes = static_cast<uint32_t>(n) * R::kRowBytes;
         const uint32_t full = smem_u32(&bars[s]);
         const uint32_t dst = smem_u32(stages + s * R::kStageBytes);
@@ -523,13 +525,16 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
               __threadfence();
               for (int q = 0; q < nq; ++q) {
                 const float* P0 = p.part + (row * nq + q) * p.part_stride * kPartFloats;
-                float MM = -INFINITY;
-                for (int k = 0; k < nseg; ++k) MM = fmaxf(MM, __ldcg(P0 + k * kPartFloats));
-                float SS = 0.f, AA = 0.f;
+                float MM = -INFINITY, SS = 0.f, AA = 0.f;   // one pass, rescaling as the max grows
                 for (int k = 0; k < nseg; ++k) {
-                  const float f = rescale(__ldcg(P0 + k * kPartFloats), MM);
-                  SS = fmaf(f, __ldcg(P0 + k * kPartFloats + 1), SS);
-                  AA = fmaf(f, __ldcg(P0 + k * kPartFloats + 4 + tid), AA);
+                  const float mk = __ldcg(P0 + k * kPartFloats);
+                  const float sk = __ldcg(P0 + k * kPartFloats + 1);
+                  const float ak = __ldcg(P0 + k * kPartFloats + 4 + tid);
+                  const float M2 = fmaxf(MM, mk);
+                  const float f0 = rescale(MM, M2), f1 = rescale(mk, M2);
+                  SS = SS * f0 + sk * f1;
+                  AA = AA * f0 + ak * f1;
+                  MM = M2;
                 }
                 p.out[qrow(cur.b, cur.lh, q) * kDh + tid] = SS > 0.f ? AA / SS : 0.f;
               }
@@ -631,11 +636,13 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStre
   prm.key_len = a.key_len;
   prm.out = a.out;
   prm.counters = static_cast<unsigned int*>(a.workspace);
-  prm.part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + counters_bytes(a.B, a.L, a.H));
+  prm.part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + counters_bytes(a.B, a.nl, a.H));
   prm.status = dev.status_word;
   prm.B = a.B;
   prm.T = a.T;
-  prm.LH = a.L * a.H;
+  prm.LH = a.nl * a.H;
+  prm.LHc = a.L * a.H;
+  prm.lh0 = a.l0 * a.H;
   prm.nq = a.nq;
   prm.part_stride = (a.T + kPartChunk - 1) / kPartChunk;
   prm.qscale = a.scale * 1.4426950408889634f;   // scale * log2(e)

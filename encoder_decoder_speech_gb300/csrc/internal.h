@@ -33,9 +33,29 @@ struct DecodeLaunch {
   const int* key_len;  // [B]
   float* out;          // [B][nq][L][H][64]
   int nq;              // query rows per cache row (1..8)
+  int l0, nl;          // decoded layers [l0, l0 + nl) of the cache's L
   void* workspace;
   int B, T, L, H;
   float scale;         // > 0
+  bool cache_bf16;
+};
+
+// One decoder layer's cross-attention block for one step (see block.cu).
+struct BlockLaunch {
+  const void* Kc;
+  const void* Vc;
+  float* x;              // [B][d] residual stream, updated in place
+  const float* gamma;    // [d] or NULL (1)
+  const float* beta;     // [d] or NULL (0)
+  float eps;
+  const float* WQ;       // [d][d] (d_in, d_out)
+  const float* bQ;       // [d] or NULL
+  const float* WO;       // [d][d]
+  const float* bO;       // [d] or NULL
+  const int* key_len;    // [B]
+  void* workspace;
+  int B, T, L, H, layer;
+  float scale;
   bool cache_bf16;
 };
 
@@ -61,6 +81,8 @@ cudaError_t launch_populate(const PopulateLaunch& a, const DeviceInfo& dev, cuda
                             std::string* msg);
 cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStream_t stream,
                           std::string* msg);
+cudaError_t launch_block(const BlockLaunch& a, const DeviceInfo& dev, cudaStream_t stream, std::string* msg);
+size_t block_workspace_bytes(int B, int T, int H);
 
 // Bytes at the start of a decode workspace that hold the per-row arrival
 // counters (the part that must be zero before a decode kernel starts).

@@ -43,6 +43,14 @@ SIGNATURES = {
     "cxa_decode_shared": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                          ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t,
                                          ctypes.c_void_p]),
+    "cxa_decode_layers": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
+                                         ctypes.c_size_t, ctypes.c_void_p]),
+    "cxa_cross_block_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 5),
+    "cxa_cross_block": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
+                                       ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
 }
 
 # most query rows cxa_decode_shared takes per cache row (CXA_MAX_SHARED_QUERIES)
@@ -140,6 +148,22 @@ def cxa_decode_shared(handle, nq, Q, key_len, out, scale, workspace, workspace_b
                                     workspace_bytes, _stream(stream))
 
 
+def cxa_decode_layers(handle, l0, nl, Q, key_len, out, scale, workspace, workspace_bytes, stream=None) -> int:
+    return load().cxa_decode_layers(handle, l0, nl, _ptr(Q), _ptr(key_len), _ptr(out), float(scale),
+                                    _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def cxa_cross_block_workspace_bytes(B, T, L, H, dh=64) -> int:
+    return load().cxa_cross_block_workspace_bytes(B, T, L, H, dh)
+
+
+def cxa_cross_block(handle, layer, x, ln_gamma, ln_beta, ln_eps, WQ, bQ, WO, bO, key_len, scale, workspace,
+                    workspace_bytes, stream=None) -> int:
+    return load().cxa_cross_block(handle, layer, _ptr(x), _ptr(ln_gamma), _ptr(ln_beta), float(ln_eps), _ptr(WQ),
+                                  _ptr(bQ), _ptr(WO), _ptr(bO), _ptr(key_len), float(scale), _ptr(workspace),
+                                  workspace_bytes, _stream(stream))
+
+
 def cxa_decode_noalloc(handle, Q, key_len, out, scale, stream=None) -> int:
     """cxa_decode with its scratch in libcxa's fixed device array: for callers
     that cannot allocate device memory. Calls must be ordered on one stream."""
@@ -199,6 +223,7 @@ class CrossAttentionCache:
         self.decode_ws = torch.zeros(max(self.decode_ws_bytes, 256), dtype=torch.uint8, device=device)
         self._pop_ws = {}
         self._shared_ws = None
+        self._block_ws = None
         rc, h = cxa_cache_create(self.Kc, self.Vc, B, T, L, H, dh, _DTYPES[cache_dtype])
         check(rc, "cxa_cache_create")
         self.handle = h
@@ -245,6 +270,26 @@ class CrossAttentionCache:
         check(cxa_decode_shared(self.handle, nq, Q, key_len, out, scale, self._shared_ws, self._shared_ws.numel(),
                                 stream), "cxa_decode_shared")
         return out
+
+    def decode_layers(self, l0: int, Q, key_len, out=None, scale: float = 0.0, stream=None):
+        """Q [B, nl, H, 64] fp32 for layers [l0, l0+nl). Returns out of the same shape."""
+        import torch
+        if out is None:
+            out = torch.empty_like(Q)
+        check(cxa_decode_layers(self.handle, l0, Q.shape[1], Q, key_len, out, scale, self.decode_ws,
+                                self.decode_ws_bytes, stream), "cxa_decode_layers")
+        return out
+
+    def cross_block(self, layer: int, x, WQ, WO, key_len, ln_gamma=None, ln_beta=None, ln_eps: float = 1e-5,
+                    bQ=None, bO=None, scale: float = 0.0, stream=None):
+        """One decoder layer's cross-attention block, in place on x [B, d] fp32."""
+        import torch
+        need = cxa_cross_block_workspace_bytes(self.B, self.T, self.L, self.H, self.dh)
+        if self._block_ws is None or self._block_ws.numel() < need:
+            self._block_ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=self.Kc.device)
+        check(cxa_cross_block(self.handle, layer, x, ln_gamma, ln_beta, ln_eps, WQ, bQ, WO, bO, key_len, scale,
+                              self._block_ws, self._block_ws.numel(), stream), "cxa_cross_block")
+        return x
 
     def invalidate(self, b: int = -1) -> None:
         check(cxa_invalidate(self.handle, b), "cxa_invalidate")

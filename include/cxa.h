@@ -174,6 +174,47 @@ CXA_API int cxa_decode_shared(const cxa_cache* c, int nq, const float* Q, const 
                               void* stream);
 
 /*
+ * Decode layers [l0, l0 + nl) only: the per-layer form a real decoder calls
+ * between its other sub-layers (the trace page's decoder body interleaves
+ * cross_attn with the self-attention and MLP of each layer).
+ *
+ *   Q, out   device fp32 [B][nl][H][dh]: row (b, i, h) is layer l0 + i.
+ *   workspace  at least cxa_decode_workspace_bytes(B, T, nl, H, dh) bytes.
+ * Otherwise as cxa_decode; CXA_EINVAL unless 0 <= l0 and l0 + nl <= L.
+ */
+CXA_API int cxa_decode_layers(const cxa_cache* c, int l0, int nl, const float* Q, const int* key_len,
+                              float* out, float scale, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
+ * The cross-attention block of one decoder layer for one decode step, in place
+ * on the decoder's residual stream x ("Whisper: Trace One Encoder Tensor into
+ * Every Decoder Layer", "The concept": Q_l = decoder_hidden_l x WQ_l, and the
+ * decoder body's cross_attn_norm -> cross_q_proj -> cross_attn -> cross_out_proj):
+ *
+ *   h = LayerNorm(x[b]) over d     (biased variance, ln_eps; ln_gamma/ln_beta
+ *                                   may be NULL for 1 / 0)
+ *   q = h x WQ + bQ                (bQ may be NULL)
+ *   a = attention of q over layer `layer`'s cached K/V (as cxa_decode_layers)
+ *   x[b] = x[b] + a x WO + bO      (bO may be NULL)
+ *
+ *   x        device fp32 [B][d], 16-byte aligned, read and overwritten.
+ *   WQ, WO   device fp32 [d][d] indexed (d_in, d_out), like WK and WV; 16-byte
+ *            aligned. d must be a multiple of 32 and at most 1280.
+ *   ln_gamma, ln_beta, bQ, bO  device fp32 [d].
+ *   workspace  at least cxa_cross_block_workspace_bytes(B, T, L, H, dh) bytes,
+ *            256-byte aligned (decode scratch, q and a), counters zero as for
+ *            cxa_decode.
+ * Errors as for cxa_decode, and CXA_EINVAL for a layer out of range.
+ */
+CXA_API size_t cxa_cross_block_workspace_bytes(int B, int T, int L, int H, int dh);
+
+CXA_API int cxa_cross_block(const cxa_cache* c, int layer, float* x, const float* ln_gamma,
+                            const float* ln_beta, float ln_eps, const float* WQ, const float* bQ,
+                            const float* WO, const float* bO, const int* key_len, float scale,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Mark slot b (or every slot when b == -1) not ready: installing new encoder
  * memory invalidates the projection cache by flag ("View 3": encoder_kv_ready = 0;
  * the circuit's invalidation trigger is an encoder memory update). Host only,

@@ -24,6 +24,10 @@ What it computes, and where the pages define it:
   clamped softmax denominator (WhisperKit case study §2 and §4).
 * ``decode_shared`` -- several query rows (hypotheses) per (slot, layer, head)
   over the slot's one cache (WhisperKit case study §3, SharedSplitKVCached).
+* ``decode_layers`` / ``layer_norm`` / ``cross_block`` -- the per-layer form a
+  decoder calls: LayerNorm, Q projection, attention over one layer's cache, out
+  projection and residual ("The concept": Q_l = decoder_hidden_l x WQ_l and the
+  cross_attn_norm -> cross_q_proj -> cross_attn -> cross_out_proj operations).
 * ``full_window`` -- the "whole window" formula kept as a check beside one-query
   decode ("Recurrence as feeds", "What it opened").
 
@@ -171,6 +175,47 @@ def full_window(Qblock, K, V, n: int, scale: float) -> np.ndarray:
     P = np.exp(S)
     P = P / P.sum(axis=1, keepdims=True)
     return P @ V[:n]
+
+
+def decode_layers(Q, Kc, Vc, key_len, l0: int, scale: float | None = None) -> np.ndarray:
+    """Decode of layers [l0, l0 + nl) only: Q ``[B, nl, H, dh]`` -> out of the same shape."""
+    Q = _f64(Q)
+    nl = Q.shape[1]
+    return decode(Q, np.asarray(Kc)[:, l0:l0 + nl], np.asarray(Vc)[:, l0:l0 + nl], key_len, scale)
+
+
+def layer_norm(x, gamma=None, beta=None, eps: float = 1e-5) -> np.ndarray:
+    """LayerNorm over the last axis with the biased variance (the cross_attn_norm
+    of the decoder body, "The concept"; the pages name the norm, its form is
+    Whisper's LayerNorm)."""
+    x = _f64(x)
+    mean = x.mean(axis=-1, keepdims=True)
+    var = ((x - mean) ** 2).mean(axis=-1, keepdims=True)
+    y = (x - mean) / np.sqrt(var + eps)
+    if gamma is not None:
+        y = y * _f64(gamma)
+    if beta is not None:
+        y = y + _f64(beta)
+    return y
+
+
+def cross_block(x, layer: int, Kc, Vc, key_len, WQ, WO, gamma=None, beta=None, eps: float = 1e-5,
+                bQ=None, bO=None, scale: float | None = None) -> np.ndarray:
+    """One decoder layer's cross-attention block for one step ("The concept":
+    Q_l = decoder_hidden_l x WQ_l; cross_attn_norm -> cross_q_proj -> cross_attn
+    -> cross_out_proj), with the residual add: returns the new x ``[B, d]``."""
+    x = _f64(x)
+    B, d = x.shape
+    H = np.shape(Kc)[2]
+    dh = d // H
+    q = layer_norm(x, gamma, beta, eps) @ _f64(WQ)
+    if bQ is not None:
+        q = q + _f64(bQ)
+    a = decode_layers(q.reshape(B, 1, H, dh), Kc, Vc, key_len, layer, scale).reshape(B, d)
+    y = a @ _f64(WO)
+    if bO is not None:
+        y = y + _f64(bO)
+    return x + y
 
 
 def cross_attention_from_memory(Q, E, WK, WV, bV, key_len, H: int, scale: float | None = None):

@@ -236,6 +236,46 @@ def pin_shared_decode():
     return err
 
 
+def bf_layer_norm(x, gamma, beta, eps):
+    x = list(x)
+    d = len(x)
+    mean = math.fsum(x) / d
+    var = math.fsum((v - mean) ** 2 for v in x) / d
+    return [(v - mean) / math.sqrt(var + eps) * g + b for v, g, b in zip(x, gamma, beta)]
+
+
+def pin_cross_block():
+    """LayerNorm closed forms; the block against a pure-Python restatement
+    (fsum sums); WO = 0 leaves x unchanged; decode_layers equals decode on the
+    layer slice."""
+    errs = []
+    # LayerNorm: constant row -> beta; normalised row has mean 0, variance 1
+    errs.append(np.abs(O.layer_norm(np.full((1, 8), 3.0), np.ones(8), np.arange(8.0), 1e-5) - np.arange(8.0)).max())
+    y = O.layer_norm(_rand((3, 64), 110), eps=0.0)
+    errs.append(np.abs(y.mean(axis=1)).max())
+    errs.append(np.abs(y.var(axis=1) - 1.0).max())
+    B, L, H, T, dh = 2, 3, 2, 6, 64
+    d = H * dh
+    Kc, Vc = _rand((B, L, H, T, dh), 111), _rand((B, L, H, T, dh), 112)
+    x = _rand((B, d), 113)
+    WQ, WO = _rand((d, d), 114, d ** -0.5), _rand((d, d), 115, d ** -0.5)
+    g, be, bQ, bO = _rand((d,), 116), _rand((d,), 117), _rand((d,), 118), _rand((d,), 119)
+    kl = np.array([6, 4])
+    out = O.cross_block(x, 1, Kc, Vc, kl, WQ, WO, g, be, 1e-5, bQ, bO)
+    for b in range(B):
+        hb = bf_layer_norm(x[b], g, be, 1e-5)
+        q = [math.fsum(hb[i] * WQ[i][j] for i in range(d)) + bQ[j] for j in range(d)]
+        a = []
+        for h in range(H):
+            a += bf_attend(q[h * dh:(h + 1) * dh], Kc[b, 1, h], Vc[b, 1, h], int(kl[b]), 0.125)
+        ref = [x[b][j] + math.fsum(a[i] * WO[i][j] for i in range(d)) + bO[j] for j in range(d)]
+        errs.append(np.abs(out[b] - np.array(ref)).max())
+    errs.append(np.abs(O.cross_block(x, 2, Kc, Vc, kl, WQ, np.zeros((d, d))) - x).max())
+    Ql = _rand((B, 2, H, dh), 120)
+    errs.append(np.abs(O.decode_layers(Ql, Kc, Vc, kl, 1) - O.decode(Ql, Kc[:, 1:3], Vc[:, 1:3], kl)).max())
+    return float(max(errs))
+
+
 # ---------------------------------------------------------------------------
 # the pins on the real oracle
 # ---------------------------------------------------------------------------
@@ -277,6 +317,10 @@ def test_scale_applies_to_scores():
 
 def test_shared_decode_matches_full_window_and_bruteforce():
     assert pin_shared_decode() < 1e-12
+
+
+def test_cross_block_layer_norm_and_projections():
+    assert pin_cross_block() < 1e-11
 
 
 def test_geometry_fails_closed():
