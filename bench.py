@@ -57,6 +57,9 @@ def parse_args(argv=None):
     p.add_argument("--block", action="store_true",
                    help="time the per-layer cross-attention block (LayerNorm, Q projection, attention, out "
                         "projection + residual) for all 6 layers of a batched Whisper-Base decode step")
+    p.add_argument("--selfattn", action="store_true",
+                   help="time the self-attention KV-cache step (append + decode over positions 0..pos) over a "
+                        "full 448-token sequence of the batched Whisper-Base decoder (16 slots, 6 layers, 8x64)")
     p.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--budget-s", type=float, default=12.0, help=argparse.SUPPRESS)
     p.add_argument("--max-slots", type=int, default=16, help=argparse.SUPPRESS)
@@ -596,6 +599,50 @@ def run_block(args):
     return 0
 
 
+def run_selfattn(args):
+    """Self-attention KV cache (max_seq_len 448): one token step = append the new
+    K/V row at position pos in every (slot, layer, head), then decode positions
+    0..pos. A whole 448-step sequence is timed (CUDA events around all steps) and
+    reported per step; bytes = K/V rows read + new rows written + Q and out."""
+    import numpy as np
+    import torch
+    from encoder_decoder_speech_gb300 import _build, cxa
+    from encoder_decoder_speech_gb300 import workloads as W
+    _build.build_library()
+    cxa.load()
+    torch.cuda.set_device(0)
+    peaks = load_peaks()
+    B, L, H, T = 16, 6, 8, 448
+    rng = np.random.default_rng(11)
+    Qs = torch.from_numpy(rng.standard_normal((T, B, L, H, 64)).astype(np.float32)).to("cuda")
+    Ks = torch.from_numpy(rng.standard_normal((T, B, L, H, 64)).astype(np.float32)).to("cuda")
+    Vs = torch.from_numpy(rng.standard_normal((T, B, L, H, 64)).astype(np.float32)).to("cuda")
+    pos = [torch.full((B,), s, dtype=torch.int32, device="cuda") for s in range(T)]
+    for cd, esz in (("f32", 4), ("bf16", 2)):
+        cache = cxa.CrossAttentionCache(B, T, L, H, 64, cd)
+        out = torch.empty((B, L, H, 64), device="cuda")
+        for s in range(min(args.warmup, T)):
+            cache.self_attention_step(pos[s], Qs[s], Ks[s], Vs[s], out=out)
+        torch.cuda.synchronize()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for s in range(T):
+            cache.self_attention_step(pos[s], Qs[s], Ks[s], Vs[s], out=out)
+        b_.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b_) * 1000.0 / T
+        rows = B * L * H
+        byts = sum(2 * rows * (s + 1) * 64 * esz for s in range(T)) / T + rows * 64 * (2 * esz + 2 * 4 + 2 * 4)
+        print(json.dumps({"self_attention_step": {"B": B, "L": L, "H": H, "max_seq_len": T, "cache_dtype": cd},
+                          "us_per_step_mean": round(us, 2), "tokens_per_s": round(B / (us * 1e-6), 1),
+                          "GBps_mean": round(byts / (us * 1e-6) / 1e9, 1),
+                          "frac_of_measured_hbm": round(byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 3),
+                          "kernels_per_step": 2}), flush=True)
+        cache.close()
+    assert cxa.cxa_device_status(1) == cxa.CXA_OK
+    return 0
+
+
 def run_profile(args):
     """A handful of launches of one kernel on the bench workload's inputs, for
     Nsight Compute: one populate (weight repack + GEMM), then two more populate
@@ -723,6 +770,8 @@ def main(argv=None):
         return run_shared(args)
     if args.block:
         return run_block(args)
+    if args.selfattn:
+        return run_selfattn(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_cxa(args)

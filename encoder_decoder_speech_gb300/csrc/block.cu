@@ -269,6 +269,7 @@ cudaError_t launch_block(const BlockLaunch& a, const DeviceInfo& dev, cudaStream
   dl.nq = 1;
   dl.l0 = a.layer;
   dl.nl = 1;
+  dl.key_len_add = 0;
   dl.workspace = ws;
   dl.B = a.B;
   dl.T = a.T;

@@ -212,7 +212,7 @@ int cxa_populate(cxa_cache* c, int b0, int nb, const void* E, const void* WK, co
 
 static int decode_common(const char* who, const cxa_cache* c, int l0, int nl, int nq, const float* Q,
                          const int* key_len, float* out, float scale, void* workspace, size_t workspace_bytes,
-                         void* stream) {
+                         void* stream, int key_len_add = 0) {
   const std::string w(who);
   if (c == nullptr) return fail(CXA_EINVAL, w + ": cache descriptor is NULL");
   if (nl == -1) nl = c->L;
@@ -247,6 +247,7 @@ static int decode_common(const char* who, const cxa_cache* c, int l0, int nl, in
   a.nq = nq;
   a.l0 = l0;
   a.nl = nl;
+  a.key_len_add = key_len_add;
   a.workspace = workspace;
   a.B = c->B;
   a.T = c->T;
@@ -275,6 +276,52 @@ int cxa_decode_shared(const cxa_cache* c, int nq, const float* Q, const int* key
                       float scale, void* workspace, size_t workspace_bytes, void* stream) {
   return decode_common("cxa_decode_shared", c, 0, -1, nq, Q, key_len, out, scale, workspace, workspace_bytes,
                        stream);
+}
+
+int cxa_cache_append(cxa_cache* c, const int* pos, const float* K_new, const float* V_new, void* stream) {
+  if (c == nullptr) return fail(CXA_EINVAL, "cxa_cache_append: cache descriptor is NULL");
+  if (pos == nullptr || K_new == nullptr || V_new == nullptr)
+    return fail(CXA_EINVAL, "cxa_cache_append: a pointer argument is NULL");
+  if (!aligned(pos, 4) || !aligned(K_new, 16) || !aligned(V_new, 16))
+    return fail(CXA_EINVAL, "cxa_cache_append: K_new and V_new must be 16-byte aligned");
+  std::string msg;
+  cxa::DeviceInfo dev;
+  cudaError_t e = cxa::current_device_info(&dev, &msg);
+  if (e != cudaSuccess) return fail_cuda(e, "cxa_cache_append: " + msg);
+  cxa::AppendLaunch a;
+  a.Kc = c->Kc;
+  a.Vc = c->Vc;
+  a.pos = pos;
+  a.K_new = K_new;
+  a.V_new = V_new;
+  a.B = c->B;
+  a.T = c->T;
+  a.L = c->L;
+  a.H = c->H;
+  a.cache_bf16 = c->dtype == CXA_BF16;
+  e = cxa::launch_append(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "cxa_cache_append: launch");
+  for (auto& r : c->ready) r = 1;
+  return CXA_OK;
+}
+
+int cxa_self_attention_step(cxa_cache* c, const int* pos, const float* Q, const float* K_new, const float* V_new,
+                            float* out, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (c == nullptr) return fail(CXA_EINVAL, "cxa_self_attention_step: cache descriptor is NULL");
+  // every check of the decode first, so a failing call enqueues nothing
+  if (Q == nullptr || out == nullptr || workspace == nullptr || pos == nullptr)
+    return fail(CXA_EINVAL, "cxa_self_attention_step: a pointer argument is NULL");
+  if (!aligned(Q, 16) || !aligned(out, 16) || !aligned(workspace, 256))
+    return fail(CXA_EINVAL, "cxa_self_attention_step: Q and out must be 16-byte aligned, the workspace 256-byte aligned");
+  if (static_cast<const void*>(Q) == static_cast<const void*>(out))
+    return fail(CXA_EINVAL, "cxa_self_attention_step: out must not alias Q");
+  if (!std::isfinite(scale)) return fail(CXA_EINVAL, "cxa_self_attention_step: scale must be finite");
+  if (workspace_bytes < cxa::decode_workspace_bytes(c->B, c->T, c->L, c->H, 1))
+    return fail(CXA_EINVAL, "cxa_self_attention_step: workspace smaller than cxa_decode_workspace_bytes()");
+  const int rc = cxa_cache_append(c, pos, K_new, V_new, stream);
+  if (rc != CXA_OK) return rc;
+  return decode_common("cxa_self_attention_step", c, 0, -1, 1, Q, pos, out, scale, workspace, workspace_bytes,
+                       stream, 1);
 }
 
 size_t cxa_cross_block_workspace_bytes(int B, int T, int L, int H, int dh) {

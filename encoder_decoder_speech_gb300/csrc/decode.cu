@@ -113,6 +113,7 @@ struct DecodeParams {
   int LHc;             // rows per slot in the cache (L x H)
   int lh0;             // first cache row of the call within a slot (l0 x H)
   int nq;              // query rows per cache row (<= kNQ)
+  int key_len_add;     // valid keys = clamp(key_len[b] + key_len_add, 0, T)
   int part_stride;     // partial slots per (row, query) (ceil(T / 64))
   float qscale;        // scale * log2(e)
 };
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
       const int b = base + lane;
       int nch = 0;
       if (b < p.B) {
-        const int kl = min(max(__ldg(p.key_len + b), 0), p.T);
+        const int kl = min(max(__ldg(p.key_len + b) + p.key_len_add, 0), p.T);
         nch = (kl + R::kChunkKeys - 1) / R::kChunkKeys;
         s_nch[b] = nch;
       }
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
     Cursor c = pcur;
     npre = (g1 - g0) < kStages ? (g1 - g0) : kStages;
     for (long long i = 0; i < npre; ++i) {
-      const int kl = min(max(__ldg(p.key_len + c.b), 0), p.T);
+      const int kl = min(max(__ldg(p.key_len + c.b) + p.key_len_add, 0), p.T);
       const int n = min(R::kChunkKeys, kl - c.c * R::kChunkKeys);
       const long long crow = static_cast<long long>(c.b) * p.LHc + p.lh0 + c.lh;   // cache row
       const size_t off = (static_cast<size_t>(crow) * p.T + static_cast<size_t>(c.c) * R::kChunkKeys) * R::kRowBytes;
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
           ok = false;
           break;
         }
-        const int kl = min(max(__ldg(p.key_len + cur.b), 0), p.T);
+        const int kl = min(max(__ldg(p.key_len + cur.b) + p.key_len_add, 0), p.T);
         const int t0 = cur.c * R::kChunkKeys;
         const int n = min(R::kChunkKeys, kl - t0);
         const long long crow = static_cast<long long>(cur.b) * p.LHc + p.lh0 + cur.lh;   // cache row
@@ -373,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
         s_flags[0] = 1;
         atomicOr(p.status, 1u);
       }
-      const int kl = min(max(__ldg(p.key_len + cur.b), 0), p.T);
+      const int kl = min(max(__ldg(p.key_len + cur.b) + p.key_len_add, 0), p.T);
       const int nch = s_nch[cur.b];
       const int n = min(R::kChunkKeys, kl - cur.c * R::kChunkKeys);
       if (ok) {
@@ -644,6 +645,7 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStre
   prm.LHc = a.L * a.H;
   prm.lh0 = a.l0 * a.H;
   prm.nq = a.nq;
+  prm.key_len_add = a.key_len_add;
   prm.part_stride = (a.T + kPartChunk - 1) / kPartChunk;
   prm.qscale = a.scale * 1.4426950408889634f;   // scale * log2(e)
   cudaError_t e = a.cache_bf16 ? launch_nq<true>(prm, dev, stream) : launch_nq<false>(prm, dev, stream);

@@ -34,6 +34,7 @@ struct DecodeLaunch {
   float* out;          // [B][nq][L][H][64]
   int nq;              // query rows per cache row (1..8)
   int l0, nl;          // decoded layers [l0, l0 + nl) of the cache's L
+  int key_len_add;     // valid keys = clamp(key_len[b] + key_len_add, 0, T)
   void* workspace;
   int B, T, L, H;
   float scale;         // > 0
@@ -56,6 +57,17 @@ struct BlockLaunch {
   void* workspace;
   int B, T, L, H, layer;
   float scale;
+  bool cache_bf16;
+};
+
+// One new K/V row per (slot, layer, head) written at position pos[b] (append.cu).
+struct AppendLaunch {
+  void* Kc;
+  void* Vc;
+  const int* pos;        // [B] device
+  const float* K_new;    // [B][L][H][64]
+  const float* V_new;
+  int B, T, L, H;
   bool cache_bf16;
 };
 
@@ -82,6 +94,7 @@ cudaError_t launch_populate(const PopulateLaunch& a, const DeviceInfo& dev, cuda
 cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStream_t stream,
                           std::string* msg);
 cudaError_t launch_block(const BlockLaunch& a, const DeviceInfo& dev, cudaStream_t stream, std::string* msg);
+cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream);
 size_t block_workspace_bytes(int B, int T, int H);
 
 // Bytes at the start of a decode workspace that hold the per-row arrival

@@ -51,6 +51,11 @@ SIGNATURES = {
                                        ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
                                        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "cxa_cache_append": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p]),
+    "cxa_self_attention_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
+                                               ctypes.c_size_t, ctypes.c_void_p]),
 }
 
 # most query rows cxa_decode_shared takes per cache row (CXA_MAX_SHARED_QUERIES)
@@ -162,6 +167,15 @@ def cxa_cross_block(handle, layer, x, ln_gamma, ln_beta, ln_eps, WQ, bQ, WO, bO,
     return load().cxa_cross_block(handle, layer, _ptr(x), _ptr(ln_gamma), _ptr(ln_beta), float(ln_eps), _ptr(WQ),
                                   _ptr(bQ), _ptr(WO), _ptr(bO), _ptr(key_len), float(scale), _ptr(workspace),
                                   workspace_bytes, _stream(stream))
+
+
+def cxa_cache_append(handle, pos, K_new, V_new, stream=None) -> int:
+    return load().cxa_cache_append(handle, _ptr(pos), _ptr(K_new), _ptr(V_new), _stream(stream))
+
+
+def cxa_self_attention_step(handle, pos, Q, K_new, V_new, out, scale, workspace, workspace_bytes, stream=None) -> int:
+    return load().cxa_self_attention_step(handle, _ptr(pos), _ptr(Q), _ptr(K_new), _ptr(V_new), _ptr(out), float(scale),
+                                          _ptr(workspace), workspace_bytes, _stream(stream))
 
 
 def cxa_decode_noalloc(handle, Q, key_len, out, scale, stream=None) -> int:
@@ -290,6 +304,19 @@ class CrossAttentionCache:
         check(cxa_cross_block(self.handle, layer, x, ln_gamma, ln_beta, ln_eps, WQ, bQ, WO, bO, key_len, scale,
                               self._block_ws, self._block_ws.numel(), stream), "cxa_cross_block")
         return x
+
+    def append(self, pos, K_new, V_new, stream=None) -> None:
+        """Write K_new/V_new [B, L, H, 64] fp32 at position pos[b] (device int32 [B])."""
+        check(cxa_cache_append(self.handle, pos, K_new, V_new, stream), "cxa_cache_append")
+
+    def self_attention_step(self, pos, Q, K_new, V_new, out=None, scale: float = 0.0, stream=None):
+        """Append the new rows at pos, then decode Q over positions 0 .. pos[b]."""
+        import torch
+        if out is None:
+            out = torch.empty_like(Q)
+        check(cxa_self_attention_step(self.handle, pos, Q, K_new, V_new, out, scale, self.decode_ws,
+                                      self.decode_ws_bytes, stream), "cxa_self_attention_step")
+        return out
 
     def invalidate(self, b: int = -1) -> None:
         check(cxa_invalidate(self.handle, b), "cxa_invalidate")

@@ -143,6 +143,16 @@ CXA_API int cxa_populate(cxa_cache* c, int b0, int nb, const void* E, const void
  *            share a workspace must be ordered on one stream.
  *
  * Returns CXA_ENOTREADY, launching nothing, unless every slot is ready.
+ *
+ * Launch overlap: the decode kernel is launched with programmatic dependent
+ * launch. When the kernel just before it on the stream allows that (the
+ * library's own decode kernels do), the decode starts while that kernel drains
+ * and reads the cache rows and key_len early; it waits for the earlier kernel
+ * to finish before it reads Q or writes out or the workspace. So Q and out may
+ * be produced and consumed by neighbouring kernels freely, but the cache and
+ * key_len must not be written by an immediately preceding kernel that itself
+ * triggers programmatic launch (an ordinary kernel, a copy or cxa_populate /
+ * cxa_cache_append in between is always safe).
  */
 CXA_API int cxa_decode(const cxa_cache* c, const float* Q, const int* key_len, float* out,
                float scale, void* workspace, size_t workspace_bytes, void* stream);
@@ -172,6 +182,34 @@ CXA_API size_t cxa_decode_shared_workspace_bytes(int B, int T, int L, int H, int
 CXA_API int cxa_decode_shared(const cxa_cache* c, int nq, const float* Q, const int* key_len,
                               float* out, float scale, void* workspace, size_t workspace_bytes,
                               void* stream);
+
+/*
+ * Self-attention KV cache: append one row per (slot, layer, head) at position
+ * pos[b] -- the new token's key and value of a decoder step ("Caso de estudio:
+ * WhisperKit", §4: a fixed max_seq_len cache updated by a one-hot masked blend at
+ * the current position; "Recurrence as feeds", "What it opened": the new rows
+ * are written with scatter). A cache created with T = max_seq_len serves as the
+ * decoder's self-attention cache: cxa_decode with key_len = pos + 1 then attends
+ * positions 0 .. pos, the causal row of the whole-window formula.
+ *
+ *   pos      device int32 [B]; a slot whose pos is outside [0, T) is left as is.
+ *   K_new, V_new  device fp32 [B][L][H][dh], 16-byte aligned (rounded to bf16
+ *            for a bf16 cache).
+ * Marks every slot ready. Asynchronous on stream.
+ */
+CXA_API int cxa_cache_append(cxa_cache* c, const int* pos, const float* K_new, const float* V_new,
+                             void* stream);
+
+/*
+ * One self-attention decoder step: cxa_cache_append(pos, K_new, V_new) then the
+ * decode of Q over positions 0 .. pos[b] of every slot (key_len = pos + 1).
+ * Arguments as for cxa_cache_append and cxa_decode (workspace of
+ * cxa_decode_workspace_bytes size). Every argument is checked before anything
+ * is enqueued.
+ */
+CXA_API int cxa_self_attention_step(cxa_cache* c, const int* pos, const float* Q, const float* K_new,
+                                    const float* V_new, float* out, float scale, void* workspace,
+                                    size_t workspace_bytes, void* stream);
 
 /*
  * Decode layers [l0, l0 + nl) only: the per-layer form a real decoder calls

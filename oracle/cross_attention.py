@@ -28,6 +28,10 @@ What it computes, and where the pages define it:
   decoder calls: LayerNorm, Q projection, attention over one layer's cache, out
   projection and residual ("The concept": Q_l = decoder_hidden_l x WQ_l and the
   cross_attn_norm -> cross_q_proj -> cross_attn -> cross_out_proj operations).
+* ``masked_blend_update`` / ``self_attention_steps`` / ``causal_full_window`` --
+  the decoder's self-attention KV cache: a fixed-length cache updated by a
+  one-hot masked blend (WhisperKit case study §4), one token per step, checked
+  against the causal whole-window formula ("Recurrence as feeds").
 * ``full_window`` -- the "whole window" formula kept as a check beside one-query
   decode ("Recurrence as feeds", "What it opened").
 
@@ -216,6 +220,51 @@ def cross_block(x, layer: int, Kc, Vc, key_len, WQ, WO, gamma=None, beta=None, e
     if bO is not None:
         y = y + _f64(bO)
     return x + y
+
+
+def masked_blend_update(cache, new_row, pos):
+    """One-hot masked blend of a new row into a fixed-length cache
+    ("Caso de estudio: WhisperKit", §4): cache*(1 - onehot(pos)) + new*onehot(pos).
+    cache ``[T, dh]``, new_row ``[dh]``; returns the updated cache (fp64)."""
+    cache = _f64(cache)
+    T = cache.shape[0]
+    mask = np.zeros((T, 1))
+    if 0 <= pos < T:
+        mask[pos, 0] = 1.0
+    return cache * (1.0 - mask) + _f64(new_row)[None, :] * mask
+
+
+def self_attention_steps(Qs, Ks, Vs, scale: float | None = None) -> np.ndarray:
+    """Token-by-token self-attention decode: step i appends key/value row i to an
+    empty cache (by the masked blend) and attends positions 0 .. i.
+    Qs, Ks, Vs ``[S, dh]``; returns ``[S, dh]``."""
+    Qs, Ks, Vs = _f64(Qs), _f64(Ks), _f64(Vs)
+    S, dh = Qs.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(dh)
+    Kc, Vc = np.zeros((S, dh)), np.zeros((S, dh))
+    out = np.zeros((S, dh))
+    for i in range(S):
+        Kc = masked_blend_update(Kc, Ks[i], i)
+        Vc = masked_blend_update(Vc, Vs[i], i)
+        out[i] = attend_row(Qs[i], Kc, Vc, i + 1, scale)
+    return out
+
+
+def causal_full_window(Qs, Ks, Vs, scale: float | None = None) -> np.ndarray:
+    """The whole window at once with a causal mask: row i attends keys 0 .. i
+    ("Recurrence as feeds": the run-the-whole-window formula kept as a check of
+    one-token decode)."""
+    Qs, Ks, Vs = _f64(Qs), _f64(Ks), _f64(Vs)
+    S, dh = Qs.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(dh)
+    Sc = scale * (Qs @ Ks.T)
+    Sc = np.where(np.tril(np.ones((S, S), dtype=bool)), Sc, -np.inf)
+    Sc = Sc - Sc.max(axis=1, keepdims=True)
+    P = np.exp(Sc)
+    P = P / P.sum(axis=1, keepdims=True)
+    return P @ Vs
 
 
 def cross_attention_from_memory(Q, E, WK, WV, bV, key_len, H: int, scale: float | None = None):

@@ -276,6 +276,28 @@ def pin_cross_block():
     return float(max(errs))
 
 
+def pin_self_attention():
+    """Token-by-token decode over a masked-blend cache equals the causal
+    whole-window formula ("Recurrence as feeds": the two formulas match); the
+    blend writes exactly one row and leaves the others."""
+    errs = []
+    for S, dh in ((1, 64), (2, 2), (7, 64), (20, 64)):
+        Qs, Ks, Vs = _rand((S, dh), 130 + S), _rand((S, dh), 131 + S), _rand((S, dh), 132 + S)
+        a = O.self_attention_steps(Qs, Ks, Vs)
+        b = O.causal_full_window(Qs, Ks, Vs)
+        errs.append(np.abs(a - b).max())
+        errs.append(np.abs(a[0] - Vs[0]).max())            # the first token sees only itself
+        if S >= 2:
+            ref = bf_attend(Qs[1], Ks[:2], Vs[:2], 2, 1.0 / math.sqrt(dh))
+            errs.append(np.abs(a[1] - np.array(ref)).max())
+    c = _rand((5, 4), 140)
+    u = O.masked_blend_update(c, np.full(4, 9.0), 3)
+    errs.append(np.abs(np.delete(u, 3, axis=0) - np.delete(c, 3, axis=0)).max())
+    errs.append(np.abs(u[3] - 9.0).max())
+    errs.append(np.abs(O.masked_blend_update(c, np.full(4, 9.0), 5) - c).max())   # out of range: unchanged
+    return float(max(errs))
+
+
 # ---------------------------------------------------------------------------
 # the pins on the real oracle
 # ---------------------------------------------------------------------------
@@ -321,6 +343,10 @@ def test_shared_decode_matches_full_window_and_bruteforce():
 
 def test_cross_block_layer_norm_and_projections():
     assert pin_cross_block() < 1e-11
+
+
+def test_self_attention_cache_matches_causal_window():
+    assert pin_self_attention() < 1e-12
 
 
 def test_geometry_fails_closed():
