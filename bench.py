@@ -60,6 +60,9 @@ def parse_args(argv=None):
     p.add_argument("--selfattn", action="store_true",
                    help="time the self-attention KV-cache step (append + decode over positions 0..pos) over a "
                         "full 448-token sequence of the batched Whisper-Base decoder (16 slots, 6 layers, 8x64)")
+    p.add_argument("--align", action="store_true",
+                   help="time the alignment-head weights call on batched Whisper-Base (6 heads) and "
+                        "Whisper-large dims (16 heads)")
     p.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--budget-s", type=float, default=12.0, help=argparse.SUPPRESS)
     p.add_argument("--max-slots", type=int, default=16, help=argparse.SUPPRESS)
@@ -643,6 +646,56 @@ def run_selfattn(args):
     return 0
 
 
+def run_align(args):
+    """cxa_alignment_weights: softmax rows of selected (layer, head) pairs and their
+    mean, per decode step. Bytes = K rows of the selected heads (valid keys) + the
+    weights rows written (+ the mean)."""
+    import numpy as np
+    import torch
+    from encoder_decoder_speech_gb300 import _build, cxa
+    from encoder_decoder_speech_gb300 import workloads as W
+    _build.build_library()
+    cxa.load()
+    torch.cuda.set_device(0)
+    peaks = load_peaks()
+    for name, heads in (("batched_base", [(3, 1), (4, 2), (4, 6), (5, 0), (5, 3), (5, 7)]),
+                        ("large", [(l, (7 * l) % 20) for l in range(16, 32)])):
+        w = W.WORKLOADS[name]
+        dt = torch.bfloat16 if w.in_dtype == "bf16" else torch.float32
+        cd = w.cache_dtypes[0]
+        esz = 2 if cd == "bf16" else 4
+        E = torch.randn(w.B, w.T, w.d, device="cuda").to(dt)
+        WK = (torch.randn(w.L, w.d, w.d, device="cuda") / w.d ** 0.5).to(dt)
+        bV = torch.zeros(w.L, w.d, device="cuda")
+        kl_h = W.make_key_len(w)
+        kl = torch.from_numpy(kl_h).to("cuda")
+        cache = cxa.CrossAttentionCache(w.B, w.T, w.L, w.H, 64, cd)
+        cache.populate(E, WK, WK, bV)
+        Q = torch.randn(w.B, w.L, w.H, 64, device="cuda")
+        wt = torch.empty((w.B, len(heads), w.T), device="cuda")
+        mean = torch.empty((w.B, w.T), device="cuda")
+        for _ in range(args.warmup):
+            cxa.check(cxa.cxa_alignment_weights(cache.handle, Q, kl, heads, wt, mean, 0.0), "align")
+        torch.cuda.synchronize()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            cxa.check(cxa.cxa_alignment_weights(cache.handle, Q, kl, heads, wt, mean, 0.0), "align")
+        b_.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b_) * 1000.0 / args.steps
+        byts = len(heads) * 64 * esz * int(np.clip(kl_h, 0, w.T).sum()) + w.B * (len(heads) + 1) * w.T * 4 * 2
+        print(json.dumps({"alignment_weights": {"workload": name, "heads": len(heads), "cache_dtype": cd},
+                          "us_per_call": round(us, 2), "GBps": round(byts / (us * 1e-6) / 1e9, 1),
+                          "frac_of_measured_hbm": round(byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 3)}),
+              flush=True)
+        cache.close()
+        del E, WK
+        torch.cuda.empty_cache()
+    assert cxa.cxa_device_status(1) == cxa.CXA_OK
+    return 0
+
+
 def run_profile(args):
     """A handful of launches of one kernel on the bench workload's inputs, for
     Nsight Compute: one populate (weight repack + GEMM), then two more populate
@@ -772,6 +825,8 @@ def main(argv=None):
         return run_block(args)
     if args.selfattn:
         return run_selfattn(args)
+    if args.align:
+        return run_align(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_cxa(args)

@@ -324,6 +324,50 @@ int cxa_self_attention_step(cxa_cache* c, const int* pos, const float* Q, const 
                        stream, 1);
 }
 
+int cxa_alignment_weights(const cxa_cache* c, const float* Q, const int* key_len, const int* heads_lh, int nsel,
+                          float* weights, float* mean, float scale, void* stream) {
+  if (c == nullptr) return fail(CXA_EINVAL, "cxa_alignment_weights: cache descriptor is NULL");
+  if (nsel < 1 || nsel > cxa::kMaxAlignHeads)
+    return fail(CXA_EINVAL, "cxa_alignment_weights: nsel must be in [1, " + std::to_string(cxa::kMaxAlignHeads) + "]");
+  if (Q == nullptr || key_len == nullptr || heads_lh == nullptr || weights == nullptr)
+    return fail(CXA_EINVAL, "cxa_alignment_weights: a pointer argument is NULL");
+  if (!aligned(Q, 16) || !aligned(key_len, 4) || !aligned(weights, 4) || (mean != nullptr && !aligned(mean, 4)))
+    return fail(CXA_EINVAL, "cxa_alignment_weights: Q must be 16-byte aligned");
+  if (!std::isfinite(scale)) return fail(CXA_EINVAL, "cxa_alignment_weights: scale must be finite");
+  cxa::AlignHeads hs;
+  hs.n = nsel;
+  for (int k = 0; k < nsel; ++k) {
+    const int l = heads_lh[2 * k], h = heads_lh[2 * k + 1];
+    if (l < 0 || l >= c->L || h < 0 || h >= c->H)
+      return fail(CXA_EINVAL, "cxa_alignment_weights: head " + std::to_string(k) + " out of range");
+    hs.l[k] = l;
+    hs.h[k] = h;
+  }
+  for (int b = 0; b < c->B; ++b)
+    if (!c->ready[static_cast<size_t>(b)])
+      return fail(CXA_ENOTREADY, "cxa_alignment_weights: slot " + std::to_string(b) + " is not populated");
+  std::string msg;
+  cxa::DeviceInfo dev;
+  cudaError_t e = cxa::current_device_info(&dev, &msg);
+  if (e != cudaSuccess) return fail_cuda(e, "cxa_alignment_weights: " + msg);
+  cxa::AlignLaunch a;
+  a.Kc = c->Kc;
+  a.Q = Q;
+  a.key_len = key_len;
+  a.weights = weights;
+  a.mean = mean;
+  a.heads = hs;
+  a.B = c->B;
+  a.T = c->T;
+  a.L = c->L;
+  a.H = c->H;
+  a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(c->dh));
+  a.cache_bf16 = c->dtype == CXA_BF16;
+  e = cxa::launch_alignment(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "cxa_alignment_weights: launch");
+  return CXA_OK;
+}
+
 size_t cxa_cross_block_workspace_bytes(int B, int T, int L, int H, int dh) {
   if (B <= 0 || T <= 0 || L <= 0 || H <= 0 || dh != 64) return 0;
   return cxa::block_workspace_bytes(B, T, H);

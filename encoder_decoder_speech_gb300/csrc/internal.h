@@ -71,6 +71,27 @@ struct AppendLaunch {
   bool cache_bf16;
 };
 
+// Selected (layer, head) pairs, passed by value as a kernel parameter.
+constexpr int kMaxAlignHeads = 64;
+struct AlignHeads {
+  int n;
+  int l[kMaxAlignHeads];
+  int h[kMaxAlignHeads];
+};
+
+// Cross-attention weights of selected heads (alignment.cu).
+struct AlignLaunch {
+  const void* Kc;
+  const float* Q;        // [B][L][H][64]
+  const int* key_len;    // [B]
+  float* weights;        // [B][nsel][T]
+  float* mean;           // [B][T] or NULL
+  AlignHeads heads;
+  int B, T, L, H;
+  float scale;
+  bool cache_bf16;
+};
+
 // Device facts of the current device, queried once per device.
 struct DeviceInfo {
   int device;
@@ -95,6 +116,7 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStre
                           std::string* msg);
 cudaError_t launch_block(const BlockLaunch& a, const DeviceInfo& dev, cudaStream_t stream, std::string* msg);
 cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream);
+cudaError_t launch_alignment(const AlignLaunch& a, cudaStream_t stream);
 size_t block_workspace_bytes(int B, int T, int H);
 
 // Bytes at the start of a decode workspace that hold the per-row arrival

@@ -56,6 +56,9 @@ SIGNATURES = {
     "cxa_self_attention_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
                                                ctypes.c_size_t, ctypes.c_void_p]),
+    "cxa_alignment_weights": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
+                                             ctypes.c_void_p]),
 }
 
 # most query rows cxa_decode_shared takes per cache row (CXA_MAX_SHARED_QUERIES)
@@ -176,6 +179,14 @@ def cxa_cache_append(handle, pos, K_new, V_new, stream=None) -> int:
 def cxa_self_attention_step(handle, pos, Q, K_new, V_new, out, scale, workspace, workspace_bytes, stream=None) -> int:
     return load().cxa_self_attention_step(handle, _ptr(pos), _ptr(Q), _ptr(K_new), _ptr(V_new), _ptr(out), float(scale),
                                           _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def cxa_alignment_weights(handle, Q, key_len, heads, weights, mean, scale, stream=None) -> int:
+    """heads: host sequence of (layer, head) pairs."""
+    flat = [int(v) for pair in heads for v in pair]
+    arr = (ctypes.c_int * max(len(flat), 1))(*flat)
+    return load().cxa_alignment_weights(handle, _ptr(Q), _ptr(key_len), ctypes.cast(arr, ctypes.c_void_p), len(heads),
+                                        _ptr(weights), _ptr(mean), float(scale), _stream(stream))
 
 
 def cxa_decode_noalloc(handle, Q, key_len, out, scale, stream=None) -> int:
@@ -317,6 +328,15 @@ class CrossAttentionCache:
         check(cxa_self_attention_step(self.handle, pos, Q, K_new, V_new, out, scale, self.decode_ws,
                                       self.decode_ws_bytes, stream), "cxa_self_attention_step")
         return out
+
+    def alignment_weights(self, Q, key_len, heads, scale: float = 0.0, with_mean: bool = True, stream=None):
+        """Softmax rows [B, nsel, T] of the (layer, head) pairs in `heads` for queries
+        Q [B, L, H, 64], and their mean over heads [B, T] (or None)."""
+        import torch
+        w = torch.empty((self.B, len(heads), self.T), dtype=torch.float32, device=self.Kc.device)
+        m = torch.empty((self.B, self.T), dtype=torch.float32, device=self.Kc.device) if with_mean else None
+        check(cxa_alignment_weights(self.handle, Q, key_len, heads, w, m, scale, stream), "cxa_alignment_weights")
+        return w, m
 
     def invalidate(self, b: int = -1) -> None:
         check(cxa_invalidate(self.handle, b), "cxa_invalidate")

@@ -212,6 +212,27 @@ CXA_API int cxa_self_attention_step(cxa_cache* c, const int* pos, const float* Q
                                     size_t workspace_bytes, void* stream);
 
 /*
+ * Cross-attention weights of selected alignment heads for one decode step
+ * ("Caso de estudio: WhisperKit", §6: the cross-attention of chosen alignment
+ * heads returns its weights, and their mean over heads is returned as an extra
+ * output for word timestamps):
+ *
+ *   weights[b][k][t] = softmax over t < key_len[b] of scale * q . K for head
+ *                      (l_k, h_k) of slot b, and 0 for t >= key_len[b]
+ *   mean[b][t]       = average of weights[b][k][t] over the nsel heads
+ *
+ *   Q         device fp32 [B][L][H][dh] (the decode step's queries), 16-byte aligned.
+ *   heads_lh  HOST int32 [nsel][2]: (layer, head) pairs, checked against L and H.
+ *   nsel      1 .. 64.
+ *   weights   device fp32 [B][nsel][T] (written completely).
+ *   mean      device fp32 [B][T], or NULL to skip it.
+ * Errors as for cxa_decode, and CXA_EINVAL for bad nsel or head indices.
+ */
+CXA_API int cxa_alignment_weights(const cxa_cache* c, const float* Q, const int* key_len,
+                                  const int* heads_lh, int nsel, float* weights, float* mean,
+                                  float scale, void* stream);
+
+/*
  * Decode layers [l0, l0 + nl) only: the per-layer form a real decoder calls
  * between its other sub-layers (the trace page's decoder body interleaves
  * cross_attn with the self-attention and MLP of each layer).

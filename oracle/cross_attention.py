@@ -28,6 +28,8 @@ What it computes, and where the pages define it:
   decoder calls: LayerNorm, Q projection, attention over one layer's cache, out
   projection and residual ("The concept": Q_l = decoder_hidden_l x WQ_l and the
   cross_attn_norm -> cross_q_proj -> cross_attn -> cross_out_proj operations).
+* ``attention_weights`` -- the softmax rows of chosen alignment heads and their
+  mean over heads, returned for word timestamps (WhisperKit case study §6).
 * ``masked_blend_update`` / ``self_attention_steps`` / ``causal_full_window`` --
   the decoder's self-attention KV cache: a fixed-length cache updated by a
   one-hot masked blend (WhisperKit case study §4), one token per step, checked
@@ -220,6 +222,27 @@ def cross_block(x, layer: int, Kc, Vc, key_len, WQ, WO, gamma=None, beta=None, e
     if bO is not None:
         y = y + _f64(bO)
     return x + y
+
+
+def attention_weights(Q, Kc, key_len, heads, scale: float | None = None):
+    """Softmax rows of the selected (layer, head) pairs ("Caso de estudio:
+    WhisperKit", §6, alignment-head weights) and their mean over the heads.
+    Q ``[B, L, H, dh]``; returns (weights ``[B, nsel, T]``, mean ``[B, T]``),
+    zero beyond key_len."""
+    Q, Kc = _f64(Q), _f64(Kc)
+    B, L, H, T, dh = Kc.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(dh)
+    n = clamp_key_len(key_len, T)
+    w = np.zeros((B, len(heads), T))
+    for b in range(B):
+        if n[b] == 0:
+            continue
+        for k, (l, h) in enumerate(heads):
+            s = scale * (Kc[b, l, h, :n[b]] @ Q[b, l, h])
+            e = np.exp(s - s.max())
+            w[b, k, :n[b]] = e / e.sum()
+    return w, w.mean(axis=1)
 
 
 def masked_blend_update(cache, new_row, pos):

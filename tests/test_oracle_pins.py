@@ -298,6 +298,30 @@ def pin_self_attention():
     return float(max(errs))
 
 
+def pin_attention_weights():
+    """Each selected head's row sums to 1 over the valid keys and is zero beyond;
+    weighting V by it gives the decode output of that head; brute force."""
+    errs = []
+    B, L, H, T, dh = 3, 2, 3, 9, 64
+    Q, Kc, Vc = _rand((B, L, H, dh), 150), _rand((B, L, H, T, dh), 151), _rand((B, L, H, T, dh), 152)
+    kl = np.array([9, 5, 0])
+    heads = [(0, 2), (1, 0), (1, 2)]
+    w, m = O.attention_weights(Q, Kc, kl, heads)
+    dec = O.decode(Q, Kc, Vc, kl)
+    for b in range(B):
+        for k, (l, h) in enumerate(heads):
+            n = int(kl[b])
+            errs.append(abs(w[b, k].sum() - (1.0 if n > 0 else 0.0)))
+            errs.append(np.abs(w[b, k, n:]).max() if n < T else 0.0)
+            errs.append(np.abs(w[b, k] @ Vc[b, l, h] - dec[b, l, h]).max())
+            if n > 0:
+                e = [math.exp(0.125 * math.fsum(Q[b, l, h, c] * Kc[b, l, h, t, c] for c in range(dh))) for t in range(n)]
+                z = math.fsum(e)
+                errs.append(np.abs(w[b, k, :n] - np.array(e) / z).max())
+    errs.append(np.abs(m - w.mean(axis=1)).max())
+    return float(max(errs))
+
+
 # ---------------------------------------------------------------------------
 # the pins on the real oracle
 # ---------------------------------------------------------------------------
@@ -347,6 +371,10 @@ def test_cross_block_layer_norm_and_projections():
 
 def test_self_attention_cache_matches_causal_window():
     assert pin_self_attention() < 1e-12
+
+
+def test_alignment_head_weights():
+    assert pin_attention_weights() < 1e-12
 
 
 def test_geometry_fails_closed():
