@@ -539,7 +539,7 @@ def run_shared(args):
     for cd, esz in (("f32", 4), ("bf16", 2)):
         cache = cxa.CrossAttentionCache(w.B, w.T, w.L, w.H, w.dh, cd)
         cache.populate(E, WK, WV, bV)
-        for nq in (1, 2, 4, 5, 8):
+        for nq in (1, 2, 4, 5, 8) + ((16,) if cd == "bf16" else ()):
             Q = torch.from_numpy(np.random.default_rng(nq).standard_normal(
                 (w.B, nq, w.L, w.H, w.dh)).astype(np.float32)).to("cuda")
             out = torch.empty_like(Q)

@@ -150,6 +150,7 @@ size_t cxa_decode_workspace_bytes(int B, int T, int L, int H, int dh) {
 }
 
 size_t cxa_decode_shared_workspace_bytes(int B, int T, int L, int H, int dh, int nq) {
+  // (the fp32-cache limit of 8 queries is checked by cxa_decode_shared)
   if (B <= 0 || T <= 0 || L <= 0 || H <= 0 || dh != 64 || nq < 1 || nq > CXA_MAX_SHARED_QUERIES) return 0;
   return cxa::decode_workspace_bytes(B, T, L, H, nq);
 }
@@ -219,6 +220,9 @@ static int decode_common(const char* who, const cxa_cache* c, int l0, int nl, in
   if (l0 < 0 || nl < 1 || l0 + nl > c->L) return fail(CXA_EINVAL, w + ": layers [l0, l0+nl) out of range");
   if (nq < 1 || nq > CXA_MAX_SHARED_QUERIES)
     return fail(CXA_EINVAL, w + ": nq must be in [1, " + std::to_string(CXA_MAX_SHARED_QUERIES) + "]");
+  if (nq > CXA_MAX_SHARED_QUERIES_F32 && c->dtype == CXA_F32)
+    return fail(CXA_EINVAL, w + ": an fp32 cache takes at most " + std::to_string(CXA_MAX_SHARED_QUERIES_F32) +
+                                " queries per row");
   if (Q == nullptr || key_len == nullptr || out == nullptr || workspace == nullptr)
     return fail(CXA_EINVAL, w + ": a pointer argument is NULL");
   if (!aligned(Q, 16) || !aligned(out, 16) || !aligned(key_len, 4) || !aligned(workspace, 256))

@@ -629,7 +629,9 @@ size_t decode_counter_bytes(int B, int L, int H) { return counters_bytes(B, L, H
 
 cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStream_t stream,
                           std::string* msg) {
-  (void)msg;
+  // three or more queries per row of a bf16 cache: scores on the tensor cores
+  // (bf16 x bf16 products are exact; an fp32 cache keeps fp32 scores here)
+  if (a.nq >= 3 && a.cache_bf16) return launch_decode_shared_tc(a, dev, stream, msg);
   DecodeParams prm;
   prm.Q = a.Q;
   prm.Kc = static_cast<const uint8_t*>(a.Kc);

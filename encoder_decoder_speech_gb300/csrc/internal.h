@@ -116,6 +116,8 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStre
                           std::string* msg);
 cudaError_t launch_block(const BlockLaunch& a, const DeviceInfo& dev, cudaStream_t stream, std::string* msg);
 cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream);
+cudaError_t launch_decode_shared_tc(const DecodeLaunch& a, const DeviceInfo& dev, cudaStream_t stream,
+                                    std::string* msg);
 cudaError_t launch_alignment(const AlignLaunch& a, cudaStream_t stream);
 size_t block_workspace_bytes(int B, int T, int H);
 

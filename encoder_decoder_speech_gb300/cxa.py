@@ -62,7 +62,7 @@ SIGNATURES = {
 }
 
 # most query rows cxa_decode_shared takes per cache row (CXA_MAX_SHARED_QUERIES)
-CXA_MAX_SHARED_QUERIES = 8
+CXA_MAX_SHARED_QUERIES = 16
 
 # bytes of the fixed device scratch behind cxa_decode_noalloc (CXA_NOALLOC_SCRATCH_BYTES)
 CXA_NOALLOC_SCRATCH_BYTES = 8 << 20

@@ -164,7 +164,10 @@ CXA_API int cxa_decode(const cxa_cache* c, const float* Q, const int* key_len, f
  * attends one shared batch-1 cache from a batch-N query). Each K/V row is read
  * once per step for all nq queries.
  *
- *   nq       query rows per cache row, 1 .. CXA_MAX_SHARED_QUERIES.
+ *   nq       query rows per cache row, 1 .. CXA_MAX_SHARED_QUERIES (16) for a
+ *            bf16 cache, 1 .. CXA_MAX_SHARED_QUERIES_F32 (8) for an fp32 cache.
+ *            With a bf16 cache and nq >= 3 the scores run on the tensor cores
+ *            (queries rounded to bf16); otherwise in fp32 on the CUDA cores.
  *   Q, out   device fp32 [B][nq][L][H][dh]: row (b, n, l, h) is hypothesis n of
  *            slot b; out row (b, n, l, h) = softmax(scale * q.K[b,l,h]^T) V[b,l,h].
  *   key_len, scale  as for cxa_decode (key_len is per slot, shared by its rows).
@@ -173,9 +176,10 @@ CXA_API int cxa_decode(const cxa_cache* c, const float* Q, const int* key_len, f
  *            as cxa_decode's workspace.
  *
  * With nq = 1 this is exactly cxa_decode. Errors as for cxa_decode, and
- * CXA_EINVAL for nq outside [1, CXA_MAX_SHARED_QUERIES].
+ * CXA_EINVAL for nq outside those ranges.
  */
-#define CXA_MAX_SHARED_QUERIES 8
+#define CXA_MAX_SHARED_QUERIES 16
+#define CXA_MAX_SHARED_QUERIES_F32 8
 
 CXA_API size_t cxa_decode_shared_workspace_bytes(int B, int T, int L, int H, int dh, int nq);
 

@@ -28,8 +28,8 @@ def _queries(w, nq, seed):
     return rng.standard_normal((w.B, nq, w.L, w.H, 64)).astype(np.float32)
 
 
-@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("nq", [1, 2, 3, 4, 5, 7, 8])
+@pytest.mark.parametrize("cache_dtype,nq", [(c, n) for c in ("f32", "bf16") for n in (1, 2, 3, 4, 5, 7, 8)]
+                         + [("bf16", n) for n in (9, 12, 16)])
 def test_shared_decode_matches_oracle(nq, cache_dtype):
     w = W.custom("shared", B=4, T=700, d=256, L=2, H=4, ragged=True, index=940)
     d, h = inputs_on_device(w)
@@ -67,11 +67,14 @@ def test_shared_decode_back_to_back_and_invalid_nq():
     K, V = host(c.Kc), host(c.Vc)
     for q, o in zip(Qs, outs):
         assert np.abs(host(o) - O.decode_shared(q, K, V, h["key_len"])).max() <= DECODE_BF16_MAX_ABS
-    Q9 = dev(_queries(w, 9, 1))
-    out = torch.empty_like(Q9)
-    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
-    assert cxa.cxa_decode_shared(c.handle, 9, Q9, d["key_len"], out, 0.0, ws, ws.numel()) == cxa.CXA_EINVAL
-    assert cxa.cxa_decode_shared(c.handle, 0, Q9, d["key_len"], out, 0.0, ws, ws.numel()) == cxa.CXA_EINVAL
+    Q17 = dev(_queries(w, 17, 1))
+    out = torch.empty_like(Q17)
+    ws = torch.zeros(1 << 24, dtype=torch.uint8, device="cuda")
+    assert cxa.cxa_decode_shared(c.handle, 17, Q17, d["key_len"], out, 0.0, ws, ws.numel()) == cxa.CXA_EINVAL
+    assert cxa.cxa_decode_shared(c.handle, 0, Q17, d["key_len"], out, 0.0, ws, ws.numel()) == cxa.CXA_EINVAL
+    c32 = cache_for(w, "f32")
+    c32.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    assert cxa.cxa_decode_shared(c32.handle, 9, Q17, d["key_len"], out, 0.0, ws, ws.numel()) == cxa.CXA_EINVAL
 
 
 @pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
