@@ -46,7 +46,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["cxa", "reference"], default="cxa")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     p.add_argument("--no-variants", action="store_true", help="skip the bf16-cache variant")
-    p.add_argument("--profile", choices=["decode", "decode_bf16", "populate"], default=None,
+    p.add_argument("--profile", choices=["decode", "decode_bf16", "populate", "shared_bf16"], default=None,
                    help="run a few launches of one kernel on the workload's inputs (for ncu), print nothing else")
     p.add_argument("--sweep", action="store_true",
                    help="time decode and populate at every point of the decode bandwidth sweep "
@@ -739,11 +739,18 @@ def run_profile(args):
     torch.cuda.set_device(0)
     w = W.WORKLOADS[WORKLOAD]
     (E, WK, WV, bV, kl, Q, _), _ = device_inputs(torch, W, w, 0)
-    cache = cxa.CrossAttentionCache(w.B, w.T, w.L, w.H, w.dh, "bf16" if args.profile == "decode_bf16" else "f32")
+    bf16 = args.profile in ("decode_bf16", "shared_bf16")
+    cache = cxa.CrossAttentionCache(w.B, w.T, w.L, w.H, w.dh, "bf16" if bf16 else "f32")
     cache.populate(E, WK, WV, bV)
     if args.profile == "populate":
         for _ in range(2):
             cache.populate(E, WK, WV, bV)
+    elif args.profile == "shared_bf16":   # 8 hypotheses per slot on the tensor-core shared decode
+        import numpy as np
+        Qs = torch.from_numpy(np.random.default_rng(8).standard_normal(
+            (w.B, 8, w.L, w.H, w.dh)).astype(np.float32)).to("cuda")
+        for _ in range(3):
+            cache.decode_shared(Qs, kl)
     else:
         for s in range(3):
             cache.decode(Q[s], kl)
