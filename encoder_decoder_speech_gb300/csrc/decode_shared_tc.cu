@@ -6,26 +6,31 @@
 // stream decode kernel (decode.cu). A 128-key chunk goes through two tcgen05
 // products with fp32 accumulators in tensor memory:
 //
-//  * scores: S^T[128 keys x 16 queries] = K_chunk[128 x 64] Q^T (kind::f16,
+//  * scores: S^T[128 keys x 32] = K_chunk[128 x 64] [Q_hi; Q_lo]^T (kind::f16,
 //    both operands K-major, 128-byte swizzle). K arrives by TMA from a 3-D view
-//    of the cache (c, t, slot*L*H + l*H + h); the Q tile (queries pre-scaled by
-//    scale*log2(e), rounded to bf16, rows >= nq zero) is written by the MMA
-//    warp at each row start. Double-buffered in TMEM.
+//    of the cache (c, t, slot*L*H + l*H + h); the queries, pre-scaled by
+//    scale*log2(e), are split into bf16 hi and lo parts (rows >= nq zero) by the
+//    MMA warp at each row start, so that a score is K.Q_hi + K.Q_lo with Q
+//    carried to about 16 mantissa bits (K is exact: the cache is bf16).
+//    Double-buffered in TMEM.
 //  * softmax on the CUDA cores: each of the 128 consumer threads owns one key
-//    and reads its scores with one tcgen05.ld; the chunk max of a query is one
-//    redux.sync per warp plus a 4-entry shared-memory max; probabilities are
-//    written, rounded to bf16, as P^T[query][key] in the 128-byte-swizzled
-//    K-major layout, and the running sums add the same rounded values so that
-//    the weights of the final average sum to one exactly.
-//  * values: O_chunk[128 x 64] = P^T[128 x 128 keys] V_chunk[128 x 64] with V
-//    MN-major straight from its TMA tile (keys = K, channels = N). Only the
-//    first 16 rows of the A operand are queries; the other 112 rows the MMA
-//    reads fall on later shared memory and produce accumulator lanes nobody
-//    reads, so the P buffer stays 4 KB. Double-buffered in TMEM.
-//  * consumer warp 0, whose TMEM lanes hold the query rows, adds each chunk's
-//    O into a running accumulator kept in TMEM (acc = acc * corr + O_chunk,
-//    one chunk behind so that the P.V product overlaps the next softmax) and
-//    writes the segment's result or partial slot at the row's end.
+//    and reads its scores with one tcgen05.ld. Probabilities are taken against
+//    a per-query reference max that moves only when some score passes it by
+//    more than 2^8 (one bar.red.or per chunk tells); a move costs a warp
+//    redux.sync and a 4-entry shared-memory max, plus, inside a row segment, a
+//    rescale of the O accumulator in TMEM before the chunk's P.V is issued.
+//    Probabilities (<= 256) are written, rounded to bf16, as P^T[query][key] in
+//    the 128-byte-swizzled K-major layout; the running sums add the same
+//    rounded values, so the weights of the final average sum to one exactly.
+//  * values: O^T[64 channels x 16 queries] += V_chunk^T[64 x 128 keys] P[128 x 16]
+//    (M = 64, N = 16): A is V MN-major straight from its TMA tile, B is P^T as
+//    written (K-major), accumulated over the row segment's chunks in TMEM (two
+//    buffers, alternate segments). With M = 64 the accumulator rows sit in
+//    lanes 0..15 of each warp's 32-lane quarter: channel 16w + l in lane
+//    32w + l. The MMA warp issues a chunk's P.V as soon as its P^T is ready,
+//    even while it waits for the next chunk's data.
+//  * at the end of a segment each consumer warp reads its 16 channels of O^T
+//    and writes them for every query (result or the segment's partial slot).
 //
 // V rows past the key length of a tail chunk are zeroed in shared memory before
 // the product: their probabilities are 0 and stale rows may hold any bits.
@@ -48,7 +53,8 @@ constexpr int kDh = 64;
 constexpr int kPartFloats = 68;
 constexpr int kPartChunk = 64;
 constexpr int kChunk = 128;                    // keys per chunk: M of the scores, K of P.V
-constexpr int kNPad = 16;                      // query columns of the score MMA (rows >= nq zero)
+constexpr int kNPad = 16;                      // query rows (>= nq zero)
+constexpr int kSCols = 2 * kNPad;              // score MMA N: hi rows 0..15, lo rows 16..31 of Q
 constexpr int kRowBytes = kDh * 2;             // one bf16 row of 64 channels
 constexpr int kBoxRows = 32;                   // keys per TMA box
 constexpr int kBoxBytes = kBoxRows * kRowBytes;
@@ -56,20 +62,19 @@ constexpr int kTileBytes = kChunk * kRowBytes; // K or V of one chunk: 16 KB
 constexpr int kStageBytes = 2 * kTileBytes;
 constexpr int kStages = 3;
 constexpr int kPBytes = 4096;                  // P^T of a chunk: 2 key halves x 16 rows x 128 B
-constexpr int kQTileBytes = kNPad * kRowBytes; // 2 KB
+constexpr int kQTileBytes = kSCols * kRowBytes; // 4 KB
 constexpr int kConsumerWarps = 4;              // one key per consumer thread
 constexpr int kThreads = (kConsumerWarps + 2) * 32;   // + producer warp + MMA warp
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kMmaWarp = kConsumerWarps + 1;
 constexpr int kCtasPerSm = 2;
-constexpr uint32_t kTmemCols = 256;            // S: 2 x 16 at 0, O: 2 x 64 at 64, acc: 64 at 192
+constexpr uint32_t kTmemCols = 128;            // S: 2 x 32 at 0; O^T: 2 x 16 (row segments) at 64
 constexpr uint32_t kOCol = 64;
-constexpr uint32_t kAccCol = 192;
-constexpr int kBars = 2 * kStages + 10;        // full, empty, tfull, tempty, pfull, ofull, oempty
-// P buffers sit first: rows 16..127 of the P.V A operand read up to 16 KB past a
-// buffer's key half, which must stay inside this CTA's shared memory.
+constexpr float kRescaleLog2 = 8.f;            // a reference max moves only past this margin (x256)
+// K full/empty, V full/empty [kStages]; tfull, tempty, pfull, pempty, ofull, oempty [2];
+// odone, rescaled
+constexpr int kBars = 4 * kStages + 14;
 constexpr int kPRegion = 2 * kPBytes;
-static_assert(kPRegion + kStages * kStageBytes >= kPBytes + 2048 + 16 * 1024, "A-operand overread");
 
 struct TcParams {
   const float* Q;
@@ -86,13 +91,29 @@ __device__ __forceinline__ float rescale(float m, float M) { return m == -INFINI
 __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// OR of a predicate over the threads of a named barrier, which it also is.
+__device__ __forceinline__ bool named_barrier_or(int id, int count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
 __device__ __forceinline__ float warp_max(float v) {
   float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
   return r;
 }
-__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+// 2^x on the SFU (ex2.approx, flush-to-zero): 2^-inf = 0.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
@@ -149,24 +170,31 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* bp = smem_raw + (base - raw);
-  // layout: P^T x 2 | stages [K tile | V tile] x kStages | Q tiles x 2 | small arrays
+  // layout: P^T x 2 | stages [K tile | V tile] x kStages | Q tile | small arrays
   const uint32_t p_base = base;
   const uint32_t stage_base = base + kPRegion;
   const uint32_t q_base = stage_base + kStages * kStageBytes;
-  float* s_red = reinterpret_cast<float*>(bp + kPRegion + kStages * kStageBytes + 2 * kQTileBytes);  // [4][16]
-  float* s_fin = s_red + kConsumerWarps * kNPad;                      // [16] m, [16] S of the segment
-  float* s_corr = s_fin + 2 * kNPad;                                  // [2][16] per-chunk rescale factors
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_corr + 2 * kNPad);
+  float* s_red = reinterpret_cast<float*>(bp + kPRegion + kStages * kStageBytes + kQTileBytes);  // [4][16]
+  float* s_corr = s_red + kConsumerWarps * kNPad;                     // [16] factors of the last max update
+  float* s_sum = s_corr + kNPad;                                      // [2][4][16] per-warp sums of a segment
+  float* s_m = s_sum + 2 * kConsumerWarps * kNPad;                    // [2][16] references of a segment
+  int* s_pflag = reinterpret_cast<int*>(s_m + 2 * kNPad);             // [2] O rescale before the chunk's P.V
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_pflag + 2);
   long long* s_first = reinterpret_cast<long long*>(bars + kBars);
   int* s_nch = reinterpret_cast<int*>(s_first + p.B + 1);
   volatile int* s_flags = reinterpret_cast<volatile int*>(s_nch + p.B + (p.B & 1));   // abort, last, tmem base
-  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
-  auto empty_bar = [&](int s) { return smem_u32(&bars[kStages + s]); };
-  auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * kStages + a]); };
-  auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * kStages + 2 + a]); };
-  auto pfull_bar = [&](int a) { return smem_u32(&bars[2 * kStages + 4 + a]); };
-  auto ofull_bar = [&](int a) { return smem_u32(&bars[2 * kStages + 6 + a]); };
-  auto oempty_bar = [&](int a) { return smem_u32(&bars[2 * kStages + 8 + a]); };
+  auto kfull_bar = [&](int s) { return smem_u32(&bars[s]); };
+  auto kempty_bar = [&](int s) { return smem_u32(&bars[kStages + s]); };
+  auto vfull_bar = [&](int s) { return smem_u32(&bars[2 * kStages + s]); };
+  auto vempty_bar = [&](int s) { return smem_u32(&bars[3 * kStages + s]); };
+  auto tfull_bar = [&](int a) { return smem_u32(&bars[4 * kStages + a]); };
+  auto tempty_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 2 + a]); };
+  auto pfull_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 4 + a]); };
+  auto pempty_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 6 + a]); };
+  auto ofull_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 8 + a]); };
+  auto oempty_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 10 + a]); };
+  const uint32_t odone_bar = smem_u32(&bars[4 * kStages + 12]);
+  const uint32_t rescaled_bar = smem_u32(&bars[4 * kStages + 13]);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int LH = p.LH, nq = p.nq;
@@ -199,16 +227,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   if (threadIdx.x == 32) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(kfull_bar(s), 1);
+      mbar_init(kempty_bar(s), 1);
+      mbar_init(vfull_bar(s), 1);
+      mbar_init(vempty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
       mbar_init(tempty_bar(a), kConsumerWarps);
       mbar_init(pfull_bar(a), 1);
+      mbar_init(pempty_bar(a), 1);
       mbar_init(ofull_bar(a), 1);
-      mbar_init(oempty_bar(a), 1);
+      mbar_init(oempty_bar(a), kConsumerWarps);
     }
+    mbar_init(odone_bar, 1);
+    mbar_init(rescaled_bar, kConsumerWarps);
     fence_mbar_init();
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
@@ -240,15 +273,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
 
   if (active && warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // ------------------------------------------------------------ producers
+    // lane 0 streams the K tiles, lane 1 the V tiles: a K stage comes back as soon
+    // as its score MMA has run, a V stage only after the chunk's P.V.
+    if (lane < 2) {
+      const bool v_ring = lane == 1;
+      const void* tm = v_ring ? static_cast<const void*>(&tmV) : static_cast<const void*>(&tmK);
       Cursor cur = locate(g0, s_first, s_nch, p.B);
       uint32_t armed = 0, armed_parity = 0;
       bool ok = true;
       for (long long g = g0, i = 0; g < g1; ++g, ++i) {
         const int s = static_cast<int>(i % kStages);
         const uint32_t parity = static_cast<uint32_t>((i / kStages) & 1);
-        if (!mbar_wait(empty_bar(s), parity ^ 1u, s_flags)) {
+        if (!mbar_wait(v_ring ? vempty_bar(s) : kempty_bar(s), parity ^ 1u, s_flags)) {
           ok = false;
           break;
         }
@@ -256,12 +293,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int t0 = cur.c * kChunk;
         const int nbox = (min(kChunk, kl - t0) + kBoxRows - 1) / kBoxRows;   // rows past them stay stale
         const int crow = cur.b * p.LHc + p.lh0 + cur.lh;
-        const uint32_t dst = stage_base + s * kStageBytes;
-        mbar_arrive_expect_tx(full_bar(s), static_cast<uint32_t>(2 * nbox * kBoxBytes));
-        for (int j = 0; j < nbox; ++j) {
-          tma_load_3d(dst + j * kBoxBytes, &tmK, full_bar(s), 0, t0 + j * kBoxRows, crow);
-          tma_load_3d(dst + kTileBytes + j * kBoxBytes, &tmV, full_bar(s), 0, t0 + j * kBoxRows, crow);
-        }
+        const uint32_t fb = v_ring ? vfull_bar(s) : kfull_bar(s);
+        const uint32_t dst = stage_base + s * kStageBytes + (v_ring ? kTileBytes : 0);
+        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nbox * kBoxBytes));
+        for (int j = 0; j < nbox; ++j) tma_load_3d(dst + j * kBoxBytes, tm, fb, 0, t0 + j * kBoxRows, crow);
         armed |= 1u << s;
         armed_parity = (armed_parity & ~(1u << s)) | (parity << s);
         advance(cur, s_nch, p.B, LH);
@@ -270,101 +305,167 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         s_flags[0] = 1;
         atomicOr(p.status, 1u);
         for (int s = 0; s < kStages; ++s)
-          if (armed & (1u << s)) mbar_wait(full_bar(s), (armed_parity >> s) & 1u);
+          if (armed & (1u << s)) mbar_wait(v_ring ? vfull_bar(s) : kfull_bar(s), (armed_parity >> s) & 1u);
       }
     }
     __syncwarp();
   } else if (active && warp == kMmaWarp) {
     // ------------------------------------------------------------ Q tiles + MMA issue
-    constexpr uint32_t idesc_s = make_idesc(1u, kChunk, kNPad);
-    constexpr uint32_t idesc_o = make_idesc(1u, 128, kDh) | (1u << 16);   // B (V) MN-major
+    // A polling loop that never blocks on one condition: chunk ns gets its scores
+    // once its K tile is in and its score buffer is free; chunk np (<= ns) gets its
+    // P.V once its P^T, its V tile and (at a segment start) the O buffer are ready.
+    constexpr uint32_t idesc_s = make_idesc(1u, kChunk, kSCols);
+    constexpr uint32_t idesc_o = make_idesc(1u, kDh, kNPad) | (1u << 15);   // A (V^T) MN-major
+    const long long nck = g1 - g0;
     Cursor cur = locate(g0, s_first, s_nch, p.B);
-    int qbuf = 1, prev_b = -1, prev_lh = -1;
+    int prev_b = -1, prev_lh = -1, seg = -1;
+    uint32_t info = 0;     // 4 bits per chunk mod 4: first, last, segment parity, (segment / 2) parity
+    long long ns = 0, np = 0;
+    int pv_phase = 0;      // chunk np: 0 wait P^T, 1 wait the O rescale, 2 wait V tile (+ O buffer)
+    uint32_t resc = 0;     // O rescales served so far
     bool ok = true;
-    // P.V of chunk j: A = P^T buffer j&1, B = V of its stage, D = O buffer j&1.
-    auto issue_pv = [&](long long j) {
-      const int b = static_cast<int>(j & 1);
-      const uint32_t par = static_cast<uint32_t>((j >> 1) & 1);
-      if (!mbar_wait(pfull_bar(b), par, s_flags) || !mbar_wait(oempty_bar(b), par ^ 1u, s_flags)) {
-        ok = false;
-        return;
-      }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t pt = p_base + b * kPBytes;
-        const uint32_t vt = stage_base + static_cast<uint32_t>(j % kStages) * kStageBytes + kTileBytes;
-        const uint32_t d_tmem = tmem_base + kOCol + static_cast<uint32_t>(b) * kDh;
+    uint64_t t_move = globaltimer_ns();
+    uint32_t idle = 0;
+    while (np < nck) {
+      bool moved = false;
+      if (ns < nck) {
+        // ---- scores of chunk ns
+        const int a = static_cast<int>(ns & 1), s = static_cast<int>(ns % kStages);
+        const bool first = cur.b != prev_b || cur.lh != prev_lh;   // a new row segment
+        int ready = 0;
+        if (lane == 0)
+          ready = mbar_test_wait(tempty_bar(a), static_cast<uint32_t>(((ns >> 1) & 1) ^ 1)) &&
+                  mbar_test_wait(kfull_bar(s), static_cast<uint32_t>((ns / kStages) & 1)) &&
+                  (!first || ns == 0 ||
+                   mbar_test_wait(tfull_bar(static_cast<int>((ns - 1) & 1)), static_cast<uint32_t>(((ns - 1) >> 1) & 1)));
+        if (__shfl_sync(0xffffffffu, ready, 0)) {
+          if (first) {
+            // Its queries become the B operand of the scores, as bf16 hi (rows 0..15)
+            // and lo (rows 16..31) parts: K.(hi + lo) carries Q to about 16 mantissa
+            // bits. The single Q tile is rewritten after the previous chunk's score
+            // MMA (and so every earlier MMA) has finished, as just tested.
+            ++seg;
+            const int qr = lane >> 1, half = lane & 1;   // query row, half of the channels
+            const bool valid = qr < nq;
+            const float* src = p.Q + qrow(cur.b, cur.lh, valid ? qr : 0) * kDh + half * 32;
 #pragma unroll
-        for (int kb = 0; kb < kChunk / 16; ++kb) {
-          const uint64_t ad = smem_desc_k_sw128(pt + (kb >> 2) * 2048 + (kb & 3) * 32);
-          const uint64_t bd = smem_desc_mn_sw128(vt + kb * 2048);
-          mma_bf16(d_tmem, ad, bd, idesc_o, kb != 0 ? 1u : 0u);
-        }
-        tc_commit(ofull_bar(b));
-        tc_commit(empty_bar(static_cast<int>(j % kStages)));
-      }
-      __syncwarp();
-    };
-    long long i = 0;
-    for (long long g = g0; g < g1 && ok; ++g, ++i) {
-      const int s = static_cast<int>(i % kStages);
-      const uint32_t parity = static_cast<uint32_t>((i / kStages) & 1);
-      const int acc = static_cast<int>(i & 1);
-      const uint32_t acc_parity = static_cast<uint32_t>((i >> 1) & 1);
-      if (!mbar_wait(tempty_bar(acc), acc_parity ^ 1u, s_flags)) {
-        ok = false;
-        break;
-      }
-      if (cur.b != prev_b || cur.lh != prev_lh) {
-        // A new row: its queries become the B operand of the scores. The buffer was
-        // last read by the MMAs of the row before the previous one, finished since
-        // the consumers released the score accumulator just waited on.
-        qbuf ^= 1;
-        const uint32_t qt = q_base + qbuf * kQTileBytes;
-        // 16 rows x 64 channels: lane handles row (lane / 2), half (lane & 1) of the channels
-        const int qr = lane >> 1, half = lane & 1;
-        const bool valid = qr < nq;
-        const float* src = p.Q + qrow(cur.b, cur.lh, valid ? qr : 0) * kDh + half * 32;
+            for (int j = 0; j < 4; ++j) {
+              uint32_t wh[4], wl[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t w[4];
+              for (int k = 0; k < 2; ++k) {
+                const float4 f = valid ? __ldg(reinterpret_cast<const float4*>(src) + 2 * j + k)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float x[4] = {f.x * p.qscale, f.y * p.qscale, f.z * p.qscale, f.w * p.qscale};
 #pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const float4 f = valid ? __ldg(reinterpret_cast<const float4*>(src) + 2 * j + k)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-            __nv_bfloat162 lo = __floats2bfloat162_rn(f.x * p.qscale, f.y * p.qscale);
-            __nv_bfloat162 hi = __floats2bfloat162_rn(f.z * p.qscale, f.w * p.qscale);
-            w[2 * k] = *reinterpret_cast<uint32_t*>(&lo);
-            w[2 * k + 1] = *reinterpret_cast<uint32_t*>(&hi);
+                for (int e = 0; e < 2; ++e) {
+                  __nv_bfloat162 hi = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+                  __nv_bfloat162 lo =
+                      __floats2bfloat162_rn(x[2 * e] - __low2float(hi), x[2 * e + 1] - __high2float(hi));
+                  wh[2 * k + e] = *reinterpret_cast<uint32_t*>(&hi);
+                  wl[2 * k + e] = *reinterpret_cast<uint32_t*>(&lo);
+                }
+              }
+              // a row is 128 bytes = 8 chunks of 8 bf16; this lane writes chunks 4*half .. 4*half+3
+              const uint32_t chunk = static_cast<uint32_t>(4 * half + j);
+              const int rl = qr + kNPad;
+              st_shared_v4(q_base + qr * 128 + ((chunk ^ (qr & 7)) << 4), wh[0], wh[1], wh[2], wh[3]);
+              st_shared_v4(q_base + rl * 128 + ((chunk ^ (rl & 7)) << 4), wl[0], wl[1], wl[2], wl[3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            prev_b = cur.b;
+            prev_lh = cur.lh;
           }
-          // row qr: 128 bytes = 8 chunks of 8 bf16; this lane writes chunks 4*half .. 4*half+3
-          const uint32_t chunk = static_cast<uint32_t>(4 * half + j);
-          st_shared_v4(qt + qr * 128 + ((chunk ^ (qr & 7)) << 4), w[0], w[1], w[2], w[3]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        prev_b = cur.b;
-        prev_lh = cur.lh;
-      }
-      if (!mbar_wait(full_bar(s), parity, s_flags)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t kt = stage_base + s * kStageBytes;
-        const uint32_t qt = q_base + qbuf * kQTileBytes;
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kNPad);
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t kt = stage_base + s * kStageBytes;
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * kSCols);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(d_tmem, smem_desc_k_sw128(kt + k * 32), smem_desc_k_sw128(qt + k * 32), idesc_s, k != 0 ? 1u : 0u);
-        tc_commit(tfull_bar(acc));
+            for (int k = 0; k < 4; ++k)
+              mma_bf16(d_tmem, smem_desc_k_sw128(kt + k * 32), smem_desc_k_sw128(q_base + k * 32), idesc_s,
+                       k != 0 ? 1u : 0u);
+            tc_commit(tfull_bar(a));
+            tc_commit(kempty_bar(s));
+          }
+          __syncwarp();
+          const bool last = (cur.c == s_nch[cur.b] - 1) || (g0 + ns + 1 == g1);
+          const uint32_t bits = (first ? 1u : 0u) | (last ? 2u : 0u) | (static_cast<uint32_t>(seg & 3) << 2);
+          const int sh = static_cast<int>(ns & 3) * 4;
+          info = (info & ~(0xFu << sh)) | (bits << sh);
+          advance(cur, s_nch, p.B, LH);
+          ++ns;
+          moved = true;
+        }
       }
-      __syncwarp();
-      if (i > 0) issue_pv(i - 1);   // the previous chunk's P.V overlaps this chunk's softmax
-      advance(cur, s_nch, p.B, LH);
+      if (np < ns) {
+        // ---- P.V of chunk np: A = its V tile (as V^T), B = P^T buffer np&1,
+        // D = the segment's O^T buffer (accumulating from its first chunk)
+        const int b = static_cast<int>(np & 1), st = static_cast<int>(np % kStages);
+        const uint32_t bits = (info >> (static_cast<int>(np & 3) * 4)) & 0xFu;
+        const bool first = bits & 1u, last = bits & 2u;
+        const int rb = static_cast<int>((bits >> 2) & 1u);
+        const uint32_t rb_parity = (bits >> 3) & 1u;
+        if (pv_phase == 0) {
+          int ready = lane == 0 ? mbar_test_wait(pfull_bar(b), static_cast<uint32_t>((np >> 1) & 1)) : 0;
+          if (__shfl_sync(0xffffffffu, ready, 0)) {
+            // the consumers ask for an O rescale once every P.V issued so far has finished
+            const int flag = __shfl_sync(0xffffffffu, lane == 0 ? s_pflag[b] : 0, 0);
+            if (flag && lane == 0) tc_commit(odone_bar);
+            __syncwarp();
+            pv_phase = flag ? 1 : 2;
+            moved = true;
+          }
+        }
+        if (pv_phase == 1) {
+          const int ready = lane == 0 ? mbar_test_wait(rescaled_bar, resc & 1u) : 0;
+          if (__shfl_sync(0xffffffffu, ready, 0)) {
+            ++resc;
+            pv_phase = 2;
+            moved = true;
+          }
+        }
+        if (pv_phase == 2) {
+          int ready = 0;
+          if (lane == 0)
+            ready = (!first || mbar_test_wait(oempty_bar(rb), rb_parity ^ 1u)) &&
+                    mbar_test_wait(vfull_bar(st), static_cast<uint32_t>((np / kStages) & 1));
+          if (__shfl_sync(0xffffffffu, ready, 0)) {
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t pt = p_base + b * kPBytes;
+              const uint32_t vt = stage_base + st * kStageBytes + kTileBytes;
+              const uint32_t d_tmem = tmem_base + kOCol + static_cast<uint32_t>(rb * kNPad);
+#pragma unroll
+              for (int kb = 0; kb < kChunk / 16; ++kb) {
+                const uint64_t ad = smem_desc_mn_sw128(vt + kb * 2048);
+                const uint64_t bd = smem_desc_k_sw128(pt + (kb >> 2) * 2048 + (kb & 3) * 32);
+                mma_bf16(d_tmem, ad, bd, idesc_o, (first && kb == 0) ? 0u : 1u);
+              }
+              tc_commit(pempty_bar(b));
+              tc_commit(vempty_bar(st));
+              if (last) tc_commit(ofull_bar(rb));
+            }
+            __syncwarp();
+            ++np;
+            pv_phase = 0;
+            moved = true;
+          }
+        }
+      }
+      if (moved) {
+        idle = 0;
+        if (lane == 0) t_move = globaltimer_ns();
+        continue;
+      }
+      if ((++idle & 255u) == 0) {
+        int stop = 0;
+        if (lane == 0) stop = s_flags[0] != 0 || globaltimer_ns() - t_move > kWaitLimitNs || idle >= kWaitPollLimit;
+        if (__shfl_sync(0xffffffffu, stop, 0)) {
+          ok = false;
+          break;
+        }
+      }
     }
-    if (ok && i > 0) issue_pv(i - 1);
     if (!ok) {
       s_flags[0] = 1;
       atomicOr(p.status, 1u);
@@ -373,73 +474,128 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // ------------------------------------------------------------ consumers
     const int tid = threadIdx.x;                   // 0..127: key of the chunk for the softmax
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    // P^T address of (query q, key tid) in buffer 0: key half, 8-row group, swizzled 16-byte chunk
+    // P^T byte offset of (query 0, key tid) in buffer 0: key half, swizzled 16-byte chunk
     const int kk = tid & 63;
     const uint32_t p_key = static_cast<uint32_t>((tid >> 6) * 2048 + (kk & 7) * 2);
     const uint32_t p_chunk = static_cast<uint32_t>(kk >> 3);
     Cursor cur = locate(g0, s_first, s_nch, p.B);
     int seg_c0 = cur.c;
-    float m_run[kNQT], s_run[kNQT];
+    // m_ref: the reference max the probabilities are taken against (log2 units); it
+    // moves only when a score exceeds it by more than kRescaleLog2.
+    float m_ref[kNQT], s_run[kNQT];
 #pragma unroll
     for (int q = 0; q < kNQT; ++q) {
-      m_run[q] = -INFINITY;
+      m_ref[q] = -INFINITY;
       s_run[q] = 0.f;
     }
-    bool ok = true, pending = false, acc_empty = true;
+    bool ok = true;
+    int seg = 0;          // index of the current row segment
+    uint32_t resc = 0;    // O rescales done so far
+    // A finished segment waiting to be written out (one chunk later, so that its
+    // last P.V has run by then).
+    bool f_pending = false, f_whole = false;
+    int f_seg = 0, f_b = 0, f_lh = 0, f_pseg = 0, f_nseg = 1;
+    long long f_row = 0;
     auto fail = [&]() {
       ok = false;
       s_flags[0] = 1;
       atomicOr(p.status, 1u);
     };
-    // Warp 0 only: acc = acc * corr_j + O_j in TMEM (lane q = query q). With final
-    // set, lane q < nq writes mul * (acc * corr_j + O_j) to dst instead (16 channels
-    // at a time; zeros after a failed wait).
-    auto add_chunk = [&](long long j, bool final, float* dst, float mul) {
-      const int b = static_cast<int>(j & 1);
-      if (ok && !mbar_wait(ofull_bar(b), static_cast<uint32_t>((j >> 1) & 1), s_flags)) fail();
+    // Write the finished segment f_seg: O^T from TMEM through a free P^T buffer
+    // (as [query][channel] floats) to the output rows or the segment's partial
+    // slots; the last segment of a split row merges all of them.
+    auto flush = [&](int free_pbuf) {
+      const int rb = f_seg & 1;
+      if (ok && !mbar_wait(ofull_bar(rb), static_cast<uint32_t>((f_seg >> 1) & 1), s_flags)) fail();
       tc_fence_after();
-      const float corr = lane < kNPad ? s_corr[b * kNPad + lane] : 0.f;
-#pragma unroll
-      for (int h = 0; h < kDh / 16; ++h) {
-        uint32_t o[16], acc[16];
-        tmem_ld_32x32b_x16(tmem_base + kOCol + static_cast<uint32_t>(b * kDh + h * 16), o);
-        if (!acc_empty) tmem_ld_32x32b_x16(tmem_base + kAccCol + static_cast<uint32_t>(h * 16), acc);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          acc[c] = __float_as_uint(acc_empty ? __uint_as_float(o[c])
-                                             : fmaf(__uint_as_float(acc[c]), corr, __uint_as_float(o[c])));
-        if (final) {
-          if (lane < nq) {
-#pragma unroll
-            for (int c = 0; c < 16; c += 4)
-              *reinterpret_cast<float4*>(dst + h * 16 + c) =
-                  ok ? make_float4(__uint_as_float(acc[c]) * mul, __uint_as_float(acc[c + 1]) * mul,
-                                   __uint_as_float(acc[c + 2]) * mul, __uint_as_float(acc[c + 3]) * mul)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        } else {
-          tmem_st_32x32b_x16(tmem_base + kAccCol + static_cast<uint32_t>(h * 16), acc);
-        }
-      }
-      if (!final) tmem_st_wait();
+      uint32_t o[16];
+      tmem_ld_32x32b_x16(tmem_base + lane_base + kOCol + static_cast<uint32_t>(rb * kNPad), o);
+      tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(oempty_bar(b));
-      acc_empty = final;
+      if (lane == 0) mbar_arrive(oempty_bar(rb));
+      float* sO = reinterpret_cast<float*>(bp + free_pbuf * kPBytes);   // [16][64]
+      if (lane < 16) {   // lane l of warp w: channel 16w + l
+#pragma unroll
+        for (int q = 0; q < kNQT; ++q) sO[q * kDh + 16 * warp + lane] = __uint_as_float(o[q]);
+      }
+      named_barrier(1, kConsumerWarps * 32);
+      const float* sum = s_sum + rb * kConsumerWarps * kNPad;
+      for (int e = tid; e < nq * (kDh / 4); e += kConsumerWarps * 32) {
+        const int q = e / (kDh / 4), c4 = e % (kDh / 4);
+        float4 v = *reinterpret_cast<const float4*>(sO + q * kDh + 4 * c4);
+        if (f_whole) {
+          const float S = sum[q] + sum[kNPad + q] + sum[2 * kNPad + q] + sum[3 * kNPad + q];
+          const float inv = S > 0.f ? 1.f / S : 0.f;
+          v = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+          if (ok) *reinterpret_cast<float4*>(p.out + qrow(f_b, f_lh, q) * kDh + 4 * c4) = v;
+        } else {
+          *reinterpret_cast<float4*>(p.part + ((f_row * nq + q) * p.part_stride + f_pseg) * kPartFloats + 4 +
+                                     4 * c4) = ok ? v : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      if (!f_whole) {
+        if (tid < nq) {
+          float* P = p.part + ((f_row * nq + tid) * p.part_stride + f_pseg) * kPartFloats;
+          P[0] = ok ? s_m[rb * kNPad + tid] : -INFINITY;
+          P[1] = ok ? sum[tid] + sum[kNPad + tid] + sum[2 * kNPad + tid] + sum[3 * kNPad + tid] : 0.f;
+        }
+        __threadfence();
+        named_barrier(1, kConsumerWarps * 32);
+        if (tid == 0) {
+          const unsigned int prev = atomicAdd(p.counters + f_row, 1u);
+          s_flags[1] = (prev == static_cast<unsigned int>(f_nseg - 1)) ? 1 : 0;
+        }
+        named_barrier(1, kConsumerWarps * 32);
+        if (s_flags[1]) {
+          __threadfence();
+#pragma unroll 2
+          for (int e = tid; e < nq * kDh; e += kConsumerWarps * 32) {   // (query, channel)
+            const int q = e / kDh, c = e % kDh;
+            const float* P0 = p.part + (f_row * nq + q) * p.part_stride * kPartFloats;
+            float MM = -INFINITY, SS = 0.f, AA = 0.f;
+            for (int k0 = 0; k0 < f_nseg; k0 += 4) {
+              float mk[4], sk[4], ak[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const bool in = k0 + u < f_nseg;
+                const float* Pk = P0 + (k0 + u) * kPartFloats;
+                mk[u] = in ? __ldcg(Pk) : -INFINITY;
+                sk[u] = in ? __ldcg(Pk + 1) : 0.f;
+                ak[u] = in ? __ldcg(Pk + 4 + c) : 0.f;
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float M2 = fmaxf(MM, mk[u]);
+                const float f0 = rescale(MM, M2), f1 = rescale(mk[u], M2);
+                SS = SS * f0 + sk[u] * f1;
+                AA = AA * f0 + ak[u] * f1;
+                MM = M2;
+              }
+            }
+            p.out[qrow(f_b, f_lh, q) * kDh + c] = SS > 0.f ? AA / SS : 0.f;
+          }
+          if (tid == 0) p.counters[f_row] = 0u;
+        }
+      }
+      named_barrier(1, kConsumerWarps * 32);   // the staging buffer and the flags are free again
+      f_pending = false;
     };
 
-    for (long long g = g0, i = 0; g < g1; ++g, ++i) {
+    long long i = 0;
+    for (long long g = g0; g < g1; ++g, ++i) {
       const int s = static_cast<int>(i % kStages);
       const int a = static_cast<int>(i & 1);
       const uint32_t acc_parity = static_cast<uint32_t>((i >> 1) & 1);
       const int kl = min(max(__ldg(p.key_len + cur.b), 0), p.T);
       const int nch = s_nch[cur.b];
       const int n = min(kChunk, kl - cur.c * kChunk);
+      const bool seg_first = cur.c == seg_c0;
       if (ok && !mbar_wait(tfull_bar(a), acc_parity, s_flags)) fail();
       tc_fence_after();
-      uint32_t sr[16];
-      tmem_ld_32x32b_x16(tmem_base + lane_base + static_cast<uint32_t>(a * kNPad), sr);
+      uint32_t sh[16], sl[16];   // K.Q_hi, K.Q_lo
+      tmem_ld_32x32b_x16(tmem_base + lane_base + static_cast<uint32_t>(a * kSCols), sh);
+      tmem_ld_32x32b_x16(tmem_base + lane_base + static_cast<uint32_t>(a * kSCols + kNPad), sl);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
@@ -448,128 +604,118 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // ---- softmax of the chunk: thread tid owns key tid
       const bool valid_key = tid < n && ok;
       float sc[kNQT];
+      bool need = false;
 #pragma unroll
       for (int q = 0; q < kNQT; ++q) {
-        sc[q] = valid_key ? __uint_as_float(sr[q]) : -INFINITY;
-        const float mq = warp_max(sc[q]);
-        if (lane == 0) s_red[warp * kNPad + q] = mq;
+        sc[q] = valid_key ? __uint_as_float(sh[q]) + __uint_as_float(sl[q]) : -INFINITY;
+        need |= sc[q] > m_ref[q] + kRescaleLog2;
       }
-      named_barrier(1, kConsumerWarps * 32);
-      const uint32_t pt = p_base + a * kPBytes + p_key;
+      bool rescale_o = false;
+      if (named_barrier_or(1, kConsumerWarps * 32, need)) {
+        // some score passed its reference by more than the margin: move every
+        // reference to the running max (warp redux, then a 4-entry max)
+        float mq[kNQT];
+#pragma unroll
+        for (int q = 0; q < kNQT; ++q) mq[q] = warp_max(sc[q]);
+        if (lane == 0) {
+#pragma unroll
+          for (int q4 = 0; q4 < kNQT / 4; ++q4)
+            *reinterpret_cast<float4*>(s_red + warp * kNPad + 4 * q4) =
+                make_float4(mq[4 * q4], mq[4 * q4 + 1], mq[4 * q4 + 2], mq[4 * q4 + 3]);
+        }
+        named_barrier(1, kConsumerWarps * 32);
+#pragma unroll
+        for (int q = 0; q < kNQT; ++q) {
+          float M = m_ref[q];
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s_red[w * kNPad + q]);
+          const float corr = m_ref[q] == -INFINITY ? 0.f : ex2(m_ref[q] - M);
+          s_run[q] *= corr;
+          if (tid == 0) s_corr[q] = corr;   // the same in every thread
+          m_ref[q] = M;
+        }
+        rescale_o = !seg_first;
+      }
+      // the P^T buffer is free once the P.V of chunk i-2 has finished
+      if (ok && !mbar_wait(pempty_bar(a), acc_parity ^ 1u, s_flags)) fail();
+      const uint32_t p_off = static_cast<uint32_t>(a * kPBytes) + p_key;
 #pragma unroll
       for (int q = 0; q < kNQT; ++q) {
-        float M = m_run[q];
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s_red[w * kNPad + q]);
-        const float corr = M == -INFINITY ? 1.f : rescale(m_run[q], M);
-        m_run[q] = M;
-        const __nv_bfloat16 pb = __float2bfloat16_rn(valid_key ? exp2f(sc[q] - M) : 0.f);
-        s_run[q] = s_run[q] * corr + __bfloat162float(pb);
-        if (tid == 0) s_corr[a * kNPad + q] = corr;   // the same in every thread
+        const __nv_bfloat16 pb = __float2bfloat16_rn(valid_key ? ex2(sc[q] - m_ref[q]) : 0.f);
+        s_run[q] += __bfloat162float(pb);
         const int r = q & 7;
-        st_shared_u16(pt + (q >> 3) * 1024 + r * 128 + ((p_chunk ^ static_cast<uint32_t>(r)) << 4),
-                      __bfloat16_as_ushort(pb));
+        *reinterpret_cast<uint16_t*>(bp + p_off + (q >> 3) * 1024 + r * 128 +
+                                     ((p_chunk ^ static_cast<uint32_t>(r)) << 4)) = __bfloat16_as_ushort(pb);
       }
       if (n < kChunk) {
         // tail chunk: zero the V rows of keys >= n (their P is 0; the rows may hold any bits)
-        if (ok && !mbar_wait(full_bar(s), static_cast<uint32_t>((i / kStages) & 1), s_flags)) fail();
+        if (ok && !mbar_wait(vfull_bar(s), static_cast<uint32_t>((i / kStages) & 1), s_flags)) fail();
         const uint32_t vt = stage_base + s * kStageBytes + kTileBytes;
         for (int u = n * (kRowBytes / 16) + tid; u < kTileBytes / 16; u += kConsumerWarps * 32)
           st_shared_v4(vt + u * 16, 0u, 0u, 0u, 0u);
       }
+      if (tid == 0) s_pflag[a] = rescale_o ? 1 : 0;
       fence_proxy_async_smem();
       named_barrier(1, kConsumerWarps * 32);                 // P^T (and the V tail) complete
       if (tid == 0) mbar_arrive(pfull_bar(a));
-      if (warp == 0 && pending) add_chunk(i - 1, false, nullptr, 0.f);
-      pending = true;
+      if (rescale_o) {
+        // O^T (chunks before this one) *= corr per query column, after their P.V and
+        // before this chunk's; each warp scales its own 16 channel lanes
+        if (ok && !mbar_wait(odone_bar, resc & 1u, s_flags)) fail();
+        tc_fence_after();
+        uint32_t o[16];
+        tmem_ld_32x32b_x16(tmem_base + lane_base + kOCol + static_cast<uint32_t>((seg & 1) * kNPad), o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < kNQT; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * s_corr[q]);
+        tmem_st_32x32b_x16(tmem_base + lane_base + kOCol + static_cast<uint32_t>((seg & 1) * kNPad), o);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(rescaled_bar);
+        ++resc;
+      }
+      // the previous segment's P.V has run by now; its P^T buffer (the other one) stages O
+      if (f_pending) flush(a ^ 1);
 
-      const bool row_ends = (cur.c == nch - 1) || (g + 1 == g1);
-      if (row_ends) {
-        // ---- sums over the keys (threads) per query
+      if ((cur.c == nch - 1) || (g + 1 == g1)) {
+        // ---- the segment ends: per-warp sums over the keys, references; written out next chunk
+        const int rb = seg & 1;
 #pragma unroll
         for (int q = 0; q < kNQT; ++q) {
           float sq = s_run[q];
 #pragma unroll
           for (int off = 16; off >= 1; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-          if (lane == 0) s_red[warp * kNPad + q] = sq;
+          s_run[q] = sq;
         }
-        named_barrier(1, kConsumerWarps * 32);
-        if (tid < kNQT) {
-          float S = 0.f;
+        if (lane == 0) {
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) S += s_red[w * kNPad + tid];
-          s_fin[kNPad + tid] = S;
+          for (int q4 = 0; q4 < kNQT / 4; ++q4)
+            *reinterpret_cast<float4*>(s_sum + (rb * kConsumerWarps + warp) * kNPad + 4 * q4) =
+                make_float4(s_run[4 * q4], s_run[4 * q4 + 1], s_run[4 * q4 + 2], s_run[4 * q4 + 3]);
         }
-        if (tid == 0) {   // the running maxima are the same in every thread
+        if (tid == 0) {   // the references are the same in every thread
 #pragma unroll
-          for (int q = 0; q < kNQT; ++q) s_fin[q] = m_run[q];
+          for (int q = 0; q < kNQT; ++q) s_m[rb * kNPad + q] = m_ref[q];
         }
-        named_barrier(1, kConsumerWarps * 32);
-        const long long row = static_cast<long long>(cur.b) * LH + cur.lh;
-        const bool whole_row = seg_c0 == 0 && cur.c == nch - 1;
-        long long first_owner = 0;
-        int nseg = 1, seg = 0;
-        if (!whole_row) {
+        f_pending = true;
+        f_seg = seg;
+        f_b = cur.b;
+        f_lh = cur.lh;
+        f_row = static_cast<long long>(cur.b) * LH + cur.lh;
+        f_whole = seg_c0 == 0 && cur.c == nch - 1;
+        f_nseg = 1;
+        f_pseg = 0;
+        if (!f_whole) {
           const long long grow = s_first[cur.b] + static_cast<long long>(cur.lh) * nch;
-          first_owner = owner_of(grow, total, ranges);
-          nseg = static_cast<int>(owner_of(grow + nch - 1, total, ranges) - first_owner + 1);
-          seg = static_cast<int>(blockIdx.x - first_owner);
+          const long long first_owner = owner_of(grow, total, ranges);
+          f_nseg = static_cast<int>(owner_of(grow + nch - 1, total, ranges) - first_owner + 1);
+          f_pseg = static_cast<int>(blockIdx.x - first_owner);
         }
-        if (warp == 0) {
-          const int ql = lane < nq ? lane : nq - 1;
-          const float S = s_fin[kNPad + ql];
-          float* dst;
-          float mul = 1.f;
-          if (whole_row) {
-            dst = p.out + qrow(cur.b, cur.lh, ql) * kDh;
-            mul = S > 0.f ? 1.f / S : 0.f;
-          } else {
-            float* P = p.part + ((row * nq + ql) * p.part_stride + seg) * kPartFloats;
-            if (lane < nq) {
-              P[0] = ok ? s_fin[ql] : -INFINITY;
-              P[1] = ok ? S : 0.f;
-            }
-            dst = P + 4;
-          }
-          add_chunk(i, true, dst, mul);
-          pending = false;
-        } else {
-          pending = false;
-        }
-        if (!whole_row) {
-          __threadfence();
-          named_barrier(1, kConsumerWarps * 32);
-          if (tid == 0) {
-            const unsigned int prev = atomicAdd(p.counters + row, 1u);
-            s_flags[1] = (prev == static_cast<unsigned int>(nseg - 1)) ? 1 : 0;
-          }
-          named_barrier(1, kConsumerWarps * 32);
-          if (s_flags[1]) {
-            __threadfence();
-            if (tid < kDh) {
-              for (int q = 0; q < nq; ++q) {
-                const float* P0 = p.part + (row * nq + q) * p.part_stride * kPartFloats;
-                float MM = -INFINITY, SS = 0.f, AA = 0.f;
-                for (int k = 0; k < nseg; ++k) {
-                  const float mk = __ldcg(P0 + k * kPartFloats);
-                  const float sk = __ldcg(P0 + k * kPartFloats + 1);
-                  const float ak = __ldcg(P0 + k * kPartFloats + 4 + tid);
-                  const float M2 = fmaxf(MM, mk);
-                  const float f0 = rescale(MM, M2), f1 = rescale(mk, M2);
-                  SS = SS * f0 + sk * f1;
-                  AA = AA * f0 + ak * f1;
-                  MM = M2;
-                }
-                p.out[qrow(cur.b, cur.lh, q) * kDh + tid] = SS > 0.f ? AA / SS : 0.f;
-              }
-            }
-            if (tid == 0) p.counters[row] = 0u;
-          }
-        }
-        named_barrier(1, kConsumerWarps * 32);
+        ++seg;
 #pragma unroll
         for (int q = 0; q < kNQT; ++q) {
-          m_run[q] = -INFINITY;
+          m_ref[q] = -INFINITY;
           s_run[q] = 0.f;
         }
       }
@@ -577,6 +723,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       advance(cur, s_nch, p.B, LH);
       if (cur.b != pb || cur.lh != plh) seg_c0 = cur.c;
     }
+    // the last segment: every P.V has been issued; both P^T buffers are free once it has run
+    if (f_pending) flush(0);
   }
   tc_fence_before();
   __syncthreads();
@@ -605,8 +753,8 @@ EncodeTiledFn encoder() {
 }
 
 size_t smem_bytes(int B) {
-  size_t n = 1024 + kPRegion + static_cast<size_t>(kStages) * kStageBytes + 2 * kQTileBytes;
-  n += (kConsumerWarps * kNPad + 4 * kNPad) * 4 + kBars * 8;
+  size_t n = 1024 + kPRegion + static_cast<size_t>(kStages) * kStageBytes + kQTileBytes;
+  n += (kConsumerWarps * kNPad + kNPad + 2 * kConsumerWarps * kNPad + 2 * kNPad) * 4 + 2 * 4 + kBars * 8;
   n += static_cast<size_t>(B + 1) * 8 + static_cast<size_t>(B + (B & 1)) * 4 + 16;
   return n;
 }
@@ -666,7 +814,7 @@ cudaError_t launch_tc(const TcParams& prm, const void* Kc, const void* Vc, const
   if (per_sm < kCtasPerSm) {
     // The occupancy query reports one CTA per SM for kernels that allocate tensor
     // memory. Two of these fit by registers, shared memory and TMEM columns
-    // (2 x 256 of 512), and no CTA waits on another, so the count is taken from
+    // (2 x 128 of 512), and no CTA waits on another, so the count is taken from
     // the register and shared-memory budgets instead.
     static int fits[128] = {};
     const int d = dev.device >= 0 && dev.device < 128 ? dev.device : 0;

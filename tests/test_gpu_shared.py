@@ -88,3 +88,33 @@ def test_batched_base_beam5(cache_dtype):
     out = host(c.decode_shared(dev(Q), d["key_len"]))
     ref = O.decode_shared(Q, host(c.Kc), host(c.Vc), h["key_len"])
     assert np.abs(out - ref).max() <= TOL[cache_dtype]
+
+
+@pytest.mark.parametrize("nq", [3, 8, 16])
+def test_shared_decode_growing_scores_move_the_reference(nq):
+    """Key rows scaled up along t make later chunks' scores pass the running max
+    by far more than the 2^8 margin inside row segments, so the tensor-core
+    decode rescales its O accumulator in tensor memory; the result must still
+    match the oracle."""
+    w = W.custom("shared_grow", B=8, T=1500, d=512, L=2, H=8, ragged=True, index=943)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, "bf16")
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    ramp = 1.0 + torch.arange(w.T, device="cuda", dtype=torch.float32) / 48.0
+    c.Kc.mul_(ramp.to(c.Kc.dtype)[:, None])
+    Q = (3.0 * _queries(w, nq, 60 + nq)).astype(np.float32)
+    K, V = host(c.Kc), host(c.Vc)
+    # precondition: chunk maxima (log2 units) jump past the running max by > 8
+    s = np.einsum("bqlhc,blhtc->bqlht", Q.astype(np.float64), K) * (64 ** -0.5) / np.log(2.0)
+    jumps = 0
+    for b in range(w.B):
+        n = int(h["key_len"][b])
+        cm = [s[b, ..., t0:min(n, t0 + 128)].max(-1) for t0 in range(0, n, 128)]
+        run = cm[0]
+        for m in cm[1:]:
+            jumps += int(np.sum(m > run + 8.0))
+            run = np.maximum(run, m)
+    assert jumps > 100
+    out = host(c.decode_shared(dev(Q), d["key_len"]))
+    ref = O.decode_shared(Q, K, V, h["key_len"])
+    assert np.abs(out - ref).max() <= DECODE_BF16_MAX_ABS
