@@ -19,6 +19,8 @@
 //    more than 2^8 (one bar.red.or per chunk tells); a move costs a warp
 //    redux.sync and a 4-entry shared-memory max, plus, inside a row segment, a
 //    rescale of the O accumulator in TMEM before the chunk's P.V is issued.
+//    The MMA warp only builds Q tiles and issues the score MMAs; K and V stream
+//    through separate rings (a K stage returns once its score MMA has run).
 //    Probabilities (<= 256) are written, rounded to bf16, as P^T[query][key] in
 //    the 128-byte-swizzled K-major layout; the running sums add the same
 //    rounded values, so the weights of the final average sum to one exactly.
@@ -27,8 +29,9 @@
 //    written (K-major), accumulated over the row segment's chunks in TMEM (two
 //    buffers, alternate segments). With M = 64 the accumulator rows sit in
 //    lanes 0..15 of each warp's 32-lane quarter: channel 16w + l in lane
-//    32w + l. The MMA warp issues a chunk's P.V as soon as its P^T is ready,
-//    even while it waits for the next chunk's data.
+//    32w + l. One consumer thread issues the chunk's P.V right after the
+//    barrier that completes P^T; an O rescale (rare) waits for the previous
+//    P.V's commit and runs before it.
 //  * at the end of a segment each consumer warp reads its 16 channels of O^T
 //    and writes them for every query (result or the segment's partial slot).
 //
@@ -71,9 +74,8 @@ constexpr int kCtasPerSm = 2;
 constexpr uint32_t kTmemCols = 128;            // S: 2 x 32 at 0; O^T: 2 x 16 (row segments) at 64
 constexpr uint32_t kOCol = 64;
 constexpr float kRescaleLog2 = 8.f;            // a reference max moves only past this margin (x256)
-// K full/empty, V full/empty [kStages]; tfull, tempty, pfull, pempty, ofull, oempty [2];
-// odone, rescaled
-constexpr int kBars = 4 * kStages + 14;
+// K full/empty, V full/empty [kStages]; tfull, tempty, pempty, ofull [2]
+constexpr int kBars = 4 * kStages + 8;
 constexpr int kPRegion = 2 * kPBytes;
 
 struct TcParams {
@@ -178,8 +180,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   float* s_corr = s_red + kConsumerWarps * kNPad;                     // [16] factors of the last max update
   float* s_sum = s_corr + kNPad;                                      // [2][4][16] per-warp sums of a segment
   float* s_m = s_sum + 2 * kConsumerWarps * kNPad;                    // [2][16] references of a segment
-  int* s_pflag = reinterpret_cast<int*>(s_m + 2 * kNPad);             // [2] O rescale before the chunk's P.V
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_pflag + 2);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_m + 2 * kNPad);
   long long* s_first = reinterpret_cast<long long*>(bars + kBars);
   int* s_nch = reinterpret_cast<int*>(s_first + p.B + 1);
   volatile int* s_flags = reinterpret_cast<volatile int*>(s_nch + p.B + (p.B & 1));   // abort, last, tmem base
@@ -189,12 +190,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   auto vempty_bar = [&](int s) { return smem_u32(&bars[3 * kStages + s]); };
   auto tfull_bar = [&](int a) { return smem_u32(&bars[4 * kStages + a]); };
   auto tempty_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 2 + a]); };
-  auto pfull_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 4 + a]); };
-  auto pempty_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 6 + a]); };
-  auto ofull_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 8 + a]); };
-  auto oempty_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 10 + a]); };
-  const uint32_t odone_bar = smem_u32(&bars[4 * kStages + 12]);
-  const uint32_t rescaled_bar = smem_u32(&bars[4 * kStages + 13]);
+  auto pempty_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 4 + a]); };
+  auto ofull_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 6 + a]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int LH = p.LH, nq = p.nq;
@@ -235,13 +232,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
       mbar_init(tempty_bar(a), kConsumerWarps);
-      mbar_init(pfull_bar(a), 1);
       mbar_init(pempty_bar(a), 1);
       mbar_init(ofull_bar(a), 1);
-      mbar_init(oempty_bar(a), kConsumerWarps);
     }
-    mbar_init(odone_bar, 1);
-    mbar_init(rescaled_bar, kConsumerWarps);
     fence_mbar_init();
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
@@ -310,161 +303,75 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     __syncwarp();
   } else if (active && warp == kMmaWarp) {
-    // ------------------------------------------------------------ Q tiles + MMA issue
-    // A polling loop that never blocks on one condition: chunk ns gets its scores
-    // once its K tile is in and its score buffer is free; chunk np (<= ns) gets its
-    // P.V once its P^T, its V tile and (at a segment start) the O buffer are ready.
+    // ------------------------------------------------------------ Q tiles + score MMAs
     constexpr uint32_t idesc_s = make_idesc(1u, kChunk, kSCols);
-    constexpr uint32_t idesc_o = make_idesc(1u, kDh, kNPad) | (1u << 15);   // A (V^T) MN-major
-    const long long nck = g1 - g0;
     Cursor cur = locate(g0, s_first, s_nch, p.B);
-    int prev_b = -1, prev_lh = -1, seg = -1;
-    uint32_t info = 0;     // 4 bits per chunk mod 4: first, last, segment parity, (segment / 2) parity
-    long long ns = 0, np = 0;
-    int pv_phase = 0;      // chunk np: 0 wait P^T, 1 wait the O rescale, 2 wait V tile (+ O buffer)
-    uint32_t resc = 0;     // O rescales served so far
+    int prev_b = -1, prev_lh = -1;
     bool ok = true;
-    uint64_t t_move = globaltimer_ns();
-    uint32_t idle = 0;
-    while (np < nck) {
-      bool moved = false;
-      if (ns < nck) {
-        // ---- scores of chunk ns
-        const int a = static_cast<int>(ns & 1), s = static_cast<int>(ns % kStages);
-        const bool first = cur.b != prev_b || cur.lh != prev_lh;   // a new row segment
-        int ready = 0;
-        if (lane == 0)
-          ready = mbar_test_wait(tempty_bar(a), static_cast<uint32_t>(((ns >> 1) & 1) ^ 1)) &&
-                  mbar_test_wait(kfull_bar(s), static_cast<uint32_t>((ns / kStages) & 1)) &&
-                  (!first || ns == 0 ||
-                   mbar_test_wait(tfull_bar(static_cast<int>((ns - 1) & 1)), static_cast<uint32_t>(((ns - 1) >> 1) & 1)));
-        if (__shfl_sync(0xffffffffu, ready, 0)) {
-          if (first) {
-            // Its queries become the B operand of the scores, as bf16 hi (rows 0..15)
-            // and lo (rows 16..31) parts: K.(hi + lo) carries Q to about 16 mantissa
-            // bits. The single Q tile is rewritten after the previous chunk's score
-            // MMA (and so every earlier MMA) has finished, as just tested.
-            ++seg;
-            const int qr = lane >> 1, half = lane & 1;   // query row, half of the channels
-            const bool valid = qr < nq;
-            const float* src = p.Q + qrow(cur.b, cur.lh, valid ? qr : 0) * kDh + half * 32;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t wh[4], wl[4];
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const float4 f = valid ? __ldg(reinterpret_cast<const float4*>(src) + 2 * j + k)
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-                const float x[4] = {f.x * p.qscale, f.y * p.qscale, f.z * p.qscale, f.w * p.qscale};
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                  __nv_bfloat162 hi = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-                  __nv_bfloat162 lo =
-                      __floats2bfloat162_rn(x[2 * e] - __low2float(hi), x[2 * e + 1] - __high2float(hi));
-                  wh[2 * k + e] = *reinterpret_cast<uint32_t*>(&hi);
-                  wl[2 * k + e] = *reinterpret_cast<uint32_t*>(&lo);
-                }
-              }
-              // a row is 128 bytes = 8 chunks of 8 bf16; this lane writes chunks 4*half .. 4*half+3
-              const uint32_t chunk = static_cast<uint32_t>(4 * half + j);
-              const int rl = qr + kNPad;
-              st_shared_v4(q_base + qr * 128 + ((chunk ^ (qr & 7)) << 4), wh[0], wh[1], wh[2], wh[3]);
-              st_shared_v4(q_base + rl * 128 + ((chunk ^ (rl & 7)) << 4), wl[0], wl[1], wl[2], wl[3]);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            prev_b = cur.b;
-            prev_lh = cur.lh;
-          }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t kt = stage_base + s * kStageBytes;
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * kSCols);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_bf16(d_tmem, smem_desc_k_sw128(kt + k * 32), smem_desc_k_sw128(q_base + k * 32), idesc_s,
-                       k != 0 ? 1u : 0u);
-            tc_commit(tfull_bar(a));
-            tc_commit(kempty_bar(s));
-          }
-          __syncwarp();
-          const bool last = (cur.c == s_nch[cur.b] - 1) || (g0 + ns + 1 == g1);
-          const uint32_t bits = (first ? 1u : 0u) | (last ? 2u : 0u) | (static_cast<uint32_t>(seg & 3) << 2);
-          const int sh = static_cast<int>(ns & 3) * 4;
-          info = (info & ~(0xFu << sh)) | (bits << sh);
-          advance(cur, s_nch, p.B, LH);
-          ++ns;
-          moved = true;
-        }
+    for (long long g = g0, i = 0; g < g1; ++g, ++i) {
+      const int s = static_cast<int>(i % kStages);
+      const int a = static_cast<int>(i & 1);
+      if (!mbar_wait(tempty_bar(a), static_cast<uint32_t>(((i >> 1) & 1) ^ 1), s_flags)) {
+        ok = false;
+        break;
       }
-      if (np < ns) {
-        // ---- P.V of chunk np: A = its V tile (as V^T), B = P^T buffer np&1,
-        // D = the segment's O^T buffer (accumulating from its first chunk)
-        const int b = static_cast<int>(np & 1), st = static_cast<int>(np % kStages);
-        const uint32_t bits = (info >> (static_cast<int>(np & 3) * 4)) & 0xFu;
-        const bool first = bits & 1u, last = bits & 2u;
-        const int rb = static_cast<int>((bits >> 2) & 1u);
-        const uint32_t rb_parity = (bits >> 3) & 1u;
-        if (pv_phase == 0) {
-          int ready = lane == 0 ? mbar_test_wait(pfull_bar(b), static_cast<uint32_t>((np >> 1) & 1)) : 0;
-          if (__shfl_sync(0xffffffffu, ready, 0)) {
-            // the consumers ask for an O rescale once every P.V issued so far has finished
-            const int flag = __shfl_sync(0xffffffffu, lane == 0 ? s_pflag[b] : 0, 0);
-            if (flag && lane == 0) tc_commit(odone_bar);
-            __syncwarp();
-            pv_phase = flag ? 1 : 2;
-            moved = true;
-          }
-        }
-        if (pv_phase == 1) {
-          const int ready = lane == 0 ? mbar_test_wait(rescaled_bar, resc & 1u) : 0;
-          if (__shfl_sync(0xffffffffu, ready, 0)) {
-            ++resc;
-            pv_phase = 2;
-            moved = true;
-          }
-        }
-        if (pv_phase == 2) {
-          int ready = 0;
-          if (lane == 0)
-            ready = (!first || mbar_test_wait(oempty_bar(rb), rb_parity ^ 1u)) &&
-                    mbar_test_wait(vfull_bar(st), static_cast<uint32_t>((np / kStages) & 1));
-          if (__shfl_sync(0xffffffffu, ready, 0)) {
-            tc_fence_after();
-            if (lane == 0) {
-              const uint32_t pt = p_base + b * kPBytes;
-              const uint32_t vt = stage_base + st * kStageBytes + kTileBytes;
-              const uint32_t d_tmem = tmem_base + kOCol + static_cast<uint32_t>(rb * kNPad);
-#pragma unroll
-              for (int kb = 0; kb < kChunk / 16; ++kb) {
-                const uint64_t ad = smem_desc_mn_sw128(vt + kb * 2048);
-                const uint64_t bd = smem_desc_k_sw128(pt + (kb >> 2) * 2048 + (kb & 3) * 32);
-                mma_bf16(d_tmem, ad, bd, idesc_o, (first && kb == 0) ? 0u : 1u);
-              }
-              tc_commit(pempty_bar(b));
-              tc_commit(vempty_bar(st));
-              if (last) tc_commit(ofull_bar(rb));
-            }
-            __syncwarp();
-            ++np;
-            pv_phase = 0;
-            moved = true;
-          }
-        }
-      }
-      if (moved) {
-        idle = 0;
-        if (lane == 0) t_move = globaltimer_ns();
-        continue;
-      }
-      if ((++idle & 255u) == 0) {
-        int stop = 0;
-        if (lane == 0) stop = s_flags[0] != 0 || globaltimer_ns() - t_move > kWaitLimitNs || idle >= kWaitPollLimit;
-        if (__shfl_sync(0xffffffffu, stop, 0)) {
+      if (cur.b != prev_b || cur.lh != prev_lh) {
+        // A new row segment: its queries become the B operand of the scores, as bf16
+        // hi (rows 0..15) and lo (rows 16..31) parts: K.(hi + lo) carries Q to about
+        // 16 mantissa bits. The single Q tile is rewritten once the previous chunk's
+        // score MMA (and so every earlier one) has finished.
+        if (i > 0 && !mbar_wait(tfull_bar(static_cast<int>((i - 1) & 1)), static_cast<uint32_t>(((i - 1) >> 1) & 1),
+                                s_flags)) {
           ok = false;
           break;
         }
+        const int qr = lane >> 1, half = lane & 1;   // query row, half of the channels
+        const bool valid = qr < nq;
+        const float* src = p.Q + qrow(cur.b, cur.lh, valid ? qr : 0) * kDh + half * 32;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t wh[4], wl[4];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const float4 f = valid ? __ldg(reinterpret_cast<const float4*>(src) + 2 * j + k)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float x[4] = {f.x * p.qscale, f.y * p.qscale, f.z * p.qscale, f.w * p.qscale};
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              __nv_bfloat162 hi = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+              __nv_bfloat162 lo = __floats2bfloat162_rn(x[2 * e] - __low2float(hi), x[2 * e + 1] - __high2float(hi));
+              wh[2 * k + e] = *reinterpret_cast<uint32_t*>(&hi);
+              wl[2 * k + e] = *reinterpret_cast<uint32_t*>(&lo);
+            }
+          }
+          // a row is 128 bytes = 8 chunks of 8 bf16; this lane writes chunks 4*half .. 4*half+3
+          const uint32_t chunk = static_cast<uint32_t>(4 * half + j);
+          const int rl = qr + kNPad;
+          st_shared_v4(q_base + qr * 128 + ((chunk ^ (qr & 7)) << 4), wh[0], wh[1], wh[2], wh[3]);
+          st_shared_v4(q_base + rl * 128 + ((chunk ^ (rl & 7)) << 4), wl[0], wl[1], wl[2], wl[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        prev_b = cur.b;
+        prev_lh = cur.lh;
       }
+      if (!mbar_wait(kfull_bar(s), static_cast<uint32_t>((i / kStages) & 1), s_flags)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint64_t kd = smem_desc_k_sw128(stage_base + s * kStageBytes);
+        const uint64_t qd = smem_desc_k_sw128(q_base);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * kSCols);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)   // +32 bytes along K per MMA: +2 in the address field
+          mma_bf16(d_tmem, kd + 2 * k, qd + 2 * k, idesc_s, k != 0 ? 1u : 0u);
+        tc_commit(tfull_bar(a));
+        tc_commit(kempty_bar(s));
+      }
+      __syncwarp();
+      advance(cur, s_nch, p.B, LH);
     }
     if (!ok) {
       s_flags[0] = 1;
@@ -473,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   } else if (active) {
     // ------------------------------------------------------------ consumers
     const int tid = threadIdx.x;                   // 0..127: key of the chunk for the softmax
+    constexpr uint32_t idesc_o = make_idesc(1u, kDh, kNPad) | (1u << 15);   // A (V^T) MN-major
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     // P^T byte offset of (query 0, key tid) in buffer 0: key half, swizzled 16-byte chunk
     const int kk = tid & 63;
@@ -490,7 +398,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     bool ok = true;
     int seg = 0;          // index of the current row segment
-    uint32_t resc = 0;    // O rescales done so far
     // A finished segment waiting to be written out (one chunk later, so that its
     // last P.V has run by then).
     bool f_pending = false, f_whole = false;
@@ -512,8 +419,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       tmem_ld_32x32b_x16(tmem_base + lane_base + kOCol + static_cast<uint32_t>(rb * kNPad), o);
       tmem_ld_wait();
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(oempty_bar(rb));
       float* sO = reinterpret_cast<float*>(bp + free_pbuf * kPBytes);   // [16][64]
       if (lane < 16) {   // lane l of warp w: channel 16w + l
 #pragma unroll
@@ -591,6 +496,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int nch = s_nch[cur.b];
       const int n = min(kChunk, kl - cur.c * kChunk);
       const bool seg_first = cur.c == seg_c0;
+      const bool seg_ends = (cur.c == nch - 1) || (g + 1 == g1);
       if (ok && !mbar_wait(tfull_bar(a), acc_parity, s_flags)) fail();
       tc_fence_after();
       uint32_t sh[16], sl[16];   // K.Q_hi, K.Q_lo
@@ -654,33 +560,45 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         for (int u = n * (kRowBytes / 16) + tid; u < kTileBytes / 16; u += kConsumerWarps * 32)
           st_shared_v4(vt + u * 16, 0u, 0u, 0u, 0u);
       }
-      if (tid == 0) s_pflag[a] = rescale_o ? 1 : 0;
       fence_proxy_async_smem();
       named_barrier(1, kConsumerWarps * 32);                 // P^T (and the V tail) complete
-      if (tid == 0) mbar_arrive(pfull_bar(a));
+      const int rb = seg & 1;
       if (rescale_o) {
         // O^T (chunks before this one) *= corr per query column, after their P.V and
         // before this chunk's; each warp scales its own 16 channel lanes
-        if (ok && !mbar_wait(odone_bar, resc & 1u, s_flags)) fail();
+        if (ok && !mbar_wait(pempty_bar(a ^ 1), static_cast<uint32_t>(((i - 1) >> 1) & 1), s_flags)) fail();
         tc_fence_after();
         uint32_t o[16];
-        tmem_ld_32x32b_x16(tmem_base + lane_base + kOCol + static_cast<uint32_t>((seg & 1) * kNPad), o);
+        tmem_ld_32x32b_x16(tmem_base + lane_base + kOCol + static_cast<uint32_t>(rb * kNPad), o);
         tmem_ld_wait();
 #pragma unroll
         for (int q = 0; q < kNQT; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * s_corr[q]);
-        tmem_st_32x32b_x16(tmem_base + lane_base + kOCol + static_cast<uint32_t>((seg & 1) * kNPad), o);
+        tmem_st_32x32b_x16(tmem_base + lane_base + kOCol + static_cast<uint32_t>(rb * kNPad), o);
         tmem_st_wait();
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(rescaled_bar);
-        ++resc;
+        named_barrier(1, kConsumerWarps * 32);
+      }
+      if (tid == 0) {
+        // ---- P.V of this chunk: A = its V tile (as V^T), B = P^T, D = the segment's
+        // O^T (accumulating from the segment's first chunk on)
+        if (ok && !mbar_wait(vfull_bar(s), static_cast<uint32_t>((i / kStages) & 1), s_flags)) fail();
+        tc_fence_after();
+        const uint64_t vd = smem_desc_mn_sw128(stage_base + s * kStageBytes + kTileBytes);
+        const uint64_t pd = smem_desc_k_sw128(p_base + a * kPBytes);
+        const uint32_t d_tmem = tmem_base + kOCol + static_cast<uint32_t>(rb * kNPad);
+#pragma unroll
+        for (int kb = 0; kb < kChunk / 16; ++kb)   // 16 keys: 2048 bytes of V, 32 bytes of a P^T row
+          mma_bf16(d_tmem, vd + kb * (2048 >> 4), pd + (kb >> 2) * (2048 >> 4) + (kb & 3) * 2, idesc_o,
+                   (seg_first && kb == 0) ? 0u : 1u);
+        tc_commit(pempty_bar(a));
+        tc_commit(vempty_bar(s));
+        if (seg_ends) tc_commit(ofull_bar(rb));
       }
       // the previous segment's P.V has run by now; its P^T buffer (the other one) stages O
       if (f_pending) flush(a ^ 1);
 
-      if ((cur.c == nch - 1) || (g + 1 == g1)) {
+      if (seg_ends) {
         // ---- the segment ends: per-warp sums over the keys, references; written out next chunk
-        const int rb = seg & 1;
 #pragma unroll
         for (int q = 0; q < kNQT; ++q) {
           float sq = s_run[q];
@@ -754,7 +672,7 @@ EncodeTiledFn encoder() {
 
 size_t smem_bytes(int B) {
   size_t n = 1024 + kPRegion + static_cast<size_t>(kStages) * kStageBytes + kQTileBytes;
-  n += (kConsumerWarps * kNPad + kNPad + 2 * kConsumerWarps * kNPad + 2 * kNPad) * 4 + 2 * 4 + kBars * 8;
+  n += (kConsumerWarps * kNPad + kNPad + 2 * kConsumerWarps * kNPad + 2 * kNPad) * 4 + kBars * 8;
   n += static_cast<size_t>(B + 1) * 8 + static_cast<size_t>(B + (B & 1)) * 4 + 16;
   return n;
 }
