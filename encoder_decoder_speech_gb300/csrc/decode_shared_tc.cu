@@ -183,7 +183,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_m + 2 * kNPad);
   long long* s_first = reinterpret_cast<long long*>(bars + kBars);
   int* s_nch = reinterpret_cast<int*>(s_first + p.B + 1);
-  volatile int* s_flags = reinterpret_cast<volatile int*>(s_nch + p.B + (p.B & 1));   // abort, last, tmem base
+  int* s_kl = s_nch + p.B + (p.B & 1);                                 // key lengths, clamped to [0, T]
+  volatile int* s_flags = reinterpret_cast<volatile int*>(s_kl + p.B + (p.B & 1));   // abort, last, tmem base
   auto kfull_bar = [&](int s) { return smem_u32(&bars[s]); };
   auto kempty_bar = [&](int s) { return smem_u32(&bars[kStages + s]); };
   auto vfull_bar = [&](int s) { return smem_u32(&bars[2 * kStages + s]); };
@@ -206,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int kl = min(max(__ldg(p.key_len + b), 0), p.T);
         nch = (kl + kChunk - 1) / kChunk;
         s_nch[b] = nch;
+        s_kl[b] = kl;
       }
       long long v = static_cast<long long>(nch) * LH;
 #pragma unroll
@@ -255,12 +257,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const long long g1 = active ? (blockIdx.x + 1) * total / ranges : 0;
   auto qrow = [&](int b, int lh, int n) { return (static_cast<long long>(b) * nq + n) * LH + lh; };
 
-  // Q, out and the workspace may belong to the previous grid.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  {
+  // Q, out and the workspace may belong to the previous grid; the cache and key_len
+  // are read before it has finished (no decode writes them), so the producer warp
+  // starts streaming without waiting.
+  if (warp != kProducerWarp) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (warp < kConsumerWarps) {   // rows of slots without any valid key: out = 0
     const long long per_slot = static_cast<long long>(nq) * LH * (kDh / 4);
-    for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < p.B * per_slot;
-         i += static_cast<long long>(gridDim.x) * kThreads)
+    for (long long i = static_cast<long long>(blockIdx.x) * (kConsumerWarps * 32) + threadIdx.x; i < p.B * per_slot;
+         i += static_cast<long long>(gridDim.x) * (kConsumerWarps * 32))
       if (s_nch[static_cast<int>(i / per_slot)] == 0)
         reinterpret_cast<float4*>(p.out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
@@ -282,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           ok = false;
           break;
         }
-        const int kl = min(max(__ldg(p.key_len + cur.b), 0), p.T);
+        const int kl = s_kl[cur.b];
         const int t0 = cur.c * kChunk;
         const int nbox = (min(kChunk, kl - t0) + kBoxRows - 1) / kBoxRows;   // rows past them stay stale
         const int crow = cur.b * p.LHc + p.lh0 + cur.lh;
@@ -445,15 +449,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           P[0] = ok ? s_m[rb * kNPad + tid] : -INFINITY;
           P[1] = ok ? sum[tid] + sum[kNPad + tid] + sum[2 * kNPad + tid] + sum[3 * kNPad + tid] : 0.f;
         }
-        __threadfence();
+        // the barrier orders every thread's partial writes before thread 0's
+        // device-scope fence and the counter update that publishes them
         named_barrier(1, kConsumerWarps * 32);
         if (tid == 0) {
+          __threadfence();
           const unsigned int prev = atomicAdd(p.counters + f_row, 1u);
           s_flags[1] = (prev == static_cast<unsigned int>(f_nseg - 1)) ? 1 : 0;
+          __threadfence();
         }
         named_barrier(1, kConsumerWarps * 32);
         if (s_flags[1]) {
-          __threadfence();
 #pragma unroll 2
           for (int e = tid; e < nq * kDh; e += kConsumerWarps * 32) {   // (query, channel)
             const int q = e / kDh, c = e % kDh;
@@ -492,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int s = static_cast<int>(i % kStages);
       const int a = static_cast<int>(i & 1);
       const uint32_t acc_parity = static_cast<uint32_t>((i >> 1) & 1);
-      const int kl = min(max(__ldg(p.key_len + cur.b), 0), p.T);
+      const int kl = s_kl[cur.b];
       const int nch = s_nch[cur.b];
       const int n = min(kChunk, kl - cur.c * kChunk);
       const bool seg_first = cur.c == seg_c0;
@@ -673,7 +679,7 @@ EncodeTiledFn encoder() {
 size_t smem_bytes(int B) {
   size_t n = 1024 + kPRegion + static_cast<size_t>(kStages) * kStageBytes + kQTileBytes;
   n += (kConsumerWarps * kNPad + kNPad + 2 * kConsumerWarps * kNPad + 2 * kNPad) * 4 + kBars * 8;
-  n += static_cast<size_t>(B + 1) * 8 + static_cast<size_t>(B + (B & 1)) * 4 + 16;
+  n += static_cast<size_t>(B + 1) * 8 + 2 * static_cast<size_t>(B + (B & 1)) * 4 + 16;
   return n;
 }
 
