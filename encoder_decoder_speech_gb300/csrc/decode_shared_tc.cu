@@ -67,15 +67,16 @@ constexpr int kStages = 3;
 constexpr int kPBytes = 4096;                  // P^T of a chunk: 2 key halves x 16 rows x 128 B
 constexpr int kQTileBytes = kSCols * kRowBytes; // 4 KB
 constexpr int kConsumerWarps = 4;              // one key per consumer thread
-constexpr int kThreads = (kConsumerWarps + 2) * 32;   // + producer warp + MMA warp
+constexpr int kThreads = (kConsumerWarps + 3) * 32;   // + producer, score-MMA and P.V-MMA warps
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kMmaWarp = kConsumerWarps + 1;
+constexpr int kPvWarp = kConsumerWarps + 2;
 constexpr int kCtasPerSm = 2;
 constexpr uint32_t kTmemCols = 128;            // S: 2 x 32 at 0; O^T: 2 x 16 (row segments) at 64
 constexpr uint32_t kOCol = 64;
 constexpr float kRescaleLog2 = 8.f;            // a reference max moves only past this margin (x256)
-// K full/empty, V full/empty [kStages]; tfull, tempty, pempty, ofull [2]
-constexpr int kBars = 4 * kStages + 8;
+// K full/empty, V full/empty [kStages]; tfull, tempty, pfull, pempty, ofull [2]
+constexpr int kBars = 4 * kStages + 10;
 constexpr int kPRegion = 2 * kPBytes;
 
 struct TcParams {
@@ -193,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   auto tempty_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 2 + a]); };
   auto pempty_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 4 + a]); };
   auto ofull_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 6 + a]); };
+  auto pfull_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 8 + a]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int LH = p.LH, nq = p.nq;
@@ -236,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       mbar_init(tempty_bar(a), kConsumerWarps);
       mbar_init(pempty_bar(a), 1);
       mbar_init(ofull_bar(a), 1);
+      mbar_init(pfull_bar(a), 1);
     }
     fence_mbar_init();
     prefetch_tmap(&tmK);
@@ -312,6 +315,29 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     Cursor cur = locate(g0, s_first, s_nch, p.B);
     int prev_b = -1, prev_lh = -1;
     bool ok = true;
+    // lane: query row (lane / 2), half (lane & 1) of its channels. The rows of the
+    // next segment are loaded into registers while the current one runs.
+    const int qr = lane >> 1, half = lane & 1;
+    const bool q_valid = qr < nq;
+    float4 qn[8];
+    auto load_q = [&](int b, int lh) {
+      const float* src = p.Q + qrow(b, lh, q_valid ? qr : 0) * kDh + half * 32;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        qn[j] = q_valid ? __ldg(reinterpret_cast<const float4*>(src) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    // the segment after the row (b, lh), whose chunk 0 is g, if this CTA's range reaches it
+    auto load_next_segment = [&](int b, int lh, long long g) {
+      if (g + s_nch[b] >= g1) return;
+      if (++lh == LH) {
+        lh = 0;
+        do {
+          ++b;
+        } while (b < p.B && s_nch[b] == 0);
+      }
+      load_q(b, lh);
+    };
+    load_q(cur.b, cur.lh);
     for (long long g = g0, i = 0; g < g1; ++g, ++i) {
       const int s = static_cast<int>(i % kStages);
       const int a = static_cast<int>(i & 1);
@@ -323,22 +349,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // A new row segment: its queries become the B operand of the scores, as bf16
         // hi (rows 0..15) and lo (rows 16..31) parts: K.(hi + lo) carries Q to about
         // 16 mantissa bits. The single Q tile is rewritten once the previous chunk's
-        // score MMA (and so every earlier one) has finished.
+        // score MMA (and so every earlier one from this thread) has finished.
         if (i > 0 && !mbar_wait(tfull_bar(static_cast<int>((i - 1) & 1)), static_cast<uint32_t>(((i - 1) >> 1) & 1),
                                 s_flags)) {
           ok = false;
           break;
         }
-        const int qr = lane >> 1, half = lane & 1;   // query row, half of the channels
-        const bool valid = qr < nq;
-        const float* src = p.Q + qrow(cur.b, cur.lh, valid ? qr : 0) * kDh + half * 32;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint32_t wh[4], wl[4];
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
-            const float4 f = valid ? __ldg(reinterpret_cast<const float4*>(src) + 2 * j + k)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 f = qn[2 * j + k];
             const float x[4] = {f.x * p.qscale, f.y * p.qscale, f.z * p.qscale, f.w * p.qscale};
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -358,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         __syncwarp();
         prev_b = cur.b;
         prev_lh = cur.lh;
+        load_next_segment(cur.b, cur.lh, g - cur.c);
       }
       if (!mbar_wait(kfull_bar(s), static_cast<uint32_t>((i / kStages) & 1), s_flags)) {
         ok = false;
@@ -381,10 +404,52 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       s_flags[0] = 1;
       atomicOr(p.status, 1u);
     }
+  } else if (active && warp == kPvWarp) {
+    // ------------------------------------------------------------ P.V MMAs
+    // Each chunk's P.V once its P^T and V tile are ready: A = the V tile (as V^T),
+    // B = P^T, D = the row segment's O^T buffer (accumulating from its first chunk).
+    if (lane == 0) {
+      constexpr uint32_t idesc_o = make_idesc(1u, kDh, kNPad) | (1u << 15);   // A (V^T) MN-major
+      Cursor cur = locate(g0, s_first, s_nch, p.B);
+      int prev_b = -1, prev_lh = -1, seg = -1;
+      bool ok = true;
+      for (long long g = g0, i = 0; g < g1; ++g, ++i) {
+        const int b = static_cast<int>(i & 1), st = static_cast<int>(i % kStages);
+        const bool first = cur.b != prev_b || cur.lh != prev_lh;
+        if (first) {
+          ++seg;
+          prev_b = cur.b;
+          prev_lh = cur.lh;
+        }
+        const bool last = (cur.c == s_nch[cur.b] - 1) || (g + 1 == g1);
+        if (!mbar_wait(pfull_bar(b), static_cast<uint32_t>((i >> 1) & 1), s_flags) ||
+            !mbar_wait(vfull_bar(st), static_cast<uint32_t>((i / kStages) & 1), s_flags)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int rb = seg & 1;
+        const uint64_t vd = smem_desc_mn_sw128(stage_base + st * kStageBytes + kTileBytes);
+        const uint64_t pd = smem_desc_k_sw128(p_base + b * kPBytes);
+        const uint32_t d_tmem = tmem_base + kOCol + static_cast<uint32_t>(rb * kNPad);
+#pragma unroll
+        for (int kb = 0; kb < kChunk / 16; ++kb)   // 16 keys: 2048 bytes of V, 32 bytes of a P^T row
+          mma_bf16(d_tmem, vd + kb * (2048 >> 4), pd + (kb >> 2) * (2048 >> 4) + (kb & 3) * 2, idesc_o,
+                   (first && kb == 0) ? 0u : 1u);
+        tc_commit(pempty_bar(b));
+        tc_commit(vempty_bar(st));
+        if (last) tc_commit(ofull_bar(rb));
+        advance(cur, s_nch, p.B, LH);
+      }
+      if (!ok) {
+        s_flags[0] = 1;
+        atomicOr(p.status, 1u);
+      }
+    }
+    __syncwarp();
   } else if (active) {
     // ------------------------------------------------------------ consumers
     const int tid = threadIdx.x;                   // 0..127: key of the chunk for the softmax
-    constexpr uint32_t idesc_o = make_idesc(1u, kDh, kNPad) | (1u << 15);   // A (V^T) MN-major
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     // P^T byte offset of (query 0, key tid) in buffer 0: key half, swizzled 16-byte chunk
     const int kk = tid & 63;
@@ -584,22 +649,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         tc_fence_before();
         named_barrier(1, kConsumerWarps * 32);
       }
-      if (tid == 0) {
-        // ---- P.V of this chunk: A = its V tile (as V^T), B = P^T, D = the segment's
-        // O^T (accumulating from the segment's first chunk on)
-        if (ok && !mbar_wait(vfull_bar(s), static_cast<uint32_t>((i / kStages) & 1), s_flags)) fail();
-        tc_fence_after();
-        const uint64_t vd = smem_desc_mn_sw128(stage_base + s * kStageBytes + kTileBytes);
-        const uint64_t pd = smem_desc_k_sw128(p_base + a * kPBytes);
-        const uint32_t d_tmem = tmem_base + kOCol + static_cast<uint32_t>(rb * kNPad);
-#pragma unroll
-        for (int kb = 0; kb < kChunk / 16; ++kb)   // 16 keys: 2048 bytes of V, 32 bytes of a P^T row
-          mma_bf16(d_tmem, vd + kb * (2048 >> 4), pd + (kb >> 2) * (2048 >> 4) + (kb & 3) * 2, idesc_o,
-                   (seg_first && kb == 0) ? 0u : 1u);
-        tc_commit(pempty_bar(a));
-        tc_commit(vempty_bar(s));
-        if (seg_ends) tc_commit(ofull_bar(rb));
-      }
+      if (tid == 0) mbar_arrive(pfull_bar(a));               // the MMA warp issues this chunk's P.V
       // the previous segment's P.V has run by now; its P^T buffer (the other one) stages O
       if (f_pending) flush(a ^ 1);
 
