@@ -610,6 +610,10 @@ def run_block(args):
         with torch.cuda.graph(graph):
             step()
         torch.cuda.synchronize()
+        n0 = cxa.cxa_launch_count()
+        step()
+        torch.cuda.synchronize()
+        kernels_per_step = cxa.cxa_launch_count() - n0
         for mode in ("eager", "graph"):
             run = step if mode == "eager" else graph.replay
             for _ in range(args.warmup):
@@ -626,7 +630,7 @@ def run_block(args):
                               "us_per_step": round(us, 2), "tokens_per_s": round(w.B / (us * 1e-6), 1),
                               "GBps": round(byts / (us * 1e-6) / 1e9, 1),
                               "frac_of_measured_hbm": round(byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 3),
-                              "kernels_per_step": 3 * w.L}), flush=True)
+                              "kernels_per_step": kernels_per_step}), flush=True)
         del graph
         cache.close()
     assert cxa.cxa_device_status(1) == cxa.CXA_OK

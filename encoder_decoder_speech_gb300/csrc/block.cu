@@ -255,6 +255,14 @@ cudaError_t launch_block(const BlockLaunch& a, const DeviceInfo& dev, cudaStream
   const size_t rows = align256(static_cast<size_t>(a.B) * d * sizeof(float));
   float* q = reinterpret_cast<float*>(ws + dec_bytes);
   float* att = reinterpret_cast<float*>(ws + dec_bytes + rows);
+  if (fused_block_supported(a.H, 64)) {
+    // up to 8 heads: LayerNorm, query, attention (and, when a cluster of H CTAs per
+    // slot fits for every slot at once, the out projection too) in one kernel
+    bool gathered = false;
+    cudaError_t e = launch_block_fused(a, att, &gathered, dev, stream);
+    if (e != cudaSuccess || gathered) return e;
+    return launch_gemv<false>(att, nullptr, nullptr, 0.f, a.WO, a.bO, a.x, a.x, a.B, d, dev.device, stream);
+  }
 
   // 1. h = LayerNorm(x); q = h x WQ + bQ
   cudaError_t e = launch_gemv<true>(a.x, a.gamma, a.beta, a.eps, a.WQ, a.bQ, nullptr, q, a.B, d, dev.device, stream);

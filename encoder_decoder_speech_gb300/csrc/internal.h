@@ -119,6 +119,12 @@ cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream);
 cudaError_t launch_decode_shared_tc(const DecodeLaunch& a, const DeviceInfo& dev, cudaStream_t stream,
                                     std::string* msg);
 cudaError_t launch_alignment(const AlignLaunch& a, cudaStream_t stream);
+// The block as one kernel per layer: a cluster of H CTAs per slot (block_fused.cu).
+bool fused_block_supported(int H, int dh);
+// With *gathered set the launch did the whole block; otherwise it wrote the attention
+// rows to att [B][d] and the out projection remains to be launched.
+cudaError_t launch_block_fused(const BlockLaunch& a, float* att, bool* gathered, const DeviceInfo& dev,
+                               cudaStream_t stream);
 size_t block_workspace_bytes(int B, int T, int H);
 
 // Bytes at the start of a decode workspace that hold the per-row arrival

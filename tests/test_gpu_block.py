@@ -73,6 +73,28 @@ def test_cross_block(cache_dtype, with_affine):
 
 
 @pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("H", [1, 6, 10])
+def test_cross_block_head_counts(cache_dtype, H):
+    """Up to 8 heads the block runs as one kernel (a cluster of H CTAs per slot),
+    beyond that as three; an empty slot (key_len 0) gets x += bO only."""
+    w = W.custom("blockH%d" % H, B=3, T=300, d=64 * H, L=2, H=H, ragged=True, index=960 + H)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, cache_dtype)
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    p = _block_params(w.d, 62 + H)
+    kl = h["key_len"].copy()
+    kl[1] = 0
+    x0 = _rand((w.B, w.d), 63 + H)
+    x = dev(x0)
+    dp = {k: dev(v) for k, v in p.items()}
+    c.cross_block(1, x, dp["WQ"], dp["WO"], dev(kl, torch.int32), ln_gamma=dp["gamma"], ln_beta=dp["beta"],
+                  bQ=dp["bQ"], bO=dp["bO"])
+    ref = O.cross_block(x0, 1, host(c.Kc), host(c.Vc), kl, p["WQ"], p["WO"], p["gamma"], p["beta"], 1e-5,
+                        p["bQ"], p["bO"])
+    assert np.abs(host(x) - ref).max() <= BLOCK_TOL[cache_dtype]
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
 def test_interleaved_layers_batched_base(cache_dtype):
     """Batched Whisper-Base: the six layers' blocks applied in turn to the residual
     stream, as a decoder step does, launched back to back without syncs."""
