@@ -213,7 +213,8 @@ int cxa_populate(cxa_cache* c, int b0, int nb, const void* E, const void* WK, co
 
 static int decode_common(const char* who, const cxa_cache* c, int l0, int nl, int nq, const float* Q,
                          const int* key_len, float* out, float scale, void* workspace, size_t workspace_bytes,
-                         void* stream, int key_len_add = 0) {
+                         void* stream, int key_len_add = 0, const float* K_new = nullptr,
+                         const float* V_new = nullptr) {
   const std::string w(who);
   if (c == nullptr) return fail(CXA_EINVAL, w + ": cache descriptor is NULL");
   if (nl == -1) nl = c->L;
@@ -259,6 +260,8 @@ static int decode_common(const char* who, const cxa_cache* c, int l0, int nl, in
   a.H = c->H;
   a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(c->dh));
   a.cache_bf16 = c->dtype == CXA_BF16;
+  a.K_new = K_new;
+  a.V_new = V_new;
   e = cxa::launch_decode(a, dev, static_cast<cudaStream_t>(stream), &msg);
   if (e != cudaSuccess) return fail_cuda(e, w + ": launch");
   return CXA_OK;
@@ -322,10 +325,15 @@ int cxa_self_attention_step(cxa_cache* c, const int* pos, const float* Q, const 
   if (!std::isfinite(scale)) return fail(CXA_EINVAL, "cxa_self_attention_step: scale must be finite");
   if (workspace_bytes < cxa::decode_workspace_bytes(c->B, c->T, c->L, c->H, 1))
     return fail(CXA_EINVAL, "cxa_self_attention_step: workspace smaller than cxa_decode_workspace_bytes()");
-  const int rc = cxa_cache_append(c, pos, K_new, V_new, stream);
-  if (rc != CXA_OK) return rc;
+  if (K_new == nullptr || V_new == nullptr)
+    return fail(CXA_EINVAL, "cxa_self_attention_step: a pointer argument is NULL");
+  if (!aligned(pos, 4) || !aligned(K_new, 16) || !aligned(V_new, 16))
+    return fail(CXA_EINVAL, "cxa_self_attention_step: K_new and V_new must be 16-byte aligned");
+  // appending makes every slot a valid (partly filled) self-attention cache
+  for (auto& r : c->ready) r = 1;
+  // one kernel: the append is fused into the decode over positions 0 .. pos[b]
   return decode_common("cxa_self_attention_step", c, 0, -1, 1, Q, pos, out, scale, workspace, workspace_bytes,
-                       stream, 1);
+                       stream, 1, K_new, V_new);
 }
 
 int cxa_alignment_weights(const cxa_cache* c, const float* Q, const int* key_len, const int* heads_lh, int nsel,

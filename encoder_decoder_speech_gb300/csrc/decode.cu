@@ -37,6 +37,7 @@
 //  * Programmatic dependent launch: the next decode grid on the stream starts
 //    streaming K/V while this one drains; it waits for this grid before
 //    reading queries or writing anything.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -116,7 +117,27 @@ struct DecodeParams {
   int key_len_add;     // valid keys = clamp(key_len[b] + key_len_add, 0, T)
   int part_stride;     // partial slots per (row, query) (ceil(T / 64))
   float qscale;        // scale * log2(e)
+  const float* Knew;   // kAppend: [B][L][H][64] rows for position key_len[b] (fp32)
+  const float* Vnew;
 };
+
+// kAppend: the new row of each (slot, layer, head) at its position, as the lane
+// slice of a cache row holds it (rounded to the cache dtype).
+template <bool kBF16, int kEPL>
+__device__ __forceinline__ void load_new_slice(const float* src, float* f) {
+#pragma unroll
+  for (int e4 = 0; e4 < kEPL / 4; ++e4) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(src) + e4);
+    f[4 * e4 + 0] = v.x;
+    f[4 * e4 + 1] = v.y;
+    f[4 * e4 + 2] = v.z;
+    f[4 * e4 + 3] = v.w;
+  }
+  if constexpr (kBF16) {
+#pragma unroll
+    for (int e = 0; e < kEPL; ++e) f[e] = __bfloat162float(__float2bfloat16_rn(f[e]));
+  }
+}
 
 // One lane's slice of a cache row -> fp32 values
 template <bool kBF16, int kSlice>
@@ -201,7 +222,12 @@ constexpr int min_ctas_per_sm() {
   return kNQ >= 4 ? 2 : CXA_DECODE_CTAS_PER_SM;
 }
 
-template <bool kBF16, int kNQ>
+// kAppend (self-attention step): the kernel also writes each row's new K/V at
+// position key_len[b] (when in [0, T)) and attends positions 0 .. key_len[b]; the
+// lane that meets that key takes it from Knew/Vnew rather than the cache copy it
+// streamed, so nothing in the grid waits for the writes. The previous step wrote
+// rows this one reads, so here the cache is read only after the grid dependency wait.
+template <bool kBF16, int kNQ, bool kAppend = false>
 __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
     decode_stream_kernel(const DecodeParams p) {
   using R = Traits<kBF16, kNQ>;
@@ -271,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
   const uint64_t pol = policy_evict_first();
   Cursor pcur{0, 0, 0};
   long long npre = 0;
+  if constexpr (kAppend) wait_prior_grid();
   if (active && producer) {
     pcur = locate(g0, s_first, s_nch, p.B, LH);
     Cursor c = pcur;
@@ -298,6 +325,33 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
          i += static_cast<long long>(gridDim.x) * kThreads) {
       if (s_nch[static_cast<int>(i / per_slot)] == 0)
         reinterpret_cast<float4*>(p.out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  if constexpr (kAppend) {
+    // the new rows into the cache: 16 lanes x 4 values per (slot, layer, head)
+    const long long rows = static_cast<long long>(p.B) * LH;
+    for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < rows * 16;
+         i += static_cast<long long>(gridDim.x) * kThreads) {
+      const long long row = i / 16;
+      const int l16 = static_cast<int>(i % 16);
+      const int b = static_cast<int>(row / LH), lh = static_cast<int>(row % LH);
+      const int t = __ldg(p.key_len + b);
+      if (t < 0 || t >= p.T) continue;
+      const long long crow = static_cast<long long>(b) * p.LHc + p.lh0 + lh;
+      const size_t dst = (static_cast<size_t>(crow) * p.T + t) * kDh + l16 * 4;
+      const float4 k = __ldg(reinterpret_cast<const float4*>(p.Knew + crow * kDh) + l16);
+      const float4 v = __ldg(reinterpret_cast<const float4*>(p.Vnew + crow * kDh) + l16);
+      if constexpr (kBF16) {
+        __nv_bfloat162 k01 = __floats2bfloat162_rn(k.x, k.y), k23 = __floats2bfloat162_rn(k.z, k.w);
+        __nv_bfloat162 v01 = __floats2bfloat162_rn(v.x, v.y), v23 = __floats2bfloat162_rn(v.z, v.w);
+        *reinterpret_cast<uint2*>(const_cast<uint8_t*>(p.Kc) + dst * 2) =
+            make_uint2(*reinterpret_cast<uint32_t*>(&k01), *reinterpret_cast<uint32_t*>(&k23));
+        *reinterpret_cast<uint2*>(const_cast<uint8_t*>(p.Vc) + dst * 2) =
+            make_uint2(*reinterpret_cast<uint32_t*>(&v01), *reinterpret_cast<uint32_t*>(&v23));
+      } else {
+        *reinterpret_cast<float4*>(const_cast<uint8_t*>(p.Kc) + dst * 4) = k;
+        *reinterpret_cast<float4*>(const_cast<uint8_t*>(p.Vc) + dst * 4) = v;
+      }
     }
   }
   if (!active) return;
@@ -377,6 +431,18 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
       const int kl = min(max(__ldg(p.key_len + cur.b) + p.key_len_add, 0), p.T);
       const int nch = s_nch[cur.b];
       const int n = min(R::kChunkKeys, kl - cur.c * R::kChunkKeys);
+      int subst = -1;   // kAppend: the chunk row that is the new key
+      const float* knew_row = nullptr;
+      const float* vnew_row = nullptr;
+      if constexpr (kAppend) {
+        const int t = __ldg(p.key_len + cur.b) - cur.c * R::kChunkKeys;
+        if (__ldg(p.key_len + cur.b) < p.T && t >= 0 && t < n) {
+          subst = t;
+          const long long crow = static_cast<long long>(cur.b) * p.LHc + p.lh0 + cur.lh;
+          knew_row = p.Knew + crow * kDh + sub * EPL;
+          vnew_row = p.Vnew + crow * kDh + sub * EPL;
+        }
+      }
       if (ok) {
         const uint8_t* sK = stages + s * R::kStageBytes;
         const uint8_t* sV = sK + R::kKVBytes;
@@ -410,6 +476,9 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
             const int r = warp * R::kKeysPerWarp + it * R::kRowsPerPass + grp;
             float f[EPL];
             load_slice<kBF16, R::kSliceBytes>(sK + r * R::kRowBytes + sub * R::kSliceBytes, f);
+            if constexpr (kAppend) {
+              if (r == subst) load_new_slice<kBF16, EPL>(knew_row, f);
+            }
 #pragma unroll
             for (int q = 0; q < kNQ; ++q) {
               float dot = 0.f;
@@ -438,6 +507,9 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
             if (r < n) {
               float f[EPL];
               load_slice<kBF16, R::kSliceBytes>(sV + r * R::kRowBytes + sub * R::kSliceBytes, f);
+              if constexpr (kAppend) {
+                if (r == subst) load_new_slice<kBF16, EPL>(vnew_row, f);
+              }
 #pragma unroll
               for (int q = 0; q < kNQ; ++q) {
                 const float pw = exp2f(sc[pb][q] - m[q]);
@@ -576,7 +648,7 @@ size_t dynamic_smem_bytes(int B) {
   return n;
 }
 
-template <bool kBF16, int kNQ>
+template <bool kBF16, int kNQ, bool kAppend = false>
 cudaError_t launch(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t stream) {
   static std::mutex mu;
   static size_t attr_bytes[128] = {};
@@ -586,14 +658,14 @@ cudaError_t launch(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t 
     std::lock_guard<std::mutex> lock(mu);
     const int d = dev.device >= 0 && dev.device < 128 ? dev.device : 0;
     if (attr_bytes[d] < smem) {
-      e = cudaFuncSetAttribute(decode_stream_kernel<kBF16, kNQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      e = cudaFuncSetAttribute(decode_stream_kernel<kBF16, kNQ, kAppend>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem));
       if (e != cudaSuccess) return e;
       attr_bytes[d] = smem;
     }
   }
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<kBF16, kNQ>, kThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<kBF16, kNQ, kAppend>, kThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int grid = dev.num_sms * (per_sm < CXA_DECODE_CTAS_PER_SM ? per_sm : CXA_DECODE_CTAS_PER_SM);
@@ -607,7 +679,7 @@ cudaError_t launch(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t 
   attr[0].val.programmaticStreamSerializationAllowed = CXA_DECODE_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_stream_kernel<kBF16, kNQ>, prm);
+  return cudaLaunchKernelEx(&cfg, decode_stream_kernel<kBF16, kNQ, kAppend>, prm);
 }
 
 template <bool kBF16>
@@ -650,7 +722,13 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStre
   prm.key_len_add = a.key_len_add;
   prm.part_stride = (a.T + kPartChunk - 1) / kPartChunk;
   prm.qscale = a.scale * 1.4426950408889634f;   // scale * log2(e)
-  cudaError_t e = a.cache_bf16 ? launch_nq<true>(prm, dev, stream) : launch_nq<false>(prm, dev, stream);
+  prm.Knew = a.K_new;
+  prm.Vnew = a.V_new;
+  cudaError_t e;
+  if (a.K_new != nullptr)   // the self-attention step: append fused into a one-query decode
+    e = a.cache_bf16 ? launch<true, 1, true>(prm, dev, stream) : launch<false, 1, true>(prm, dev, stream);
+  else
+    e = a.cache_bf16 ? launch_nq<true>(prm, dev, stream) : launch_nq<false>(prm, dev, stream);
   if (e == cudaSuccess) count_launches(1);
   return e;
 }

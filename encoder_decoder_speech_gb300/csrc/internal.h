@@ -39,6 +39,8 @@ struct DecodeLaunch {
   int B, T, L, H;
   float scale;         // > 0
   bool cache_bf16;
+  const float* K_new = nullptr;   // self-attention step: rows appended at key_len[b] (nq == 1)
+  const float* V_new = nullptr;
 };
 
 // One decoder layer's cross-attention block for one step (see block.cu).
