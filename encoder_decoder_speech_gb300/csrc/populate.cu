@@ -62,6 +62,7 @@ struct GemmParams {
   int mt_per_slot;     // ceil(T / 128)
   int num_m_tiles;     // nb * mt_per_slot
   int num_tiles;       // num_m_tiles * num_n_tiles
+  int raster_n;        // 1: consecutive tiles walk N under one M tile (E rows reused), 0: walk M
   int num_kb;          // d / k-block elements
   int num_heads_total; // 2 * L * H
   int cache_bf16;
@@ -137,8 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t armed = 0, armed_parity = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        const int mtg = tile % p.num_m_tiles;
-        const int nt = tile / p.num_m_tiles;
+        const int mtg = p.raster_n ? tile / (p.num_tiles / p.num_m_tiles) : tile % p.num_m_tiles;
+        const int nt = p.raster_n ? tile % (p.num_tiles / p.num_m_tiles) : tile / p.num_m_tiles;
         const int slot = mtg / p.mt_per_slot;
         const int mt = mtg - slot * p.mt_per_slot;
         for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -239,8 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int mtg = tile % p.num_m_tiles;
-      const int nt = tile / p.num_m_tiles;
+      const int mtg = p.raster_n ? tile / (p.num_tiles / p.num_m_tiles) : tile % p.num_m_tiles;
+      const int nt = p.raster_n ? tile % (p.num_tiles / p.num_m_tiles) : tile / p.num_m_tiles;
       const int slot = mtg / p.mt_per_slot;
       const int mt = mtg - slot * p.mt_per_slot;
       const int t0w = mt * kBM + quad * 32;     // first token of this warp's rows
@@ -510,6 +511,11 @@ cudaError_t run(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t str
   p.num_m_tiles = a.nb * p.mt_per_slot;
   const int num_n_tiles = (N + kBN - 1) / kBN;
   p.num_tiles = p.num_m_tiles * num_n_tiles;
+  // Walk N under one M tile when all packed weights stay in L2 while the cache writes
+  // stream past (E rows are then read once); otherwise walk M, so that each wave
+  // shares one weight tile and E (the smaller operand) is what L2 holds.
+  const size_t w_bytes = static_cast<size_t>(N) * a.d * (kBF16In ? 2 : 4);
+  p.raster_n = w_bytes <= (32u << 20) ? 1 : 0;
   p.num_kb = a.d / kKElems;
   p.num_heads_total = 2 * a.L * a.H;
   p.cache_bf16 = a.cache_bf16 ? 1 : 0;
