@@ -338,6 +338,17 @@ def measure(torch, cxa, W, w, dev_inputs, cache_dtype, K, Wu, rank, world, dist,
     assert cxa.cxa_device_status(1) == cxa.CXA_OK, "a kernel reported a bounded-wait timeout"
     res = {"total_ms": total_ms, "populate_ms": pop_ms, "decode_window_ms": dec_ms,
            "decode_launch_us": 1000.0 * dec_ms / w.steps, "launches": launches, "clocks": clocks}
+    # spread over the K windows (this rank's events): window, populate and decode-loop times
+    import numpy as np
+
+    def pct(xs):
+        a = np.asarray(xs, dtype=np.float64)
+        return {"p10": round(float(np.percentile(a, 10)), 4), "median": round(float(np.median(a)), 4),
+                "p90": round(float(np.percentile(a, 90)), 4), "n": int(a.size)}
+
+    res["spread_ms"] = {"window": pct([e[0].elapsed_time(e[2]) for e in ev]),
+                        "populate": pct([e[0].elapsed_time(e[1]) for e in ev]),
+                        "decode_128_steps": pct([e[1].elapsed_time(e[2]) for e in ev])}
     cache.close()
     return res
 
@@ -838,6 +849,7 @@ def run_cxa(args):
             "frac": large["flops_per_call"] / (large["ms"] * 1e-3) / 1e12 / peaks["bf16_tflops"],
             "ms": large["ms"]},
         "clocks": main["clocks"],
+        "spread_ms": main["spread_ms"],
         "e2e": {"value": tokens / (e2e_ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "note": "E, key_len and 128 Q copied in, 128 outputs copied out per "
                                                      "window from/to pinned host memory on a copy stream that "
