@@ -118,3 +118,19 @@ def test_shared_decode_growing_scores_move_the_reference(nq):
     out = host(c.decode_shared(dev(Q), d["key_len"]))
     ref = O.decode_shared(Q, K, V, h["key_len"])
     assert np.abs(out - ref).max() <= DECODE_BF16_MAX_ABS
+
+
+@pytest.mark.parametrize("nq", [3, 8, 16])
+def test_shared_decode_tensor_core_key_length_edges(nq):
+    """Key lengths at and around the 32-key TMA boxes and 128-key chunks (1, 2, 31,
+    32, 33, 127, 128, 129, T) on a bf16 cache: tail rows of a chunk are stale data
+    that must not reach the output."""
+    w = W.custom("shared_edges", B=9, T=333, d=256, L=2, H=4, ragged=False, index=944)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, "bf16")
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    kl = np.array([1, 2, 31, 32, 33, 127, 128, 129, 333], dtype=np.int32)
+    Q = _queries(w, nq, 70 + nq)
+    out = host(c.decode_shared(dev(Q), dev(kl, torch.int32)))
+    ref = O.decode_shared(Q, host(c.Kc), host(c.Vc), kl)
+    assert np.abs(out - ref).max() <= DECODE_BF16_MAX_ABS
