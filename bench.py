@@ -54,6 +54,8 @@ def parse_args(argv=None):
     p.add_argument("--shared", action="store_true",
                    help="time shared-cache decode (nq hypotheses per memory) on the batched Whisper-Base "
                         "workload for nq = 1, 2, 4, 5, 8; one JSON line per (nq, cache dtype)")
+    p.add_argument("--small", action="store_true",
+                   help="Whisper-Tiny / Whisper-Base single-memory decode, warm-L2 and cold, and populate")
     p.add_argument("--block", action="store_true",
                    help="time the per-layer cross-attention block (LayerNorm, Q projection, attention, out "
                         "projection + residual) for all 6 layers of a batched Whisper-Base decode step")
@@ -575,6 +577,70 @@ def run_shared(args):
     return 0
 
 
+def run_small(args):
+    """The single-memory configurations (Whisper-Tiny dims, Whisper-Base dims): their
+    fp32 caches (18-37 MB of valid K/V) fit in the 129 MB L2, so each decode is timed
+    warm (steps back to back, the cache stays in L2) and cold (a 256 MB buffer written
+    between steps evicts it; only the decode's own events are counted), plus one timed
+    populate."""
+    import numpy as np
+    import torch
+    from encoder_decoder_speech_gb300 import _build, cxa
+    from encoder_decoder_speech_gb300 import workloads as W
+    _build.build_library()
+    cxa.load()
+    torch.cuda.set_device(0)
+    peaks = load_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for name in ("tiny", "base"):
+        w = W.WORKLOADS[name]
+        (E, WK, WV, bV, kl, Qs, kl_h), _ = device_inputs(torch, W, w, 0)
+        for cd, esz in (("f32", 4), ("bf16", 2)):
+            cache = cxa.CrossAttentionCache(w.B, w.T, w.L, w.H, w.dh, cd)
+            out = torch.empty((w.B, w.L, w.H, w.dh), device="cuda")
+            for _ in range(args.warmup):
+                cache.populate(E, WK, WV, bV)
+            torch.cuda.synchronize()
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            cache.populate(E, WK, WV, bV)
+            b_.record()
+            torch.cuda.synchronize()
+            pop_ms = a.elapsed_time(b_)
+            n = args.steps
+            for s in range(args.warmup):
+                cache.decode(Qs[s % Qs.shape[0]], kl, out=out)
+            torch.cuda.synchronize()
+            a.record()
+            for s in range(n):
+                cache.decode(Qs[s % Qs.shape[0]], kl, out=out)
+            b_.record()
+            torch.cuda.synchronize()
+            warm_us = a.elapsed_time(b_) * 1000.0 / n
+            cold = []
+            for s in range(min(n, 50)):
+                flush.fill_(s & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                cache.decode(Qs[s % Qs.shape[0]], kl, out=out)
+                e1.record()
+                torch.cuda.synchronize()
+                cold.append(e0.elapsed_time(e1) * 1000.0)
+            cold_us = float(np.median(cold))
+            byts = decode_bytes(w.L, w.H, w.dh, esz, kl_h, w.B)
+            print(json.dumps({"small_config": {"workload": name, "T_enc": w.T, "d": w.d, "L": w.L, "H": w.H,
+                                               "cache_dtype": cd},
+                              "decode_us_warm_l2": round(warm_us, 2), "decode_us_cold": round(cold_us, 2),
+                              "decode_GBps_cold": round(byts / (cold_us * 1e-6) / 1e9, 1),
+                              "frac_of_measured_hbm_cold": round(byts / (cold_us * 1e-6) / 1e9 / peaks["hbm_gbs"], 3),
+                              "populate_ms": round(pop_ms, 4),
+                              "populate_TFLOPs": round(populate_flops(w.L, w.d, w.B, w.T) / (pop_ms * 1e-3) / 1e12, 1)}),
+                  flush=True)
+            cache.close()
+    assert cxa.cxa_device_status(1) == cxa.CXA_OK
+    return 0
+
+
 def run_block(args):
     """One decoder step of batched Whisper-Base through the per-layer entry point:
     for l = 0..5, x = x + CrossAttn_l(LayerNorm(x)) (cxa_cross_block), fp32 weights."""
@@ -878,6 +944,8 @@ def main(argv=None):
         return run_sweep(args)
     if args.shared:
         return run_shared(args)
+    if args.small:
+        return run_small(args)
     if args.block:
         return run_block(args)
     if args.selfattn:
