@@ -24,6 +24,7 @@
 #include <mutex>
 #include <string>
 
+#include "cluster.cuh"
 #include "internal.h"
 
 namespace cxa {
@@ -36,22 +37,6 @@ constexpr int kGemvThreads = 256;
 constexpr int kColQuads = kColsPerCta / 4;      // 8 threads cover a 32-column row (float4 each)
 constexpr int kRowGroups = kGemvThreads / kColQuads;   // 32 row groups
 constexpr int kMaxSlice = 160;                  // d_in rows per CTA (d <= 1280)
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
-  uint32_t laddr = static_cast<uint32_t>(__cvta_generic_to_shared(local)), raddr;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(laddr), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(raddr) : "memory");
-  return v;
-}
 
 // out[b][j] = (residual ? residual[b][j] : 0) + (bias ? bias[j] : 0)
 //             + sum_i norm(in)[b][i] * W[i][j]

@@ -32,6 +32,8 @@
 #include <mutex>
 #include <string>
 
+#include "chunk_stream.cuh"
+#include "cluster.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -80,20 +82,9 @@ struct FusedParams {
   float eps, qscale;   // qscale = scale * log2(e)
 };
 
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
-  uint32_t laddr = static_cast<uint32_t>(__cvta_generic_to_shared(local)), raddr;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(laddr), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(raddr) : "memory");
-  return v;
-}
 __device__ __forceinline__ void consumer_barrier() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
 }
-__device__ __forceinline__ float rescale(float m, float M) { return m == -INFINITY ? 0.f : exp2f(m - M); }
 
 // The 16-byte slice of a cached row at byte offset off, as kChanPerLane floats.
 template <bool kBF16>

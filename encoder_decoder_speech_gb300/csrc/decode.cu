@@ -46,6 +46,7 @@
 #include <string>
 
 #include "internal.h"
+#include "chunk_stream.cuh"
 #include "ptx.cuh"
 
 namespace cxa {
@@ -166,56 +167,11 @@ __device__ __forceinline__ void load_slice(const uint8_t* p, float* f) {
   }
 }
 
-// Weight of a softmax state with running max m against a merged max M (0 for an
-// empty state, m == -inf).
-__device__ __forceinline__ float rescale(float m, float M) { return m == -INFINITY ? 0.f : exp2f(m - M); }
-
 // Programmatic dependent launch: let the next grid on the stream be scheduled
 // as this grid's CTAs retire, and wait for the previous grid to complete (and
 // its memory to be visible) before touching anything it may have written.
 __device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-__device__ __forceinline__ void named_barrier(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// Position in the dense chunk numbering: slot b, row-in-slot lh, chunk c.
-struct Cursor {
-  int b, lh, c;
-};
-
-// The chunk numbering lives in shared memory: s_nch[b] = chunks per row of
-// slot b, s_first[b] = number of the first chunk of slot b (s_first[B] = total).
-__device__ __forceinline__ Cursor locate(long long g, const long long* s_first, const int* s_nch, int B, int LH) {
-  int lo = 0, hi = B - 1;   // last b with s_first[b] <= g
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_first[mid] <= g) lo = mid; else hi = mid - 1;
-  }
-  const long long local = g - s_first[lo];
-  Cursor cur;
-  cur.b = lo;
-  cur.lh = static_cast<int>(local / s_nch[lo]);
-  cur.c = static_cast<int>(local - static_cast<long long>(cur.lh) * s_nch[lo]);
-  return cur;
-}
-
-__device__ __forceinline__ void advance(Cursor& cur, const int* s_nch, int B, int LH) {
-  if (++cur.c < s_nch[cur.b]) return;
-  cur.c = 0;
-  if (++cur.lh < LH) return;
-  cur.lh = 0;
-  do {
-    ++cur.b;
-  } while (cur.b < B && s_nch[cur.b] == 0);
-}
-
-// The CTA that owns dense chunk g when total chunks are split into `ranges`
-// equal ranges [j*total/ranges, (j+1)*total/ranges).
-__device__ __forceinline__ long long owner_of(long long g, long long total, long long ranges) {
-  return ((g + 1) * ranges + total - 1) / total - 1;
-}
 
 template <bool kBF16, int kNQ>
 constexpr int min_ctas_per_sm() {
@@ -299,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
   long long npre = 0;
   if constexpr (kAppend) wait_prior_grid();
   if (active && producer) {
-    pcur = locate(g0, s_first, s_nch, p.B, LH);
+    pcur = locate(g0, s_first, s_nch, p.B);
     Cursor c = pcur;
     npre = (g1 - g0) < kStages ? (g1 - g0) : kStages;
     for (long long i = 0; i < npre; ++i) {
@@ -408,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
     const int sub = lane % LPR;          // slice of a key row this lane reads
     const int grp = lane / LPR;          // lane group = independent softmax stream
     const int tid = threadIdx.x;         // 0..127
-    Cursor cur = locate(g0, s_first, s_nch, p.B, LH);
+    Cursor cur = locate(g0, s_first, s_nch, p.B);
     int seg_c0 = cur.c;                  // first chunk of the current row in this CTA
     float m[kNQ], ssum[kNQ], acc[kNQ][EPL];
 #pragma unroll

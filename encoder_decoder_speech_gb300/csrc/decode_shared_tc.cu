@@ -47,6 +47,7 @@
 #include <string>
 
 #include "internal.h"
+#include "chunk_stream.cuh"
 #include "ptx.cuh"
 
 namespace cxa {
@@ -90,10 +91,6 @@ struct TcParams {
   float qscale;
 };
 
-__device__ __forceinline__ float rescale(float m, float M) { return m == -INFINITY ? 0.f : exp2f(m - M); }
-__device__ __forceinline__ void named_barrier(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
 // OR of a predicate over the threads of a named barrier, which it also is.
 __device__ __forceinline__ bool named_barrier_or(int id, int count, bool v) {
   uint32_t r;
@@ -134,35 +131,6 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
-}
-
-struct Cursor {
-  int b, lh, c;
-};
-__device__ __forceinline__ Cursor locate(long long g, const long long* s_first, const int* s_nch, int B) {
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_first[mid] <= g) lo = mid; else hi = mid - 1;
-  }
-  const long long local = g - s_first[lo];
-  Cursor cur;
-  cur.b = lo;
-  cur.lh = static_cast<int>(local / s_nch[lo]);
-  cur.c = static_cast<int>(local - static_cast<long long>(cur.lh) * s_nch[lo]);
-  return cur;
-}
-__device__ __forceinline__ void advance(Cursor& cur, const int* s_nch, int B, int LH) {
-  if (++cur.c < s_nch[cur.b]) return;
-  cur.c = 0;
-  if (++cur.lh < LH) return;
-  cur.lh = 0;
-  do {
-    ++cur.b;
-  } while (cur.b < B && s_nch[cur.b] == 0);
-}
-__device__ __forceinline__ long long owner_of(long long g, long long total, long long ranges) {
-  return ((g + 1) * ranges + total - 1) / total - 1;
 }
 
 template <int kNQT>   // query columns the softmax handles (4, 8 or 16 >= nq)
