@@ -134,3 +134,22 @@ def test_block_argument_checks():
     assert cxa.cxa_cross_block(*args(-1)) == cxa.CXA_EINVAL
     c.invalidate(0)
     assert cxa.cxa_cross_block(*args(0)) == cxa.CXA_ENOTREADY
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+def test_cross_block_clamps_key_lengths(cache_dtype):
+    """key_len outside [0, T]: negative attends nothing (x += bO), beyond T attends all T."""
+    w = W.custom("blockclamp", B=3, T=250, d=256, L=2, H=4, ragged=False, index=966)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, cache_dtype)
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    p = _block_params(w.d, 67)
+    kl = np.array([-3, 400, 120], dtype=np.int32)
+    x0 = _rand((w.B, w.d), 68)
+    x = dev(x0)
+    dp = {k: dev(v) for k, v in p.items()}
+    c.cross_block(0, x, dp["WQ"], dp["WO"], dev(kl, torch.int32), ln_gamma=dp["gamma"], ln_beta=dp["beta"],
+                  bQ=dp["bQ"], bO=dp["bO"])
+    ref = O.cross_block(x0, 0, host(c.Kc), host(c.Vc), np.clip(kl, 0, w.T), p["WQ"], p["WO"], p["gamma"],
+                        p["beta"], 1e-5, p["bQ"], p["bO"])
+    assert np.abs(host(x) - ref).max() <= BLOCK_TOL[cache_dtype]

@@ -134,3 +134,17 @@ def test_shared_decode_tensor_core_key_length_edges(nq):
     out = host(c.decode_shared(dev(Q), dev(kl, torch.int32)))
     ref = O.decode_shared(Q, host(c.Kc), host(c.Vc), kl)
     assert np.abs(out - ref).max() <= DECODE_BF16_MAX_ABS
+
+
+def test_shared_decode_clamps_key_lengths():
+    """key_len outside [0, T] is clamped (negative -> no key -> zeros; > T -> T)."""
+    w = W.custom("shared_clamp", B=4, T=200, d=256, L=2, H=4, ragged=False, index=945)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, "bf16")
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    kl = np.array([-5, 0, 200, 100000], dtype=np.int32)
+    Q = _queries(w, 6, 80)
+    out = host(c.decode_shared(dev(Q), dev(kl, torch.int32)))
+    ref = O.decode_shared(Q, host(c.Kc), host(c.Vc), np.clip(kl, 0, w.T))
+    assert np.abs(out - ref).max() <= DECODE_BF16_MAX_ABS
+    assert np.all(out[0] == 0.0) and np.all(out[1] == 0.0)
