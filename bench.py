@@ -46,7 +46,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["cxa", "reference"], default="cxa")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     p.add_argument("--no-variants", action="store_true", help="skip the bf16-cache variant")
-    p.add_argument("--profile", choices=["decode", "decode_bf16", "populate", "shared_bf16"], default=None,
+    p.add_argument("--profile", choices=["decode", "decode_bf16", "populate", "shared_bf16", "align"], default=None,
                    help="run a few launches of one kernel on the workload's inputs (for ncu), print nothing else")
     p.add_argument("--sweep", action="store_true",
                    help="time decode and populate at every point of the decode bandwidth sweep "
@@ -119,9 +119,16 @@ def populate_flops(L, d, B, T):
     return 4 * L * d * d * B * T
 
 
-def source_sha(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+DECODE_SOURCES = ("decode.cu", "chunk_stream.cuh", "ptx.cuh", "internal.h")
+
+
+def source_sha(paths):
+    """First 16 hex digits of the SHA-256 over the given files, concatenated in order."""
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic():
@@ -135,8 +142,8 @@ def recorded_traffic():
     s = re.search(r"decode_source_sha256_16:\s*([0-9a-f]+)", text)
     if not m or not s:
         return None
-    src = os.path.join(ROOT, "encoder_decoder_speech_gb300", "csrc", "decode.cu")
-    if source_sha(src) != s.group(1):
+    srcs = [os.path.join(ROOT, "encoder_decoder_speech_gb300", "csrc", f) for f in DECODE_SOURCES]
+    if source_sha(srcs) != s.group(1):
         return None
     return float(m.group(1))
 
@@ -788,21 +795,55 @@ def run_align(args):
         Q = torch.randn(w.B, w.L, w.H, 64, device="cuda")
         wt = torch.empty((w.B, len(heads), w.T), device="cuda")
         mean = torch.empty((w.B, w.T), device="cuda")
+
+        def call():
+            cxa.check(cxa.cxa_alignment_weights(cache.handle, Q, kl, heads, wt, mean, 0.0), "align")
+
+        per_graph = 50   # calls captured in one CUDA graph
         for _ in range(args.warmup):
-            cxa.check(cxa.cxa_alignment_weights(cache.handle, Q, kl, heads, wt, mean, 0.0), "align")
+            call()
         torch.cuda.synchronize()
-        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(args.steps):
-            cxa.check(cxa.cxa_alignment_weights(cache.handle, Q, kl, heads, wt, mean, 0.0), "align")
-        b_.record()
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            call()
+        torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
-        us = a.elapsed_time(b_) * 1000.0 / args.steps
+        with torch.cuda.graph(graph):
+            for _ in range(per_graph):
+                call()
+        torch.cuda.synchronize()
+        n0 = cxa.cxa_launch_count()
+        call()
+        torch.cuda.synchronize()
+        kernels_per_call = cxa.cxa_launch_count() - n0
         byts = len(heads) * 64 * esz * int(np.clip(kl_h, 0, w.T).sum()) + w.B * (len(heads) + 1) * w.T * 4 * 2
-        print(json.dumps({"alignment_weights": {"workload": name, "heads": len(heads), "cache_dtype": cd},
-                          "us_per_call": round(us, 2), "GBps": round(byts / (us * 1e-6) / 1e9, 1),
-                          "frac_of_measured_hbm": round(byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 3)}),
-              flush=True)
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for mode in ("eager", "graph"):
+            reps = max(1, args.steps // per_graph) if mode == "graph" else args.steps
+            run = call if mode == "eager" else graph.replay
+            for _ in range(args.warmup):
+                run()
+            torch.cuda.synchronize()
+            h0 = time.perf_counter()
+            a.record()
+            for _ in range(reps):
+                run()
+            b_.record()
+            h1 = time.perf_counter()
+            torch.cuda.synchronize()
+            calls = reps * (per_graph if mode == "graph" else 1)
+            us = a.elapsed_time(b_) * 1000.0 / calls
+            line = {"alignment_weights": {"workload": name, "heads": len(heads), "cache_dtype": cd,
+                                          "launch": mode},
+                    "us_per_call": round(us, 2), "GBps": round(byts / (us * 1e-6) / 1e9, 1),
+                    "frac_of_measured_hbm": round(byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 3),
+                    "kernels_per_call": kernels_per_call}
+            if mode == "eager":
+                line["host_us_per_call"] = round((h1 - h0) * 1e6 / calls, 2)
+            print(json.dumps(line), flush=True)
+        del graph
         cache.close()
         del E, WK
         torch.cuda.empty_cache()
@@ -813,7 +854,7 @@ def run_align(args):
 def run_profile(args):
     """A handful of launches of one kernel on the bench workload's inputs, for
     Nsight Compute: one populate (weight repack + GEMM), then two more populate
-    calls or three decode steps."""
+    calls, three decode steps or three alignment-weight calls."""
     import torch
     from encoder_decoder_speech_gb300 import _build, cxa
     from encoder_decoder_speech_gb300 import workloads as W
@@ -834,6 +875,10 @@ def run_profile(args):
             (w.B, 8, w.L, w.H, w.dh)).astype(np.float32)).to("cuda")
         for _ in range(3):
             cache.decode_shared(Qs, kl)
+    elif args.profile == "align":         # six alignment heads of the last three layers
+        heads = [(3, 1), (4, 2), (4, 6), (5, 0), (5, 3), (5, 7)]
+        for s in range(3):
+            cache.alignment_weights(Q[s], kl, heads)
     else:
         for s in range(3):
             cache.decode(Q[s], kl)
@@ -923,7 +968,7 @@ def run_cxa(args):
         "gpu_launches": main["launches"],
         "variants": variants,
         "device": {"name": props.name, "sms": props.multi_processor_count,
-                   "lib_sha": source_sha(os.path.join(ROOT, "encoder_decoder_speech_gb300", "_lib", "libcxa.so"))},
+                   "lib_sha": source_sha([os.path.join(ROOT, "encoder_decoder_speech_gb300", "_lib", "libcxa.so")])},
     }
     if cpu_base is not None:
         line["cpu_baseline"] = cpu_base

@@ -7,183 +7,355 @@
 //                    = 0                                                    t >= key_len[b]
 //   mean[b][t]       = (1 / nsel) sum_k weights[b][k][t]
 //
-// Three launches, chained by programmatic dependent launch:
-//  1. scores: a CTA per (block of 128 keys, selected head, slot) writes the base-2
-//     logits scale * log2(e) * q . K_t into the weights row, every thread's row
-//     loads of the block issued together (16 lanes per fp32 row / 8 per bf16 row);
-//  2. normalise: a CTA per (selected head, slot) takes the row max, sums 2^(s - max)
-//     and scales the row, writing 0 past key_len;
-//  3. mean over the selected heads (optional).
-// The K rows of the selected heads are the only large reads; splitting each row
-// over many CTAs keeps enough of them in flight.
+// One launch. Slot b is a cluster of C CTAs (the largest of 16, 8, 4, 2, 1 whose
+// B clusters are resident together); CTA x takes the keys [x*tc, (x+1)*tc) of the
+// slot's valid range for EVERY selected head, so the head mean of a key needs
+// nothing from other CTAs. The only cross-CTA step is the softmax denominator:
+//  1. scores: each head's key range is one contiguous span of the cache; the CTA
+//     streams its spans in 4 KB bulk copies through a 16-stage shared-memory ring.
+//     Chunk j belongs to warp j % 8 alone, which waits for it, takes the dot
+//     products of its rows (16 lanes per fp32 row / 8 per bf16 row, the 8 rows'
+//     reductions interleaved) and refills the stage with chunk j + 16; the first
+//     copies are issued before the grid dependency wait. The base-2 logits
+//     scale*log2(e)*q.K_t are staged in shared memory (or, when nsel times the
+//     CTA's keys exceeds 4096, in the weights rows);
+//  2. per head, a group of lanes takes the max and the sum of 2^(logit - max)
+//     over the CTA's keys and stores the pair into every cluster CTA's shared
+//     memory (distributed shared memory);
+//  3. after one cluster barrier each CTA merges the C pairs of every head from
+//     its own shared memory (log-sum-exp);
+//  4. every CTA writes the weights of its own keys and their mean over heads,
+//     and zeroes its share of the keys t >= key_len[b].
 #include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 #include <string>
 
+#include "cluster.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace cxa {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
 
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float* s_red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    const float o = __shfl_xor_sync(0xffffffffu, v, off);
-    v = is_max ? fmaxf(v, o) : v + o;
-  }
-  __syncthreads();
-  if (lane == 0) s_red[warp] = v;
-  __syncthreads();
-  float r = is_max ? -INFINITY : 0.f;
-  for (int w = 0; w < kThreads / 32; ++w) r = is_max ? fmaxf(r, s_red[w]) : r + s_red[w];
-  return r;
+template <bool kBF16>
+struct RowGeom {
+  static constexpr int kElem = kBF16 ? 2 : 4;
+  static constexpr int kRowBytes = 64 * kElem;
+  static constexpr int kLanesPerRow = kRowBytes / 16;           // 16 / 8
+  static constexpr int kEPL = 16 / kElem;                       // 4 / 8 channels per lane
+  static constexpr int kRowsPerWarpPass = 32 / kLanesPerRow;    // 2 / 4
+  static constexpr int kChunkBytes = 4096;
+  static constexpr int kChunkKeys = kChunkBytes / kRowBytes;    // 16 / 32
+  static constexpr int kWarpPasses = kChunkKeys / kRowsPerWarpPass;   // 8: one interleaved reduction
+};
+constexpr int kStages = 16;                                     // warp w owns stages w and w + 8
+constexpr size_t kRingBytes = static_cast<size_t>(kStages) * 4096;
+constexpr int kStageFloats = 4096;   // logits held in shared memory when nsel * keys per CTA fits
+constexpr int kMaxCluster = 16;
+
+// Dynamic shared memory: the ring, the logits, the scaled queries [nsel][64] and the
+// partials [nsel][C] (max, then sum) every cluster CTA stores into every other.
+__host__ __device__ constexpr size_t dyn_smem_bytes(int nsel, int C) {
+  return kRingBytes + kStageFloats * sizeof(float) + static_cast<size_t>(nsel) * 64 * sizeof(float) +
+         static_cast<size_t>(nsel) * C * 2 * sizeof(float);
 }
 
-constexpr int kBlockKeys = 128;   // keys per score CTA
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+template <bool kBF16>
+__device__ __forceinline__ void unpack(const uint4 u, float (&f)[RowGeom<kBF16>::kEPL]) {
+  if constexpr (kBF16) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  } else {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+  }
+}
 
 template <bool kBF16>
 __global__ void __launch_bounds__(kThreads)
-    alignment_scores_kernel(const float* __restrict__ Q, const uint8_t* __restrict__ Kc,
-                            const int* __restrict__ key_len, const AlignHeads heads, float* __restrict__ weights,
-                            int T, int L, int H, float qscale) {
-  constexpr int kElem = kBF16 ? 2 : 4;
-  constexpr int kRowBytes = 64 * kElem;
-  constexpr int kLanesPerRow = kRowBytes / 16;          // 16 / 8
-  constexpr int kEPL = 16 / kElem;                      // 4 / 8 channels per lane
-  constexpr int kRowsPerPass = kThreads / kLanesPerRow; // 16 / 32 keys per CTA pass
-  constexpr int kPasses = kBlockKeys / kRowsPerPass;    // 8 / 4
+    alignment_kernel(const float* __restrict__ Q, const uint8_t* __restrict__ Kc, const int* __restrict__ key_len,
+                     const AlignHeads heads, float* weights, float* __restrict__ mean, int T, int L, int H,
+                     float qscale, unsigned int* status) {
+  using G = RowGeom<kBF16>;
+  extern __shared__ __align__(128) uint8_t ring[];              // see dyn_smem_bytes
+  __shared__ float s_M[kMaxAlignHeads], s_inv[kMaxAlignHeads];  // merged max and 1 / sum
+  __shared__ __align__(8) uint64_t bars[kStages];               // full[s]: chunk landed
+  __shared__ int s_last[kStages];                               // last chunk issued into stage s
+  __shared__ int s_abort;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int k = blockIdx.y, b = blockIdx.z;
-  const int n = min(max(__ldg(key_len + b), 0), T);
-  const int t0 = blockIdx.x * kBlockKeys;
-  if (t0 >= n) return;
-  const int l = heads.l[k], h = heads.h[k];
-  const long long crow = (static_cast<long long>(b) * L + l) * H + h;
-  float* wrow = weights + (static_cast<long long>(b) * gridDim.y + k) * T;
-  const int sub = threadIdx.x % kLanesPerRow, r0 = threadIdx.x / kLanesPerRow;
-  // the cache rows first (no decode writes them), then Q and the weights (which
-  // neighbouring kernels may produce or read)
-  uint4 u[kPasses];
-#pragma unroll
-  for (int ps = 0; ps < kPasses; ++ps) {
-    const int t = t0 + ps * kRowsPerPass + r0;
-    u[ps] = t < n ? __ldg(reinterpret_cast<const uint4*>(Kc + (crow * T + t) * kRowBytes) + sub)
-                  : make_uint4(0u, 0u, 0u, 0u);
+  cluster_arrive();   // this CTA is running; peers wait for that before storing into its shared memory
+  const int C = gridDim.x, x = blockIdx.x, b = blockIdx.y, nsel = heads.n;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  if (tid == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(smem_u32(&bars[st]), 1);
+      s_last[st] = -1;
+    }
+    s_abort = 0;
+    fence_mbar_init();
   }
+  const int n = min(max(__ldg(key_len + b), 0), T);
+  const int tc = (n + C - 1) / C;
+  const int t_lo = min(n, x * tc);
+  const int cnt = min(n, t_lo + tc) - t_lo;
+  const int nchk = (cnt + G::kChunkKeys - 1) / G::kChunkKeys;   // chunks per head
+  const int nchunks = nsel * nchk;                              // chunk j: head j / nchk, part j % nchk
+  float* wslot = weights + static_cast<long long>(b) * nsel * T;
+  volatile int* abort_flag = &s_abort;
+  // the CTA's logits: [nsel][cnt] in shared memory when they fit, else in place in
+  // the weights rows (same code through a generic pointer)
+  const bool lg_smem = nsel * cnt <= kStageFloats;
+  float* const s_lg = reinterpret_cast<float*>(ring + kRingBytes);
+  float* const s_q = s_lg + kStageFloats;                       // [nsel][64]
+  float* const s_pm = s_q + nsel * 64;                          // [nsel][C] partial max of CTA r at [k][r]
+  float* const s_ps = s_pm + nsel * C;                          // [nsel][C] partial sum
+  float* stage = lg_smem ? s_lg : wslot + t_lo;
+  const long long ldst = lg_smem ? cnt : T;
+
+  auto issue = [&](int j) {
+    const int st = j % kStages, k = j / nchk, c = j - k * nchk;
+    const int rows = min(G::kChunkKeys, cnt - c * G::kChunkKeys);
+    const long long crow = (static_cast<long long>(b) * L + heads.l[k]) * H + heads.h[k];
+    const uint32_t full = smem_u32(&bars[st]);
+    const uint32_t bytes = static_cast<uint32_t>(rows) * G::kRowBytes;
+    s_last[st] = j;
+    mbar_arrive_expect_tx(full, bytes);
+    bulk_g2s(smem_u32(ring + st * G::kChunkBytes), Kc + (crow * T + t_lo + c * G::kChunkKeys) * G::kRowBytes,
+             bytes, full);
+  };
+  __syncthreads();                                              // the barriers are initialised
+  // the cache rows and key_len first (no decode writes them); Q and the weights
+  // after the wait (neighbouring kernels may produce or read them). Chunk j is
+  // processed by warp j % 8, which also refills its stage with chunk j + kStages.
+  if (lane == 0)
+    for (int j = warp; j < min(nchunks, kStages); j += kWarps) issue(j);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  float q[kEPL];
-#pragma unroll
-  for (int e4 = 0; e4 < kEPL / 4; ++e4) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(Q + crow * 64 + sub * kEPL) + e4);
-    q[4 * e4 + 0] = v.x * qscale;
-    q[4 * e4 + 1] = v.y * qscale;
-    q[4 * e4 + 2] = v.z * qscale;
-    q[4 * e4 + 3] = v.w * qscale;
+  for (int i = tid; i < nsel * 16; i += kThreads) {
+    const int k = i >> 4, c4 = i & 15;
+    const long long crow = (static_cast<long long>(b) * L + heads.l[k]) * H + heads.h[k];
+    float4 v = __ldg(reinterpret_cast<const float4*>(Q + crow * 64) + c4);
+    v.x *= qscale;
+    v.y *= qscale;
+    v.z *= qscale;
+    v.w *= qscale;
+    reinterpret_cast<float4*>(s_q)[i] = v;
   }
-  float dot[kPasses];
+  __syncthreads();
+
+  // ---- 1. scores of every chunk, staged as base-2 logits
+  const int sub = lane % G::kLanesPerRow, grp = lane / G::kLanesPerRow;
+  bool ok = true;
+  for (int j = warp; j < nchunks; j += kWarps) {
+    const int st = j % kStages, k = j / nchk, c = j - k * nchk;
+    if (ok && !mbar_wait(smem_u32(&bars[st]), static_cast<uint32_t>((j / kStages) & 1), abort_flag)) {
+      ok = false;
+      *abort_flag = 1;
+      atomicOr(status, 1u);
+    }
+    const int rows = ok ? min(G::kChunkKeys, cnt - c * G::kChunkKeys) : 0;
+    const uint8_t* tile = ring + st * G::kChunkBytes + sub * 16;
+    float q[G::kEPL];
 #pragma unroll
-  for (int ps = 0; ps < kPasses; ++ps) {
-    float f[kEPL];
-    if constexpr (kBF16) {
-      const uint32_t w[4] = {u[ps].x, u[ps].y, u[ps].z, u[ps].w};
+    for (int e4 = 0; e4 < G::kEPL / 4; ++e4) {
+      const float4 v = reinterpret_cast<const float4*>(s_q + k * 64 + sub * G::kEPL)[e4];
+      q[4 * e4 + 0] = v.x;
+      q[4 * e4 + 1] = v.y;
+      q[4 * e4 + 2] = v.z;
+      q[4 * e4 + 3] = v.w;
+    }
+    float* lg = stage + k * ldst + c * G::kChunkKeys;
+    float dot[G::kWarpPasses];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    for (int i = 0; i < G::kWarpPasses; ++i) {
+      const int r = i * G::kRowsPerWarpPass + grp;
+      const uint4 u = r < rows ? *reinterpret_cast<const uint4*>(tile + r * G::kRowBytes) : make_uint4(0u, 0u, 0u, 0u);
+      float f[G::kEPL];
+      unpack<kBF16>(u, f);
+      float d = 0.f;
+#pragma unroll
+      for (int e = 0; e < G::kEPL; ++e) d = fmaf(q[e], f[e], d);
+      dot[i] = d;
+    }
+#pragma unroll
+    for (int off = G::kLanesPerRow / 2; off >= 1; off >>= 1)
+#pragma unroll
+      for (int i = 0; i < G::kWarpPasses; ++i) dot[i] += __shfl_xor_sync(0xffffffffu, dot[i], off);
+    if (sub == 0) {
+#pragma unroll
+      for (int i = 0; i < G::kWarpPasses; ++i) {
+        const int r = i * G::kRowsPerWarpPass + grp;
+        if (r < rows) lg[r] = dot[i];
       }
-    } else {
-      f[0] = __uint_as_float(u[ps].x);
-      f[1] = __uint_as_float(u[ps].y);
-      f[2] = __uint_as_float(u[ps].z);
-      f[3] = __uint_as_float(u[ps].w);
     }
-    float d = 0.f;
-#pragma unroll
-    for (int e = 0; e < kEPL; ++e) d = fmaf(q[e], f[e], d);
-    dot[ps] = d;
+    __syncwarp();
+    if (lane == 0 && j + kStages < nchunks && *abort_flag == 0) issue(j + kStages);
   }
-#pragma unroll
-  for (int off = kLanesPerRow / 2; off >= 1; off >>= 1)
-#pragma unroll
-    for (int ps = 0; ps < kPasses; ++ps) dot[ps] += __shfl_xor_sync(0xffffffffu, dot[ps], off);
-  if (sub == 0) {
-#pragma unroll
-    for (int ps = 0; ps < kPasses; ++ps) {
-      const int t = t0 + ps * kRowsPerPass + r0;
-      if (t < n) wrow[t] = dot[ps];
+  __syncthreads();
+  if (*abort_flag != 0 && tid == 0) {
+    // let the copies still in flight land before the shared memory is released
+    for (int st = 0; st < kStages; ++st)
+      if (s_last[st] >= 0) mbar_wait(smem_u32(&bars[st]), static_cast<uint32_t>((s_last[st] / kStages) & 1));
+  }
+
+  // ---- 2. per-head partial max and sum over this CTA's keys, by groups of gl lanes
+  //         (a warp per head up to 8 heads, fewer lanes per head beyond), stored into
+  //         every cluster CTA's partial arrays (every peer has started: see the
+  //         arrive at the top)
+  cluster_wait();
+  {
+    const int gl = nsel <= 8 ? 32 : nsel <= 16 ? 16 : nsel <= 32 ? 8 : 4;
+    const int gi = tid / gl, gsub = tid % gl, ngroups = kThreads / gl;
+    for (int k0 = 0; k0 < nsel; k0 += ngroups) {              // uniform trip count: shuffles stay converged
+      const int k = k0 + gi;
+      const float* lk = stage + min(k, nsel - 1) * ldst;
+      float m = -INFINITY;
+      if (k < nsel)
+        for (int t = gsub; t < cnt; t += gl) m = fmaxf(m, lk[t]);
+      for (int off = gl / 2; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      float s = 0.f;
+      if (k < nsel)
+        for (int t = gsub; t < cnt; t += gl) s += exp2f(lk[t] - m);
+      for (int off = gl / 2; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if (k < nsel)
+        for (int r = gsub; r < C; r += gl) {                    // lanes r, r + gl, ... store into CTA r
+          st_dsmem(s_pm + k * C + x, static_cast<uint32_t>(r), m);
+          st_dsmem(s_ps + k * C + x, static_cast<uint32_t>(r), s);
+        }
     }
   }
+  cluster_sync();     // every partial has arrived; nothing remote is touched after this
+
+  // ---- 3. merge each head's C partials (log-sum-exp)
+  for (int k = warp; k < nsel; k += kWarps) {
+    const float m = lane < C ? s_pm[k * C + lane] : -INFINITY;
+    const float s = lane < C ? s_ps[k * C + lane] : 0.f;
+    const float M = warp_max(m);
+    const float S = warp_sum(s > 0.f ? s * exp2f(m - M) : 0.f);
+    if (lane == 0) {
+      s_M[k] = M;
+      s_inv[k] = S > 0.f ? 1.f / S : 0.f;
+    }
+  }
+  __syncthreads();
+
+  // ---- 4. normalise this CTA's keys, their head mean, and its share of the padding
+  const float inv_nsel = 1.f / static_cast<float>(nsel);
+  float* mrow = mean != nullptr ? mean + static_cast<long long>(b) * T : nullptr;
+  for (int t = t_lo + tid; t < t_lo + cnt; t += kThreads) {
+    float acc = 0.f;
+    for (int k = 0; k < nsel; ++k) {
+      const float w = exp2f(stage[k * ldst + (t - t_lo)] - s_M[k]) * s_inv[k];
+      wslot[static_cast<long long>(k) * T + t] = w;
+      acc += w;
+    }
+    if (mrow != nullptr) mrow[t] = acc * inv_nsel;
+  }
+  const int zc = (T - n + C - 1) / C;
+  const int z_lo = min(T, n + x * zc), z_hi = min(T, z_lo + zc);
+  for (int t = z_lo + tid; t < z_hi; t += kThreads) {
+    for (int k = 0; k < nsel; ++k) wslot[static_cast<long long>(k) * T + t] = 0.f;
+    if (mrow != nullptr) mrow[t] = 0.f;
+  }
 }
 
-// Row (slot blockIdx.y, selected head blockIdx.x) of base-2 logits -> softmax weights.
-__global__ void __launch_bounds__(kThreads)
-    alignment_normalise_kernel(const int* __restrict__ key_len, float* __restrict__ weights, int T) {
-  __shared__ float s_red[kThreads / 32];
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int b = blockIdx.y;
-  const int n = min(max(__ldg(key_len + b), 0), T);
-  float* wrow = weights + (static_cast<long long>(b) * gridDim.x + blockIdx.x) * T;
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // the scores
-  float mx = -INFINITY;
-  for (int t = threadIdx.x; t < n; t += kThreads) mx = fmaxf(mx, wrow[t]);
-  const float M = block_reduce(mx, true, s_red);
-  float sum = 0.f;
-  for (int t = threadIdx.x; t < n; t += kThreads) sum += exp2f(wrow[t] - M);
-  const float S = block_reduce(sum, false, s_red);
-  const float inv = S > 0.f ? 1.f / S : 0.f;
-  for (int t = threadIdx.x; t < T; t += kThreads) wrow[t] = t < n ? exp2f(wrow[t] - M) * inv : 0.f;
+// Largest cluster size C in {16, 8, 4, 2, 1} whose B clusters are all resident at
+// once (one wave; 16 needs the non-portable size), else 1. The resident-cluster
+// counts are queried once per device.
+template <bool kBF16>
+int cluster_size(int B, const DeviceInfo& dev) {
+  static std::mutex mu;
+  static int fit[128][5] = {};                 // resident clusters of size 16, 8, 4, 2, 1; -1 = query failed
+  static bool queried[128] = {};
+  const int dv = dev.device >= 0 && dev.device < 128 ? dev.device : 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!queried[dv]) {
+    if (cudaFuncSetAttribute(alignment_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(dyn_smem_bytes(kMaxAlignHeads, kMaxCluster))) != cudaSuccess) {
+      cudaGetLastError();
+      return -1;
+    }
+    const bool big = cudaFuncSetAttribute(alignment_kernel<kBF16>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                          1) == cudaSuccess;
+    for (int i = 0; i < 5; ++i) {
+      const int c = 16 >> i;
+      int n = 0;
+      if (c <= 8 || big) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(c, 1, 1);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = dyn_smem_bytes(kMaxAlignHeads, kMaxCluster);   // the largest launch
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = c;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, alignment_kernel<kBF16>, &cfg) != cudaSuccess) n = 0;
+      }
+      fit[dv][i] = n;
+    }
+    cudaGetLastError();
+    queried[dv] = true;
+  }
+  for (int i = 0; i < 5; ++i)
+    if (fit[dv][i] >= B) return 16 >> i;
+  return 1;
 }
 
-__global__ void __launch_bounds__(kThreads)
-    head_mean_kernel(const float* __restrict__ weights, float* __restrict__ mean, int nsel, int T) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int b = blockIdx.y;
-  const int t = blockIdx.x * kThreads + threadIdx.x;
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // the normalised weights
-  if (t >= T) return;
-  float s = 0.f;
-  for (int k = 0; k < nsel; ++k) s += weights[(static_cast<long long>(b) * nsel + k) * T + t];
-  mean[static_cast<long long>(b) * T + t] = s / static_cast<float>(nsel);
-}
-
-template <typename Kernel, typename... Args>
-cudaError_t launch_pdl(Kernel kernel, dim3 grid, cudaStream_t stream, Args... args) {
+template <bool kBF16>
+cudaError_t launch(const AlignLaunch& a, const DeviceInfo& dev, cudaStream_t stream) {
+  const int C = cluster_size<kBF16>(a.B, dev);
+  if (C < 0) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
+  cfg.gridDim = dim3(C, a.B, 1);
   cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = dyn_smem_bytes(a.heads.n, C);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = C;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
-  if (e == cudaSuccess) count_launches(1);
-  return e;
+  cfg.numAttrs = 2;
+  const float qscale = a.scale * 1.4426950408889634f;
+  return cudaLaunchKernelEx(&cfg, alignment_kernel<kBF16>, a.Q, static_cast<const uint8_t*>(a.Kc), a.key_len,
+                            a.heads, a.weights, a.mean, a.T, a.L, a.H, qscale, dev.status_word);
 }
 
 }  // namespace
 
-cudaError_t launch_alignment(const AlignLaunch& a, cudaStream_t stream) {
-  const float qscale = a.scale * 1.4426950408889634f;
-  const dim3 grid((a.T + kBlockKeys - 1) / kBlockKeys, a.heads.n, a.B);
-  const uint8_t* Kc = static_cast<const uint8_t*>(a.Kc);
-  cudaError_t e = a.cache_bf16
-                      ? launch_pdl(alignment_scores_kernel<true>, grid, stream, a.Q, Kc, a.key_len, a.heads,
-                                   a.weights, a.T, a.L, a.H, qscale)
-                      : launch_pdl(alignment_scores_kernel<false>, grid, stream, a.Q, Kc, a.key_len, a.heads,
-                                   a.weights, a.T, a.L, a.H, qscale);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(alignment_normalise_kernel, dim3(a.heads.n, a.B), stream, a.key_len, a.weights, a.T);
-  if (e != cudaSuccess) return e;
-  if (a.mean != nullptr)
-    e = launch_pdl(head_mean_kernel, dim3((a.T + kThreads - 1) / kThreads, a.B), stream,
-                   static_cast<const float*>(a.weights), a.mean, a.heads.n, a.T);
+cudaError_t launch_alignment(const AlignLaunch& a, const DeviceInfo& dev, cudaStream_t stream) {
+  if (a.B > 65535) return cudaErrorInvalidValue;
+  const cudaError_t e = a.cache_bf16 ? launch<true>(a, dev, stream) : launch<false>(a, dev, stream);
+  if (e == cudaSuccess) count_launches(1);
   return e;
 }
 

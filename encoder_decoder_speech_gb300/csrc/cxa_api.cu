@@ -375,7 +375,7 @@ int cxa_alignment_weights(const cxa_cache* c, const float* Q, const int* key_len
   a.H = c->H;
   a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(c->dh));
   a.cache_bf16 = c->dtype == CXA_BF16;
-  e = cxa::launch_alignment(a, static_cast<cudaStream_t>(stream));
+  e = cxa::launch_alignment(a, dev, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "cxa_alignment_weights: launch");
   return CXA_OK;
 }

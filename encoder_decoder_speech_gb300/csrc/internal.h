@@ -120,7 +120,7 @@ cudaError_t launch_block(const BlockLaunch& a, const DeviceInfo& dev, cudaStream
 cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream);
 cudaError_t launch_decode_shared_tc(const DecodeLaunch& a, const DeviceInfo& dev, cudaStream_t stream,
                                     std::string* msg);
-cudaError_t launch_alignment(const AlignLaunch& a, cudaStream_t stream);
+cudaError_t launch_alignment(const AlignLaunch& a, const DeviceInfo& dev, cudaStream_t stream);
 // The block as one kernel per layer: a cluster of H CTAs per slot (block_fused.cu).
 bool fused_block_supported(int H, int dh);
 // With *gathered set the launch did the whole block; otherwise it wrote the attention

@@ -231,6 +231,9 @@ CXA_API int cxa_self_attention_step(cxa_cache* c, const int* pos, const float* Q
  *   weights   device fp32 [B][nsel][T] (written completely).
  *   mean      device fp32 [B][T], or NULL to skip it.
  * Errors as for cxa_decode, and CXA_EINVAL for bad nsel or head indices.
+ * One kernel, launched like cxa_decode's (programmatic dependent launch: the
+ * cache and key_len are read before the preceding kernel has finished, Q and
+ * the outputs only after). Out-of-range key_len values are clamped to [0, T].
  */
 CXA_API int cxa_alignment_weights(const cxa_cache* c, const float* Q, const int* key_len,
                                   const int* heads_lh, int nsel, float* weights, float* mean,

@@ -75,3 +75,41 @@ def test_alignment_argument_checks():
     assert cxa.cxa_alignment_weights(c.handle, Q, d["key_len"], [(2, 0)], wt, None, 0.0) == cxa.CXA_EINVAL
     assert cxa.cxa_alignment_weights(c.handle, Q, d["key_len"], [(0, 2)], wt, None, 0.0) == cxa.CXA_EINVAL
     assert cxa.cxa_alignment_weights(c.handle, Q, d["key_len"], [], wt, None, 0.0) == cxa.CXA_EINVAL
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+def test_alignment_key_lengths_around_cluster_split(cache_dtype):
+    """Key lengths shorter than, equal to and just past the per-CTA key ranges of a
+    slot's cluster, negative and beyond T; outputs pre-filled with NaN must be
+    overwritten everywhere."""
+    kls = [1, 7, 8, 9, 15, 16, 17, 31, 33, 129, 300, -4, 5000, 0]
+    w = W.custom("align_edges", B=len(kls), T=300, d=256, L=2, H=4, ragged=False, index=962)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, cache_dtype)
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    kl = np.array(kls, dtype=np.int32)
+    heads = [(1, 2), (0, 0), (1, 3)]
+    Q = W.make_Q(w, 4)
+    wt = torch.full((w.B, len(heads), w.T), float("nan"), device="cuda")
+    mean = torch.full((w.B, w.T), float("nan"), device="cuda")
+    assert cxa.cxa_alignment_weights(c.handle, dev(Q), dev(kl, torch.int32), heads, wt, mean, 0.0) == cxa.CXA_OK
+    wt, mean = host(wt), host(mean)
+    ref_w, ref_m = O.attention_weights(Q, host(c.Kc), np.clip(kl, 0, w.T), heads)
+    assert np.all(np.isfinite(wt)) and np.all(np.isfinite(mean))
+    assert np.abs(wt - ref_w).max() <= WEIGHT_MAX_ABS
+    assert np.abs(mean - ref_m).max() <= WEIGHT_MAX_ABS
+
+
+def test_alignment_many_heads_long_rows_no_mean():
+    """64 selected heads (the maximum, with repeats) over 8192 keys: several load
+    batches per CTA; the mean is not requested."""
+    w = W.custom("align_many", B=3, T=8192, d=256, L=4, H=4, ragged=True, index=963)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, "f32")
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    heads = [((5 * k) % w.L, (3 * k + 1) % w.H) for k in range(64)]
+    Q = W.make_Q(w, 5)
+    wt, mean = c.alignment_weights(dev(Q), d["key_len"], heads, with_mean=False)
+    assert mean is None
+    ref_w, _ = O.attention_weights(Q, host(c.Kc), h["key_len"], heads)
+    assert np.abs(host(wt) - ref_w).max() <= WEIGHT_MAX_ABS
