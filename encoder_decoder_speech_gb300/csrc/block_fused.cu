@@ -105,6 +105,24 @@ __device__ __forceinline__ void load_slice(const uint8_t* p, float (&v)[FusedTra
   }
 }
 
+// (n, mean, M2) <- the moments of the union of two disjoint sets of values, M2 being
+// the sum of squared deviations from the mean (Chan, Golub and LeVeque's pairwise update).
+__device__ __forceinline__ void merge_moments(float& n, float& mean, float& m2, float nb, float mb, float m2b) {
+  if (nb == 0.f) return;
+  if (n == 0.f) {
+    n = nb;
+    mean = mb;
+    m2 = m2b;
+    return;
+  }
+  const float nn = n + nb;
+  const float dl = mb - mean;
+  const float f = nb / nn;
+  mean = fmaf(dl, f, mean);
+  m2 = m2 + m2b + dl * dl * n * f;
+  n = nn;
+}
+
 // y[c] = sum_i in[i] W[i][col0 + c] for c < 64, by the 256 consumer threads: thread
 // (row group rg = t / 16, column quad cq = t % 16) owns rows [rg R, rg R + R) of the
 // slice, held in w (R = d / 16 rows); the 16 partial quads meet in red[16][64].
@@ -147,8 +165,8 @@ __global__ void __maxnreg__(224) fused_block_kernel(const FusedParams p) {
   float* s_q = s_red + kRowGroups * kDh;                  // [64] scaled query
   float* s_o = s_q + kDh;                                 // [64] this head's attention output (read by peers)
   float* s_st = s_o + kDh;                                // [kGroups][66] softmax states
-  float* s_stat = s_st + R_::kGroups * (kDh + 2);         // [8] reduction scratch, [2] mean / rstd
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_stat + 16);   // full[kStages]
+  float* s_stat = s_st + R_::kGroups * (kDh + 2);         // [8][3] LayerNorm moments per warp
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_stat + 32);   // full[kStages]
   unsigned int* s_done = reinterpret_cast<unsigned int*>(bars + kStages);   // [kStages] warps done with a stage
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_done + kStages);
 
@@ -174,7 +192,9 @@ __global__ void __maxnreg__(224) fused_block_kernel(const FusedParams p) {
   const int rg = tid >> 4, cq = tid & 15;
   float4 w[kMaxRowsPerGroup];                             // WQ slice, then the WO slice
 
-  // chunk i of the row into stage i % kStages
+  // chunk i of the row into stage i % kStages; the K/V rows are read once per step,
+  // so they go in L2 as evict-first and the layer's weights stay resident
+  const uint64_t pol = policy_evict_first();
   auto issue = [&](int i) {
     const int s = i % kStages;
     const int n = min(R_::kChunkKeys, kl - i * R_::kChunkKeys);
@@ -183,48 +203,63 @@ __global__ void __maxnreg__(224) fused_block_kernel(const FusedParams p) {
     const uint32_t full = smem_u32(&bars[s]);
     const uint32_t dst = smem_u32(ring + s * R_::kStageBytes);
     mbar_arrive_expect_tx(full, 2 * bytes);
-    bulk_g2s(dst, p.Kc + off, bytes, full);
-    bulk_g2s(dst + R_::kTileBytes, p.Vc + off, bytes, full);
+    bulk_g2s_hint(dst, p.Kc + off, bytes, full, pol);
+    bulk_g2s_hint(dst + R_::kTileBytes, p.Vc + off, bytes, full, pol);
   };
   if (tid == 0)
     for (int i = 0; i < min(nch, kStages); ++i) issue(i);
   {
     // ------------------------------------------------------------ consumers
     load_weights(w, p.WQ, d, h * kDh, R, rg, cq);          // no earlier kernel writes the weights
+    float gv[kMaxD / kConsumers], bv[kMaxD / kConsumers];   // this thread's LayerNorm gain and bias
+#pragma unroll
+    for (int e = 0; e < kMaxD / kConsumers; ++e) {
+      const int i = tid + e * kConsumers;
+      gv[e] = p.gamma && i < d ? __ldg(p.gamma + i) : 1.f;
+      bv[e] = p.beta && i < d ? __ldg(p.beta + i) : 0.f;
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");     // x may come from the previous grid
 
-    // ---- h = LayerNorm(x_b)
-    for (int i = tid; i < d / 4; i += kConsumers)
-      reinterpret_cast<float4*>(s_x)[i] = reinterpret_cast<const float4*>(p.x + static_cast<size_t>(b) * d)[i];
-    consumer_barrier();
-    float part = 0.f;
-    for (int i = tid; i < d; i += kConsumers) part += s_x[i];
+    // ---- h = LayerNorm(x_b), biased variance. One pass: each thread's elements
+    //      i = tid, tid + 256 give a (count, mean, squared deviations) triple; the
+    //      triples merge pairwise (Chan, Golub and LeVeque's update) across the warp
+    //      by shuffles, then across the eight warps through shared memory.
+    const float* xb = p.x + static_cast<size_t>(b) * d;
+    float xv[kMaxD / kConsumers];
+    float cn = 0.f, cm = 0.f, c2 = 0.f;
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    if (lane == 0) s_stat[warp] = part;
-    consumer_barrier();
-    float mean = 0.f;
-#pragma unroll
-    for (int k = 0; k < kConsumerWarps; ++k) mean += s_stat[k];
-    mean /= static_cast<float>(d);
-    part = 0.f;
-    for (int i = tid; i < d; i += kConsumers) {
-      const float c = s_x[i] - mean;
-      part = fmaf(c, c, part);
+    for (int e = 0; e < kMaxD / kConsumers; ++e) {
+      const int i = tid + e * kConsumers;
+      xv[e] = i < d ? xb[i] : 0.f;
+      if (i < d) {
+        s_x[i] = xv[e];
+        cn += 1.f;
+        const float dl = xv[e] - cm;
+        cm += dl / cn;
+        c2 = fmaf(dl, xv[e] - cm, c2);
+      }
     }
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    consumer_barrier();                                    // every warp has read the first sums
-    if (lane == 0) s_stat[warp] = part;
+    for (int off = 16; off >= 1; off >>= 1) {
+      const float on = __shfl_xor_sync(0xffffffffu, cn, off);
+      const float om = __shfl_xor_sync(0xffffffffu, cm, off);
+      const float o2 = __shfl_xor_sync(0xffffffffu, c2, off);
+      merge_moments(cn, cm, c2, on, om, o2);
+    }
+    if (lane == 0) {
+      s_stat[3 * warp] = cn;
+      s_stat[3 * warp + 1] = cm;
+      s_stat[3 * warp + 2] = c2;
+    }
     consumer_barrier();
-    float var = 0.f;
+    float n_all = s_stat[0], mean = s_stat[1], m2 = s_stat[2];
 #pragma unroll
-    for (int k = 0; k < kConsumerWarps; ++k) var += s_stat[k];
-    const float rstd = rsqrtf(var / static_cast<float>(d) + p.eps);
-    for (int i = tid; i < d; i += kConsumers) {
-      const float g = p.gamma ? __ldg(p.gamma + i) : 1.f;
-      const float be = p.beta ? __ldg(p.beta + i) : 0.f;
-      s_h[i] = fmaf((s_x[i] - mean) * rstd, g, be);
+    for (int k = 1; k < kConsumerWarps; ++k) merge_moments(n_all, mean, m2, s_stat[3 * k], s_stat[3 * k + 1], s_stat[3 * k + 2]);
+    const float rstd = rsqrtf(m2 / static_cast<float>(d) + p.eps);
+#pragma unroll
+    for (int e = 0; e < kMaxD / kConsumers; ++e) {
+      const int i = tid + e * kConsumers;
+      if (i < d) s_h[i] = fmaf((xv[e] - mean) * rstd, gv[e], bv[e]);
     }
     consumer_barrier();
 
@@ -367,7 +402,7 @@ template <bool kBF16>
 size_t fused_smem_bytes() {
   using R_ = FusedTraits<kBF16>;
   return 128 + static_cast<size_t>(kStages) * R_::kStageBytes +
-         (2 * kMaxD + kRowGroups * kDh + 2 * kDh + R_::kGroups * (kDh + 2) + 16) * sizeof(float) +
+         (2 * kMaxD + kRowGroups * kDh + 2 * kDh + R_::kGroups * (kDh + 2) + 32) * sizeof(float) +
          kStages * (sizeof(uint64_t) + sizeof(unsigned int)) + 16;
 }
 
