@@ -9,7 +9,8 @@
 //
 // A thread-block cluster of H CTAs per slot b, CTA h of the cluster owning head h
 // (H <= 8: a portable cluster). Each CTA
-//   * streams its (b, layer, h) K/V row through a 6-stage bulk-copy ring from its
+//   * streams its (b, layer, h) K/V row through a 4-stage bulk-copy ring (96 fp32 /
+//     192 bf16 keys of K and V per stage: fewer, larger chunks cost less) from its
 //     first instruction (no earlier kernel writes the cache); the last warp to
 //     finish a chunk refills its stage (a shared-memory count), so every warp
 //     computes and the register file holds both weight slices;
@@ -44,7 +45,17 @@ constexpr int kDh = 64;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers;
-constexpr int kStages = 6;
+// Ring shape (compile-time; the defaults were chosen by timing on GB300).
+#ifndef CXA_BLOCK_STAGES
+#define CXA_BLOCK_STAGES 4
+#endif
+#ifndef CXA_BLOCK_CHUNK_F32
+#define CXA_BLOCK_CHUNK_F32 96
+#endif
+#ifndef CXA_BLOCK_CHUNK_BF16
+#define CXA_BLOCK_CHUNK_BF16 192
+#endif
+constexpr int kStages = CXA_BLOCK_STAGES;
 constexpr int kMaxHeads = 8;                       // portable cluster size
 constexpr int kMaxD = kMaxHeads * kDh;
 constexpr int kRowGroups = 16;                     // projection: 16 groups of d/16 input rows
@@ -54,7 +65,7 @@ template <bool kBF16>
 struct FusedTraits {
   static constexpr int kElem = kBF16 ? 2 : 4;
   static constexpr int kRowBytes = kDh * kElem;              // 256 / 128
-  static constexpr int kChunkKeys = kBF16 ? 128 : 64;        // 16 KB of K per chunk
+  static constexpr int kChunkKeys = kBF16 ? CXA_BLOCK_CHUNK_BF16 : CXA_BLOCK_CHUNK_F32;   // keys per stage
   static constexpr int kTileBytes = kChunkKeys * kRowBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;         // K then V
   static constexpr int kLanesPerKey = kBF16 ? 8 : 16;        // one 16-byte slice of a row per lane

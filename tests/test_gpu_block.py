@@ -153,3 +153,24 @@ def test_cross_block_clamps_key_lengths(cache_dtype):
     ref = O.cross_block(x0, 0, host(c.Kc), host(c.Vc), np.clip(kl, 0, w.T), p["WQ"], p["WO"], p["gamma"],
                         p["beta"], 1e-5, p["bQ"], p["bO"])
     assert np.abs(host(x) - ref).max() <= BLOCK_TOL[cache_dtype]
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+def test_cross_block_key_lengths_around_chunks(cache_dtype):
+    """Rows ending just before, on and after the ring's chunk boundaries (96 fp32 /
+    192 bf16 keys per stage) and past the ring's depth."""
+    kls = [1, 95, 96, 97, 191, 192, 193, 383, 384, 385, 700]
+    w = W.custom("blockchunks", B=len(kls), T=700, d=256, L=2, H=4, ragged=False, index=967)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, cache_dtype)
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    p = _block_params(w.d, 69)
+    kl = np.array(kls, dtype=np.int32)
+    x0 = _rand((w.B, w.d), 70)
+    x = dev(x0)
+    dp = {k: dev(v) for k, v in p.items()}
+    c.cross_block(1, x, dp["WQ"], dp["WO"], dev(kl, torch.int32), ln_gamma=dp["gamma"], ln_beta=dp["beta"],
+                  bQ=dp["bQ"], bO=dp["bO"])
+    ref = O.cross_block(x0, 1, host(c.Kc), host(c.Vc), kl, p["WQ"], p["WO"], p["gamma"], p["beta"], 1e-5,
+                        p["bQ"], p["bO"])
+    assert np.abs(host(x) - ref).max() <= BLOCK_TOL[cache_dtype]
