@@ -174,3 +174,26 @@ def test_cross_block_key_lengths_around_chunks(cache_dtype):
     ref = O.cross_block(x0, 1, host(c.Kc), host(c.Vc), kl, p["WQ"], p["WO"], p["gamma"], p["beta"], 1e-5,
                         p["bQ"], p["bO"])
     assert np.abs(host(x) - ref).max() <= BLOCK_TOL[cache_dtype]
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B", [16, 17, 19, 21])
+def test_cross_block_slot_counts(cache_dtype, B):
+    """Eight heads and more slots than the head clusters that fit at once: the
+    block clusters along the slots (4 or 2 per cluster, the grid padded to whole
+    clusters) or not at all, whichever fits; every form must agree with the oracle."""
+    w = W.custom("blockB%d" % B, B=B, T=300, d=512, L=2, H=8, ragged=True, index=970 + B)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, cache_dtype)
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    p = _block_params(w.d, 71 + B)
+    kl = h["key_len"].copy()
+    kl[B // 2] = 0
+    x0 = _rand((w.B, w.d), 72 + B)
+    x = dev(x0)
+    dp = {k: dev(v) for k, v in p.items()}
+    c.cross_block(1, x, dp["WQ"], dp["WO"], dev(kl, torch.int32), ln_gamma=dp["gamma"], ln_beta=dp["beta"],
+                  bQ=dp["bQ"], bO=dp["bO"])
+    ref = O.cross_block(x0, 1, host(c.Kc), host(c.Vc), kl, p["WQ"], p["WO"], p["gamma"], p["beta"], 1e-5,
+                        p["bQ"], p["bO"])
+    assert np.abs(host(x) - ref).max() <= BLOCK_TOL[cache_dtype]
