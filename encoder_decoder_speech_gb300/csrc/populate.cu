@@ -18,7 +18,8 @@
 //                   accumulator, two accumulators in TMEM (512 columns) so the
 //                   epilogue of one tile overlaps the main loop of the next.
 //        warps 2-5  epilogue: tcgen05.ld rows out of TMEM, add bV on V columns,
-//                   optionally round to bf16, store 64-element head rows at
+//                   optionally round to bf16, stage 128-row boxes in shared
+//                   memory and write them with coalesced 16-byte stores to
 //                   Kc/Vc[b][l][h][t][:].
 //      Tiles never straddle two encoder memories (M tiles are per slot; rows
 //      t >= T are zero-filled by TMA and never stored).
@@ -32,6 +33,7 @@
 #include <type_traits>
 
 #include "internal.h"
+#include "chunk_stream.cuh"
 #include "ptx.cuh"
 
 namespace cxa {
@@ -47,8 +49,9 @@ constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kTmemCols = 2 * kBN;        // two accumulators
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
-constexpr uint32_t kBoxBytes = 32 * 128;       // one store box: 32 rows x 128 bytes
-constexpr uint32_t kStagingBytes = kEpiWarps * 2 * kBoxBytes;   // double-buffered per warp
+constexpr uint32_t kBoxBytes = kBM * 128;      // one store box: the tile's 128 rows x 128 bytes
+constexpr uint32_t kStagingBytes = 2 * kBoxBytes;   // double-buffered, shared by the epilogue warps
+constexpr int kEpiBarrier = 1;                 // named barrier of the 4 epilogue warps
 constexpr int kNumBarriers = 2 * kStages + 4 + 1;
 constexpr size_t kSmemBytes =
     1024 + size_t(kStages) * kStageBytes + kStagingBytes + 8 * kNumBarriers + 16;
@@ -68,6 +71,10 @@ struct GemmParams {
   int cache_bf16;
 };
 
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
+}
+
 __device__ __forceinline__ void report_timeout(unsigned int* status, volatile int* abort) {
   *abort = 1;
   atomicOr(status, 1u);
@@ -77,8 +84,7 @@ template <bool kBF16In>
 __global__ void __launch_bounds__(kThreads, 1)
     populate_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB,
-                         const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV, const GemmParams p) {
+                         const GemmParams p) {
   constexpr int kKElems = kBF16In ? 64 : 32;   // elements per 128-byte k-block row
   constexpr int kKStep = kBF16In ? 16 : 8;     // K of one MMA instruction
   constexpr int kMmasPerBlock = kKElems / kKStep;
@@ -118,8 +124,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    prefetch_tmap(&tmK);
-    prefetch_tmap(&tmV);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -220,32 +224,65 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     // Each warp owns TMEM lanes 32*quad .. 32*quad+31 = 32 consecutive tokens t of
-    // one memory. For every 64-column head block it reads the accumulator rows,
-    // adds bV on V columns, writes them into a 128-byte-swizzled staging box in
-    // shared memory (conflict-free: the 16-byte chunk j of row r lands at slot
-    // j ^ (r & 7)) and one lane TMA-stores the box into the head-major cache,
-    // viewed as (c, t, slot*L*H + l*H + h): the 32 rows are contiguous there, and
-    // rows t >= T fall outside the tensor and are not written.
+    // one memory. For every 64-column head block the four warps read their
+    // accumulator rows, add bV on V columns and write them into one 128-row box of
+    // 128 bytes per row in shared memory (128-byte swizzle, conflict-free: the
+    // 16-byte chunk j of row r lands at slot j ^ (r & 7)); the 128 threads then
+    // read the box back in row order and write it with 16-byte stores into the
+    // head-major cache, where the tile's rows t are contiguous; rows t >= T are
+    // skipped. A tile goes out as 8 boxes (fp32 cache) or 4 (bf16). Storing the
+    // boxes with TMA instead (first a box per warp, then a box per CTA) was slower.
     const int quad = warp & 3;
-    const int ew = warp - 2;                    // staging owner 0..3
-    const uint32_t my_staging = staging + static_cast<uint32_t>(ew) * 2u * kBoxBytes;
+    const bool leader = warp == 2 && lane == 0;  // reads the abort flag for the epilogue
+    const uint32_t ces = p.cache_bf16 ? 2u : 4u; // cache element bytes
     const int LH = p.L * p.H;
     const uint32_t swz = static_cast<uint32_t>(lane & 7);
     int acc = 0;
     uint32_t acc_phase = 0;
     int sbuf = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) {
-        report_timeout(p.status, abort_flag);
-        break;
+    // one box: write this warp's 32 rows into the staging buffer, then all 128
+    // threads read the box back in row order and store it with 16-byte global
+    // stores (a warp writes four whole 128-byte rows per instruction); rows t >= T
+    // are skipped. The buffer alternates, so one barrier per box suffices: a
+    // buffer is rewritten two boxes later, after every thread has passed the
+    // barrier that follows its last read of it.
+    auto put_box = [&](const uint32_t (&w)[8][4], uint8_t* cache, int c0, int t0, int row3) {
+      const uint32_t buf = staging + static_cast<uint32_t>(sbuf) * kBoxBytes;
+      const uint32_t mine = buf + static_cast<uint32_t>(quad * 32 + lane) * 128u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) st_shared_v4(mine + ((static_cast<uint32_t>(j) ^ swz) << 4), w[j][0], w[j][1], w[j][2], w[j][3]);
+      named_barrier(kEpiBarrier, kEpiWarps * 32);             // every row is written
+      const int et = (warp - 2) * 32 + lane;                  // epilogue thread 0..127
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int q = et + m * kEpiWarps * 32;                // 16-byte chunk q of the box
+        const int row = q >> 3, j = q & 7;
+        if (t0 + row < p.T) {
+          uint32_t v0, v1, v2, v3;
+          ld_shared_v4(buf + static_cast<uint32_t>(row) * 128u + ((static_cast<uint32_t>(j ^ (row & 7))) << 4), v0, v1, v2, v3);
+          uint8_t* dst = cache + (static_cast<size_t>(row3) * p.T + (t0 + row)) * (64u * ces) + c0 * ces + j * 16;
+          *reinterpret_cast<uint4*>(dst) = make_uint4(v0, v1, v2, v3);
+        }
       }
+      sbuf ^= 1;
+    };
+    __shared__ int s_epi_stop;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+      // The four warps must take the same path through the tile (named barriers):
+      // each reports its own wait's timeout, then one thread reads the abort flag
+      // once for all of them.
+      const bool got = mbar_wait(tfull_bar(acc), acc_phase, abort_flag);
+      if (!got && lane == 0) report_timeout(p.status, abort_flag);
+      named_barrier(kEpiBarrier, kEpiWarps * 32);
+      if (leader) s_epi_stop = *abort_flag;
+      named_barrier(kEpiBarrier, kEpiWarps * 32);
+      if (s_epi_stop != 0) break;
       tc_fence_after();
       const int mtg = p.raster_n ? tile / (p.num_tiles / p.num_m_tiles) : tile % p.num_m_tiles;
       const int nt = p.raster_n ? tile % (p.num_tiles / p.num_m_tiles) : tile / p.num_m_tiles;
       const int slot = mtg / p.mt_per_slot;
       const int mt = mtg - slot * p.mt_per_slot;
-      const int t0w = mt * kBM + quad * 32;     // first token of this warp's rows
-      const bool any_row = t0w < p.T;
+      const int t0 = mt * kBM;                  // first token of the tile
       const int b = p.b0 + slot;
 #pragma unroll 1
       for (int g = 0; g < kBN / 64; ++g) {
@@ -255,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lh = head - kv * LH;
         const int l = lh / p.H;
         const int h = lh - l * p.H;
-        const CUtensorMap* tm = kv ? &tmV : &tmK;
+        uint8_t* cache = static_cast<uint8_t*>(kv ? p.Vc : p.Kc);
         const int row3 = b * LH + lh;
         uint32_t r[2][32];
 #pragma unroll
@@ -278,50 +315,29 @@ __global__ void __launch_bounds__(kThreads, 1)
               r[half][4 * i + 3] = __float_as_uint(__uint_as_float(r[half][4 * i + 3]) + bb.w);
             }
         }
-        if (!any_row) continue;                 // warp-uniform: every row of this warp is past T
         if (p.cache_bf16) {
           // one box: 64 bf16 channels = 128 bytes per row
-          if (lane == 0) bulk_wait_group_read<1>();
-          __syncwarp();
-          const uint32_t box = my_staging + static_cast<uint32_t>(sbuf) * kBoxBytes + static_cast<uint32_t>(lane) * 128u;
+          uint32_t w[8][4];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint32_t w[4];
+          for (int j = 0; j < 8; ++j)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int c = 8 * j + 2 * k;      // channels c, c+1
-              const float lo = __uint_as_float(r[c >> 5][c & 31]);
-              const float hi = __uint_as_float(r[(c + 1) >> 5][(c + 1) & 31]);
-              __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
-              w[k] = *reinterpret_cast<uint32_t*>(&pr);
+              __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(r[c >> 5][c & 31]),
+                                                        __uint_as_float(r[(c + 1) >> 5][(c + 1) & 31]));
+              w[j][k] = *reinterpret_cast<uint32_t*>(&pr);
             }
-            st_shared_v4(box + ((static_cast<uint32_t>(j) ^ swz) << 4), w[0], w[1], w[2], w[3]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(tm, my_staging + static_cast<uint32_t>(sbuf) * kBoxBytes, 0, t0w, row3);
-            bulk_commit_group();
-          }
-          sbuf ^= 1;
+          put_box(w, cache, 0, t0, row3);
         } else {
           // two boxes: channels 0-31 and 32-63, 128 bytes of fp32 per row each
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
-            if (lane == 0) bulk_wait_group_read<1>();
-            __syncwarp();
-            const uint32_t box = my_staging + static_cast<uint32_t>(sbuf) * kBoxBytes + static_cast<uint32_t>(lane) * 128u;
+            uint32_t w[8][4];
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              st_shared_v4(box + ((static_cast<uint32_t>(j) ^ swz) << 4), r[half][4 * j], r[half][4 * j + 1],
-                           r[half][4 * j + 2], r[half][4 * j + 3]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_3d(tm, my_staging + static_cast<uint32_t>(sbuf) * kBoxBytes, half * 32, t0w, row3);
-              bulk_commit_group();
-            }
-            sbuf ^= 1;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) w[j][k] = r[half][4 * j + k];
+            put_box(w, cache, half * 32, t0, row3);
           }
         }
       }
@@ -331,7 +347,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if (lane == 0) bulk_wait_group_all();   // every store done before the CTA exits
     __syncwarp();
   }
 
@@ -464,26 +479,6 @@ cudaError_t run(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t str
     }
   }
 
-  // the cache as (c, t, slot*L*H + l*H + h): boxes of 32 tokens x 128 bytes
-  CUtensorMap tmK, tmV;
-  {
-    const int cesz = a.cache_bf16 ? 2 : 4;
-    const CUtensorMapDataType cdt = a.cache_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(a.T), static_cast<cuuint64_t>(a.B) * a.L * a.H};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(64) * cesz, static_cast<cuuint64_t>(a.T) * 64 * cesz};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / cesz), 32, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    for (int kv = 0; kv < 2; ++kv) {
-      CUresult r = encode(kv ? &tmV : &tmK, cdt, 3, kv ? a.Vc : a.Kc, dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-      if (r != CUDA_SUCCESS) {
-        *msg = "cuTensorMapEncodeTiled failed for the cache (code " + std::to_string(static_cast<int>(r)) + ")";
-        return cudaErrorInvalidValue;
-      }
-    }
-  }
-
   cudaError_t e = set_smem_attr_once<kBF16In>(dev.device);
   if (e != cudaSuccess) return e;
 
@@ -521,7 +516,7 @@ cudaError_t run(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t str
   p.cache_bf16 = a.cache_bf16 ? 1 : 0;
 
   const int grid = p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms;
-  populate_gemm_kernel<kBF16In><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, tmK, tmV, p);
+  populate_gemm_kernel<kBF16In><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   count_launches(1);
