@@ -724,8 +724,9 @@ def run_block(args):
 def run_selfattn(args):
     """Self-attention KV cache (max_seq_len 448): one token step = append the new
     K/V row at position pos in every (slot, layer, head), then decode positions
-    0..pos. A whole 448-step sequence is timed (CUDA events around all steps) and
-    reported per step; bytes = K/V rows read + new rows written + Q and out."""
+    0..pos. A whole 448-step sequence is timed (CUDA events around all steps),
+    launched call by call and as one CUDA graph, and reported per step; bytes = K/V
+    rows read + new rows written + Q and out."""
     import numpy as np
     import torch
     from encoder_decoder_speech_gb300 import _build, cxa
@@ -743,25 +744,54 @@ def run_selfattn(args):
     for cd, esz in (("f32", 4), ("bf16", 2)):
         cache = cxa.CrossAttentionCache(B, T, L, H, 64, cd)
         out = torch.empty((B, L, H, 64), device="cuda")
+
+        def sequence():
+            for s in range(T):
+                cache.self_attention_step(pos[s], Qs[s], Ks[s], Vs[s], out=out)
+
         for s in range(min(args.warmup, T)):
             cache.self_attention_step(pos[s], Qs[s], Ks[s], Vs[s], out=out)
         torch.cuda.synchronize()
-        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         n0 = cxa.cxa_launch_count()
-        a.record()
-        for s in range(T):
-            cache.self_attention_step(pos[s], Qs[s], Ks[s], Vs[s], out=out)
-        b_.record()
+        sequence()
         torch.cuda.synchronize()
         kernels_per_step = (cxa.cxa_launch_count() - n0) / T
-        us = a.elapsed_time(b_) * 1000.0 / T
+        # the whole sequence launched one C-ABI call per step from Python, then
+        # replayed as one captured CUDA graph (how a decoder loop would run it)
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            sequence()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph):
+            sequence()
+        torch.cuda.synchronize()
         rows = B * L * H
         byts = sum(2 * rows * (s + 1) * 64 * esz for s in range(T)) / T + rows * 64 * (2 * esz + 2 * 4 + 2 * 4)
-        print(json.dumps({"self_attention_step": {"B": B, "L": L, "H": H, "max_seq_len": T, "cache_dtype": cd},
-                          "us_per_step_mean": round(us, 2), "tokens_per_s": round(B / (us * 1e-6), 1),
-                          "GBps_mean": round(byts / (us * 1e-6) / 1e9, 1),
-                          "frac_of_measured_hbm": round(byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 3),
-                          "kernels_per_step": kernels_per_step}), flush=True)
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for mode in ("eager", "graph"):
+            run = sequence if mode == "eager" else graph.replay
+            run()
+            torch.cuda.synchronize()
+            h0 = time.perf_counter()
+            a.record()
+            run()
+            b_.record()
+            h1 = time.perf_counter()
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b_) * 1000.0 / T
+            line = {"self_attention_step": {"B": B, "L": L, "H": H, "max_seq_len": T, "cache_dtype": cd,
+                                            "launch": mode},
+                    "us_per_step_mean": round(us, 2), "tokens_per_s": round(B / (us * 1e-6), 1),
+                    "GBps_mean": round(byts / (us * 1e-6) / 1e9, 1),
+                    "frac_of_measured_hbm": round(byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 3),
+                    "kernels_per_step": kernels_per_step}
+            if mode == "eager":
+                line["host_us_per_step"] = round((h1 - h0) * 1e6 / T, 2)
+            print(json.dumps(line), flush=True)
+        del graph
         cache.close()
     assert cxa.cxa_device_status(1) == cxa.CXA_OK
     return 0

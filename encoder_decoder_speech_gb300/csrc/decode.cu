@@ -182,7 +182,9 @@ constexpr int min_ctas_per_sm() {
 // position key_len[b] (when in [0, T)) and attends positions 0 .. key_len[b]; the
 // lane that meets that key takes it from Knew/Vnew rather than the cache copy it
 // streamed, so nothing in the grid waits for the writes. The previous step wrote
-// rows this one reads, so here the cache is read only after the grid dependency wait.
+// row pos - 1, so only chunks of keys below min(pos, T) - 1 are streamed before the
+// grid dependency wait, and this instance lets the next grid start only after its
+// own wait.
 template <bool kBF16, int kNQ, bool kAppend = false>
 __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
     decode_stream_kernel(const DecodeParams p) {
@@ -204,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
   const int lane = threadIdx.x & 31;
   const int LH = p.LH;
   const int nq = p.nq;
-  allow_dependent_launch();
+  if constexpr (!kAppend) allow_dependent_launch();
 
   // ---- chunk numbering (every CTA computes the same prefix from key_len)
   if (warp == 0) {
@@ -250,27 +252,48 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
 
   // The cache and key_len are inputs no decode writes: the producer starts
   // streaming the first stages' K and V rows before the previous grid is done.
+  // The self-attention step (kAppend) reads early only the chunks whose keys all
+  // lie below min(pos, T) - 1: the row at pos - 1 is the one the previous step
+  // wrote, and that step (like this one) lets its successor start only after its
+  // own dependency wait, so everything written before it is complete.
   const uint64_t pol = policy_evict_first();
   Cursor pcur{0, 0, 0};
-  long long npre = 0;
-  if constexpr (kAppend) wait_prior_grid();
+  Cursor pc{0, 0, 0};                    // the next chunk to pre-issue
+  long long npre = 0, nissued = 0;
+  auto issue_stage = [&](long long i, const Cursor& c) {
+    const int kl = min(max(__ldg(p.key_len + c.b) + p.key_len_add, 0), p.T);
+    const int n = min(R::kChunkKeys, kl - c.c * R::kChunkKeys);
+    const long long crow = static_cast<long long>(c.b) * p.LHc + p.lh0 + c.lh;   // cache row
+    const size_t off = (static_cast<size_t>(crow) * p.T + static_cast<size_t>(c.c) * R::kChunkKeys) * R::kRowBytes;
+    const uint32_t kv_bytes = static_cast<uint32_t>(n) * R::kRowBytes;
+    const uint32_t full = smem_u32(&bars[i]);
+    const uint32_t dst = smem_u32(stages + i * R::kStageBytes);
+    mbar_arrive_expect_tx(full, 2 * kv_bytes + static_cast<uint32_t>(nq) * kQRowBytes);
+    bulk_g2s_hint(dst, p.Kc + off, kv_bytes, full, pol);
+    bulk_g2s_hint(dst + R::kKVBytes, p.Vc + off, kv_bytes, full, pol);
+  };
   if (active && producer) {
     pcur = locate(g0, s_first, s_nch, p.B);
-    Cursor c = pcur;
+    pc = pcur;
     npre = (g1 - g0) < kStages ? (g1 - g0) : kStages;
-    for (long long i = 0; i < npre; ++i) {
-      const int kl = min(max(__ldg(p.key_len + c.b) + p.key_len_add, 0), p.T);
-      const int n = min(R::kChunkKeys, kl - c.c * R::kChunkKeys);
-      const long long crow = static_cast<long long>(c.b) * p.LHc + p.lh0 + c.lh;   // cache row
-      const size_t off = (static_cast<size_t>(crow) * p.T + static_cast<size_t>(c.c) * R::kChunkKeys) * R::kRowBytes;
-      const uint32_t kv_bytes = static_cast<uint32_t>(n) * R::kRowBytes;
-      const uint32_t full = smem_u32(&bars[i]);
-      const uint32_t dst = smem_u32(stages + i * R::kStageBytes);
-      mbar_arrive_expect_tx(full, 2 * kv_bytes + static_cast<uint32_t>(nq) * kQRowBytes);
-      bulk_g2s_hint(dst, p.Kc + off, kv_bytes, full, pol);
-      bulk_g2s_hint(dst + R::kKVBytes, p.Vc + off, kv_bytes, full, pol);
-      advance(c, s_nch, p.B, LH);
+    for (; nissued < npre; ++nissued) {
+      if constexpr (kAppend) {
+        const int kl = min(max(__ldg(p.key_len + pc.b) + p.key_len_add, 0), p.T);
+        const int end = pc.c * R::kChunkKeys + min(R::kChunkKeys, kl - pc.c * R::kChunkKeys);
+        if (end > min(__ldg(p.key_len + pc.b), p.T) - 1) break;   // may hold the previous step's row
+      }
+      issue_stage(nissued, pc);
+      advance(pc, s_nch, p.B, LH);
     }
+  }
+  if constexpr (kAppend) {
+    wait_prior_grid();
+    allow_dependent_launch();
+    if (active && producer)
+      for (; nissued < npre; ++nissued) {
+        issue_stage(nissued, pc);
+        advance(pc, s_nch, p.B, LH);
+      }
   }
   // Q, out and the workspace may belong to the previous grid: wait for it.
   wait_prior_grid();

@@ -210,6 +210,17 @@ CXA_API int cxa_cache_append(cxa_cache* c, const int* pos, const float* K_new, c
  * Arguments as for cxa_cache_append and cxa_decode (workspace of
  * cxa_decode_workspace_bytes size). Every argument is checked before anything
  * is enqueued.
+ *
+ * Launch overlap: one kernel, launched with programmatic dependent launch. It
+ * streams slot b's cache rows t < min(pos[b], T) - 1 before the kernel just
+ * before it on the stream has finished, and everything else (row pos[b] - 1,
+ * which the previous step writes in a decoding loop, Q, the new rows, out) only
+ * after. It lets the next kernel start only after that wait, so a step never
+ * overlaps work older than its immediate predecessor. Hence the kernel just
+ * before a step must not write rows t < pos[b] - 1 while launched with
+ * programmatic launch: consecutive steps that advance pos[b] by at most one
+ * (or move it back), and any cxa_cache_append, cxa_populate, ordinary kernel or
+ * copy in between, are always safe.
  */
 CXA_API int cxa_self_attention_step(cxa_cache* c, const int* pos, const float* Q, const float* K_new,
                                     const float* V_new, float* out, float scale, void* workspace,

@@ -70,3 +70,45 @@ def test_end_of_cache_and_out_of_range_positions():
     out = host(c.self_attention_step(dev(np.array([447, 500, 0], np.int32), torch.int32), dev(Q), dev(K0), dev(V0)))
     ref = O.decode(Q, host(c.Kc), host(c.Vc), np.array([448, 500 + 1, 1]))
     assert np.abs(out - ref).max() <= DECODE_F32_MAX_ABS
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+def test_long_sequence_rewind_and_interleaved_decodes(cache_dtype):
+    """300 steps, then both slots start a new sequence at position 0 for 160 more, with
+    a cross-attention decode (a kernel that lets its successor start at once) launched
+    between every two steps and no host syncs. A step streams the rows below pos - 1
+    before the previous kernel has finished: every output must still match the
+    oracle's token-by-token decode of its own sequence."""
+    from _gpu_common import cache_for, inputs_on_device
+    B, L, H, T, S1, S2 = 2, 1, 2, 448, 300, 160
+    c = cxa.CrossAttentionCache(B, T, L, H, 64, cache_dtype)
+    w = W.custom("sa_cross", B=B, T=200, d=128, L=L, H=H, index=980)
+    d, _ = inputs_on_device(w)
+    cross = cache_for(w, "f32")
+    cross.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    Qc = dev(W.make_Q(w, 1))
+    seqs = []
+    for k, S in enumerate((S1, S2)):
+        Qs, Ks, Vs = _rand((S, B, L, H, 64), 20 + k), _rand((S, B, L, H, 64), 30 + k), _rand((S, B, L, H, 64), 40 + k)
+        if cache_dtype == "bf16":
+            Ks, Vs = W.bf16_round(Ks), W.bf16_round(Vs)
+        seqs.append((Qs, Ks, Vs))
+    outs = []
+    torch.cuda.synchronize()
+    for Qs, Ks, Vs in seqs:
+        S = Qs.shape[0]
+        pos = [dev(np.full(B, s, np.int32), torch.int32) for s in range(S)]
+        Qd, Kd, Vd = [dev(q) for q in Qs], [dev(x) for x in Ks], [dev(x) for x in Vs]
+        o = [torch.empty((B, L, H, 64), device="cuda") for _ in range(S)]
+        for s in range(S):
+            c.self_attention_step(pos[s], Qd[s], Kd[s], Vd[s], out=o[s])
+            cross.decode(Qc, d["key_len"])
+        outs.append(o)
+    torch.cuda.synchronize()
+    for (Qs, Ks, Vs), o in zip(seqs, outs):
+        got = np.stack([host(x) for x in o])
+        for b in range(B):
+            for l in range(L):
+                for h in range(H):
+                    ref = O.self_attention_steps(Qs[:, b, l, h], Ks[:, b, l, h], Vs[:, b, l, h])
+                    assert np.abs(got[:, b, l, h] - ref).max() <= TOL[cache_dtype]
