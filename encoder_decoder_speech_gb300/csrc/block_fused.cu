@@ -180,6 +180,7 @@ __global__ void __maxnreg__(224) fused_block_kernel(const FusedParams p) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_stat + 32);   // full[kStages]
   unsigned int* s_done = reinterpret_cast<unsigned int*>(bars + kStages);   // [kStages] warps done with a stage
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_done + kStages);
+  int* s_last = reinterpret_cast<int*>(s_done + kStages + 1);   // [kStages] last chunk issued into stage s
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int h = blockIdx.x;                               // head = column block = cluster rank
@@ -190,6 +191,7 @@ __global__ void __maxnreg__(224) fused_block_kernel(const FusedParams p) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bars[s]), 1);
       s_done[s] = 0u;
+      s_last[s] = -1;
     }
     *s_abort = 0;
     fence_mbar_init();
@@ -213,6 +215,7 @@ __global__ void __maxnreg__(224) fused_block_kernel(const FusedParams p) {
     const size_t off = row_off + static_cast<size_t>(i) * R_::kTileBytes;
     const uint32_t full = smem_u32(&bars[s]);
     const uint32_t dst = smem_u32(ring + s * R_::kStageBytes);
+    s_last[s] = i;
     mbar_arrive_expect_tx(full, 2 * bytes);
     bulk_g2s_hint(dst, p.Kc + off, bytes, full, pol);
     bulk_g2s_hint(dst + R_::kTileBytes, p.Vc + off, bytes, full, pol);
@@ -373,6 +376,10 @@ __global__ void __maxnreg__(224) fused_block_kernel(const FusedParams p) {
 #pragma unroll
     for (int c = 0; c < CPL; ++c) st[2 + sl * CPL + c] = acc[c];
     consumer_barrier();
+    // every warp has left the loop: after a timeout, let the copies still in flight land
+    if (*s_abort != 0 && tid == 0)
+      for (int s = 0; s < kStages; ++s)
+        if (s_last[s] >= 0) mbar_wait(smem_u32(&bars[s]), static_cast<uint32_t>((s_last[s] / kStages) & 1));
     if (tid < kDh) {
       float M = -INFINITY;
       for (int g = 0; g < R_::kGroups; ++g) M = fmaxf(M, s_st[g * (kDh + 2)]);
@@ -414,7 +421,7 @@ size_t fused_smem_bytes() {
   using R_ = FusedTraits<kBF16>;
   return 128 + static_cast<size_t>(kStages) * R_::kStageBytes +
          (2 * kMaxD + kRowGroups * kDh + 2 * kDh + R_::kGroups * (kDh + 2) + 32) * sizeof(float) +
-         kStages * (sizeof(uint64_t) + sizeof(unsigned int)) + 16;
+         kStages * (sizeof(uint64_t) + sizeof(unsigned int) + sizeof(int)) + 16;
 }
 
 template <bool kBF16, bool kGather>
