@@ -13,6 +13,7 @@
 
 #include "cxa.h"
 #include "internal.h"
+#include "ptx.cuh"
 
 // Device-side status word: kernels OR in 1 when a bounded wait expires.
 static __device__ unsigned int g_cxa_status_word = 0;
@@ -104,6 +105,24 @@ bool cache_geometry(const cxa_cache* c, int* B, int* T, int* L, int* H, int* dh)
   return true;
 }
 
+}  // namespace cxa
+
+namespace cxa {
+namespace {
+
+// Failure-detection self-test: one thread waits, through the same bounded wait the
+// kernels use, on an mbarrier that nothing ever arrives on; when the limit expires it
+// sets the device status word, as a kernel whose copies never land would, and returns.
+__global__ void wait_timeout_selftest_kernel(unsigned int* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    if (!mbar_wait(smem_u32(&bar), 0u, nullptr, limit_ns)) atomicOr(status, 1u);
+  }
+}
+
+}  // namespace
 }  // namespace cxa
 
 extern "C" {
@@ -463,6 +482,20 @@ const char* cxa_strerror(int code) {
 const char* cxa_last_error_message(void) { return g_last_msg.c_str(); }
 
 unsigned long long cxa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int cxa_selftest_wait_timeout(unsigned int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000)
+    return fail(CXA_EINVAL, "cxa_selftest_wait_timeout: limit_us must be in [1, 1000000]");
+  std::string msg;
+  cxa::DeviceInfo dev;
+  cudaError_t e = cxa::current_device_info(&dev, &msg);
+  if (e != cudaSuccess) return fail_cuda(e, "cxa_selftest_wait_timeout: " + msg);
+  cxa::wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      dev.status_word, static_cast<unsigned long long>(limit_us) * 1000ull);
+  if ((e = cudaGetLastError()) != cudaSuccess) return fail_cuda(e, "cxa_selftest_wait_timeout: launch");
+  cxa::count_launches(1);
+  return CXA_OK;
+}
 
 int cxa_device_status(int clear) {
   std::string msg;

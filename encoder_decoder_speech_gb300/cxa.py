@@ -37,6 +37,7 @@ SIGNATURES = {
     "cxa_last_error_message": (ctypes.c_char_p, []),
     "cxa_launch_count": (ctypes.c_ulonglong, []),
     "cxa_device_status": (ctypes.c_int, [ctypes.c_int]),
+    "cxa_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint, ctypes.c_void_p]),
     "cxa_decode_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                           ctypes.c_float, ctypes.c_void_p]),
     "cxa_decode_shared_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 6),
@@ -217,6 +218,11 @@ def cxa_launch_count() -> int:
 
 def cxa_device_status(clear=0) -> int:
     return load().cxa_device_status(clear)
+
+
+def cxa_selftest_wait_timeout(limit_us: int, stream=None) -> int:
+    """Enqueue the bounded-wait self-test kernel (its wait expires after limit_us)."""
+    return load().cxa_selftest_wait_timeout(limit_us, _stream(stream))
 
 
 # ---------------------------------------------------------------- owner object

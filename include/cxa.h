@@ -321,6 +321,17 @@ CXA_API unsigned long long cxa_launch_count(void);
 CXA_API int cxa_device_status(int clear);
 
 /*
+ * Failure-detection self-test (no counterpart in the source pages). Enqueues on
+ * `stream` one kernel whose single waiting thread waits, through the same bounded
+ * wait every kernel of this library uses, on a barrier that nothing completes;
+ * after limit_us microseconds (1 .. 1000000) the wait gives up, the kernel sets
+ * the device status word and returns, and cxa_device_status then reports
+ * CXA_ETIMEOUT. Nothing faults or hangs, and the context stays usable. Returns
+ * CXA_EINVAL for a limit outside that range, CXA_ECUDA if the launch fails.
+ */
+CXA_API int cxa_selftest_wait_timeout(unsigned int limit_us, void* stream);
+
+/*
  * Allocation-free decode (no counterpart in the source pages: an addition of
  * this library for callers that cannot allocate device memory).
  *
