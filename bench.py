@@ -68,6 +68,7 @@ def parse_args(argv=None):
     p.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--budget-s", type=float, default=12.0, help=argparse.SUPPRESS)
     p.add_argument("--max-slots", type=int, default=16, help=argparse.SUPPRESS)
+    p.add_argument("--procs", type=int, default=1, help=argparse.SUPPRESS)
     a = p.parse_args(argv)
     if a.warmup < 3 and not a.oracle_sample:
         p.error("--warmup must be >= 3")
@@ -210,7 +211,7 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- oracle legs
-def oracle_sample(budget_s: float, max_slots: int, warmup_slots: int = 0):
+def oracle_sample(budget_s: float, max_slots: int, warmup_slots: int = 0, first_slot: int = 0):
     """Time the fp64 oracle on whole windows of the workload (one memory: its
     populate, then its 128 decode steps), one memory after another, until
     max_slots windows are timed or the time budget is spent. warmup_slots
@@ -231,10 +232,10 @@ def oracle_sample(budget_s: float, max_slots: int, warmup_slots: int = 0):
         return time.perf_counter() - t0
 
     for i in range(warmup_slots):
-        window(i % w.B)
+        window((first_slot + i) % w.B)
     tokens, slots, spent = 0, 0, 0.0
     for i in range(max_slots):
-        spent += window(i % w.B)
+        spent += window((first_slot + i) % w.B)
         tokens += w.steps
         slots += 1
         if spent >= budget_s:
@@ -242,12 +243,45 @@ def oracle_sample(budget_s: float, max_slots: int, warmup_slots: int = 0):
     return {"tokens": tokens, "seconds": spent, "slots": slots}
 
 
-def run_oracle_subprocess(budget_s: float, max_slots: int, warmup_slots: int = 0):
-    """The oracle timed in a fresh single-threaded process (BLAS pinned to one thread)."""
+def _oracle_worker(args):
+    budget_s, max_slots, first_slot = args
+    return oracle_sample(budget_s, max_slots, 1, first_slot)
+
+
+def oracle_sample_procs(budget_s: float, max_slots: int, procs: int):
+    """The same windows on procs worker processes at once (started with spawn, each
+    single-threaded): windows are independent, so this is the oracle as it stands
+    on procs host cores. Returns tokens over the wall time of the timed windows."""
+    import multiprocessing as mp
+    with mp.get_context("spawn").Pool(procs) as pool:
+        pool.map(_oracle_worker, [(0.0, 0, i) for i in range(procs)])   # imports and first window untimed
+        t0 = time.perf_counter()
+        res = pool.map(_oracle_worker, [(budget_s, max_slots, i) for i in range(procs)])
+        wall = time.perf_counter() - t0
+    return {"tokens": sum(r["tokens"] for r in res), "seconds": wall, "slots": sum(r["slots"] for r in res),
+            "procs": procs}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name as the OS reports it (best effort)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def run_oracle_subprocess(budget_s: float, max_slots: int, warmup_slots: int = 0, procs: int = 1):
+    """The oracle timed in a fresh process (BLAS pinned to one thread per process),
+    single-threaded or on procs worker processes."""
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
                RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", "--budget-s", str(budget_s),
-                        "--max-slots", str(max_slots), "--warmup", str(warmup_slots)],
+                        "--max-slots", str(max_slots), "--warmup", str(warmup_slots), "--procs", str(procs)],
                        capture_output=True, text=True, env=env, timeout=3600)
     if r.returncode != 0:
         raise RuntimeError("oracle sample failed: " + r.stderr[-2000:])
@@ -255,9 +289,12 @@ def run_oracle_subprocess(budget_s: float, max_slots: int, warmup_slots: int = 0
 
 
 def cpu_baseline_obj(res):
-    return {"value": res["tokens"] / res["seconds"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+    procs = res.get("procs", 1)
+    how = "single thread" if procs == 1 else f"{procs} single-threaded processes at once, wall time"
+    return {"value": res["tokens"] / res["seconds"], "unit": "tokens/s", "cores": procs, "kind": "oracle",
             "sample": f"{res['slots']} whole window(s) of the workload (one memory each: fp64 populate + "
-                      f"128 decode steps), {res['tokens']} tokens in {res['seconds']:.1f} s, single thread"}
+                      f"128 decode steps), {res['tokens']} tokens in {res['seconds']:.1f} s, {how}",
+            "cpu_model": cpu_model(), "nproc": os.cpu_count()}
 
 
 def run_reference(args):
@@ -920,9 +957,14 @@ def run_profile(args):
 def run_cxa(args):
     rank, world, local = dist_env()
     cpu_base = None
+    cpu_base_mc = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # the oracle leg runs first, in its own process, before any GPU work
+        # the oracle legs run first, in their own processes, before any GPU work:
+        # single-threaded, then as many single-threaded processes as the host has cores
         cpu_base = cpu_baseline_obj(run_oracle_subprocess(args.budget_s, args.max_slots))
+        ncores = os.cpu_count() or 1
+        if ncores > 1:
+            cpu_base_mc = cpu_baseline_obj(run_oracle_subprocess(args.budget_s, args.max_slots, procs=ncores))
 
     import torch
     from encoder_decoder_speech_gb300 import _build, cxa
@@ -1002,6 +1044,8 @@ def run_cxa(args):
     }
     if cpu_base is not None:
         line["cpu_baseline"] = cpu_base
+    if cpu_base_mc is not None:
+        line["cpu_baseline_multicore"] = cpu_base_mc
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
@@ -1011,7 +1055,10 @@ def run_cxa(args):
 def main(argv=None):
     args = parse_args(argv)
     if args.oracle_sample:
-        print(json.dumps(oracle_sample(args.budget_s, args.max_slots, args.warmup)))
+        if args.procs > 1:
+            print(json.dumps(oracle_sample_procs(args.budget_s, args.max_slots, args.procs)))
+        else:
+            print(json.dumps(oracle_sample(args.budget_s, args.max_slots, args.warmup)))
         return 0
     if args.profile:
         return run_profile(args)
