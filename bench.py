@@ -517,8 +517,24 @@ def measure_populate_large(torch, cxa, W, Wu, reps=10):
     b.record()
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / reps
+    # the decode on the same cache: 8 x 32 x 20 query rows over 1500 keys each (1.97 GB)
+    kl_h = W.make_key_len(w)
+    kl = torch.from_numpy(kl_h).to("cuda")
+    Qs = [torch.from_numpy(W.make_Q(w, s)).to("cuda") for s in range(4)]
+    out = torch.empty_like(Qs[0])
+    for s in range(max(Wu, 3)):
+        cache.decode(Qs[s % 4], kl, out=out)
+    torch.cuda.synchronize()
+    steps = 40
+    a.record()
+    for s in range(steps):
+        cache.decode(Qs[s % 4], kl, out=out)
+    b.record()
+    torch.cuda.synchronize()
+    dec_us = a.elapsed_time(b) * 1000.0 / steps
     cache.close()
-    return {"ms": ms, "flops_per_call": populate_flops(w.L, w.d, w.B, w.T)}
+    return {"ms": ms, "flops_per_call": populate_flops(w.L, w.d, w.B, w.T), "decode_us": dec_us,
+            "decode_bytes": decode_bytes(w.L, w.H, w.dh, 2, kl_h, w.B), "B": w.B}
 
 
 def run_sweep(args):
@@ -1031,6 +1047,13 @@ def run_cxa(args):
             "peak": peaks["bf16_tflops"], "peak_note": f"{peaks['source']} bf16 burst",
             "frac": large["flops_per_call"] / (large["ms"] * 1e-3) / 1e12 / peaks["bf16_tflops"],
             "ms": large["ms"]},
+        "decode_large_bf16": None if large is None else {
+            "bound": "hbm", "kernel": "decode_stream_kernel<bf16>",
+            "workload": "whisper-large dims: 8 memories x 1500 keys, 32 layers, 20x64 heads, bf16 cache, 40 steps",
+            "us_per_step": large["decode_us"], "tokens_per_s": large["B"] / (large["decode_us"] * 1e-6),
+            "achieved": large["decode_bytes"] / (large["decode_us"] * 1e-6) / 1e9, "unit": "GB/s",
+            "peak": peaks["hbm_gbs"],
+            "frac": large["decode_bytes"] / (large["decode_us"] * 1e-6) / 1e9 / peaks["hbm_gbs"]},
         "clocks": main["clocks"],
         "spread_ms": main["spread_ms"],
         "e2e": {"value": tokens / (e2e_ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
