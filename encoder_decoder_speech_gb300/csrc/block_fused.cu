@@ -9,11 +9,11 @@
 //
 // A thread-block cluster of H CTAs per slot b, CTA h of the cluster owning head h
 // (H <= 8: a portable cluster). Each CTA
-//   * streams its (b, layer, h) K/V row through a 4-stage bulk-copy ring (96 fp32 /
-//     192 bf16 keys of K and V per stage: fewer, larger chunks cost less) from its
-//     first instruction (no earlier kernel writes the cache); the last warp to
-//     finish a chunk refills its stage (a shared-memory count), so every warp
-//     computes and the register file holds both weight slices;
+//   * streams its (b, layer, h) K/V row through a 16-stage bulk-copy ring (24 fp32 /
+//     48 bf16 keys of K and V per stage) from its first instruction (no earlier
+//     kernel writes the cache); chunk i belongs to warp i % 8 alone, which waits
+//     for it, runs it through its lane groups' softmax states and refills the
+//     stage with chunk i + 16, so no warp waits for another within the loop;
 //   * loads its 64-column slice of WQ into registers before waiting on the
 //     previous grid (programmatic dependent launch), then normalises x_b and
 //     projects its head's query;
@@ -47,15 +47,16 @@ constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers;
 // Ring shape (compile-time; the defaults were chosen by timing on GB300).
 #ifndef CXA_BLOCK_STAGES
-#define CXA_BLOCK_STAGES 4
+#define CXA_BLOCK_STAGES 16
 #endif
 #ifndef CXA_BLOCK_CHUNK_F32
-#define CXA_BLOCK_CHUNK_F32 96
+#define CXA_BLOCK_CHUNK_F32 24
 #endif
 #ifndef CXA_BLOCK_CHUNK_BF16
-#define CXA_BLOCK_CHUNK_BF16 192
+#define CXA_BLOCK_CHUNK_BF16 48
 #endif
 constexpr int kStages = CXA_BLOCK_STAGES;
+static_assert(kStages % kConsumerWarps == 0, "each warp owns kStages / 8 stages");
 constexpr int kMaxHeads = 8;                       // portable cluster size
 constexpr int kMaxD = kMaxHeads * kDh;
 constexpr int kRowGroups = 16;                     // projection: 16 groups of d/16 input rows
@@ -72,8 +73,8 @@ struct FusedTraits {
   static constexpr int kKeysPerPass = 32 / kLanesPerKey;     // keys per warp per pass
   static constexpr int kChanPerLane = 16 / kElem;            // 4 / 8 channels
   static constexpr int kGroups = kConsumerWarps * kKeysPerPass;   // softmax states per CTA
-  static constexpr int kPasses = kChunkKeys / kGroups;
-  static_assert(kPasses * kGroups == kChunkKeys, "chunk = whole passes");
+  static constexpr int kPasses = kChunkKeys / kKeysPerPass;  // passes of one warp over a chunk
+  static_assert(kPasses * kKeysPerPass == kChunkKeys, "chunk = whole passes");
 };
 
 struct FusedParams {
@@ -178,9 +179,8 @@ __global__ void __maxnreg__(224) fused_block_kernel(const FusedParams p) {
   float* s_st = s_o + kDh;                                // [kGroups][66] softmax states
   float* s_stat = s_st + R_::kGroups * (kDh + 2);         // [8][3] LayerNorm moments per warp
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_stat + 32);   // full[kStages]
-  unsigned int* s_done = reinterpret_cast<unsigned int*>(bars + kStages);   // [kStages] warps done with a stage
-  volatile int* s_abort = reinterpret_cast<volatile int*>(s_done + kStages);
-  int* s_last = reinterpret_cast<int*>(s_done + kStages + 1);   // [kStages] last chunk issued into stage s
+  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + kStages);
+  int* s_last = const_cast<int*>(s_abort) + 1;             // [kStages] last chunk issued into stage s
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int h = blockIdx.x;                               // head = column block = cluster rank
@@ -190,7 +190,6 @@ __global__ void __maxnreg__(224) fused_block_kernel(const FusedParams p) {
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bars[s]), 1);
-      s_done[s] = 0u;
       s_last[s] = -1;
     }
     *s_abort = 0;
@@ -220,8 +219,10 @@ __global__ void __maxnreg__(224) fused_block_kernel(const FusedParams p) {
     bulk_g2s_hint(dst, p.Kc + off, bytes, full, pol);
     bulk_g2s_hint(dst + R_::kTileBytes, p.Vc + off, bytes, full, pol);
   };
-  if (tid == 0)
-    for (int i = 0; i < min(nch, kStages); ++i) issue(i);
+  // chunk i belongs to warp i % 8 alone: that warp waits for it, computes it and
+  // refills its stage with chunk i + kStages (kStages is a multiple of 8)
+  if (lane == 0)
+    for (int i = warp; i < min(nch, kStages); i += kConsumerWarps) issue(i);
   {
     // ------------------------------------------------------------ consumers
     load_weights(w, p.WQ, d, h * kDh, R, rg, cq);          // no earlier kernel writes the weights
@@ -290,7 +291,8 @@ __global__ void __maxnreg__(224) fused_block_kernel(const FusedParams p) {
     // the out-projection slice: its loads run under the attention loop
     if constexpr (kGather) load_weights(w, p.WO, d, h * kDh, R, rg, cq);
 
-    // ---- attention over the ring: lane group u of warp wp takes key (pass * kGroups + wp * KPP + u)
+    // ---- attention over the ring: warp wp takes chunks wp, wp + 8, ...; within a
+    //      chunk its lane group u takes keys u, u + KPP, ... (one softmax state each)
     constexpr int LPK = R_::kLanesPerKey, CPL = R_::kChanPerLane, KPP = R_::kKeysPerPass;
     const int u = lane / LPK, sl = lane % LPK;             // key within the pass, 16-byte slice
     float qv[CPL];
@@ -300,7 +302,7 @@ __global__ void __maxnreg__(224) fused_block_kernel(const FusedParams p) {
 #pragma unroll
     for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
     bool ok = true;
-    for (int i = 0; i < nch; ++i) {
+    for (int i = warp; i < nch; i += kConsumerWarps) {
       const int s = i % kStages;
       if (ok && !mbar_wait(smem_u32(&bars[s]), static_cast<uint32_t>((i / kStages) & 1), s_abort)) {
         ok = false;
@@ -315,7 +317,7 @@ __global__ void __maxnreg__(224) fused_block_kernel(const FusedParams p) {
       float sc[R_::kPasses];
 #pragma unroll
       for (int ps = 0; ps < R_::kPasses; ++ps) {
-        const int k = ps * R_::kGroups + warp * KPP + u;
+        const int k = ps * KPP + u;
         const bool valid = k < n && ok;
         float kv[CPL];
         load_slice<kBF16>(kt + (valid ? k : 0) * R_::kRowBytes + sl * 16, kv);
@@ -331,7 +333,7 @@ __global__ void __maxnreg__(224) fused_block_kernel(const FusedParams p) {
       float cm = -INFINITY;
 #pragma unroll
       for (int ps = 0; ps < R_::kPasses; ++ps) {
-        const int k = ps * R_::kGroups + warp * KPP + u;
+        const int k = ps * KPP + u;
         if (k >= n || !ok) sc[ps] = -INFINITY;
         cm = fmaxf(cm, sc[ps]);
       }
@@ -344,7 +346,7 @@ __global__ void __maxnreg__(224) fused_block_kernel(const FusedParams p) {
         m = mn;
 #pragma unroll
         for (int ps = 0; ps < R_::kPasses; ++ps) {
-          const int k = ps * R_::kGroups + warp * KPP + u;
+          const int k = ps * KPP + u;
           if (sc[ps] != -INFINITY) {
             float vv[CPL];
             load_slice<kBF16>(vt + k * R_::kRowBytes + sl * 16, vv);
@@ -355,16 +357,8 @@ __global__ void __maxnreg__(224) fused_block_kernel(const FusedParams p) {
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) {
-        // the eighth warp done with this stage refills it with chunk i + kStages
-        __threadfence_block();
-        if (atomicAdd(&s_done[s], 1u) == kConsumerWarps - 1) {
-          __threadfence_block();
-          s_done[s] = 0u;
-          if (i + kStages < nch && *s_abort == 0) issue(i + kStages);
-        }
-      }
+      __syncwarp();                                        // every lane is done with the stage
+      if (lane == 0 && i + kStages < nch && *s_abort == 0) issue(i + kStages);
     }
     // ---- merge the kGroups states: o = sum_g acc_g 2^(m_g - M) / sum_g l_g 2^(m_g - M)
     const int gidx = warp * KPP + u;
@@ -421,7 +415,7 @@ size_t fused_smem_bytes() {
   using R_ = FusedTraits<kBF16>;
   return 128 + static_cast<size_t>(kStages) * R_::kStageBytes +
          (2 * kMaxD + kRowGroups * kDh + 2 * kDh + R_::kGroups * (kDh + 2) + 32) * sizeof(float) +
-         kStages * (sizeof(uint64_t) + sizeof(unsigned int) + sizeof(int)) + 16;
+         kStages * (sizeof(uint64_t) + sizeof(int)) + 16;
 }
 
 template <bool kBF16, bool kGather>

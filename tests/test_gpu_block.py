@@ -157,8 +157,9 @@ def test_cross_block_clamps_key_lengths(cache_dtype):
 
 @pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
 def test_cross_block_key_lengths_around_chunks(cache_dtype):
-    """Rows ending just before, on and after the ring's chunk boundaries (96 fp32 /
-    192 bf16 keys per stage) and past the ring's depth."""
+    """Rows ending just before, on and after the ring's chunk boundaries (24 fp32 /
+    48 bf16 keys per stage; 96 and 192 are whole chunks of both) and around the ring's
+    depth (16 stages: 384 fp32 keys)."""
     kls = [1, 95, 96, 97, 191, 192, 193, 383, 384, 385, 700]
     w = W.custom("blockchunks", B=len(kls), T=700, d=256, L=2, H=4, ragged=False, index=967)
     d, h = inputs_on_device(w)
