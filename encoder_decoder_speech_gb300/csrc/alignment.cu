@@ -12,13 +12,13 @@
 // slot's valid range for EVERY selected head, so the head mean of a key needs
 // nothing from other CTAs. The only cross-CTA step is the softmax denominator:
 //  1. scores: each head's key range is one contiguous span of the cache; the CTA
-//     streams its spans in 4 KB bulk copies through a 16-stage shared-memory ring.
+//     streams its spans in 6 KB bulk copies through a 16-stage shared-memory ring.
 //     Chunk j belongs to warp j % 8 alone, which waits for it, takes the dot
 //     products of its rows (16 lanes per fp32 row / 8 per bf16 row, the 8 rows'
 //     reductions interleaved) and refills the stage with chunk j + 16; the first
 //     copies are issued before the grid dependency wait. The base-2 logits
 //     scale*log2(e)*q.K_t are staged in shared memory (or, when nsel times the
-//     CTA's keys exceeds 4096, in the weights rows);
+//     CTA's keys exceeds 2048, in the weights rows);
 //  2. per head, a group of lanes takes the max and the sum of 2^(logit - max)
 //     over the CTA's keys and stores the pair into every cluster CTA's shared
 //     memory (distributed shared memory);
@@ -50,13 +50,13 @@ struct RowGeom {
   static constexpr int kLanesPerRow = kRowBytes / 16;           // 16 / 8
   static constexpr int kEPL = 16 / kElem;                       // 4 / 8 channels per lane
   static constexpr int kRowsPerWarpPass = 32 / kLanesPerRow;    // 2 / 4
-  static constexpr int kChunkBytes = 4096;
-  static constexpr int kChunkKeys = kChunkBytes / kRowBytes;    // 16 / 32
-  static constexpr int kWarpPasses = kChunkKeys / kRowsPerWarpPass;   // 8: one interleaved reduction
+  static constexpr int kChunkBytes = 6144;
+  static constexpr int kChunkKeys = kChunkBytes / kRowBytes;    // 24 / 48
+  static constexpr int kWarpPasses = kChunkKeys / kRowsPerWarpPass;   // 12: one interleaved reduction
 };
 constexpr int kStages = 16;                                     // warp w owns stages w and w + 8
-constexpr size_t kRingBytes = static_cast<size_t>(kStages) * 4096;
-constexpr int kStageFloats = 4096;   // logits held in shared memory when nsel * keys per CTA fits
+constexpr size_t kRingBytes = static_cast<size_t>(kStages) * 6144;
+constexpr int kStageFloats = 2048;   // logits held in shared memory when nsel * keys per CTA fits
 constexpr int kMaxCluster = 16;
 
 // Dynamic shared memory: the ring, the logits, the scaled queries [nsel][64] and the
@@ -284,52 +284,57 @@ __global__ void __launch_bounds__(kThreads)
 
 // Largest cluster size C in {16, 8, 4, 2, 1} whose B clusters are all resident at
 // once (one wave; 16 needs the non-portable size), else 1. The resident-cluster
-// counts are queried once per device.
+// counts depend on the shared memory of the launch (nsel) and are queried once per
+// device and head count.
 template <bool kBF16>
-int cluster_size(int B, const DeviceInfo& dev) {
+int cluster_size(int B, int nsel, const DeviceInfo& dev) {
   static std::mutex mu;
-  static int fit[128][5] = {};                 // resident clusters of size 16, 8, 4, 2, 1; -1 = query failed
-  static bool queried[128] = {};
+  static int fit[128][kMaxAlignHeads + 1][5] = {};  // resident clusters of size 16, 8, 4, 2, 1
+  static bool attr[128] = {}, big[128] = {}, queried[128][kMaxAlignHeads + 1] = {};
   const int dv = dev.device >= 0 && dev.device < 128 ? dev.device : 0;
   std::lock_guard<std::mutex> lock(mu);
-  if (!queried[dv]) {
+  if (!attr[dv]) {
     if (cudaFuncSetAttribute(alignment_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(dyn_smem_bytes(kMaxAlignHeads, kMaxCluster))) != cudaSuccess) {
       cudaGetLastError();
       return -1;
     }
-    const bool big = cudaFuncSetAttribute(alignment_kernel<kBF16>, cudaFuncAttributeNonPortableClusterSizeAllowed,
-                                          1) == cudaSuccess;
+    big[dv] = cudaFuncSetAttribute(alignment_kernel<kBF16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+              cudaSuccess;
+    cudaGetLastError();
+    attr[dv] = true;
+  }
+  if (!queried[dv][nsel]) {
     for (int i = 0; i < 5; ++i) {
       const int c = 16 >> i;
       int n = 0;
-      if (c <= 8 || big) {
+      if (c <= 8 || big[dv]) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(c, 1, 1);
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = dyn_smem_bytes(kMaxAlignHeads, kMaxCluster);   // the largest launch
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = c;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
+        cfg.dynamicSmemBytes = dyn_smem_bytes(nsel, c);
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = c;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
         cfg.numAttrs = 1;
         if (cudaOccupancyMaxActiveClusters(&n, alignment_kernel<kBF16>, &cfg) != cudaSuccess) n = 0;
       }
-      fit[dv][i] = n;
+      fit[dv][nsel][i] = n;
     }
     cudaGetLastError();
-    queried[dv] = true;
+    queried[dv][nsel] = true;
   }
   for (int i = 0; i < 5; ++i)
-    if (fit[dv][i] >= B) return 16 >> i;
+    if (fit[dv][nsel][i] >= B) return 16 >> i;
   return 1;
 }
 
 template <bool kBF16>
 cudaError_t launch(const AlignLaunch& a, const DeviceInfo& dev, cudaStream_t stream) {
-  const int C = cluster_size<kBF16>(a.B, dev);
+  const int C = cluster_size<kBF16>(a.B, a.heads.n, dev);
   if (C < 0) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, a.B, 1);
