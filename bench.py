@@ -46,7 +46,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["cxa", "reference"], default="cxa")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     p.add_argument("--no-variants", action="store_true", help="skip the bf16-cache variant")
-    p.add_argument("--profile", choices=["decode", "decode_bf16", "populate", "shared_bf16", "align"], default=None,
+    p.add_argument("--profile", choices=["decode", "decode_bf16", "populate", "shared_bf16", "align", "block", "selfattn"],
+                   default=None,
                    help="run a few launches of one kernel on the workload's inputs (for ncu), print nothing else")
     p.add_argument("--sweep", action="store_true",
                    help="time decode and populate at every point of the decode bandwidth sweep "
@@ -937,7 +938,8 @@ def run_align(args):
 def run_profile(args):
     """A handful of launches of one kernel on the bench workload's inputs, for
     Nsight Compute: one populate (weight repack + GEMM), then two more populate
-    calls, three decode steps or three alignment-weight calls."""
+    calls, three decode steps, three alignment-weight calls, two six-layer steps of
+    the cross-attention block, or a 226-step self-attention sequence (fp32)."""
     import torch
     from encoder_decoder_speech_gb300 import _build, cxa
     from encoder_decoder_speech_gb300 import workloads as W
@@ -962,6 +964,30 @@ def run_profile(args):
         heads = [(3, 1), (4, 2), (4, 6), (5, 0), (5, 3), (5, 7)]
         for s in range(3):
             cache.alignment_weights(Q[s], kl, heads)
+    elif args.profile == "block":         # two six-layer steps of the cross-attention block
+        g = torch.Generator(device="cuda").manual_seed(0)
+
+        def t(shape, std):
+            return torch.randn(*shape, device="cuda", generator=g) * std
+
+        x = t((w.B, w.d), 1.0)
+        prm = [dict(WQ=t((w.d, w.d), w.d ** -0.5), WO=t((w.d, w.d), w.d ** -0.5), g=1 + t((w.d,), 0.1),
+                    b=t((w.d,), 0.1), bQ=t((w.d,), 0.02), bO=t((w.d,), 0.02)) for _ in range(w.L)]
+        for _ in range(2):
+            for l in range(w.L):
+                q = prm[l]
+                cache.cross_block(l, x, q["WQ"], q["WO"], kl, ln_gamma=q["g"], ln_beta=q["b"], bQ=q["bQ"], bO=q["bO"])
+    elif args.profile == "selfattn":      # the self-attention step at positions 222..225 of 448
+        import numpy as np
+        sa = cxa.CrossAttentionCache(w.B, 448, w.L, w.H, w.dh, "f32")
+        rng = np.random.default_rng(11)
+        Qs = torch.from_numpy(rng.standard_normal((4, w.B, w.L, w.H, w.dh)).astype(np.float32)).to("cuda")
+        Ks = torch.from_numpy(rng.standard_normal((4, w.B, w.L, w.H, w.dh)).astype(np.float32)).to("cuda")
+        out = torch.empty_like(Qs[0])
+        for s in range(226):
+            pos = torch.full((w.B,), s, dtype=torch.int32, device="cuda")
+            sa.self_attention_step(pos, Qs[s % 4], Ks[s % 4], Ks[(s + 1) % 4], out=out)
+        sa.close()
     else:
         for s in range(3):
             cache.decode(Q[s], kl)
