@@ -75,10 +75,12 @@ constexpr int kPartChunk = 64;         // partial-slot granularity of the worksp
 #define CXA_DECODE_PDL 1
 #endif
 constexpr int kConsumerWarps = CXA_DECODE_CONSUMER_WARPS;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kProducerWarp = kConsumerWarps;       // streams K/V (and Q) into the ring
+constexpr int kMergeWarp = kConsumerWarps + 1;      // finishes the rows (output or split-row merge)
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
 constexpr int kStages = CXA_DECODE_STAGES;
 constexpr int kQRowBytes = kDh * 4;
-static_assert(kConsumerWarps >= 2, "the row merge uses the first 64 consumer threads");
+static_assert(kConsumerWarps >= 1, "at least one consumer warp");
 
 template <bool kBF16, int kNQ>
 struct Traits {
@@ -194,13 +196,17 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
 
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * R::kStageBytes);   // full[S], empty[S]
-  long long* s_first = reinterpret_cast<long long*>(bars + 2 * kStages);
+  // full[S], empty[S], then the two row-end slots' rfull[2] (consumers -> merge warp)
+  // and rfree[2] (merge warp -> consumers)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * R::kStageBytes);
+  uint64_t* rbars = bars + 2 * kStages;
+  long long* s_first = reinterpret_cast<long long*>(rbars + 4);
   int* s_nch = reinterpret_cast<int*>(s_first + p.B + 1);
-  float* s_red = reinterpret_cast<float*>(s_nch + p.B + (p.B & 1));   // [kNQ][warps][64] acc
-  float* s_redm = s_red + kNQ * kConsumerWarps * kDh;                // [kNQ][warps] m
-  float* s_reds = s_redm + kNQ * kConsumerWarps;                     // [kNQ][warps] s
-  volatile int* s_flags = reinterpret_cast<volatile int*>(s_reds + kNQ * kConsumerWarps);   // [0] abort, [1] last
+  // a row end's per-warp states, double-buffered: slot k holds [kNQ][warps][64] acc,
+  // [kNQ][warps] m, [kNQ][warps] s and [warps] ok
+  constexpr int kSlotFloats = kNQ * kConsumerWarps * (kDh + 2) + kConsumerWarps;
+  float* s_slots = reinterpret_cast<float*>(s_nch + p.B + (p.B & 1));
+  volatile int* s_flags = reinterpret_cast<volatile int*>(s_slots + 2 * kSlotFloats);   // [0] abort
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -231,13 +237,16 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
     if (lane == 0) {
       s_first[p.B] = run;
       s_flags[0] = 0;
-      s_flags[1] = 0;
     }
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bars[s]), 1);
       mbar_init(smem_u32(&bars[kStages + s]), kConsumerWarps);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(smem_u32(&rbars[k]), kConsumerWarps);   // rfull[k]
+      mbar_init(smem_u32(&rbars[2 + k]), 1);            // rfree[k]
     }
     fence_mbar_init();
   }
@@ -248,7 +257,28 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
   const bool active = total > 0 && blockIdx.x < ranges;
   const long long g0 = active ? blockIdx.x * total / ranges : 0;
   const long long g1 = active ? (blockIdx.x + 1) * total / ranges : 0;
-  const bool producer = warp == kConsumerWarps && lane == 0;
+  const bool producer = warp == kProducerWarp && lane == 0;
+
+  // The order in which the CTA works through its range: when the range ends inside a
+  // row, that trailing segment [gA, g1) first, then [g0, gA). Both rows the CTA shares
+  // with its neighbours are then finished, and merged by their last arriver, early,
+  // behind the rest of the work, and the CTA ends on a whole row (a plain output
+  // write). Position i of the sequence is chunk seq_g(i); step() moves a cursor on.
+  long long gA = g1;
+  if (active && g1 - g0 > 1) {
+    const Cursor last = locate(g1 - 1, s_first, s_nch, p.B);
+    if (last.c != s_nch[last.b] - 1 && (g1 - 1) - last.c > g0) gA = (g1 - 1) - last.c;
+  }
+  const long long nA = g1 - gA, nAll = g1 - g0;
+  auto seq_g = [&](long long i) { return i < nA ? gA + i : g0 + (i - nA); };
+  auto step = [&](Cursor& c, long long i) {   // from position i to i + 1
+    if (i + 1 == nA) c = locate(g0, s_first, s_nch, p.B);
+    else advance(c, s_nch, p.B, LH);
+  };
+  // the segment at position i ends there: the row's last chunk, or the end of a part
+  auto seg_ends = [&](const Cursor& c, long long i) {
+    return c.c == s_nch[c.b] - 1 || i + 1 == nA || i + 1 == nAll;
+  };
 
   // The cache and key_len are inputs no decode writes: the producer starts
   // streaming the first stages' K and V rows before the previous grid is done.
@@ -273,9 +303,9 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
     bulk_g2s_hint(dst + R::kKVBytes, p.Vc + off, kv_bytes, full, pol);
   };
   if (active && producer) {
-    pcur = locate(g0, s_first, s_nch, p.B);
+    pcur = locate(seq_g(0), s_first, s_nch, p.B);
     pc = pcur;
-    npre = (g1 - g0) < kStages ? (g1 - g0) : kStages;
+    npre = nAll < kStages ? nAll : kStages;
     for (; nissued < npre; ++nissued) {
       if constexpr (kAppend) {
         const int kl = min(max(__ldg(p.key_len + pc.b) + p.key_len_add, 0), p.T);
@@ -283,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
         if (end > min(__ldg(p.key_len + pc.b), p.T) - 1) break;   // may hold the previous step's row
       }
       issue_stage(nissued, pc);
-      advance(pc, s_nch, p.B, LH);
+      step(pc, nissued);
     }
   }
   if constexpr (kAppend) {
@@ -292,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
     if (active && producer)
       for (; nissued < npre; ++nissued) {
         issue_stage(nissued, pc);
-        advance(pc, s_nch, p.B, LH);
+        step(pc, nissued);
       }
   }
   // Q, out and the workspace may belong to the previous grid: wait for it.
@@ -338,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
   // query row n of cache row (b, lh): Q[b][n][lh][:]
   auto qrow = [&](int b, int lh, int n) { return (static_cast<long long>(b) * nq + n) * LH + lh; };
 
-  if (warp == kConsumerWarps) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       Cursor cur = pcur;
@@ -346,11 +376,11 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
         const uint32_t qdst = smem_u32(stages + i * R::kStageBytes) + 2 * R::kKVBytes;
         for (int n = 0; n < nq; ++n)
           bulk_g2s(qdst + n * kQRowBytes, p.Q + qrow(cur.b, cur.lh, n) * kDh, kQRowBytes, smem_u32(&bars[i]));
-        advance(cur, s_nch, p.B, LH);
+        step(cur, i);
       }
       uint32_t armed = static_cast<uint32_t>((1u << npre) - 1u), armed_parity = 0;
       bool ok = true;
-      for (long long g = g0 + npre, i = npre; g < g1; ++g, ++i) {
+      for (long long i = npre; i < nAll; ++i) {
         const int s = static_cast<int>(i % kStages);
         const uint32_t parity = static_cast<uint32_t>((i / kStages) & 1);
         if (!mbar_wait(smem_u32(&bars[kStages + s]), parity ^ 1u, s_flags)) {
@@ -372,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
           bulk_g2s(dst + 2 * R::kKVBytes + qn * kQRowBytes, p.Q + qrow(cur.b, cur.lh, qn) * kDh, kQRowBytes, full);
         armed |= 1u << s;
         armed_parity = (armed_parity & ~(1u << s)) | (parity << s);
-        advance(cur, s_nch, p.B, LH);
+        step(cur, i);
       }
       if (!ok) {
         s_flags[0] = 1;
@@ -382,13 +412,120 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
       }
     }
     __syncwarp();
+  } else if (warp == kMergeWarp) {
+    // ------------------------------------------------------------ merge warp
+    // Walks the same chunk sequence as the consumers; at each row end it takes the
+    // consumers' states from slot re & 1, frees the slot, and writes the row (whole
+    // rows) or its partial, the last arriver of a split row merging all partials.
+    // Lane l owns channels l and l + 32.
+    Cursor cur = locate(seq_g(0), s_first, s_nch, p.B);
+    int seg_c0 = cur.c;
+    int re = 0;
+    for (long long i = 0; i < nAll; ++i) {
+      const int nch = s_nch[cur.b];
+      if (seg_ends(cur, i)) {
+        const int slot = re & 1;
+        bool okr = mbar_wait(smem_u32(&rbars[slot]), static_cast<uint32_t>((re >> 1) & 1), s_flags);
+        if (!okr) {
+          s_flags[0] = 1;
+          if (lane == 0) atomicOr(p.status, 1u);
+        }
+        const float* sl_red = s_slots + slot * kSlotFloats;
+        const float* sl_m = sl_red + kNQ * kConsumerWarps * kDh;
+        const float* sl_s = sl_m + kNQ * kConsumerWarps;
+        const float* sl_ok = sl_s + kNQ * kConsumerWarps;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) okr = okr && sl_ok[w] != 0.f;
+        float Mq[kNQ], Sq[kNQ], Aq[kNQ][2];
+#pragma unroll
+        for (int q = 0; q < kNQ; ++q) {
+          float M = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sl_m[q * kConsumerWarps + w]);
+          float S = 0.f, A0 = 0.f, A1 = 0.f;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float f = rescale(sl_m[q * kConsumerWarps + w], M);
+            S = fmaf(sl_s[q * kConsumerWarps + w], f, S);
+            A0 = fmaf(sl_red[(q * kConsumerWarps + w) * kDh + lane], f, A0);
+            A1 = fmaf(sl_red[(q * kConsumerWarps + w) * kDh + lane + 32], f, A1);
+          }
+          Mq[q] = M;
+          Sq[q] = S;
+          Aq[q][0] = A0;
+          Aq[q][1] = A1;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&rbars[2 + slot]));   // the slot may be rewritten
+        ++re;
+        const long long row = static_cast<long long>(cur.b) * LH + cur.lh;
+        const bool whole_row = seg_c0 == 0 && cur.c == nch - 1;
+        if (whole_row) {
+#pragma unroll
+          for (int q = 0; q < kNQ; ++q)
+            if (q < nq && okr) {
+              float* o = p.out + qrow(cur.b, cur.lh, q) * kDh;
+              o[lane] = Sq[q] > 0.f ? Aq[q][0] / Sq[q] : 0.f;
+              o[lane + 32] = Sq[q] > 0.f ? Aq[q][1] / Sq[q] : 0.f;
+            }
+        } else {
+          const long long grow = s_first[cur.b] + static_cast<long long>(cur.lh) * nch;   // chunk 0 of row
+          const long long first_owner = owner_of(grow, total, ranges);
+          const int nseg = static_cast<int>(owner_of(grow + nch - 1, total, ranges) - first_owner + 1);
+          const int seg = static_cast<int>(blockIdx.x - first_owner);
+#pragma unroll
+          for (int q = 0; q < kNQ; ++q) {
+            if (q >= nq) continue;
+            float* P = p.part + ((row * nq + q) * p.part_stride + seg) * kPartFloats;
+            P[4 + lane] = okr ? Aq[q][0] : 0.f;
+            P[4 + lane + 32] = okr ? Aq[q][1] : 0.f;
+            if (lane == 0) {
+              P[0] = okr ? Mq[q] : -INFINITY;
+              P[1] = okr ? Sq[q] : 0.f;
+            }
+          }
+          __syncwarp();
+          unsigned int last = 0u;
+          if (lane == 0) {
+            __threadfence();
+            const unsigned int prev = atomicAdd(p.counters + row, 1u);
+            last = prev == static_cast<unsigned int>(nseg - 1) ? 1u : 0u;
+          }
+          if (__shfl_sync(0xffffffffu, last, 0)) {
+            __threadfence();
+            for (int q = 0; q < nq; ++q) {
+              const float* P0 = p.part + (row * nq + q) * p.part_stride * kPartFloats;
+              float MM = -INFINITY, SS = 0.f, A0 = 0.f, A1 = 0.f;   // one pass, rescaling as the max grows
+              for (int k = 0; k < nseg; ++k) {
+                const float mk = __ldcg(P0 + k * kPartFloats);
+                const float sk = __ldcg(P0 + k * kPartFloats + 1);
+                const float a0 = __ldcg(P0 + k * kPartFloats + 4 + lane);
+                const float a1 = __ldcg(P0 + k * kPartFloats + 4 + lane + 32);
+                const float M2 = fmaxf(MM, mk);
+                const float f0 = rescale(MM, M2), f1 = rescale(mk, M2);
+                SS = SS * f0 + sk * f1;
+                A0 = A0 * f0 + a0 * f1;
+                A1 = A1 * f0 + a1 * f1;
+                MM = M2;
+              }
+              float* o = p.out + qrow(cur.b, cur.lh, q) * kDh;
+              o[lane] = SS > 0.f ? A0 / SS : 0.f;
+              o[lane + 32] = SS > 0.f ? A1 / SS : 0.f;
+            }
+            if (lane == 0) p.counters[row] = 0u;
+          }
+        }
+      }
+      const int prev_b = cur.b, prev_lh = cur.lh;
+      step(cur, i);
+      if (cur.b != prev_b || cur.lh != prev_lh) seg_c0 = cur.c;
+    }
   } else {
     // ------------------------------------------------------------ consumers
     const int sub = lane % LPR;          // slice of a key row this lane reads
     const int grp = lane / LPR;          // lane group = independent softmax stream
-    const int tid = threadIdx.x;         // 0..127
-    Cursor cur = locate(g0, s_first, s_nch, p.B);
-    int seg_c0 = cur.c;                  // first chunk of the current row in this CTA
+    Cursor cur = locate(seq_g(0), s_first, s_nch, p.B);
+    int seg_c0 = cur.c;                  // first chunk of the current row segment
     float m[kNQ], ssum[kNQ], acc[kNQ][EPL];
 #pragma unroll
     for (int q = 0; q < kNQ; ++q) {
@@ -398,8 +535,9 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
       for (int e = 0; e < EPL; ++e) acc[q][e] = 0.f;
     }
     bool ok = true;
+    int re = 0;                          // row ends handed to the merge warp so far
 
-    for (long long g = g0, i = 0; g < g1; ++g, ++i) {
+    for (long long i = 0; i < nAll; ++i) {
       const int s = static_cast<int>(i % kStages);
       const uint32_t parity = static_cast<uint32_t>((i / kStages) & 1);
       if (ok && !mbar_wait(smem_u32(&bars[s]), parity, s_flags)) {
@@ -408,7 +546,6 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
         atomicOr(p.status, 1u);
       }
       const int kl = min(max(__ldg(p.key_len + cur.b) + p.key_len_add, 0), p.T);
-      const int nch = s_nch[cur.b];
       const int n = min(R::kChunkKeys, kl - cur.c * R::kChunkKeys);
       int subst = -1;   // kAppend: the chunk row that is the new key
       const float* knew_row = nullptr;
@@ -503,9 +640,20 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
 
-      const bool row_ends = (cur.c == nch - 1) || (g + 1 == g1);
+      const bool row_ends = seg_ends(cur, i);
       if (row_ends) {
-        // ---- merge the lane groups of this warp, then the warps, per query
+        // ---- hand the row's state to the merge warp: merge this warp's lane groups,
+        //      leave the warp's state in slot re & 1 and go on with the next chunk
+        const int slot = re & 1;
+        if (re >= 2 && !mbar_wait(smem_u32(&rbars[2 + slot]), static_cast<uint32_t>(((re >> 1) - 1) & 1), s_flags)) {
+          ok = false;                                      // the merge warp has not read this slot
+          s_flags[0] = 1;
+          atomicOr(p.status, 1u);
+        }
+        float* sl_red = s_slots + slot * kSlotFloats;
+        float* sl_m = sl_red + kNQ * kConsumerWarps * kDh;
+        float* sl_s = sl_m + kNQ * kConsumerWarps;
+        float* sl_ok = sl_s + kNQ * kConsumerWarps;
 #pragma unroll
         for (int q = 0; q < kNQ; ++q) {
 #pragma unroll
@@ -524,77 +672,17 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
           }
           if (lane < LPR) {
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) s_red[(q * kConsumerWarps + warp) * kDh + sub * EPL + e] = acc[q][e];
+            for (int e = 0; e < EPL; ++e) sl_red[(q * kConsumerWarps + warp) * kDh + sub * EPL + e] = acc[q][e];
           }
           if (lane == 0) {
-            s_redm[q * kConsumerWarps + warp] = m[q];
-            s_reds[q * kConsumerWarps + warp] = ssum[q];
+            sl_m[q * kConsumerWarps + warp] = m[q];
+            sl_s[q * kConsumerWarps + warp] = ssum[q];
           }
         }
-        named_barrier(1, kConsumerWarps * 32);
-        const long long row = static_cast<long long>(cur.b) * LH + cur.lh;
-        const bool whole_row = seg_c0 == 0 && cur.c == nch - 1;
-        if (tid < kDh) {
-          long long first_owner = 0;
-          int nseg = 1, seg = 0;
-          if (!whole_row) {
-            const long long grow = s_first[cur.b] + static_cast<long long>(cur.lh) * nch;   // chunk 0 of row
-            first_owner = owner_of(grow, total, ranges);
-            nseg = static_cast<int>(owner_of(grow + nch - 1, total, ranges) - first_owner + 1);
-            seg = static_cast<int>(blockIdx.x - first_owner);
-          }
-          for (int q = 0; q < nq; ++q) {
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s_redm[q * kConsumerWarps + w]);
-            float S = 0.f, A = 0.f;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-              const float f = rescale(s_redm[q * kConsumerWarps + w], M);
-              S = fmaf(s_reds[q * kConsumerWarps + w], f, S);
-              A = fmaf(s_red[(q * kConsumerWarps + w) * kDh + tid], f, A);
-            }
-            if (whole_row) {
-              if (ok) p.out[qrow(cur.b, cur.lh, q) * kDh + tid] = S > 0.f ? A / S : 0.f;
-            } else {
-              float* P = p.part + ((row * nq + q) * p.part_stride + seg) * kPartFloats;
-              P[4 + tid] = ok ? A : 0.f;
-              if (tid == 0) {
-                P[0] = ok ? M : -INFINITY;
-                P[1] = ok ? S : 0.f;
-              }
-            }
-          }
-          if (!whole_row) {
-            named_barrier(2, kDh);
-            if (tid == 0) {
-              __threadfence();
-              const unsigned int prev = atomicAdd(p.counters + row, 1u);
-              s_flags[1] = (prev == static_cast<unsigned int>(nseg - 1)) ? 1 : 0;
-            }
-            named_barrier(2, kDh);
-            if (s_flags[1]) {
-              __threadfence();
-              for (int q = 0; q < nq; ++q) {
-                const float* P0 = p.part + (row * nq + q) * p.part_stride * kPartFloats;
-                float MM = -INFINITY, SS = 0.f, AA = 0.f;   // one pass, rescaling as the max grows
-                for (int k = 0; k < nseg; ++k) {
-                  const float mk = __ldcg(P0 + k * kPartFloats);
-                  const float sk = __ldcg(P0 + k * kPartFloats + 1);
-                  const float ak = __ldcg(P0 + k * kPartFloats + 4 + tid);
-                  const float M2 = fmaxf(MM, mk);
-                  const float f0 = rescale(MM, M2), f1 = rescale(mk, M2);
-                  SS = SS * f0 + sk * f1;
-                  AA = AA * f0 + ak * f1;
-                  MM = M2;
-                }
-                p.out[qrow(cur.b, cur.lh, q) * kDh + tid] = SS > 0.f ? AA / SS : 0.f;
-              }
-              if (tid == 0) p.counters[row] = 0u;
-            }
-          }
-        }
-        named_barrier(1, kConsumerWarps * 32);
+        if (lane == 0) sl_ok[warp] = ok ? 1.f : 0.f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&rbars[slot]));   // release: the slot's writes come first
+        ++re;
 #pragma unroll
         for (int q = 0; q < kNQ; ++q) {
           m[q] = -INFINITY;
@@ -604,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
         }
       }
       const int prev_b = cur.b, prev_lh = cur.lh;
-      advance(cur, s_nch, p.B, LH);
+      step(cur, i);
       if (cur.b != prev_b || cur.lh != prev_lh) seg_c0 = cur.c;
     }
   }
@@ -620,10 +708,10 @@ template <bool kBF16, int kNQ>
 size_t dynamic_smem_bytes(int B) {
   using R = Traits<kBF16, kNQ>;
   size_t n = static_cast<size_t>(kStages) * R::kStageBytes;
-  n += 2 * kStages * sizeof(uint64_t);
+  n += (2 * kStages + 4) * sizeof(uint64_t);
   n += static_cast<size_t>(B + 1) * sizeof(long long);
   n += static_cast<size_t>(B + (B & 1)) * sizeof(int);
-  n += static_cast<size_t>(kNQ) * kConsumerWarps * (kDh + 2) * sizeof(float) + 4 * sizeof(int);
+  n += 2 * (static_cast<size_t>(kNQ) * kConsumerWarps * (kDh + 2) + kConsumerWarps) * sizeof(float) + 4 * sizeof(int);
   return n;
 }
 
@@ -682,7 +770,7 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStre
                           std::string* msg) {
   // three or more queries per row of a bf16 cache: scores on the tensor cores
   // (bf16 x bf16 products are exact; an fp32 cache keeps fp32 scores here)
-  if (a.nq >= 3 && a.cache_bf16) return launch_decode_shared_tc(a, dev, stream, msg);
+  if (a.nq >= 2 && a.cache_bf16) return launch_decode_shared_tc(a, dev, stream, msg);
   DecodeParams prm;
   prm.Q = a.Q;
   prm.Kc = static_cast<const uint8_t*>(a.Kc);

@@ -166,7 +166,7 @@ CXA_API int cxa_decode(const cxa_cache* c, const float* Q, const int* key_len, f
  *
  *   nq       query rows per cache row, 1 .. CXA_MAX_SHARED_QUERIES (16) for a
  *            bf16 cache, 1 .. CXA_MAX_SHARED_QUERIES_F32 (8) for an fp32 cache.
- *            With a bf16 cache and nq >= 3 the scores run on the tensor cores
+ *            With a bf16 cache and nq >= 2 the scores run on the tensor cores
  *            (queries as bf16 hi + lo parts); otherwise in fp32 on the CUDA cores.
  *   Q, out   device fp32 [B][nq][L][H][dh]: row (b, n, l, h) is hypothesis n of
  *            slot b; out row (b, n, l, h) = softmax(scale * q.K[b,l,h]^T) V[b,l,h].
