@@ -93,6 +93,12 @@ struct Traits {
   static constexpr int kRowsPerPass = 32 / kLanesPerRow;             // keys per warp pass
   static constexpr int kElemsPerLane = kSliceBytes / kElemBytes;     // channels per lane
   static constexpr int kChunkKeys = kBF16 ? CXA_DECODE_CHUNK_BF16 : CXA_DECODE_CHUNK_F32;   // 16 KB of K
+  // fp32 cache with four or more queries: scores with one key per lane (no shuffles)
+  static constexpr bool kKeyLanes = !kBF16 && kNQ >= 4;
+  static constexpr int kPFloats = kKeyLanes ? kConsumerWarps * 32 * (kNQ / 2) : 0;   // probabilities
+  // per query, the states a row end leaves for the merge warp: one per consumer warp,
+  // or one per key half when the warps split the queries
+  static constexpr int kSlotWarps = kKeyLanes ? 2 : kConsumerWarps;
   static constexpr int kKVBytes = kChunkKeys * kRowBytes;
   static constexpr int kStageBytes = 2 * kKVBytes + kNQ * kQRowBytes;
   static constexpr int kKeysPerWarp = kChunkKeys / kConsumerWarps;
@@ -169,6 +175,13 @@ __device__ __forceinline__ void load_slice(const uint8_t* p, float* f) {
   }
 }
 
+// Maximum over the warp's 32 lanes.
+__device__ __forceinline__ float warp_max_f32(float v) {
+  float r;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
 // Programmatic dependent launch: let the next grid on the stream be scheduled
 // as this grid's CTAs retire, and wait for the previous grid to complete (and
 // its memory to be visible) before touching anything it may have written.
@@ -177,6 +190,7 @@ __device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol
 
 template <bool kBF16, int kNQ>
 constexpr int min_ctas_per_sm() {
+  if (!kBF16 && kNQ == 4) return 3;   // key-lane consumers: registers and shared memory fit three
   return kNQ >= 4 ? 2 : CXA_DECODE_CTAS_PER_SM;
 }
 
@@ -204,9 +218,12 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
   int* s_nch = reinterpret_cast<int*>(s_first + p.B + 1);
   // a row end's per-warp states, double-buffered: slot k holds [kNQ][warps][64] acc,
   // [kNQ][warps] m, [kNQ][warps] s and [warps] ok
-  constexpr int kSlotFloats = kNQ * kConsumerWarps * (kDh + 2) + kConsumerWarps;
+  constexpr int kSlotWarps = R::kSlotWarps;
+  constexpr int kSlotFloats = kNQ * kSlotWarps * (kDh + 2) + kConsumerWarps;
   float* s_slots = reinterpret_cast<float*>(s_nch + p.B + (p.B & 1));
   volatile int* s_flags = reinterpret_cast<volatile int*>(s_slots + 2 * kSlotFloats);   // [0] abort
+  // key-lane consumers: each warp's probabilities [32 keys][kNQ / 2]
+  float* s_p = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(s_flags + 4) + 15) & ~static_cast<uintptr_t>(15));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -431,9 +448,9 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
           if (lane == 0) atomicOr(p.status, 1u);
         }
         const float* sl_red = s_slots + slot * kSlotFloats;
-        const float* sl_m = sl_red + kNQ * kConsumerWarps * kDh;
-        const float* sl_s = sl_m + kNQ * kConsumerWarps;
-        const float* sl_ok = sl_s + kNQ * kConsumerWarps;
+        const float* sl_m = sl_red + kNQ * kSlotWarps * kDh;
+        const float* sl_s = sl_m + kNQ * kSlotWarps;
+        const float* sl_ok = sl_s + kNQ * kSlotWarps;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) okr = okr && sl_ok[w] != 0.f;
         float Mq[kNQ], Sq[kNQ], Aq[kNQ][2];
@@ -441,14 +458,14 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
         for (int q = 0; q < kNQ; ++q) {
           float M = -INFINITY;
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sl_m[q * kConsumerWarps + w]);
+          for (int w = 0; w < kSlotWarps; ++w) M = fmaxf(M, sl_m[q * kSlotWarps + w]);
           float S = 0.f, A0 = 0.f, A1 = 0.f;
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            const float f = rescale(sl_m[q * kConsumerWarps + w], M);
-            S = fmaf(sl_s[q * kConsumerWarps + w], f, S);
-            A0 = fmaf(sl_red[(q * kConsumerWarps + w) * kDh + lane], f, A0);
-            A1 = fmaf(sl_red[(q * kConsumerWarps + w) * kDh + lane + 32], f, A1);
+          for (int w = 0; w < kSlotWarps; ++w) {
+            const float f = rescale(sl_m[q * kSlotWarps + w], M);
+            S = fmaf(sl_s[q * kSlotWarps + w], f, S);
+            A0 = fmaf(sl_red[(q * kSlotWarps + w) * kDh + lane], f, A0);
+            A1 = fmaf(sl_red[(q * kSlotWarps + w) * kDh + lane + 32], f, A1);
           }
           Mq[q] = M;
           Sq[q] = S;
@@ -519,6 +536,148 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
       const int prev_b = cur.b, prev_lh = cur.lh;
       step(cur, i);
       if (cur.b != prev_b || cur.lh != prev_lh) seg_c0 = cur.c;
+    }
+  } else if constexpr (R::kKeyLanes) {
+    // ------------------------------------------------------------ consumers, several
+    // queries on an fp32 cache: warp w takes keys 32*(w & 1) .. +32 of each chunk and
+    // queries (w >> 1)*QPW .. +QPW. Scores: lane = key, a whole 64-channel dot
+    // product per query, the lane's 16-byte K slices read in an order rotated by
+    // lane & 7 (eight lanes of distinct rows then cover all banks) with each query
+    // slice read at the same rotation (eight distinct slices: one wavefront). The
+    // probabilities go to shared memory; P.V: lane = channels 2l, 2l + 1.
+    constexpr int QPW = kNQ / 2;
+    static_assert(kConsumerWarps == 4 && R::kChunkKeys == 64 && (QPW == 2 || QPW % 4 == 0),
+                  "two key halves x two query halves of a 64-key chunk");
+    const int kh = warp & 1, qh = warp >> 1;
+    float* s_pw = s_p + warp * 32 * QPW;   // this warp's probabilities, [32 keys][QPW]
+    Cursor cur = locate(seq_g(0), s_first, s_nch, p.B);
+    float m[QPW], lsum[QPW], acc[QPW][2];
+#pragma unroll
+    for (int qi = 0; qi < QPW; ++qi) {
+      m[qi] = -INFINITY;
+      lsum[qi] = 0.f;
+      acc[qi][0] = acc[qi][1] = 0.f;
+    }
+    bool ok = true;
+    int re = 0;                          // row ends handed to the merge warp so far
+    for (long long i = 0; i < nAll; ++i) {
+      const int s = static_cast<int>(i % kStages);
+      const uint32_t parity = static_cast<uint32_t>((i / kStages) & 1);
+      if (ok && !mbar_wait(smem_u32(&bars[s]), parity, s_flags)) {
+        ok = false;
+        s_flags[0] = 1;
+        atomicOr(p.status, 1u);
+      }
+      if (ok) {
+        const int kl = min(max(__ldg(p.key_len + cur.b) + p.key_len_add, 0), p.T);
+        const int n = min(R::kChunkKeys, kl - cur.c * R::kChunkKeys);
+        const uint8_t* sK = stages + s * R::kStageBytes;
+        const float* kp = reinterpret_cast<const float*>(sK + (kh * 32 + lane) * R::kRowBytes);
+        const float* qp = reinterpret_cast<const float*>(sK + 2 * R::kKVBytes) + qh * QPW * kDh;
+        float sc[QPW];
+#pragma unroll
+        for (int qi = 0; qi < QPW; ++qi) sc[qi] = 0.f;
+#pragma unroll
+        for (int j = 0; j < kDh / 4; ++j) {
+          const int c4 = ((j + (lane & 7)) & (kDh / 4 - 1)) * 4;
+          const float4 kv = *reinterpret_cast<const float4*>(kp + c4);
+#pragma unroll
+          for (int qi = 0; qi < QPW; ++qi) {
+            const float4 qv = *reinterpret_cast<const float4*>(qp + qi * kDh + c4);
+            sc[qi] = fmaf(qv.x, kv.x, sc[qi]);
+            sc[qi] = fmaf(qv.y, kv.y, sc[qi]);
+            sc[qi] = fmaf(qv.z, kv.z, sc[qi]);
+            sc[qi] = fmaf(qv.w, kv.w, sc[qi]);
+          }
+        }
+        const bool valid = kh * 32 + lane < n;
+        float pw[QPW];
+#pragma unroll
+        for (int qi = 0; qi < QPW; ++qi) {
+          const float sv = valid ? sc[qi] * p.qscale : -INFINITY;
+          const float mnew = fmaxf(m[qi], warp_max_f32(sv));
+          const float corr = rescale(m[qi], mnew);   // 0 while the state is empty
+          m[qi] = mnew;
+          pw[qi] = valid ? exp2f(sv - mnew) : 0.f;
+          lsum[qi] = fmaf(lsum[qi], corr, pw[qi]);
+          acc[qi][0] *= corr;
+          acc[qi][1] *= corr;
+        }
+        if constexpr (QPW % 4 == 0) {
+#pragma unroll
+          for (int q4 = 0; q4 < QPW / 4; ++q4)
+            *reinterpret_cast<float4*>(s_pw + lane * QPW + 4 * q4) =
+                make_float4(pw[4 * q4], pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]);
+        } else {
+          *reinterpret_cast<float2*>(s_pw + lane * QPW) = make_float2(pw[0], pw[1]);
+        }
+        __syncwarp();
+        const int nk = min(32, n - kh * 32);   // valid keys of this warp's half
+        const float* vp = reinterpret_cast<const float*>(sK + R::kKVBytes + kh * 32 * R::kRowBytes) + 2 * lane;
+#pragma unroll 4
+        for (int k = 0; k < nk; ++k) {
+          const float2 v2 = *reinterpret_cast<const float2*>(vp + k * kDh);
+          if constexpr (QPW == 2) {
+            const float2 pk = *reinterpret_cast<const float2*>(s_pw + k * QPW);
+            acc[0][0] = fmaf(pk.x, v2.x, acc[0][0]);
+            acc[0][1] = fmaf(pk.x, v2.y, acc[0][1]);
+            acc[1][0] = fmaf(pk.y, v2.x, acc[1][0]);
+            acc[1][1] = fmaf(pk.y, v2.y, acc[1][1]);
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < QPW / 4; ++q4) {
+            const float4 pk = *reinterpret_cast<const float4*>(s_pw + k * QPW + 4 * q4);
+            acc[4 * q4 + 0][0] = fmaf(pk.x, v2.x, acc[4 * q4 + 0][0]);
+            acc[4 * q4 + 0][1] = fmaf(pk.x, v2.y, acc[4 * q4 + 0][1]);
+            acc[4 * q4 + 1][0] = fmaf(pk.y, v2.x, acc[4 * q4 + 1][0]);
+            acc[4 * q4 + 1][1] = fmaf(pk.y, v2.y, acc[4 * q4 + 1][1]);
+            acc[4 * q4 + 2][0] = fmaf(pk.z, v2.x, acc[4 * q4 + 2][0]);
+            acc[4 * q4 + 2][1] = fmaf(pk.z, v2.y, acc[4 * q4 + 2][1]);
+            acc[4 * q4 + 3][0] = fmaf(pk.w, v2.x, acc[4 * q4 + 3][0]);
+            acc[4 * q4 + 3][1] = fmaf(pk.w, v2.y, acc[4 * q4 + 3][1]);
+          }
+        }
+      }
+      __syncwarp();                      // the probabilities are rewritten by the next chunk
+      if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
+
+      if (seg_ends(cur, i)) {
+        // ---- hand the row's state to the merge warp: this warp's queries, at its
+        //      key half's place in the slot
+        const int slot = re & 1;
+        if (re >= 2 && !mbar_wait(smem_u32(&rbars[2 + slot]), static_cast<uint32_t>(((re >> 1) - 1) & 1), s_flags)) {
+          ok = false;                                      // the merge warp has not read this slot
+          s_flags[0] = 1;
+          atomicOr(p.status, 1u);
+        }
+        float* sl_red = s_slots + slot * kSlotFloats;
+        float* sl_m = sl_red + kNQ * kSlotWarps * kDh;
+        float* sl_s = sl_m + kNQ * kSlotWarps;
+        float* sl_ok = sl_s + kNQ * kSlotWarps;
+#pragma unroll
+        for (int qi = 0; qi < QPW; ++qi) {
+          const int q = qh * QPW + qi;
+          float S = lsum[qi];
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
+          *reinterpret_cast<float2*>(sl_red + (q * kSlotWarps + kh) * kDh + 2 * lane) = make_float2(acc[qi][0], acc[qi][1]);
+          if (lane == 0) {
+            sl_m[q * kSlotWarps + kh] = m[qi];
+            sl_s[q * kSlotWarps + kh] = S;
+          }
+        }
+        if (lane == 0) sl_ok[warp] = ok ? 1.f : 0.f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&rbars[slot]));   // release: the slot's writes come first
+        ++re;
+#pragma unroll
+        for (int qi = 0; qi < QPW; ++qi) {
+          m[qi] = -INFINITY;
+          lsum[qi] = 0.f;
+          acc[qi][0] = acc[qi][1] = 0.f;
+        }
+      }
+      step(cur, i);
     }
   } else {
     // ------------------------------------------------------------ consumers
@@ -651,9 +810,9 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
           atomicOr(p.status, 1u);
         }
         float* sl_red = s_slots + slot * kSlotFloats;
-        float* sl_m = sl_red + kNQ * kConsumerWarps * kDh;
-        float* sl_s = sl_m + kNQ * kConsumerWarps;
-        float* sl_ok = sl_s + kNQ * kConsumerWarps;
+        float* sl_m = sl_red + kNQ * kSlotWarps * kDh;
+        float* sl_s = sl_m + kNQ * kSlotWarps;
+        float* sl_ok = sl_s + kNQ * kSlotWarps;
 #pragma unroll
         for (int q = 0; q < kNQ; ++q) {
 #pragma unroll
@@ -672,11 +831,11 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
           }
           if (lane < LPR) {
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) sl_red[(q * kConsumerWarps + warp) * kDh + sub * EPL + e] = acc[q][e];
+            for (int e = 0; e < EPL; ++e) sl_red[(q * kSlotWarps + warp) * kDh + sub * EPL + e] = acc[q][e];
           }
           if (lane == 0) {
-            sl_m[q * kConsumerWarps + warp] = m[q];
-            sl_s[q * kConsumerWarps + warp] = ssum[q];
+            sl_m[q * kSlotWarps + warp] = m[q];
+            sl_s[q * kSlotWarps + warp] = ssum[q];
           }
         }
         if (lane == 0) sl_ok[warp] = ok ? 1.f : 0.f;
@@ -711,7 +870,8 @@ size_t dynamic_smem_bytes(int B) {
   n += (2 * kStages + 4) * sizeof(uint64_t);
   n += static_cast<size_t>(B + 1) * sizeof(long long);
   n += static_cast<size_t>(B + (B & 1)) * sizeof(int);
-  n += 2 * (static_cast<size_t>(kNQ) * kConsumerWarps * (kDh + 2) + kConsumerWarps) * sizeof(float) + 4 * sizeof(int);
+  n += 2 * (static_cast<size_t>(kNQ) * R::kSlotWarps * (kDh + 2) + kConsumerWarps) * sizeof(float) + 4 * sizeof(int);
+  if (R::kKeyLanes) n += 16 + static_cast<size_t>(R::kPFloats) * sizeof(float);
   return n;
 }
 

@@ -136,6 +136,22 @@ def test_shared_decode_tensor_core_key_length_edges(nq):
     assert np.abs(out - ref).max() <= DECODE_BF16_MAX_ABS
 
 
+@pytest.mark.parametrize("nq", [3, 4, 5, 8])
+def test_shared_decode_fp32_key_length_edges(nq):
+    """fp32 cache, several queries (one key per lane in each 32-key half of a 64-key
+    chunk): key lengths at and around the halves and chunks (1, 2, 31, 32, 33, 63,
+    64, 65, T). Keys past the length are stale rows that must not reach the output."""
+    w = W.custom("shared_edges32", B=9, T=333, d=256, L=2, H=4, ragged=False, index=946)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, "f32")
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    kl = np.array([1, 2, 31, 32, 33, 63, 64, 65, 333], dtype=np.int32)
+    Q = _queries(w, nq, 90 + nq)
+    out = host(c.decode_shared(dev(Q), dev(kl, torch.int32)))
+    ref = O.decode_shared(Q, host(c.Kc), host(c.Vc), kl)
+    assert np.abs(out - ref).max() <= DECODE_F32_MAX_ABS
+
+
 def test_shared_decode_clamps_key_lengths():
     """key_len outside [0, T] is clamped (negative -> no key -> zeros; > T -> T)."""
     w = W.custom("shared_clamp", B=4, T=200, d=256, L=2, H=4, ragged=False, index=945)
