@@ -46,7 +46,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["cxa", "reference"], default="cxa")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     p.add_argument("--no-variants", action="store_true", help="skip the bf16-cache variant")
-    p.add_argument("--profile", choices=["decode", "decode_bf16", "populate", "shared_bf16", "align", "block", "selfattn"],
+    p.add_argument("--profile", choices=["decode", "decode_bf16", "populate", "shared_bf16", "shared_f32", "align", "block",
+                                          "selfattn"],
                    default=None,
                    help="run a few launches of one kernel on the workload's inputs (for ncu), print nothing else")
     p.add_argument("--sweep", action="store_true",
@@ -954,7 +955,7 @@ def run_profile(args):
     if args.profile == "populate":
         for _ in range(2):
             cache.populate(E, WK, WV, bV)
-    elif args.profile == "shared_bf16":   # 8 hypotheses per slot on the tensor-core shared decode
+    elif args.profile in ("shared_bf16", "shared_f32"):   # 8 hypotheses per slot
         import numpy as np
         Qs = torch.from_numpy(np.random.default_rng(8).standard_normal(
             (w.B, 8, w.L, w.H, w.dh)).astype(np.float32)).to("cuda")
