@@ -89,8 +89,8 @@ template <bool kBF16, int kNQ>
 struct Traits {
   static constexpr int kElemBytes = kBF16 ? 2 : 4;
   static constexpr int kRowBytes = kDh * kElemBytes;                 // 256 / 128
-  // One query: 8 lanes per bf16 row (16-byte slices). Several queries: 16 lanes
-  // per row for both dtypes, halving the per-lane query and accumulator registers.
+  // One query: 8 lanes per bf16 row (16-byte slices). Several queries (fp32): 16
+  // lanes per row, halving the per-lane query and accumulator registers.
   static constexpr int kLanesPerRow = (kBF16 && kNQ == 1) ? 8 : 16;
   static constexpr int kSliceBytes = kRowBytes / kLanesPerRow;       // 16 or 8
   static constexpr int kRowsPerPass = 32 / kLanesPerRow;             // keys per warp pass
@@ -151,30 +151,23 @@ __device__ __forceinline__ void load_new_slice(const float* src, float* f) {
   }
 }
 
-// One lane's slice of a cache row -> fp32 values
+// One lane's 16-byte slice of a cache row -> fp32 values (8 bf16 or 4 fp32)
 template <bool kBF16, int kSlice>
 __device__ __forceinline__ void load_slice(const uint8_t* p, float* f) {
-  if constexpr (kSlice == 16) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
-    if constexpr (kBF16) {
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  static_assert(kSlice == 16, "16-byte slices");
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  if constexpr (kBF16) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-      }
-    } else {
-      f[0] = __uint_as_float(u.x);
-      f[1] = __uint_as_float(u.y);
-      f[2] = __uint_as_float(u.z);
-      f[3] = __uint_as_float(u.w);
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
-  } else {   // 8-byte bf16 slice
-    const uint2 u = *reinterpret_cast<const uint2*>(p);
-    f[0] = __uint_as_float(u.x << 16);
-    f[1] = __uint_as_float(u.x & 0xFFFF0000u);
-    f[2] = __uint_as_float(u.y << 16);
-    f[3] = __uint_as_float(u.y & 0xFFFF0000u);
+  } else {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
   }
 }
 
@@ -912,12 +905,13 @@ cudaError_t launch(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t 
   return cudaLaunchKernelEx(&cfg, decode_stream_kernel<kBF16, kNQ, kAppend>, prm);
 }
 
-template <bool kBF16>
-cudaError_t launch_nq(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t stream) {
-  if (prm.nq == 1) return launch<kBF16, 1>(prm, dev, stream);
-  if (prm.nq == 2) return launch<kBF16, 2>(prm, dev, stream);
-  if (prm.nq <= 4) return launch<kBF16, 4>(prm, dev, stream);
-  return launch<kBF16, 8>(prm, dev, stream);
+// fp32 cache: one instance per query-count bucket (a bf16 cache with several
+// queries goes to the tensor-core kernel)
+cudaError_t launch_f32_nq(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t stream) {
+  if (prm.nq == 1) return launch<false, 1>(prm, dev, stream);
+  if (prm.nq == 2) return launch<false, 2>(prm, dev, stream);
+  if (prm.nq <= 4) return launch<false, 4>(prm, dev, stream);
+  return launch<false, 8>(prm, dev, stream);
 }
 
 }  // namespace
@@ -958,7 +952,7 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStre
   if (a.K_new != nullptr)   // the self-attention step: append fused into a one-query decode
     e = a.cache_bf16 ? launch<true, 1, true>(prm, dev, stream) : launch<false, 1, true>(prm, dev, stream);
   else
-    e = a.cache_bf16 ? launch_nq<true>(prm, dev, stream) : launch_nq<false>(prm, dev, stream);
+    e = a.cache_bf16 ? launch<true, 1>(prm, dev, stream) : launch_f32_nq(prm, dev, stream);
   if (e == cudaSuccess) count_launches(1);
   return e;
 }
