@@ -62,8 +62,11 @@ constexpr int kPartChunk = 64;         // partial-slot granularity of the worksp
 #ifndef CXA_DECODE_CONSUMER_WARPS
 #define CXA_DECODE_CONSUMER_WARPS 4
 #endif
-#ifndef CXA_DECODE_STAGES
+#ifndef CXA_DECODE_STAGES          // ring depth with several queries
 #define CXA_DECODE_STAGES 2
+#endif
+#ifndef CXA_DECODE_STAGES_1Q       // ring depth with one query per cache row
+#define CXA_DECODE_STAGES_1Q 3
 #endif
 #ifndef CXA_DECODE_CHUNK_F32
 #define CXA_DECODE_CHUNK_F32 64
@@ -71,8 +74,11 @@ constexpr int kPartChunk = 64;         // partial-slot granularity of the worksp
 #ifndef CXA_DECODE_CHUNK_BF16
 #define CXA_DECODE_CHUNK_BF16 128
 #endif
-#ifndef CXA_DECODE_CTAS_PER_SM
+#ifndef CXA_DECODE_CTAS_PER_SM     // CTAs per SM with two queries
 #define CXA_DECODE_CTAS_PER_SM 3
+#endif
+#ifndef CXA_DECODE_CTAS_PER_SM_1Q  // CTAs per SM with one query
+#define CXA_DECODE_CTAS_PER_SM_1Q 2
 #endif
 #ifndef CXA_DECODE_PDL
 #define CXA_DECODE_PDL 1
@@ -81,11 +87,10 @@ constexpr int kConsumerWarps = CXA_DECODE_CONSUMER_WARPS;
 constexpr int kProducerWarp = kConsumerWarps;       // streams K/V (and Q) into the ring
 constexpr int kMergeWarp = kConsumerWarps + 1;      // finishes the rows (output or split-row merge)
 constexpr int kThreads = (kConsumerWarps + 2) * 32;
-constexpr int kStages = CXA_DECODE_STAGES;
 constexpr int kQRowBytes = kDh * 4;
 static_assert(kConsumerWarps >= 1, "at least one consumer warp");
 
-template <bool kBF16, int kNQ>
+template <bool kBF16, int kNQ, bool kAppend = false>
 struct Traits {
   static constexpr int kElemBytes = kBF16 ? 2 : 4;
   static constexpr int kRowBytes = kDh * kElemBytes;                 // 256 / 128
@@ -96,6 +101,9 @@ struct Traits {
   static constexpr int kRowsPerPass = 32 / kLanesPerRow;             // keys per warp pass
   static constexpr int kElemsPerLane = kSliceBytes / kElemBytes;     // channels per lane
   static constexpr int kChunkKeys = kBF16 ? CXA_DECODE_CHUNK_BF16 : CXA_DECODE_CHUNK_F32;   // 16 KB of K
+  // the one-query decode streams longest: a deeper ring in fewer CTAs; the
+  // self-attention step (short rows, one step after another) keeps more CTAs
+  static constexpr int kStages = (kNQ == 1 && !kAppend) ? CXA_DECODE_STAGES_1Q : CXA_DECODE_STAGES;
   // fp32 cache with four or more queries: scores with one key per lane (no shuffles)
   static constexpr bool kKeyLanes = !kBF16 && kNQ >= 4;
   static constexpr int kPFloats = kKeyLanes ? kConsumerWarps * 32 * (kNQ / 2) : 0;   // probabilities
@@ -184,8 +192,9 @@ __device__ __forceinline__ float warp_max_f32(float v) {
 __device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-template <bool kBF16, int kNQ>
+template <bool kBF16, int kNQ, bool kAppend>
 constexpr int min_ctas_per_sm() {
+  if (kNQ == 1 && !kAppend) return CXA_DECODE_CTAS_PER_SM_1Q;
   if (!kBF16 && kNQ == 4) return 3;   // key-lane consumers: registers and shared memory fit three
   return kNQ >= 4 ? 2 : CXA_DECODE_CTAS_PER_SM;
 }
@@ -198,12 +207,13 @@ constexpr int min_ctas_per_sm() {
 // grid dependency wait, and this instance lets the next grid start only after its
 // own wait.
 template <bool kBF16, int kNQ, bool kAppend = false>
-__global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ>()))
+__global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend>()))
     decode_stream_kernel(const DecodeParams p) {
-  using R = Traits<kBF16, kNQ>;
+  using R = Traits<kBF16, kNQ, kAppend>;
   constexpr int LPR = R::kLanesPerRow;
   constexpr int EPL = R::kElemsPerLane;
 
+  constexpr int kStages = R::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stages = smem;
   // full[S], empty[S], then the two row-end slots' rfull[2] (consumers -> merge warp)
@@ -859,9 +869,10 @@ size_t counters_bytes(int B, int L, int H) {
   return (n + 255) & ~static_cast<size_t>(255);
 }
 
-template <bool kBF16, int kNQ>
+template <bool kBF16, int kNQ, bool kAppend>
 size_t dynamic_smem_bytes(int B) {
-  using R = Traits<kBF16, kNQ>;
+  using R = Traits<kBF16, kNQ, kAppend>;
+  constexpr int kStages = R::kStages;
   size_t n = static_cast<size_t>(kStages) * R::kStageBytes;
   n += (2 * kStages + 4) * sizeof(uint64_t);
   n += static_cast<size_t>(B + 1) * sizeof(long long);
@@ -875,7 +886,7 @@ template <bool kBF16, int kNQ, bool kAppend = false>
 cudaError_t launch(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t stream) {
   static std::mutex mu;
   static size_t attr_bytes[128] = {};
-  const size_t smem = dynamic_smem_bytes<kBF16, kNQ>(prm.B);
+  const size_t smem = dynamic_smem_bytes<kBF16, kNQ, kAppend>(prm.B);
   cudaError_t e;
   {
     std::lock_guard<std::mutex> lock(mu);
