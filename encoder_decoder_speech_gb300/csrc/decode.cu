@@ -884,10 +884,16 @@ size_t dynamic_smem_bytes(int B) {
 
 template <bool kBF16, int kNQ, bool kAppend = false>
 cudaError_t launch(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t stream) {
+  // per device: the largest shared memory set on the kernel so far, and the CTAs
+  // per SM for the last shared-memory size queried (the host path stays cheap)
   static std::mutex mu;
   static size_t attr_bytes[128] = {};
+  static size_t occ_bytes[128] = {};
+  static int occ_ctas[128] = {};
   const size_t smem = dynamic_smem_bytes<kBF16, kNQ, kAppend>(prm.B);
+  constexpr int kCtas = min_ctas_per_sm<kBF16, kNQ, kAppend>();
   cudaError_t e;
+  int per_sm = 0;
   {
     std::lock_guard<std::mutex> lock(mu);
     const int d = dev.device >= 0 && dev.device < 128 ? dev.device : 0;
@@ -897,12 +903,17 @@ cudaError_t launch(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t 
       if (e != cudaSuccess) return e;
       attr_bytes[d] = smem;
     }
+    if (occ_bytes[d] != smem) {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<kBF16, kNQ, kAppend>, kThreads,
+                                                        smem);
+      if (e != cudaSuccess) return e;
+      occ_bytes[d] = smem;
+      occ_ctas[d] = per_sm;
+    }
+    per_sm = occ_ctas[d];
   }
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<kBF16, kNQ, kAppend>, kThreads, smem);
-  if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  const int grid = dev.num_sms * (per_sm < CXA_DECODE_CTAS_PER_SM ? per_sm : CXA_DECODE_CTAS_PER_SM);
+  const int grid = dev.num_sms * (per_sm < kCtas ? per_sm : kCtas);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);

@@ -750,8 +750,20 @@ cudaError_t launch_tc(const TcParams& prm, const void* Kc, const void* Vc, const
     }
   }
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_shared_tc_kernel<kNQT>, kThreads, smem);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  {   // the occupancy of the last shared-memory size queried, per device
+    static size_t occ_bytes[128] = {};
+    static int occ_ctas[128] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    const int d = dev.device >= 0 && dev.device < 128 ? dev.device : 0;
+    if (occ_bytes[d] != smem) {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_shared_tc_kernel<kNQT>, kThreads, smem);
+      if (e != cudaSuccess) return e;
+      occ_bytes[d] = smem;
+      occ_ctas[d] = per_sm;
+    }
+    per_sm = occ_ctas[d];
+  }
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   if (per_sm < kCtasPerSm) {
     // The occupancy query reports one CTA per SM for kernels that allocate tensor
