@@ -43,26 +43,38 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
-template <bool kBF16>
+// The K ring: kStages chunks of kChunkBytes. Two shapes, chosen per launch (timed on
+// GB300): 16 x 6 KB (two CTAs per SM) and 8 x 8 KB (three per SM, so that a slot's
+// cluster can be twice as large when the wide ring limits it).
+template <int kChunkB, int kStg>
+struct Ring {
+  static constexpr int kChunkBytes = kChunkB;
+  static constexpr int kStages = kStg;                            // warp w owns stages w, w + 8, ...
+  static constexpr size_t kBytes = static_cast<size_t>(kStg) * kChunkB;
+  static_assert(kStg % 8 == 0 && kChunkB % 1024 == 0, "ring shape");
+};
+using RingWide = Ring<6144, 16>;
+using RingNarrow = Ring<8192, 8>;
+
+template <bool kBF16, int kChunkB>
 struct RowGeom {
   static constexpr int kElem = kBF16 ? 2 : 4;
   static constexpr int kRowBytes = 64 * kElem;
   static constexpr int kLanesPerRow = kRowBytes / 16;           // 16 / 8
   static constexpr int kEPL = 16 / kElem;                       // 4 / 8 channels per lane
   static constexpr int kRowsPerWarpPass = 32 / kLanesPerRow;    // 2 / 4
-  static constexpr int kChunkBytes = 6144;
+  static constexpr int kChunkBytes = kChunkB;
   static constexpr int kChunkKeys = kChunkBytes / kRowBytes;    // 24 / 48
   static constexpr int kWarpPasses = kChunkKeys / kRowsPerWarpPass;   // 12: one interleaved reduction
 };
-constexpr int kStages = 16;                                     // warp w owns stages w and w + 8
-constexpr size_t kRingBytes = static_cast<size_t>(kStages) * 6144;
 constexpr int kStageFloats = 2048;   // logits held in shared memory when nsel * keys per CTA fits
 constexpr int kMaxCluster = 16;
 
 // Dynamic shared memory: the ring, the logits, the scaled queries [nsel][64] and the
 // partials [nsel][C] (max, then sum) every cluster CTA stores into every other.
+template <class RG>
 __host__ __device__ constexpr size_t dyn_smem_bytes(int nsel, int C) {
-  return kRingBytes + kStageFloats * sizeof(float) + static_cast<size_t>(nsel) * 64 * sizeof(float) +
+  return RG::kBytes + kStageFloats * sizeof(float) + static_cast<size_t>(nsel) * 64 * sizeof(float) +
          static_cast<size_t>(nsel) * C * 2 * sizeof(float);
 }
 
@@ -79,7 +91,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 template <bool kBF16>
-__device__ __forceinline__ void unpack(const uint4 u, float (&f)[RowGeom<kBF16>::kEPL]) {
+__device__ __forceinline__ void unpack(const uint4 u, float (&f)[16 / (kBF16 ? 2 : 4)]) {
   if constexpr (kBF16) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -95,12 +107,14 @@ __device__ __forceinline__ void unpack(const uint4 u, float (&f)[RowGeom<kBF16>:
   }
 }
 
-template <bool kBF16>
+template <bool kBF16, class RG>
 __global__ void __launch_bounds__(kThreads)
     alignment_kernel(const float* __restrict__ Q, const uint8_t* __restrict__ Kc, const int* __restrict__ key_len,
                      const AlignHeads heads, float* weights, float* __restrict__ mean, int T, int L, int H,
                      float qscale, unsigned int* status) {
-  using G = RowGeom<kBF16>;
+  using G = RowGeom<kBF16, RG::kChunkBytes>;
+  constexpr int kStages = RG::kStages;
+  constexpr size_t kRingBytes = RG::kBytes;
   extern __shared__ __align__(128) uint8_t ring[];              // see dyn_smem_bytes
   __shared__ float s_M[kMaxAlignHeads], s_inv[kMaxAlignHeads];  // merged max and 1 / sum
   __shared__ __align__(8) uint64_t bars[kStages];               // full[s]: chunk landed
@@ -286,7 +300,7 @@ __global__ void __launch_bounds__(kThreads)
 // once (one wave; 16 needs the non-portable size), else 1. The resident-cluster
 // counts depend on the shared memory of the launch (nsel) and are queried once per
 // device and head count.
-template <bool kBF16>
+template <bool kBF16, class RG>
 int cluster_size(int B, int nsel, const DeviceInfo& dev) {
   static std::mutex mu;
   static int fit[128][kMaxAlignHeads + 1][5] = {};  // resident clusters of size 16, 8, 4, 2, 1
@@ -294,12 +308,12 @@ int cluster_size(int B, int nsel, const DeviceInfo& dev) {
   const int dv = dev.device >= 0 && dev.device < 128 ? dev.device : 0;
   std::lock_guard<std::mutex> lock(mu);
   if (!attr[dv]) {
-    if (cudaFuncSetAttribute(alignment_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(dyn_smem_bytes(kMaxAlignHeads, kMaxCluster))) != cudaSuccess) {
+    if (cudaFuncSetAttribute(alignment_kernel<kBF16, RG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(dyn_smem_bytes<RG>(kMaxAlignHeads, kMaxCluster))) != cudaSuccess) {
       cudaGetLastError();
       return -1;
     }
-    big[dv] = cudaFuncSetAttribute(alignment_kernel<kBF16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+    big[dv] = cudaFuncSetAttribute(alignment_kernel<kBF16, RG>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
               cudaSuccess;
     cudaGetLastError();
     attr[dv] = true;
@@ -312,7 +326,7 @@ int cluster_size(int B, int nsel, const DeviceInfo& dev) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(c, 1, 1);
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = dyn_smem_bytes(nsel, c);
+        cfg.dynamicSmemBytes = dyn_smem_bytes<RG>(nsel, c);
         cudaLaunchAttribute at[1];
         at[0].id = cudaLaunchAttributeClusterDimension;
         at[0].val.clusterDim.x = c;
@@ -320,7 +334,7 @@ int cluster_size(int B, int nsel, const DeviceInfo& dev) {
         at[0].val.clusterDim.z = 1;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, alignment_kernel<kBF16>, &cfg) != cudaSuccess) n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, alignment_kernel<kBF16, RG>, &cfg) != cudaSuccess) n = 0;
       }
       fit[dv][nsel][i] = n;
     }
@@ -332,14 +346,12 @@ int cluster_size(int B, int nsel, const DeviceInfo& dev) {
   return 1;
 }
 
-template <bool kBF16>
-cudaError_t launch(const AlignLaunch& a, const DeviceInfo& dev, cudaStream_t stream) {
-  const int C = cluster_size<kBF16>(a.B, a.heads.n, dev);
-  if (C < 0) return cudaErrorInvalidValue;
+template <bool kBF16, class RG>
+cudaError_t launch_ring(const AlignLaunch& a, const DeviceInfo& dev, cudaStream_t stream, int C) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, a.B, 1);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = dyn_smem_bytes(a.heads.n, C);
+  cfg.dynamicSmemBytes = dyn_smem_bytes<RG>(a.heads.n, C);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -351,8 +363,20 @@ cudaError_t launch(const AlignLaunch& a, const DeviceInfo& dev, cudaStream_t str
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   const float qscale = a.scale * 1.4426950408889634f;
-  return cudaLaunchKernelEx(&cfg, alignment_kernel<kBF16>, a.Q, static_cast<const uint8_t*>(a.Kc), a.key_len,
+  return cudaLaunchKernelEx(&cfg, alignment_kernel<kBF16, RG>, a.Q, static_cast<const uint8_t*>(a.Kc), a.key_len,
                             a.heads, a.weights, a.mean, a.T, a.L, a.H, qscale, dev.status_word);
+}
+
+// The wide ring, unless the narrow one lets a slot's cluster be larger.
+template <bool kBF16>
+cudaError_t launch(const AlignLaunch& a, const DeviceInfo& dev, cudaStream_t stream) {
+  const int Cw = cluster_size<kBF16, RingWide>(a.B, a.heads.n, dev);
+  if (Cw < 0) return cudaErrorInvalidValue;
+  if (Cw < kMaxCluster) {
+    const int Cn = cluster_size<kBF16, RingNarrow>(a.B, a.heads.n, dev);
+    if (Cn > Cw) return launch_ring<kBF16, RingNarrow>(a, dev, stream, Cn);
+  }
+  return launch_ring<kBF16, RingWide>(a, dev, stream, Cw);
 }
 
 }  // namespace

@@ -51,6 +51,27 @@ def test_alignment_weights(cache_dtype, T):
             assert np.abs(wt[b, k] @ V[b, l, hh] - out[b, l, hh]).max() <= tol
 
 
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+def test_alignment_sixteen_slots_narrow_ring(cache_dtype):
+    """Sixteen slots and six heads (the batched Whisper-Base shape of a call): the
+    launch takes the 8 x 8 KB ring there, whose clusters can be 16 CTAs, against the
+    oracle, with ragged, empty and full key lengths."""
+    w = W.custom("align16", B=16, T=1500, d=512, L=6, H=8, ragged=True, index=964)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, cache_dtype)
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    kl = h["key_len"].copy()
+    kl[5], kl[11] = 0, w.T
+    heads = [(3, 1), (4, 2), (4, 6), (5, 0), (5, 3), (5, 7)]
+    Q = W.make_Q(w, 5)
+    wt, mean = c.alignment_weights(dev(Q), dev(kl, torch.int32), heads)
+    wt, mean = host(wt), host(mean)
+    ref_w, ref_m = O.attention_weights(Q, host(c.Kc), kl, heads)
+    assert np.abs(wt - ref_w).max() <= WEIGHT_MAX_ABS
+    assert np.abs(mean - ref_m).max() <= WEIGHT_MAX_ABS
+    assert np.all(wt[5] == 0.0) and np.all(mean[5] == 0.0)
+
+
 def test_alignment_weights_large_dims():
     """Whisper-large dims (32 layers, 20 heads, bf16 cache), a spread of heads."""
     w = W.WORKLOADS["large"]
