@@ -552,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend
     // slice read at the same rotation (eight distinct slices: one wavefront). The
     // probabilities go to shared memory; P.V: lane = channels 2l, 2l + 1.
     constexpr int QPW = kNQ / 2;
-    static_assert(kConsumerWarps == 4 && R::kChunkKeys == 64 && (QPW == 2 || QPW % 4 == 0),
+    static_assert(kConsumerWarps == 4 && R::kChunkKeys == 64 && (QPW == 2 || QPW == 3 || QPW % 4 == 0),
                   "two key halves x two query halves of a 64-key chunk");
     const int kh = warp & 1, qh = warp >> 1;
     float* s_pw = s_p + warp * 32 * QPW;   // this warp's probabilities, [32 keys][QPW]
@@ -614,8 +614,11 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend
           for (int q4 = 0; q4 < QPW / 4; ++q4)
             *reinterpret_cast<float4*>(s_pw + lane * QPW + 4 * q4) =
                 make_float4(pw[4 * q4], pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]);
-        } else {
+        } else if constexpr (QPW == 2) {
           *reinterpret_cast<float2*>(s_pw + lane * QPW) = make_float2(pw[0], pw[1]);
+        } else {
+#pragma unroll
+          for (int qi = 0; qi < QPW; ++qi) s_pw[lane * QPW + qi] = pw[qi];
         }
         __syncwarp();
         const int nk = min(32, n - kh * 32);   // valid keys of this warp's half
@@ -629,6 +632,13 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend
             acc[0][1] = fmaf(pk.x, v2.y, acc[0][1]);
             acc[1][0] = fmaf(pk.y, v2.x, acc[1][0]);
             acc[1][1] = fmaf(pk.y, v2.y, acc[1][1]);
+          } else if constexpr (QPW == 3) {
+#pragma unroll
+            for (int qi = 0; qi < 3; ++qi) {
+              const float pk = s_pw[k * QPW + qi];
+              acc[qi][0] = fmaf(pk, v2.x, acc[qi][0]);
+              acc[qi][1] = fmaf(pk, v2.y, acc[qi][1]);
+            }
           }
 #pragma unroll
           for (int q4 = 0; q4 < QPW / 4; ++q4) {
@@ -933,6 +943,7 @@ cudaError_t launch_f32_nq(const DecodeParams& prm, const DeviceInfo& dev, cudaSt
   if (prm.nq == 1) return launch<false, 1>(prm, dev, stream);
   if (prm.nq == 2) return launch<false, 2>(prm, dev, stream);
   if (prm.nq <= 4) return launch<false, 4>(prm, dev, stream);
+  if (prm.nq <= 6) return launch<false, 6>(prm, dev, stream);   // a beam of five or six
   return launch<false, 8>(prm, dev, stream);
 }
 

@@ -28,7 +28,7 @@ def _queries(w, nq, seed):
     return rng.standard_normal((w.B, nq, w.L, w.H, 64)).astype(np.float32)
 
 
-@pytest.mark.parametrize("cache_dtype,nq", [(c, n) for c in ("f32", "bf16") for n in (1, 2, 3, 4, 5, 7, 8)]
+@pytest.mark.parametrize("cache_dtype,nq", [(c, n) for c in ("f32", "bf16") for n in (1, 2, 3, 4, 5, 6, 7, 8)]
                          + [("bf16", n) for n in (9, 12, 16)])
 def test_shared_decode_matches_oracle(nq, cache_dtype):
     w = W.custom("shared", B=4, T=700, d=256, L=2, H=4, ragged=True, index=940)
@@ -136,7 +136,7 @@ def test_shared_decode_tensor_core_key_length_edges(nq):
     assert np.abs(out - ref).max() <= DECODE_BF16_MAX_ABS
 
 
-@pytest.mark.parametrize("nq", [3, 4, 5, 8])
+@pytest.mark.parametrize("nq", [3, 4, 5, 6, 8])
 def test_shared_decode_fp32_key_length_edges(nq):
     """fp32 cache, several queries (one key per lane in each 32-key half of a 64-key
     chunk): key lengths at and around the halves and chunks (1, 2, 31, 32, 33, 63,
