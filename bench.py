@@ -46,8 +46,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["cxa", "reference"], default="cxa")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     p.add_argument("--no-variants", action="store_true", help="skip the bf16-cache variant")
-    p.add_argument("--profile", choices=["decode", "decode_bf16", "populate", "shared_bf16", "shared_f32", "align", "block",
-                                          "selfattn"],
+    p.add_argument("--profile", choices=["decode", "decode_bf16", "populate", "shared_bf16", "shared_bf16_16", "shared_f32",
+                                          "align", "block", "selfattn"],
                    default=None,
                    help="run a few launches of one kernel on the workload's inputs (for ncu), print nothing else")
     p.add_argument("--sweep", action="store_true",
@@ -949,16 +949,17 @@ def run_profile(args):
     torch.cuda.set_device(0)
     w = W.WORKLOADS[WORKLOAD]
     (E, WK, WV, bV, kl, Q, _), _ = device_inputs(torch, W, w, 0)
-    bf16 = args.profile in ("decode_bf16", "shared_bf16")
+    bf16 = args.profile in ("decode_bf16", "shared_bf16", "shared_bf16_16")
     cache = cxa.CrossAttentionCache(w.B, w.T, w.L, w.H, w.dh, "bf16" if bf16 else "f32")
     cache.populate(E, WK, WV, bV)
     if args.profile == "populate":
         for _ in range(2):
             cache.populate(E, WK, WV, bV)
-    elif args.profile in ("shared_bf16", "shared_f32"):   # 8 hypotheses per slot
+    elif args.profile in ("shared_bf16", "shared_f32", "shared_bf16_16"):   # 8 (or 16) hypotheses per slot
         import numpy as np
+        nq = 16 if args.profile == "shared_bf16_16" else 8
         Qs = torch.from_numpy(np.random.default_rng(8).standard_normal(
-            (w.B, 8, w.L, w.H, w.dh)).astype(np.float32)).to("cuda")
+            (w.B, nq, w.L, w.H, w.dh)).astype(np.float32)).to("cuda")
         for _ in range(3):
             cache.decode_shared(Qs, kl)
     elif args.profile == "align":         # six alignment heads of the last three layers
