@@ -112,6 +112,11 @@ def _ptr(x) -> int | None:
 def _stream(s) -> int | None:
     if s is None:
         import torch
+        # the current stream's handle without building a Stream object (a few
+        # microseconds per call on the host otherwise)
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return raw(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if hasattr(s, "cuda_stream"):
         return s.cuda_stream
