@@ -120,3 +120,14 @@ def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
     monkeypatch.setattr(cxa, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         cxa.load(str(tmp_path / "missing.so"))
+
+
+def test_binding_passes_explicit_streams_through():
+    """An explicit stream handle (int, or an object with a cuda_stream attribute) goes to
+    the C ABI unchanged; only a missing one is looked up from torch's current stream."""
+    class FakeStream:
+        cuda_stream = 0x1234
+
+    assert cxa._stream(0) == 0
+    assert cxa._stream(0x7f00) == 0x7f00
+    assert cxa._stream(FakeStream()) == 0x1234
