@@ -526,16 +526,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       f_pending = false;
     };
 
+    // One pass past the range (tail) flushes the last segment, so that the flush,
+    // the largest part of this code, is laid down once.
     long long i = 0;
-    for (long long g = g0; g < g1; ++g, ++i) {
+    for (long long g = g0;; ++g, ++i) {
+      const bool tail = g == g1;
       const int s = static_cast<int>(i % kStages);
       const int a = static_cast<int>(i & 1);
       const uint32_t acc_parity = static_cast<uint32_t>((i >> 1) & 1);
+      const int nch = tail ? 1 : s_nch[cur.b];
+      const bool seg_ends = !tail && ((cur.c == nch - 1) || (g + 1 == g1));
+      const int rb = seg & 1;
+      if (!tail) {
       const int kl = s_kl[cur.b];
-      const int nch = s_nch[cur.b];
       const int n = min(kChunk, kl - cur.c * kChunk);
       const bool seg_first = cur.c == seg_c0;
-      const bool seg_ends = (cur.c == nch - 1) || (g + 1 == g1);
       if (ok && !mbar_wait(tfull_bar(a), acc_parity, s_flags)) fail();
       tc_fence_after();
       uint32_t sh[16], sl[16];   // K.Q_hi, K.Q_lo
@@ -601,7 +606,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
       fence_proxy_async_smem();
       named_barrier(1, kConsumerWarps * 32);                 // P^T (and the V tail) complete
-      const int rb = seg & 1;
       if (rescale_o) {
         // O^T (chunks before this one) *= corr per query column, after their P.V and
         // before this chunk's; each warp scales its own 16 channel lanes
@@ -618,8 +622,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         named_barrier(1, kConsumerWarps * 32);
       }
       if (tid == 0) mbar_arrive(pfull_bar(a));               // the MMA warp issues this chunk's P.V
-      // the previous segment's P.V has run by now; its P^T buffer (the other one) stages O
-      if (f_pending) flush(a ^ 1);
+      }
+      // the previous segment's P.V has run by now; its P^T buffer (the other one) stages O.
+      // Past the range every P.V has been issued, and both buffers are free once it has run.
+      if (f_pending) flush(tail ? 0 : (a ^ 1));
+      if (tail) break;
 
       if (seg_ends) {
         // ---- the segment ends: per-warp sums over the keys, references; written out next chunk
@@ -665,8 +672,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       advance(cur, s_nch, p.B, LH);
       if (cur.b != pb || cur.lh != plh) seg_c0 = cur.c;
     }
-    // the last segment: every P.V has been issued; both P^T buffers are free once it has run
-    if (f_pending) flush(0);
   }
   tc_fence_before();
   __syncthreads();
