@@ -90,7 +90,7 @@ constexpr int kThreads = (kConsumerWarps + 2) * 32;
 constexpr int kQRowBytes = kDh * 4;
 static_assert(kConsumerWarps >= 1, "at least one consumer warp");
 
-template <bool kBF16, int kNQ, bool kAppend = false>
+template <bool kBF16, int kNQ, bool kAppend = false, bool kShallow = false>
 struct Traits {
   static constexpr int kElemBytes = kBF16 ? 2 : 4;
   static constexpr int kRowBytes = kDh * kElemBytes;                 // 256 / 128
@@ -101,9 +101,11 @@ struct Traits {
   static constexpr int kRowsPerPass = 32 / kLanesPerRow;             // keys per warp pass
   static constexpr int kElemsPerLane = kSliceBytes / kElemBytes;     // channels per lane
   static constexpr int kChunkKeys = kBF16 ? CXA_DECODE_CHUNK_BF16 : CXA_DECODE_CHUNK_F32;   // 16 KB of K
-  // the one-query decode streams longest: a deeper ring in fewer CTAs; the
-  // self-attention step (short rows, one step after another) keeps more CTAs
-  static constexpr int kStages = (kNQ == 1 && !kAppend) ? CXA_DECODE_STAGES_1Q : CXA_DECODE_STAGES;
+  // the one-query decode: a deeper ring in fewer CTAs, so the slowest CTA, which
+  // ends the launch, is relatively nearer the mean; the self-attention step (short
+  // rows, one step after another) and very long streams (kShallow) keep more CTAs
+  static constexpr bool kDeep = kNQ == 1 && !kAppend && !kShallow;
+  static constexpr int kStages = kDeep ? CXA_DECODE_STAGES_1Q : CXA_DECODE_STAGES;
   // fp32 cache with four or more queries: scores with one key per lane (no shuffles)
   static constexpr bool kKeyLanes = !kBF16 && kNQ >= 4;
   static constexpr int kPFloats = kKeyLanes ? kConsumerWarps * 32 * (kNQ / 2) : 0;   // probabilities
@@ -192,9 +194,9 @@ __device__ __forceinline__ float warp_max_f32(float v) {
 __device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-template <bool kBF16, int kNQ, bool kAppend>
+template <bool kBF16, int kNQ, bool kAppend, bool kShallow = false>
 constexpr int min_ctas_per_sm() {
-  if (kNQ == 1 && !kAppend) return CXA_DECODE_CTAS_PER_SM_1Q;
+  if (kNQ == 1 && !kAppend && !kShallow) return CXA_DECODE_CTAS_PER_SM_1Q;
   if (!kBF16 && kNQ == 4) return 3;   // key-lane consumers: registers and shared memory fit three
   return kNQ >= 4 ? 2 : CXA_DECODE_CTAS_PER_SM;
 }
@@ -206,10 +208,10 @@ constexpr int min_ctas_per_sm() {
 // row pos - 1, so only chunks of keys below min(pos, T) - 1 are streamed before the
 // grid dependency wait, and this instance lets the next grid start only after its
 // own wait.
-template <bool kBF16, int kNQ, bool kAppend = false>
-__global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend>()))
+template <bool kBF16, int kNQ, bool kAppend = false, bool kShallow = false>
+__global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend, kShallow>()))
     decode_stream_kernel(const DecodeParams p) {
-  using R = Traits<kBF16, kNQ, kAppend>;
+  using R = Traits<kBF16, kNQ, kAppend, kShallow>;
   constexpr int LPR = R::kLanesPerRow;
   constexpr int EPL = R::kElemsPerLane;
 
@@ -879,9 +881,9 @@ size_t counters_bytes(int B, int L, int H) {
   return (n + 255) & ~static_cast<size_t>(255);
 }
 
-template <bool kBF16, int kNQ, bool kAppend>
+template <bool kBF16, int kNQ, bool kAppend, bool kShallow = false>
 size_t dynamic_smem_bytes(int B) {
-  using R = Traits<kBF16, kNQ, kAppend>;
+  using R = Traits<kBF16, kNQ, kAppend, kShallow>;
   constexpr int kStages = R::kStages;
   size_t n = static_cast<size_t>(kStages) * R::kStageBytes;
   n += (2 * kStages + 4) * sizeof(uint64_t);
@@ -892,7 +894,7 @@ size_t dynamic_smem_bytes(int B) {
   return n;
 }
 
-template <bool kBF16, int kNQ, bool kAppend = false>
+template <bool kBF16, int kNQ, bool kAppend = false, bool kShallow = false>
 cudaError_t launch(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t stream) {
   // per device: the largest shared memory set on the kernel so far, and the CTAs
   // per SM for the last shared-memory size queried (the host path stays cheap)
@@ -900,21 +902,21 @@ cudaError_t launch(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t 
   static size_t attr_bytes[128] = {};
   static size_t occ_bytes[128] = {};
   static int occ_ctas[128] = {};
-  const size_t smem = dynamic_smem_bytes<kBF16, kNQ, kAppend>(prm.B);
-  constexpr int kCtas = min_ctas_per_sm<kBF16, kNQ, kAppend>();
+  const size_t smem = dynamic_smem_bytes<kBF16, kNQ, kAppend, kShallow>(prm.B);
+  constexpr int kCtas = min_ctas_per_sm<kBF16, kNQ, kAppend, kShallow>();
   cudaError_t e;
   int per_sm = 0;
   {
     std::lock_guard<std::mutex> lock(mu);
     const int d = dev.device >= 0 && dev.device < 128 ? dev.device : 0;
     if (attr_bytes[d] < smem) {
-      e = cudaFuncSetAttribute(decode_stream_kernel<kBF16, kNQ, kAppend>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      e = cudaFuncSetAttribute(decode_stream_kernel<kBF16, kNQ, kAppend, kShallow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem));
       if (e != cudaSuccess) return e;
       attr_bytes[d] = smem;
     }
     if (occ_bytes[d] != smem) {
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<kBF16, kNQ, kAppend>, kThreads,
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<kBF16, kNQ, kAppend, kShallow>, kThreads,
                                                         smem);
       if (e != cudaSuccess) return e;
       occ_bytes[d] = smem;
@@ -934,13 +936,25 @@ cudaError_t launch(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t 
   attr[0].val.programmaticStreamSerializationAllowed = CXA_DECODE_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_stream_kernel<kBF16, kNQ, kAppend>, prm);
+  return cudaLaunchKernelEx(&cfg, decode_stream_kernel<kBF16, kNQ, kAppend, kShallow>, prm);
+}
+
+// One query per row: the deep ring, unless the stream is so long (an upper bound on
+// its chunks from the host-side geometry; the key lengths live on the device) that
+// launch tails matter little and more CTAs per SM stream faster.
+constexpr long long kLongStreamChunks = 40960;
+template <bool kBF16>
+cudaError_t launch_one_query(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t stream) {
+  using R = Traits<kBF16, 1>;
+  const long long chunks = static_cast<long long>(prm.B) * prm.LH * ((prm.T + R::kChunkKeys - 1) / R::kChunkKeys);
+  if (chunks >= kLongStreamChunks) return launch<kBF16, 1, false, true>(prm, dev, stream);
+  return launch<kBF16, 1, false, false>(prm, dev, stream);
 }
 
 // fp32 cache: one instance per query-count bucket (a bf16 cache with several
 // queries goes to the tensor-core kernel)
 cudaError_t launch_f32_nq(const DecodeParams& prm, const DeviceInfo& dev, cudaStream_t stream) {
-  if (prm.nq == 1) return launch<false, 1>(prm, dev, stream);
+  if (prm.nq == 1) return launch_one_query<false>(prm, dev, stream);
   if (prm.nq == 2) return launch<false, 2>(prm, dev, stream);
   if (prm.nq <= 4) return launch<false, 4>(prm, dev, stream);
   if (prm.nq <= 6) return launch<false, 6>(prm, dev, stream);   // a beam of five or six
@@ -985,7 +999,7 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStre
   if (a.K_new != nullptr)   // the self-attention step: append fused into a one-query decode
     e = a.cache_bf16 ? launch<true, 1, true>(prm, dev, stream) : launch<false, 1, true>(prm, dev, stream);
   else
-    e = a.cache_bf16 ? launch<true, 1>(prm, dev, stream) : launch_f32_nq(prm, dev, stream);
+    e = a.cache_bf16 ? launch_one_query<true>(prm, dev, stream) : launch_f32_nq(prm, dev, stream);
   if (e == cudaSuccess) count_launches(1);
   return e;
 }
