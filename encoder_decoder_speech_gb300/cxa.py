@@ -187,11 +187,26 @@ def cxa_self_attention_step(handle, pos, Q, K_new, V_new, out, scale, workspace,
                                           _ptr(workspace), workspace_bytes, _stream(stream))
 
 
+_HEADS_ARRAYS: dict = {}
+
+
+def _heads_array(heads):
+    """The (layer, head) pairs as a C int array, kept per distinct head list (a call
+    site passes the same list every step)."""
+    key = tuple((int(l), int(h)) for l, h in heads)
+    arr = _HEADS_ARRAYS.get(key)
+    if arr is None:
+        flat = [v for pair in key for v in pair]
+        arr = (ctypes.c_int * max(len(flat), 1))(*flat)
+        if len(_HEADS_ARRAYS) < 256:
+            _HEADS_ARRAYS[key] = arr
+    return arr, len(key)
+
+
 def cxa_alignment_weights(handle, Q, key_len, heads, weights, mean, scale, stream=None) -> int:
     """heads: host sequence of (layer, head) pairs."""
-    flat = [int(v) for pair in heads for v in pair]
-    arr = (ctypes.c_int * max(len(flat), 1))(*flat)
-    return load().cxa_alignment_weights(handle, _ptr(Q), _ptr(key_len), ctypes.cast(arr, ctypes.c_void_p), len(heads),
+    arr, n = _heads_array(heads)
+    return load().cxa_alignment_weights(handle, _ptr(Q), _ptr(key_len), ctypes.cast(arr, ctypes.c_void_p), n,
                                         _ptr(weights), _ptr(mean), float(scale), _stream(stream))
 
 

@@ -131,3 +131,12 @@ def test_binding_passes_explicit_streams_through():
     assert cxa._stream(0) == 0
     assert cxa._stream(0x7f00) == 0x7f00
     assert cxa._stream(FakeStream()) == 0x1234
+
+
+def test_alignment_heads_marshalled_once_per_list():
+    """The (layer, head) list becomes one C int array, reused for an equal list."""
+    a, n = cxa._heads_array([(3, 1), (4, 2)])
+    b, m = cxa._heads_array(((3, 1), (4, 2)))
+    assert n == m == 2 and a is b and list(a) == [3, 1, 4, 2]
+    c, k = cxa._heads_array([])
+    assert k == 0
