@@ -62,10 +62,10 @@ constexpr int kPartChunk = 64;         // partial-slot granularity of the worksp
 #ifndef CXA_DECODE_CONSUMER_WARPS
 #define CXA_DECODE_CONSUMER_WARPS 4
 #endif
-#ifndef CXA_DECODE_STAGES          // ring depth with several queries
+#ifndef CXA_DECODE_STAGES          // ring depth of the 2-stage shape (more queries, self-attention, long streams)
 #define CXA_DECODE_STAGES 2
 #endif
-#ifndef CXA_DECODE_STAGES_1Q       // ring depth with one query per cache row
+#ifndef CXA_DECODE_STAGES_1Q       // ring depth with one or two queries per cache row
 #define CXA_DECODE_STAGES_1Q 3
 #endif
 #ifndef CXA_DECODE_CHUNK_F32
@@ -74,10 +74,10 @@ constexpr int kPartChunk = 64;         // partial-slot granularity of the worksp
 #ifndef CXA_DECODE_CHUNK_BF16
 #define CXA_DECODE_CHUNK_BF16 128
 #endif
-#ifndef CXA_DECODE_CTAS_PER_SM     // CTAs per SM with two queries
+#ifndef CXA_DECODE_CTAS_PER_SM     // CTAs per SM of the 2-stage shape
 #define CXA_DECODE_CTAS_PER_SM 3
 #endif
-#ifndef CXA_DECODE_CTAS_PER_SM_1Q  // CTAs per SM with one query
+#ifndef CXA_DECODE_CTAS_PER_SM_1Q  // CTAs per SM with one or two queries
 #define CXA_DECODE_CTAS_PER_SM_1Q 2
 #endif
 #ifndef CXA_DECODE_PDL
@@ -101,10 +101,10 @@ struct Traits {
   static constexpr int kRowsPerPass = 32 / kLanesPerRow;             // keys per warp pass
   static constexpr int kElemsPerLane = kSliceBytes / kElemBytes;     // channels per lane
   static constexpr int kChunkKeys = kBF16 ? CXA_DECODE_CHUNK_BF16 : CXA_DECODE_CHUNK_F32;   // 16 KB of K
-  // the one-query decode: a deeper ring in fewer CTAs, so the slowest CTA, which
-  // ends the launch, is relatively nearer the mean; the self-attention step (short
-  // rows, one step after another) and very long streams (kShallow) keep more CTAs
-  static constexpr bool kDeep = kNQ == 1 && !kAppend && !kShallow;
+  // one or two queries: a deeper ring in fewer CTAs, so the slowest CTA, which ends
+  // the launch, is relatively nearer the mean; the self-attention step (short rows,
+  // one step after another) and very long streams (kShallow) keep more CTAs
+  static constexpr bool kDeep = kNQ <= 2 && !kAppend && !kShallow;
   static constexpr int kStages = kDeep ? CXA_DECODE_STAGES_1Q : CXA_DECODE_STAGES;
   // fp32 cache with four or more queries: scores with one key per lane (no shuffles)
   static constexpr bool kKeyLanes = !kBF16 && kNQ >= 4;
@@ -196,7 +196,7 @@ __device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol
 
 template <bool kBF16, int kNQ, bool kAppend, bool kShallow = false>
 constexpr int min_ctas_per_sm() {
-  if (kNQ == 1 && !kAppend && !kShallow) return CXA_DECODE_CTAS_PER_SM_1Q;
+  if (kNQ <= 2 && !kAppend && !kShallow) return CXA_DECODE_CTAS_PER_SM_1Q;
   if (!kBF16 && kNQ == 4) return 3;   // key-lane consumers: registers and shared memory fit three
   return kNQ >= 4 ? 2 : CXA_DECODE_CTAS_PER_SM;
 }
