@@ -133,7 +133,7 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
       : "memory");
 }
 
-template <int kNQT>   // query columns the softmax handles (4, 8 or 16 >= nq)
+template <int kNQT>   // query columns the softmax handles (4, 8, 12 or 16 >= nq)
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     decode_shared_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                             const TcParams p) {
@@ -835,6 +835,7 @@ cudaError_t launch_decode_shared_tc(const DecodeLaunch& a, const DeviceInfo& dev
   prm.qscale = a.scale * 1.4426950408889634f;
   cudaError_t e = a.nq <= 4   ? launch_tc<4>(prm, a.Kc, a.Vc, dev, stream, msg)
                   : a.nq <= 8 ? launch_tc<8>(prm, a.Kc, a.Vc, dev, stream, msg)
+                  : a.nq <= 12 ? launch_tc<12>(prm, a.Kc, a.Vc, dev, stream, msg)
                               : launch_tc<16>(prm, a.Kc, a.Vc, dev, stream, msg);
   if (e == cudaSuccess) count_launches(1);
   return e;
