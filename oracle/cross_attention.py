@@ -36,13 +36,18 @@ What it computes, and where the pages define it:
   against the causal whole-window formula ("Recurrence as feeds").
 * ``full_window`` -- the "whole window" formula kept as a check beside one-query
   decode ("Recurrence as feeds", "What it opened").
+* ``round_bf16`` -- fp32 -> bfloat16 round to nearest even, the conversion in
+  front of the bf16 populate (the Whisper-large workload: fp32 E, bf16
+  tensor-core inputs) and the rounding of a bf16 cache store.
 
 Readings where the pages are silent (each one is pinned by a test):
   WK_l is ``[d_in, d_out]`` ("E x WK_l"); head h owns columns h*dh .. h*dh+dh-1;
   a layer slab is ``[H][T][dh]``; key_len is clamped to [0, T].
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against brute
-force, closed forms and the invariants the pages fix; none is "parity unpinned".
+force, closed forms, hand-computed values and the invariants the pages fix
+(``populate_head`` against ``populate`` and brute force, ``rel_frobenius``
+against hand-computed ratios); none is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -148,16 +153,6 @@ def decode(Q, Kc, Vc, key_len, scale: float | None = None) -> np.ndarray:
             for h in range(H):
                 out[b, l, h] = attend_row(Q[b, l, h], Kc[b, l, h], Vc[b, l, h], int(n[b]), scale)
     return out
-
-
-def decode_rows(Q, Kc, Vc, key_len, rows, scale: float | None = None) -> np.ndarray:
-    """Decode only the listed (b, l, h) rows; returns ``[len(rows), dh]``."""
-    B, L, H, T, dh = np.shape(Kc)
-    if scale is None:
-        scale = 1.0 / np.sqrt(dh)
-    n = clamp_key_len(key_len, T)
-    return np.stack([attend_row(np.asarray(Q)[b, l, h], Kc[b, l, h], Vc[b, l, h], int(n[b]), scale)
-                     for (b, l, h) in rows])
 
 
 def decode_shared(Q, Kc, Vc, key_len, scale: float | None = None) -> np.ndarray:
@@ -296,6 +291,37 @@ def cross_attention_from_memory(Q, E, WK, WV, bV, key_len, H: int, scale: float 
     return decode(Q, Kc, Vc, key_len, scale)
 
 
+def round_bf16(x) -> np.ndarray:
+    """fp32 values rounded to the nearest bfloat16 (8 significant bits: the fp32
+    value with its 16 low fraction bits cleared), ties to the even significand.
+    Written from the rounding rule: the two bf16 neighbours of x are x with its 16
+    low bits cleared (toward zero) and the next bf16 away from zero; the nearer
+    one is taken, the distances measured exactly in fp64 (fp32 differences are
+    exact there); a tie takes the neighbour whose last kept bit is 0. Past the
+    largest finite bf16 the upper neighbour is infinity, which the rule places at
+    2^128 (one ulp beyond); infinities and NaNs pass through. Returns float32."""
+    x32 = np.array(x, dtype=np.float32)      # a copy, of x's shape (0-d for a scalar)
+    bits = x32.view(np.uint32)
+    lo_bits = bits & np.uint32(0xFFFF0000)
+    hi_bits = lo_bits + np.uint32(0x10000)
+    xd = x32.astype(np.float64)
+    special = ~np.isfinite(xd)
+    with np.errstate(invalid="ignore"):
+        lo = lo_bits.view(np.float32).astype(np.float64)
+        hi = hi_bits.view(np.float32).astype(np.float64)
+        hi_pos = np.where(np.isinf(hi), np.copysign(2.0 ** 128, xd), hi)
+        d_lo = np.abs(xd - lo)
+        d_hi = np.abs(hi_pos - xd)
+    lo_even = ((lo_bits >> np.uint32(16)) & np.uint32(1)) == 0
+    take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ~lo_even)
+    out = np.where(take_hi, hi, lo)
+    out = np.where(special, xd, out)
+    return out.astype(np.float32)
+
+
 def rel_frobenius(x, ref) -> float:
+    """Relative Frobenius error ||x - ref||_F / ||ref||_F over all elements: the
+    measure the populate tolerance is stated in (square root of the summed
+    squared differences over the square root of the summed squared reference)."""
     x, ref = _f64(x), _f64(ref)
     return float(np.linalg.norm((x - ref).ravel()) / max(np.linalg.norm(ref.ravel()), 1e-300))

@@ -236,6 +236,81 @@ def pin_shared_decode():
     return err
 
 
+def pin_populate_head():
+    """One head's K/V block equals the head's slice of the whole projection, and
+    pure-Python brute force, on shapes where every head is checked (the first
+    and last column blocks, a bias on every column)."""
+    err = 0.0
+    for (B, T, d, L, H, dh) in [(2, 3, 4, 2, 2, 2), (1, 2, 6, 1, 3, 2), (1, 4, 8, 2, 2, 4)]:
+        E, WK, WV = _rand((B, T, d), 160), _rand((L, d, d), 161), _rand((L, d, d), 162)
+        bV = _rand((L, d), 163)
+        Kb, Vb = bf_populate(E, WK, WV, bV, H)
+        for b in range(B):
+            for l in range(L):
+                for h in range(H):
+                    K, V = O.populate_head(E[b], WK[l], WV[l], bV[l], h, dh)
+                    err = max(err, np.abs(K - Kb[b, l, h]).max(), np.abs(V - Vb[b, l, h]).max())
+    B, T, d, L, H = 2, 37, 256, 2, 4
+    E, WK, WV = _rand((B, T, d), 164), _rand((L, d, d), 165, d ** -0.5), _rand((L, d, d), 166, d ** -0.5)
+    bV = _rand((L, d), 167, 0.02)
+    Kc, Vc = O.populate(E, WK, WV, bV, H)
+    for (b, l, h) in [(0, 0, 0), (1, 1, 3), (0, 1, 2), (1, 0, 1)]:
+        K, V = O.populate_head(E[b], WK[l], WV[l], bV[l], h)
+        err = max(err, np.abs(K - Kc[b, l, h]).max() / np.abs(Kc[b, l, h]).max(),
+                  np.abs(V - Vc[b, l, h]).max() / np.abs(Vc[b, l, h]).max())
+    return float(err)
+
+
+def pin_rel_frobenius():
+    """The populate error measure against ratios computed by hand:
+    ||(8, -6)|| / ||(3, 4)|| = 10 / 5 = 2 (a perturbation orthogonal to the
+    reference, so a missing square root gives 4 or 20 and a squared
+    denominator 0.4); a 2x2 block with one element off by 3 over a reference of
+    norm 5 gives 0.6; a uniform relative error eps gives eps; equality gives 0."""
+    errs = [abs(O.rel_frobenius([11.0, -2.0], [3.0, 4.0]) - 2.0),
+            abs(O.rel_frobenius([[1.0, 2.0], [2.0, 7.0]], [[1.0, 2.0], [2.0, 4.0]]) - 0.6)]
+    ref = _rand((3, 5, 7), 170)
+    errs.append(abs(O.rel_frobenius(ref * (1.0 + 3e-4), ref) - 3e-4) / 3e-4)
+    errs.append(O.rel_frobenius(ref, ref))
+    return float(max(errs))
+
+
+def pin_round_bf16():
+    """Hand-computed roundings (exact ties to even in both directions, just past
+    a tie, negative values, the overflow threshold, subnormals: bf16's smallest
+    spacing is 2^-133, so 1.5 * 2^-133 is a tie that goes to the even 2^-132 and
+    2^-140 goes to 0), invariants
+    (idempotent, low 16 bits clear, within half an ulp, monotonic) and agreement
+    with the add-and-shift bit formulation of the same rule on 2^20 random
+    patterns. Returns the number of failures."""
+    u = 2.0 ** -8                                   # half an ulp of bf16 at 1.0
+    cases = [(1.0, 1.0), (1.0 + u, 1.0), (1.0 + 3 * u, 1.0 + 4 * u), (1.0 + u + 2.0 ** -20, 1.0 + 2 * u),
+             (-(1.0 + u + 2.0 ** -20), -(1.0 + 2 * u)), (-(1.0 + 3 * u), -(1.0 + 4 * u)), (0.0, 0.0),
+             (float(np.finfo(np.float32).max), np.inf), (-float(np.finfo(np.float32).max), -np.inf),
+             (1.5 * 2.0 ** -133, 2.0 ** -132), (1.25 * 2.0 ** -133, 2.0 ** -133), (2.0 ** -140, 0.0),
+             (np.inf, np.inf)]
+    bad = 0
+    for x, want in cases:
+        got = float(O.round_bf16(np.float32(x)))
+        bad += int(got != want)
+    bad += int(not np.isnan(O.round_bf16(np.float32(np.nan))))
+    rng = np.random.default_rng(171)
+    pat = rng.integers(0, 2 ** 32, size=1 << 20, dtype=np.uint64).astype(np.uint32)
+    x = pat.view(np.float32)
+    x = x[np.isfinite(x)]
+    r = O.round_bf16(x)
+    bad += int((r.view(np.uint32) & np.uint32(0xFFFF)).any())
+    fin = np.isfinite(r)
+    bad += int(not np.array_equal(O.round_bf16(r[fin]), r[fin]))
+    xs = np.sort(x[np.abs(x) < 1e30])
+    bad += int((np.diff(O.round_bf16(xs).astype(np.float64)) < 0).any())
+    ex = np.floor(np.log2(np.abs(xs[xs != 0].astype(np.float64))))
+    half_ulp = 2.0 ** (np.maximum(ex, -126) - 8)
+    bad += int((np.abs(O.round_bf16(xs[xs != 0]).astype(np.float64) - xs[xs != 0]) > half_ulp).any())
+    bad += int(not np.array_equal(r.view(np.uint32) >> np.uint32(16), W.bf16_bits(x).astype(np.uint32)))
+    return bad
+
+
 def bf_layer_norm(x, gamma, beta, eps):
     x = list(x)
     d = len(x)
@@ -377,6 +452,18 @@ def test_alignment_head_weights():
     assert pin_attention_weights() < 1e-12
 
 
+def test_populate_head_matches_projection_and_bruteforce():
+    assert pin_populate_head() < 1e-12
+
+
+def test_rel_frobenius_hand_computed():
+    assert pin_rel_frobenius() < 1e-12
+
+
+def test_round_bf16_hand_values_and_invariants():
+    assert pin_round_bf16() == 0
+
+
 def test_geometry_fails_closed():
     with pytest.raises(ValueError):
         O.populate(np.zeros((1, 0, 128)), np.zeros((1, 128, 128)), np.zeros((1, 128, 128)), np.zeros((1, 128)), 2)
@@ -471,15 +558,65 @@ def _mut_missing_scale(monkeypatch):
     monkeypatch.setattr(O, "attend_row", attend_row)
 
 
+def _mut_head_without_bias(monkeypatch):
+    orig = O.populate_head
+
+    def populate_head(E_b, WK_l, WV_l, bV_l, h, dh=64):
+        return orig(E_b, WK_l, WV_l, np.zeros_like(np.asarray(bV_l, float)), h, dh)
+    monkeypatch.setattr(O, "populate_head", populate_head)
+
+
+def _mut_head_neighbouring_block(monkeypatch):
+    orig = O.populate_head
+
+    def populate_head(E_b, WK_l, WV_l, bV_l, h, dh=64):
+        return orig(E_b, WK_l, WV_l, bV_l, (h + 1) % (np.shape(WK_l)[1] // dh), dh)
+    monkeypatch.setattr(O, "populate_head", populate_head)
+
+
+def _mut_frobenius_without_sqrt(monkeypatch):
+    def rel_frobenius(x, ref):
+        x, ref = np.asarray(x, float), np.asarray(ref, float)
+        return float(((x - ref) ** 2).sum() / max((ref ** 2).sum(), 1e-300))
+    monkeypatch.setattr(O, "rel_frobenius", rel_frobenius)
+
+
+def _mut_frobenius_squared_denominator(monkeypatch):
+    def rel_frobenius(x, ref):
+        x, ref = np.asarray(x, float), np.asarray(ref, float)
+        return float(np.linalg.norm((x - ref).ravel()) / max((ref ** 2).sum(), 1e-300))
+    monkeypatch.setattr(O, "rel_frobenius", rel_frobenius)
+
+
+def _mut_round_half_away(monkeypatch):
+    def round_bf16(x):
+        u = np.array(x, dtype=np.float32).view(np.uint32)
+        return ((u + np.uint32(0x8000)) & np.uint32(0xFFFF0000)).view(np.float32)
+    monkeypatch.setattr(O, "round_bf16", round_bf16)
+
+
+def _mut_round_truncate(monkeypatch):
+    def round_bf16(x):
+        u = np.array(x, dtype=np.float32).view(np.uint32)
+        return (u & np.uint32(0xFFFF0000)).view(np.float32)
+    monkeypatch.setattr(O, "round_bf16", round_bf16)
+
+
 def _all_pins_pass():
-    return (pin_populate_bruteforce() < 1e-12 and pin_decode_bruteforce() < 1e-12
-            and pin_closed_forms() < 1e-12 and pin_full_window() < 1e-13 and pin_shared_decode() < 1e-12
-            and pin_layout_offset() == 0 and pin_scale_on_scores() < 1e-13)
+    try:
+        return (pin_populate_bruteforce() < 1e-12 and pin_decode_bruteforce() < 1e-12
+                and pin_closed_forms() < 1e-12 and pin_full_window() < 1e-13 and pin_shared_decode() < 1e-12
+                and pin_layout_offset() == 0 and pin_scale_on_scores() < 1e-13
+                and pin_populate_head() < 1e-12 and pin_rel_frobenius() < 1e-12 and pin_round_bf16() == 0)
+    except (ValueError, IndexError, TypeError):   # a broken shape is a failed pin too
+        return False
 
 
 @pytest.mark.parametrize("mutation", [
     _mut_transposed_w, _mut_interleaved_heads, _mut_token_major_slab, _mut_bias_on_keys,
     _mut_sign_flip, _mut_mask_off_by_one, _mut_no_normalisation, _mut_missing_scale,
+    _mut_head_without_bias, _mut_head_neighbouring_block, _mut_frobenius_without_sqrt,
+    _mut_frobenius_squared_denominator, _mut_round_half_away, _mut_round_truncate,
 ])
 def test_planted_mistake_is_caught(monkeypatch, mutation):
     mutation(monkeypatch)
