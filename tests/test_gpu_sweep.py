@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from _gpu_common import DECODE_BF16_MAX_ABS, DECODE_F32_MAX_ABS, POPULATE_REL_FROB, dev, host
+from _gpu_common import DECODE_BF16_MAX_ABS, DECODE_F32_MAX_ABS, check_populate_head, dev, host
 from encoder_decoder_speech_gb300 import cxa
 from encoder_decoder_speech_gb300 import workloads as W
 from oracle import cross_attention as O
@@ -43,10 +43,9 @@ def test_sweep_point(T, B):
         c.populate(E, dev(WK), dev(WV), dev(bV))
         out = host(c.decode(dev(Q), dev(kl, torch.int32)))
         for (b, l, h) in picks:
-            Kr, Vr = O.populate_head(W.make_E(w, b, kl), WK[l], WV[l], bV[l], h)
             Kg, Vg = host(c.Kc[b, l, h]), host(c.Vc[b, l, h])
-            assert O.rel_frobenius(Kg, Kr) <= POPULATE_REL_FROB
-            assert O.rel_frobenius(Vg, Vr) <= POPULATE_REL_FROB
+            check_populate_head(Kg, Vg, W.make_E(w, b, kl), WK[l], WV[l], bV[l], h, "f32", cache_dtype,
+                                f"sweep T{T} B{B} ({b}, {l}, {h})")
             iso = O.attend_row(Q[b, l, h], Kg, Vg, int(kl[b]), w.scale)
             assert np.abs(out[b, l, h] - iso).max() <= TOL[cache_dtype]
         c.close()
