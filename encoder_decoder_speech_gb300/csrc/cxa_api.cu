@@ -24,12 +24,22 @@ struct cxa_cache {
   int B, T, L, H, dh;
   int dtype;
   std::vector<uint8_t> ready;   // populate sets, invalidate clears ("encoder_kv_ready")
+  // What filled the cache, fixed by the first successful writer: projections of
+  // encoder memory (cxa_populate) or self-attention rows (cxa_cache_append /
+  // cxa_self_attention_step). The other kind of writer is refused, so an append
+  // can never mark a stale (invalidated) cross-attention slot ready again.
+  int role;
 };
+
+namespace {
+constexpr int kRoleNone = 0, kRoleCross = 1, kRoleSelf = 2;
+}
 
 namespace {
 
 thread_local std::string g_last_msg;
 std::atomic<unsigned long long> g_launches{0};
+std::atomic<unsigned long long> g_timeouts_seen{0};
 
 int fail(int code, const std::string& msg) {
   g_last_msg = msg;
@@ -95,6 +105,8 @@ cudaError_t current_device_info(DeviceInfo* info, std::string* msg) {
 
 void set_last_error(const std::string& msg) { g_last_msg = msg; }
 
+unsigned long long timeout_epoch() { return g_timeouts_seen.load(std::memory_order_acquire); }
+
 bool cache_geometry(const cxa_cache* c, int* B, int* T, int* L, int* H, int* dh) {
   if (c == nullptr) return false;
   *B = c->B;
@@ -152,6 +164,7 @@ int cxa_cache_create(cxa_cache** out, void* Kc, void* Vc, int B, int T, int L, i
   c->dh = dh;
   c->dtype = cache_dtype;
   c->ready.assign(static_cast<size_t>(B), 0);
+  c->role = kRoleNone;
   *out = c;
   return CXA_OK;
 }
@@ -174,36 +187,60 @@ size_t cxa_decode_shared_workspace_bytes(int B, int T, int L, int H, int dh, int
   return cxa::decode_workspace_bytes(B, T, L, H, nq);
 }
 
-int cxa_populate(cxa_cache* c, int b0, int nb, const void* E, const void* WK, const void* WV,
-                 const float* bV, int T, int d, int L, int H, int in_dtype, void* workspace,
-                 size_t workspace_bytes, void* stream) {
-  if (c == nullptr) return fail(CXA_EINVAL, "cxa_populate: cache descriptor is NULL");
-  if (T <= 0) return fail(CXA_EINVAL, "cxa_populate: the encoder memory length T must be positive");
-  if (H <= 0 || H * c->dh != d)
-    return fail(CXA_EINVAL, "cxa_populate: num_heads * head_dim must equal the model width d");
-  if (T != c->T || L != c->L || H != c->H)
-    return fail(CXA_EINVAL, "cxa_populate: T, L, H do not match the cache descriptor");
-  if (nb <= 0 || b0 < 0 || b0 + nb > c->B)
-    return fail(CXA_EINVAL, "cxa_populate: slots [b0, b0+nb) out of range");
-  if (!valid_dtype(in_dtype)) return fail(CXA_EINVAL, "cxa_populate: in_dtype must be CXA_F32 or CXA_BF16");
-  if (E == nullptr || WK == nullptr || WV == nullptr || bV == nullptr || workspace == nullptr)
-    return fail(CXA_EINVAL, "cxa_populate: a pointer argument is NULL");
-  if (!aligned(E, 16) || !aligned(bV, 16) || !aligned(workspace, 256))
-    return fail(CXA_EINVAL, "cxa_populate: E and bV must be 16-byte aligned, the workspace 256-byte aligned");
+// Checks shared by the populate entry points (everything but the weights).
+static int populate_checks(const char* who, cxa_cache* c, int b0, int nb, const void* E, const float* bV, int T,
+                           int d, int L, int H, int in_dtype) {
+  const std::string w(who);
+  if (c == nullptr) return fail(CXA_EINVAL, w + ": cache descriptor is NULL");
+  if (T <= 0) return fail(CXA_EINVAL, w + ": the encoder memory length T must be positive");
+  if (H <= 0 || H * c->dh != d) return fail(CXA_EINVAL, w + ": num_heads * head_dim must equal the model width d");
+  if (T != c->T || L != c->L || H != c->H) return fail(CXA_EINVAL, w + ": T, L, H do not match the cache descriptor");
+  if (nb <= 0 || b0 < 0 || b0 + nb > c->B) return fail(CXA_EINVAL, w + ": slots [b0, b0+nb) out of range");
+  if (!valid_dtype(in_dtype)) return fail(CXA_EINVAL, w + ": in_dtype must be CXA_F32 or CXA_BF16");
+  if (E == nullptr || bV == nullptr) return fail(CXA_EINVAL, w + ": a pointer argument is NULL");
+  if (!aligned(E, 16) || !aligned(bV, 16)) return fail(CXA_EINVAL, w + ": E and bV must be 16-byte aligned");
+  if (c->role == kRoleSelf)
+    return fail(CXA_EINVAL, w + ": this cache holds self-attention rows (cxa_cache_append); populate a cache of "
+                                "its own");
+  return CXA_OK;
+}
+
+static int check_weights(const char* who, const void* WK, const void* WV, int in_dtype) {
+  const std::string w(who);
+  if (WK == nullptr || WV == nullptr) return fail(CXA_EINVAL, w + ": WK or WV is NULL");
   const int esz = in_dtype == CXA_BF16 ? 2 : 4;
   if (!aligned(WK, esz) || !aligned(WV, esz))
-    return fail(CXA_EINVAL, "cxa_populate: WK and WV must be aligned to their element size");
-  if (workspace_bytes < cxa::populate_workspace_bytes(d, L, in_dtype == CXA_BF16))
-    return fail(CXA_EINVAL, "cxa_populate: workspace smaller than cxa_populate_workspace_bytes()");
+    return fail(CXA_EINVAL, w + ": WK and WV must be aligned to their element size");
+  return CXA_OK;
+}
 
+static int check_packed(const char* who, const void* packed, size_t packed_bytes, int d, int L, int in_dtype) {
+  const std::string w(who);
+  if (packed == nullptr) return fail(CXA_EINVAL, w + ": the packed-weight buffer is NULL");
+  if (!aligned(packed, 256)) return fail(CXA_EINVAL, w + ": the packed-weight buffer must be 256-byte aligned");
+  if (packed_bytes < cxa::populate_workspace_bytes(d, L, in_dtype == CXA_BF16))
+    return fail(CXA_EINVAL, w + ": packed-weight buffer smaller than cxa_populate_workspace_bytes()");
+  return CXA_OK;
+}
+
+// Enqueue the populate GEMM from packed weights; the slots are not ready until it
+// is enqueued (and stay not ready if anything fails).
+static int populate_enqueue(const char* who, cxa_cache* c, int b0, int nb, const void* E, const void* WK,
+                            const void* WV, const void* packed, const float* bV, int T, int d, int L, int H,
+                            int in_dtype, void* stream) {
+  const std::string w(who);
   // New encoder memory: these slots are stale until the kernels are enqueued.
   for (int b = b0; b < b0 + nb; ++b) c->ready[static_cast<size_t>(b)] = 0;
 
   std::string msg;
   cxa::DeviceInfo dev;
   cudaError_t e = cxa::current_device_info(&dev, &msg);
-  if (e != cudaSuccess) return fail_cuda(e, "cxa_populate: " + msg);
-
+  if (e != cudaSuccess) return fail_cuda(e, w + ": " + msg);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (WK != nullptr) {   // pack into the caller's workspace first
+    e = cxa::launch_pack_weights(WK, WV, const_cast<void*>(packed), d, L, in_dtype == CXA_BF16, s);
+    if (e != cudaSuccess) return fail_cuda(e, w + ": weight packing launch");
+  }
   cxa::PopulateLaunch a;
   a.Kc = c->Kc;
   a.Vc = c->Vc;
@@ -211,7 +248,7 @@ int cxa_populate(cxa_cache* c, int b0, int nb, const void* E, const void* WK, co
   a.WK = WK;
   a.WV = WV;
   a.bV = bV;
-  a.wpack = workspace;
+  a.wpack = packed;
   a.b0 = b0;
   a.nb = nb;
   a.B = c->B;
@@ -221,13 +258,66 @@ int cxa_populate(cxa_cache* c, int b0, int nb, const void* E, const void* WK, co
   a.H = H;
   a.in_bf16 = in_dtype == CXA_BF16;
   a.cache_bf16 = c->dtype == CXA_BF16;
-  e = cxa::launch_populate(a, dev, static_cast<cudaStream_t>(stream), &msg);
+  e = cxa::launch_populate(a, dev, s, &msg);
   if (e != cudaSuccess) {
-    if (!msg.empty()) return fail(CXA_EINVAL, "cxa_populate: " + msg);
-    return fail_cuda(e, "cxa_populate: launch");
+    if (!msg.empty()) return fail(CXA_EINVAL, w + ": " + msg);
+    return fail_cuda(e, w + ": launch");
   }
   for (int b = b0; b < b0 + nb; ++b) c->ready[static_cast<size_t>(b)] = 1;
+  c->role = kRoleCross;
   return CXA_OK;
+}
+
+int cxa_populate(cxa_cache* c, int b0, int nb, const void* E, const void* WK, const void* WV,
+                 const float* bV, int T, int d, int L, int H, int in_dtype, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  int rc = populate_checks("cxa_populate", c, b0, nb, E, bV, T, d, L, H, in_dtype);
+  if (rc == CXA_OK) rc = check_weights("cxa_populate", WK, WV, in_dtype);
+  if (rc == CXA_OK) rc = check_packed("cxa_populate", workspace, workspace_bytes, d, L, in_dtype);
+  if (rc != CXA_OK) return rc;
+  return populate_enqueue("cxa_populate", c, b0, nb, E, WK, WV, workspace, bV, T, d, L, H, in_dtype, stream);
+}
+
+int cxa_pack_weights(const void* WK, const void* WV, int d, int L, int in_dtype, void* packed, size_t packed_bytes,
+                     void* stream) {
+  if (d <= 0 || d % 64 != 0 || L <= 0)
+    return fail(CXA_EINVAL, "cxa_pack_weights: d must be a positive multiple of 64 and L positive");
+  if (!valid_dtype(in_dtype)) return fail(CXA_EINVAL, "cxa_pack_weights: in_dtype must be CXA_F32 or CXA_BF16");
+  int rc = check_weights("cxa_pack_weights", WK, WV, in_dtype);
+  if (rc == CXA_OK) rc = check_packed("cxa_pack_weights", packed, packed_bytes, d, L, in_dtype);
+  if (rc != CXA_OK) return rc;
+  std::string msg;
+  cxa::DeviceInfo dev;
+  cudaError_t e = cxa::current_device_info(&dev, &msg);
+  if (e != cudaSuccess) return fail_cuda(e, "cxa_pack_weights: " + msg);
+  e = cxa::launch_pack_weights(WK, WV, packed, d, L, in_dtype == CXA_BF16, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "cxa_pack_weights: launch");
+  return CXA_OK;
+}
+
+int cxa_convert_bf16(const float* src, void* dst, size_t n, void* stream) {
+  if (src == nullptr || dst == nullptr) return fail(CXA_EINVAL, "cxa_convert_bf16: a pointer argument is NULL");
+  if (!aligned(src, 16) || !aligned(dst, 16))
+    return fail(CXA_EINVAL, "cxa_convert_bf16: src and dst must be 16-byte aligned");
+  if (n == 0) return CXA_OK;
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+  if (s0 < d0 + 2 * n && d0 < s0 + 4 * n) return fail(CXA_EINVAL, "cxa_convert_bf16: src and dst overlap");
+  std::string msg;
+  cxa::DeviceInfo dev;
+  cudaError_t e = cxa::current_device_info(&dev, &msg);
+  if (e != cudaSuccess) return fail_cuda(e, "cxa_convert_bf16: " + msg);
+  e = cxa::launch_convert_bf16(src, dst, n, dev, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "cxa_convert_bf16: launch");
+  return CXA_OK;
+}
+
+int cxa_populate_packed(cxa_cache* c, int b0, int nb, const void* E, const void* packed, size_t packed_bytes,
+                        const float* bV, int T, int d, int L, int H, int in_dtype, void* stream) {
+  int rc = populate_checks("cxa_populate_packed", c, b0, nb, E, bV, T, d, L, H, in_dtype);
+  if (rc == CXA_OK) rc = check_packed("cxa_populate_packed", packed, packed_bytes, d, L, in_dtype);
+  if (rc != CXA_OK) return rc;
+  return populate_enqueue("cxa_populate_packed", c, b0, nb, E, nullptr, nullptr, packed, bV, T, d, L, H, in_dtype,
+                          stream);
 }
 
 static int decode_common(const char* who, const cxa_cache* c, int l0, int nl, int nq, const float* Q,
@@ -310,6 +400,9 @@ int cxa_cache_append(cxa_cache* c, const int* pos, const float* K_new, const flo
     return fail(CXA_EINVAL, "cxa_cache_append: a pointer argument is NULL");
   if (!aligned(pos, 4) || !aligned(K_new, 16) || !aligned(V_new, 16))
     return fail(CXA_EINVAL, "cxa_cache_append: K_new and V_new must be 16-byte aligned");
+  if (c->role == kRoleCross)
+    return fail(CXA_EINVAL, "cxa_cache_append: this cache holds projections of encoder memory (cxa_populate); "
+                            "appending would mark its invalidated slots ready");
   std::string msg;
   cxa::DeviceInfo dev;
   cudaError_t e = cxa::current_device_info(&dev, &msg);
@@ -328,6 +421,7 @@ int cxa_cache_append(cxa_cache* c, const int* pos, const float* K_new, const flo
   e = cxa::launch_append(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "cxa_cache_append: launch");
   for (auto& r : c->ready) r = 1;
+  c->role = kRoleSelf;
   return CXA_OK;
 }
 
@@ -348,11 +442,19 @@ int cxa_self_attention_step(cxa_cache* c, const int* pos, const float* Q, const 
     return fail(CXA_EINVAL, "cxa_self_attention_step: a pointer argument is NULL");
   if (!aligned(pos, 4) || !aligned(K_new, 16) || !aligned(V_new, 16))
     return fail(CXA_EINVAL, "cxa_self_attention_step: K_new and V_new must be 16-byte aligned");
-  // appending makes every slot a valid (partly filled) self-attention cache
+  if (c->role == kRoleCross)
+    return fail(CXA_EINVAL, "cxa_self_attention_step: this cache holds projections of encoder memory "
+                            "(cxa_populate); appending would mark its invalidated slots ready");
+  // appending makes every slot a valid (partly filled) self-attention cache; the
+  // flags are restored if the step fails before anything is enqueued
+  std::vector<uint8_t> was = c->ready;
   for (auto& r : c->ready) r = 1;
   // one kernel: the append is fused into the decode over positions 0 .. pos[b]
-  return decode_common("cxa_self_attention_step", c, 0, -1, 1, Q, pos, out, scale, workspace, workspace_bytes,
-                       stream, 1, K_new, V_new);
+  const int rc = decode_common("cxa_self_attention_step", c, 0, -1, 1, Q, pos, out, scale, workspace,
+                               workspace_bytes, stream, 1, K_new, V_new);
+  if (rc == CXA_OK) c->role = kRoleSelf;
+  else c->ready.swap(was);
+  return rc;
 }
 
 int cxa_alignment_weights(const cxa_cache* c, const float* Q, const int* key_len, const int* heads_lh, int nsel,
@@ -505,6 +607,7 @@ int cxa_device_status(int clear) {
   unsigned int word = 0;
   if ((e = cudaMemcpy(&word, dev.status_word, sizeof(word), cudaMemcpyDeviceToHost)) != cudaSuccess)
     return fail_cuda(e, "cxa_device_status: read");
+  if (word) g_timeouts_seen.fetch_add(1, std::memory_order_acq_rel);
   if (clear) {
     const unsigned int zero = 0;
     if ((e = cudaMemcpy(dev.status_word, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess)

@@ -19,7 +19,7 @@ struct PopulateLaunch {
   const void* WK;      // [L][d][d] (d_in, d_out)
   const void* WV;
   const float* bV;     // [L][d]
-  void* wpack;         // workspace: [2*L*d][d] K-major packed weights
+  const void* wpack;   // [2*L*d][d] K-major packed weights (launch_pack_weights)
   int b0, nb, T, d, L, H;
   int B;               // slots of the cache (for the cache tensor maps)
   bool in_bf16;
@@ -114,6 +114,12 @@ size_t decode_workspace_bytes(int B, int T, int L, int H, int nq);
 // and describe it in *msg.
 cudaError_t launch_populate(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t stream,
                             std::string* msg);
+// WK/WV [L][d][d] (d_in, d_out) -> the K-major operand layout of the populate GEMM
+// (fp32 weights rounded to TF32), into wpack of populate_workspace_bytes(d, L, in_bf16).
+cudaError_t launch_pack_weights(const void* WK, const void* WV, void* wpack, int d, int L, bool in_bf16,
+                                cudaStream_t stream);
+// n fp32 values -> bf16 (round to nearest even); src and dst 16-byte aligned.
+cudaError_t launch_convert_bf16(const float* src, void* dst, size_t n, const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStream_t stream,
                           std::string* msg);
 cudaError_t launch_block(const BlockLaunch& a, const DeviceInfo& dev, cudaStream_t stream, std::string* msg);
@@ -135,6 +141,11 @@ size_t decode_counter_bytes(int B, int L, int H);
 
 // Geometry of a cache descriptor (false for a NULL descriptor).
 bool cache_geometry(const cxa_cache* c, int* B, int* T, int* L, int* H, int* dh);
+
+// Number of times cxa_device_status has found the status word set (a kernel's
+// bounded wait expired) in this process; scratch that a timed-out kernel may have
+// left dirty is cleared again when this number changes.
+unsigned long long timeout_epoch();
 
 // Records the calling thread's last failure text (cxa_last_error_message).
 void set_last_error(const std::string& msg);

@@ -87,9 +87,11 @@ CXA_API int cxa_cache_create(cxa_cache** out, void* Kc, void* Vc, int B, int T, 
 CXA_API void cxa_cache_destroy(cxa_cache* c);
 
 /*
- * Bytes of device workspace cxa_populate needs for width d, L layers and input
- * type in_dtype: the layer weights repacked once per call into the K-major
- * operand layout of the tensor-core GEMM (2*L*d*d elements of in_dtype).
+ * Bytes of the packed layer weights for width d, L layers and input type
+ * in_dtype: WK and WV of every layer in the K-major operand layout of the
+ * tensor-core GEMM (2*L*d*d elements of in_dtype). This is the size of
+ * cxa_populate's workspace (which it packs into on every call) and of the buffer
+ * cxa_pack_weights fills once for cxa_populate_packed.
  */
 CXA_API size_t cxa_populate_workspace_bytes(int d, int L, int in_dtype);
 
@@ -119,10 +121,59 @@ CXA_API size_t cxa_decode_workspace_bytes(int B, int T, int L, int H, int dh);
  * The slots are marked not ready first and ready again once both kernels are
  * enqueued without error, so a failed call leaves them not ready. Readiness is
  * stream-ordered: decode on the same stream (or after an event) sees the data.
+ * Refused with CXA_EINVAL on a cache that cxa_cache_append or
+ * cxa_self_attention_step has written (a self-attention cache).
+ *
+ * Two kernels: the weight packing into `workspace`, then the GEMM. A caller that
+ * populates many windows with the same weights packs them once instead
+ * (cxa_pack_weights) and calls cxa_populate_packed.
  */
 CXA_API int cxa_populate(cxa_cache* c, int b0, int nb, const void* E, const void* WK,
                  const void* WV, const float* bV, int T, int d, int L, int H,
                  int in_dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Pack the layer weights once into the operand layout of the populate GEMM.
+ * The decoder's WK_l / WV_l are static from one audio window to the next; only
+ * the encoder memory E changes ("The concept: one tensor, many consumers": E is
+ * projected once per layer at prefill, the weights belong to the model), so the
+ * repack is done once, when the weights are loaded, not per window.
+ *
+ *   WK, WV   device, [L][d][d] of in_dtype, indexed (d_in, d_out) as for
+ *            cxa_populate; d a positive multiple of 64.
+ *   packed, packed_bytes  device buffer of at least
+ *            cxa_populate_workspace_bytes(d, L, in_dtype) bytes, 256-byte aligned,
+ *            owned by the caller; it keeps the packed weights until the caller
+ *            overwrites it (fp32 weights are stored rounded to TF32, round to
+ *            nearest, ties away from zero).
+ * One kernel on `stream`. CXA_EINVAL for bad sizes or pointers.
+ */
+CXA_API int cxa_pack_weights(const void* WK, const void* WV, int d, int L, int in_dtype, void* packed,
+                             size_t packed_bytes, void* stream);
+
+/*
+ * cxa_populate from weights packed by cxa_pack_weights (same d, L and in_dtype):
+ * one kernel, the GEMM with its head-major epilogue. Arguments, ready-flag rules
+ * and errors as for cxa_populate; `packed` must hold the packed weights when the
+ * kernel runs (stream order).
+ */
+CXA_API int cxa_populate_packed(cxa_cache* c, int b0, int nb, const void* E, const void* packed,
+                                size_t packed_bytes, const float* bV, int T, int d, int L, int H,
+                                int in_dtype, void* stream);
+
+/*
+ * fp32 -> bf16 conversion, round to nearest even (NaN stays NaN, values beyond
+ * the largest bf16 round to infinity): the pass in front of the bf16 populate
+ * for an encoder memory that arrives in fp32 (the Whisper-large workload's
+ * E [1500, 1280] fp32 populated with bf16 tensor-core inputs), or for fp32
+ * weights before cxa_pack_weights with in_dtype CXA_BF16.
+ *
+ *   src   device fp32 [n], 16-byte aligned.
+ *   dst   device bf16 [n] (16-bit words), 16-byte aligned; must not overlap src.
+ * One kernel on `stream`; n == 0 enqueues nothing. CXA_EINVAL for NULL,
+ * misaligned or overlapping buffers.
+ */
+CXA_API int cxa_convert_bf16(const float* src, void* dst, size_t n, void* stream);
 
 /*
  * One decode step for every slot, layer and head.
@@ -199,7 +250,10 @@ CXA_API int cxa_decode_shared(const cxa_cache* c, int nq, const float* Q, const 
  *   pos      device int32 [B]; a slot whose pos is outside [0, T) is left as is.
  *   K_new, V_new  device fp32 [B][L][H][dh], 16-byte aligned (rounded to bf16
  *            for a bf16 cache).
- * Marks every slot ready. Asynchronous on stream.
+ * Marks every slot ready (each slot is a partly filled self-attention cache).
+ * Refused with CXA_EINVAL, launching nothing, on a cache that cxa_populate has
+ * written: marking its slots ready would un-refuse an invalidated cross-attention
+ * slot. Asynchronous on stream.
  */
 CXA_API int cxa_cache_append(cxa_cache* c, const int* pos, const float* K_new, const float* V_new,
                              void* stream);
@@ -209,7 +263,7 @@ CXA_API int cxa_cache_append(cxa_cache* c, const int* pos, const float* K_new, c
  * decode of Q over positions 0 .. pos[b] of every slot (key_len = pos + 1).
  * Arguments as for cxa_cache_append and cxa_decode (workspace of
  * cxa_decode_workspace_bytes size). Every argument is checked before anything
- * is enqueued.
+ * is enqueued; refused like cxa_cache_append on a populated cache.
  *
  * Launch overlap: one kernel, launched with programmatic dependent launch. It
  * streams slot b's cache rows t < min(pos[b], T) - 1 before the kernel just
@@ -348,14 +402,22 @@ CXA_API int cxa_selftest_wait_timeout(unsigned int limit_us, void* stream);
  * Arguments and results are those of cxa_decode without the workspace. The
  * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  * routine. Geometry whose scratch, cxa_decode_workspace_bytes(B, T, L, H, dh),
- * exceeds CXA_NOALLOC_SCRATCH_BYTES is rejected with CXA_EINVAL. Each call
- * clears the arrival counters (cudaMemsetAsync on `stream`) before its kernel.
- * All calls share the one array and it keeps the last call's contents, so
- * calls that may overlap on the GPU (different streams without ordering, or
- * several host threads) race and produce wrong results: order them on one
- * stream. The first call on a device looks up the array's device address with
- * that device current (cudaGetSymbolAddress); make that first call before any
- * stream capture begins.
+ * exceeds CXA_NOALLOC_SCRATCH_BYTES is rejected with CXA_EINVAL (and a head_dim
+ * other than 64 as unsupported geometry), launching nothing.
+ *
+ * Set-up and clearing: the first call in a CUDA context (per device; again after
+ * a device reset) looks up the array's device address with that device current
+ * (cudaGetSymbolAddress) and zeroes the array with one cudaMemsetAsync on
+ * `stream`; make that first call before any stream capture begins. After that,
+ * no call clears anything: the decode kernel leaves the arrival counters at zero
+ * whatever the geometry, so consecutive calls overlap through programmatic
+ * dependent launch exactly as cxa_decode's do. A kernel whose bounded wait
+ * expired may leave counters set; once cxa_device_status has reported
+ * CXA_ETIMEOUT, the next call zeroes the array again before its kernel.
+ *
+ * All calls share the one array and it keeps the last call's contents, so calls
+ * that may overlap on the GPU (different streams without ordering, or several
+ * host threads) race and produce wrong results: order them on one stream.
  */
 #define CXA_NOALLOC_SCRATCH_BYTES (8u << 20)
 
