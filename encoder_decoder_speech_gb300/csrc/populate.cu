@@ -10,7 +10,10 @@
 //   C[t, n] = sum_i E[t, i] * Wcat[i, n],   n = (kv*L + l)*d + h*64 + c
 // with M = T rows per slot, N = 2*L*d, K = d. Two kernels:
 //   1. pack_weights: WK/WV [L][d_in][d_out] -> Wp [2*L*d][d] (K-major, the
-//      operand layout the tensor core reads without a transpose flag).
+//      operand layout the tensor core reads without a transpose flag). The
+//      weights are static across audio windows ("The concept": only E changes),
+//      so a caller packs them once (cxa_pack_weights) and populates every later
+//      window from the packed copy (cxa_populate_packed); cxa_populate does both.
 //   2. populate_gemm: persistent, warp-specialised tcgen05 GEMM.
 //        warp 0     TMA producer (one thread): E tile 128 x 128 B and Wp tile
 //                   256 x 128 B per k-block, 128-byte swizzled, 4-stage ring.
@@ -410,6 +413,31 @@ __global__ void __launch_bounds__(kPackThreads)
   }
 }
 
+// fp32 -> bf16, round to nearest even: the conversion pass in front of the bf16
+// populate when the encoder memory (or a weight) arrives in fp32. Each thread
+// turns 8 values (two 16-byte loads) into one 16-byte store; the ragged tail of
+// n % 8 values is done one by one. HBM-bound: 6 bytes moved per value.
+constexpr int kConvertThreads = 256;
+
+__global__ void __launch_bounds__(kConvertThreads)
+    convert_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, size_t n) {
+  const size_t groups = n / 8;
+  const size_t stride = static_cast<size_t>(gridDim.x) * kConvertThreads;
+  for (size_t g = static_cast<size_t>(blockIdx.x) * kConvertThreads + threadIdx.x; g < groups; g += stride) {
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(src) + 2 * g);
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(src) + 2 * g + 1);
+    __nv_bfloat162 p0 = __floats2bfloat162_rn(a.x, a.y), p1 = __floats2bfloat162_rn(a.z, a.w);
+    __nv_bfloat162 p2 = __floats2bfloat162_rn(b.x, b.y), p3 = __floats2bfloat162_rn(b.z, b.w);
+    reinterpret_cast<uint4*>(dst)[g] =
+        make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
+                   *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
+  }
+  if (blockIdx.x == 0 && threadIdx.x < n % 8) {
+    const size_t i = groups * 8 + threadIdx.x;
+    dst[i] = __float2bfloat16_rn(src[i]);
+  }
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -449,7 +477,8 @@ cudaError_t run(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t str
   const int kKElems = 128 / esz;
   const int N = 2 * a.L * a.d;
 
-  // 1. tensor maps: E as (d, T, nb), Wp as (d, N); 128-byte rows, 128-byte swizzle
+  // 1. tensor maps: E as (d, T, nb), Wp (the packed weights) as (d, N); 128-byte
+  //    rows, 128-byte swizzle
   EncodeTiledFn encode = tensor_map_encoder(msg);
   if (encode == nullptr) return cudaErrorInvalidValue;
   const CUtensorMapDataType dt = kBF16In ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
@@ -471,7 +500,7 @@ cudaError_t run(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t str
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.d) * esz};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(kKElems), static_cast<cuuint32_t>(kBN)};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(&tmB, dt, 2, a.wpack, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    CUresult r = encode(&tmB, dt, 2, const_cast<void*>(a.wpack), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
       *msg = "cuTensorMapEncodeTiled failed for the packed weights (code " + std::to_string(static_cast<int>(r)) + ")";
@@ -482,16 +511,7 @@ cudaError_t run(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t str
   cudaError_t e = set_smem_attr_once<kBF16In>(dev.device);
   if (e != cudaSuccess) return e;
 
-  // 2. repack the weights (K-major) into the workspace
-  {
-    dim3 grid(a.d / kPackTile, a.d / kPackTile, 2 * a.L);
-    pack_weights_kernel<kBF16In><<<grid, kPackThreads, 0, stream>>>(a.WK, a.WV, a.wpack, a.d, a.L);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    count_launches(1);
-  }
-
-  // 3. the persistent GEMM
+  // 2. the persistent GEMM over the packed weights
   GemmParams p;
   p.Kc = a.Kc;
   p.Vc = a.Vc;
@@ -532,6 +552,31 @@ size_t populate_workspace_bytes(int d, int L, bool in_bf16) {
 cudaError_t launch_populate(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t stream,
                             std::string* msg) {
   return a.in_bf16 ? run<true>(a, dev, stream, msg) : run<false>(a, dev, stream, msg);
+}
+
+cudaError_t launch_convert_bf16(const float* src, void* dst, size_t n, const DeviceInfo& dev, cudaStream_t stream) {
+  const size_t groups = n / 8;
+  size_t grid = (groups + kConvertThreads - 1) / kConvertThreads;
+  const size_t cap = static_cast<size_t>(dev.num_sms) * 8;   // 8 resident CTAs of 256 threads per SM
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  convert_bf16_kernel<<<static_cast<unsigned int>(grid), kConvertThreads, 0, stream>>>(
+      src, static_cast<__nv_bfloat16*>(dst), n);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launches(1);
+  return e;
+}
+
+cudaError_t launch_pack_weights(const void* WK, const void* WV, void* wpack, int d, int L, bool in_bf16,
+                                cudaStream_t stream) {
+  const dim3 grid(d / kPackTile, d / kPackTile, 2 * L);
+  if (in_bf16)
+    pack_weights_kernel<true><<<grid, kPackThreads, 0, stream>>>(WK, WV, wpack, d, L);
+  else
+    pack_weights_kernel<false><<<grid, kPackThreads, 0, stream>>>(WK, WV, wpack, d, L);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launches(1);
+  return e;
 }
 
 }  // namespace cxa

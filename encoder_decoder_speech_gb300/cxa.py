@@ -29,6 +29,12 @@ SIGNATURES = {
     "cxa_populate": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "cxa_pack_weights": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "cxa_populate_packed": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                           ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "cxa_convert_bf16": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "cxa_decode": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
                                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "cxa_invalidate": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
@@ -146,6 +152,30 @@ def cxa_decode_workspace_bytes(B, T, L, H, dh=64) -> int:
 def cxa_populate(handle, b0, nb, E, WK, WV, bV, T, d, L, H, in_dtype, workspace, workspace_bytes, stream=None) -> int:
     return load().cxa_populate(handle, b0, nb, _ptr(E), _ptr(WK), _ptr(WV), _ptr(bV), T, d, L, H, in_dtype,
                                _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def cxa_pack_weights(WK, WV, d, L, in_dtype, packed, packed_bytes, stream=None) -> int:
+    return load().cxa_pack_weights(_ptr(WK), _ptr(WV), d, L, in_dtype, _ptr(packed), packed_bytes, _stream(stream))
+
+
+def cxa_populate_packed(handle, b0, nb, E, packed, packed_bytes, bV, T, d, L, H, in_dtype, stream=None) -> int:
+    return load().cxa_populate_packed(handle, b0, nb, _ptr(E), _ptr(packed), packed_bytes, _ptr(bV), T, d, L, H,
+                                      in_dtype, _stream(stream))
+
+
+def cxa_convert_bf16(src, dst, n, stream=None) -> int:
+    return load().cxa_convert_bf16(_ptr(src), _ptr(dst), n, _stream(stream))
+
+
+def to_bf16(x, out=None, stream=None):
+    """fp32 device tensor -> bf16 device tensor of the same shape (cxa_convert_bf16)."""
+    import torch
+    if x.dtype != torch.float32 or not x.is_contiguous():
+        raise ValueError("to_bf16 takes a contiguous float32 tensor")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    check(cxa_convert_bf16(x, out, x.numel(), stream), "cxa_convert_bf16")
+    return out
 
 
 def cxa_decode(handle, Q, key_len, out, scale, workspace, workspace_bytes, stream=None) -> int:
@@ -298,6 +328,27 @@ class CrossAttentionCache:
         ws = self.populate_workspace(in_dtype)
         check(cxa_populate(self.handle, b0, nb, E, WK, WV, bV, E.shape[-2], E.shape[-1], WK.shape[0],
                            self.H, in_dtype, ws, ws.numel(), stream), "cxa_populate")
+
+    def pack_weights(self, WK, WV, stream=None):
+        """Pack WK, WV [L, d, d] (d_in, d_out) once for populate_packed; returns the
+        packed buffer (a uint8 device tensor owned by the caller)."""
+        import torch
+        in_dtype = _dtype_code(WK.dtype)
+        if WV.dtype != WK.dtype or not WK.is_contiguous() or not WV.is_contiguous():
+            raise ValueError("WK and WV must be contiguous and of one dtype")
+        n = cxa_populate_workspace_bytes(self.d, self.L, in_dtype)
+        packed = torch.empty(n, dtype=torch.uint8, device=self.Kc.device)
+        check(cxa_pack_weights(WK, WV, self.d, self.L, in_dtype, packed, n, stream), "cxa_pack_weights")
+        return packed
+
+    def populate_packed(self, E, packed, bV, b0: int = 0, stream=None) -> None:
+        """E [nb, T, d] (fp32 or bf16, the dtype the weights were packed in); bV [L, d] fp32."""
+        in_dtype = _dtype_code(E.dtype)
+        if not E.is_contiguous() or not bV.is_contiguous():
+            raise ValueError("E and bV must be contiguous")
+        nb = E.shape[0] if E.dim() == 3 else 1
+        check(cxa_populate_packed(self.handle, b0, nb, E, packed, packed.numel(), bV, E.shape[-2], E.shape[-1],
+                                  self.L, self.H, in_dtype, stream), "cxa_populate_packed")
 
     def decode(self, Q, key_len, out=None, scale: float = 0.0, stream=None):
         """Q [B, L, H, 64] fp32, key_len [B] int32 (device). Returns out [B, L, H, 64] fp32."""

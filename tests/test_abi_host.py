@@ -140,3 +140,31 @@ def test_alignment_heads_marshalled_once_per_list():
     assert n == m == 2 and a is b and list(a) == [3, 1, 4, 2]
     c, k = cxa._heads_array([])
     assert k == 0
+
+
+def test_pack_weights_validates_before_any_cuda_call(cxa_lib):
+    n = cxa.cxa_populate_workspace_bytes(512, 6, cxa.CXA_F32)
+    assert cxa.cxa_pack_weights(FAKE, FAKE, 500, 6, cxa.CXA_F32, FAKE, n, 0) == cxa.CXA_EINVAL     # d % 64
+    assert cxa.cxa_pack_weights(0, FAKE, 512, 6, cxa.CXA_F32, FAKE, n, 0) == cxa.CXA_EINVAL        # NULL WK
+    assert cxa.cxa_pack_weights(FAKE, FAKE, 512, 6, 9, FAKE, n, 0) == cxa.CXA_EINVAL              # dtype
+    assert cxa.cxa_pack_weights(FAKE, FAKE, 512, 6, cxa.CXA_F32, FAKE + 16, n, 0) == cxa.CXA_EINVAL  # alignment
+    assert cxa.cxa_pack_weights(FAKE, FAKE, 512, 6, cxa.CXA_F32, FAKE, n - 1, 0) == cxa.CXA_EINVAL   # short
+    assert "smaller" in cxa.cxa_last_error_message()
+
+
+def test_populate_packed_validates_before_any_cuda_call(cxa_lib):
+    rc, h = make(B=2, T=1500, L=6, H=8)
+    n = cxa.cxa_populate_workspace_bytes(512, 6, cxa.CXA_F32)
+    args = dict(E=FAKE, packed=FAKE, nbytes=n, bV=FAKE)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return cxa.cxa_populate_packed(h, 0, 2, a["E"], a["packed"], a["nbytes"], a["bV"], 1500, 512, 6, 8,
+                                       cxa.CXA_F32, 0)
+    assert call(packed=0) == cxa.CXA_EINVAL
+    assert call(nbytes=n - 4) == cxa.CXA_EINVAL
+    assert call(E=FAKE + 4) == cxa.CXA_EINVAL
+    assert cxa.cxa_populate_packed(h, 1, 2, FAKE, FAKE, n, FAKE, 1500, 512, 6, 8, cxa.CXA_F32, 0) == cxa.CXA_EINVAL
+    assert cxa.cxa_populate_packed(h, 0, 2, FAKE, FAKE, n, FAKE, 1500, 512, 6, 4, cxa.CXA_F32, 0) == cxa.CXA_EINVAL
+    assert cxa.cxa_is_ready(h, 0) == 0 and cxa.cxa_is_ready(h, 1) == 0
+    cxa.cxa_cache_destroy(h)

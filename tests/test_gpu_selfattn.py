@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 import torch
 
-from _gpu_common import DECODE_BF16_MAX_ABS, DECODE_F32_MAX_ABS, dev, host
+from _gpu_common import DECODE_BF16_MAX_ABS, DECODE_F32_MAX_ABS, dev, host, inputs_on_device
 from encoder_decoder_speech_gb300 import cxa
 from encoder_decoder_speech_gb300 import workloads as W
 from oracle import cross_attention as O
@@ -112,3 +112,30 @@ def test_long_sequence_rewind_and_interleaved_decodes(cache_dtype):
                 for h in range(H):
                     ref = O.self_attention_steps(Qs[:, b, l, h], Ks[:, b, l, h], Vs[:, b, l, h])
                     assert np.abs(got[:, b, l, h] - ref).max() <= TOL[cache_dtype]
+
+
+def test_append_and_populate_refuse_each_others_cache():
+    """A populated (cross-attention) cache refuses appends, which would mark its
+    invalidated slots ready again; a self-attention cache refuses populate."""
+    w = W.custom("roles", B=2, T=64, d=128, L=1, H=2, index=942)
+    d, _ = inputs_on_device(w)
+    cross = cxa.CrossAttentionCache(w.B, w.T, w.L, w.H, 64, "f32")
+    cross.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    cross.invalidate(1)
+    pos = dev(np.array([3, 4], np.int32), torch.int32)
+    rows = dev(np.zeros((w.B, w.L, w.H, 64), np.float32))
+    launches = cxa.cxa_launch_count()
+    assert cxa.cxa_cache_append(cross.handle, pos, rows, rows) == cxa.CXA_EINVAL
+    out = torch.empty_like(rows)
+    assert cxa.cxa_self_attention_step(cross.handle, pos, rows, rows, rows, out, 0.0, cross.decode_ws,
+                                       cross.decode_ws_bytes) == cxa.CXA_EINVAL
+    assert cxa.cxa_launch_count() == launches
+    assert not cross.is_ready(1)
+    selfc = cxa.CrossAttentionCache(w.B, w.T, w.L, w.H, 64, "f32")
+    selfc.append(pos, rows, rows)
+    torch.cuda.synchronize()
+    assert selfc.is_ready(0) and selfc.is_ready(1)
+    ws = selfc.populate_workspace(cxa.CXA_F32)
+    rc = cxa.cxa_populate(selfc.handle, 0, w.B, d["E"], d["WK"], d["WV"], d["bV"], w.T, w.d, w.L, w.H, cxa.CXA_F32,
+                          ws, ws.numel())
+    assert rc == cxa.CXA_EINVAL
