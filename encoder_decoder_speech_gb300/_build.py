@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libcxa.so")
 
-SOURCES = ["cxa_api.cu", "populate.cu", "decode.cu", "decode_noalloc.cu", "block.cu", "append.cu", "alignment.cu", "decode_shared_tc.cu", "block_fused.cu"]
+SOURCES = ["cxa_api.cu", "populate.cu", "decode.cu", "decode_noalloc.cu", "block.cu", "append.cu", "alignment.cu", "decode_shared_tc.cu", "block_fused.cu", "decode_rows.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]

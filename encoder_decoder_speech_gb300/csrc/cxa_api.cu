@@ -40,6 +40,7 @@ namespace {
 thread_local std::string g_last_msg;
 std::atomic<unsigned long long> g_launches{0};
 std::atomic<unsigned long long> g_timeouts_seen{0};
+std::atomic<int> g_decode_policy{CXA_DECODE_AUTO};
 
 int fail(int code, const std::string& msg) {
   g_last_msg = msg;
@@ -106,6 +107,8 @@ cudaError_t current_device_info(DeviceInfo* info, std::string* msg) {
 void set_last_error(const std::string& msg) { g_last_msg = msg; }
 
 unsigned long long timeout_epoch() { return g_timeouts_seen.load(std::memory_order_acquire); }
+
+int decode_policy() { return g_decode_policy.load(std::memory_order_relaxed); }
 
 bool cache_geometry(const cxa_cache* c, int* B, int* T, int* L, int* H, int* dh) {
   if (c == nullptr) return false;
@@ -584,6 +587,13 @@ const char* cxa_strerror(int code) {
 const char* cxa_last_error_message(void) { return g_last_msg.c_str(); }
 
 unsigned long long cxa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int cxa_set_decode_policy(int policy) {
+  if (policy != CXA_DECODE_AUTO && policy != CXA_DECODE_STREAM && policy != CXA_DECODE_ROWS)
+    return fail(CXA_EINVAL, "cxa_set_decode_policy: unknown policy");
+  g_decode_policy.store(policy, std::memory_order_relaxed);
+  return CXA_OK;
+}
 
 int cxa_selftest_wait_timeout(unsigned int limit_us, void* stream) {
   if (limit_us < 1 || limit_us > 1000000)

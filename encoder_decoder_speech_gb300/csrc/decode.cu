@@ -996,6 +996,14 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStre
   prm.Knew = a.K_new;
   prm.Vnew = a.V_new;
   cudaError_t e;
+  if (a.nq == 1 && a.K_new == nullptr) {
+    // short streams (a single memory or a few): the latency shape, a cluster per row
+    if (decode_rows_eligible(a.B * a.nl * a.H, a.T, dev.num_sms, decode_policy())) {
+      bool done = false;
+      const cudaError_t er = launch_decode_rows(a, dev, stream, &done);
+      if (er != cudaSuccess || done) return er;
+    }
+  }
   if (a.K_new != nullptr)   // the self-attention step: append fused into a one-query decode
     e = a.cache_bf16 ? launch<true, 1, true>(prm, dev, stream) : launch<false, 1, true>(prm, dev, stream);
   else

@@ -124,6 +124,12 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DeviceInfo& dev, cudaStre
                           std::string* msg);
 cudaError_t launch_block(const BlockLaunch& a, const DeviceInfo& dev, cudaStream_t stream, std::string* msg);
 cudaError_t launch_append(const AppendLaunch& a, cudaStream_t stream);
+// The latency shape of the one-query decode (decode_rows.cu): a cluster of CTAs per
+// row. decode_rows_eligible says whether the policy lets `rows` rows of at most T
+// keys take it; launch_decode_rows then launches it and sets *done, or leaves
+// *done false (enqueuing nothing) when the rows' clusters cannot all be resident.
+bool decode_rows_eligible(int rows, int T, int num_sms, int policy);
+cudaError_t launch_decode_rows(const DecodeLaunch& a, const DeviceInfo& dev, cudaStream_t stream, bool* done);
 cudaError_t launch_decode_shared_tc(const DecodeLaunch& a, const DeviceInfo& dev, cudaStream_t stream,
                                     std::string* msg);
 cudaError_t launch_alignment(const AlignLaunch& a, const DeviceInfo& dev, cudaStream_t stream);
@@ -146,6 +152,9 @@ bool cache_geometry(const cxa_cache* c, int* B, int* T, int* L, int* H, int* dh)
 // bounded wait expired) in this process; scratch that a timed-out kernel may have
 // left dirty is cleared again when this number changes.
 unsigned long long timeout_epoch();
+
+// The process-wide decode shape policy (cxa_set_decode_policy).
+int decode_policy();
 
 // Records the calling thread's last failure text (cxa_last_error_message).
 void set_last_error(const std::string& msg);

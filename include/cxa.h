@@ -375,6 +375,32 @@ CXA_API unsigned long long cxa_launch_count(void);
 CXA_API int cxa_device_status(int clear);
 
 /*
+ * Which kernel shape runs a one-query decode (cxa_decode, cxa_decode_layers,
+ * cxa_decode_shared with nq = 1, cxa_decode_noalloc). Both compute the same
+ * result within the decode tolerance; they differ in speed:
+ *
+ *   CXA_DECODE_STREAM  the persistent split-T kernel: every valid 64-key chunk of
+ *                      every row numbered densely and dealt out in equal ranges to
+ *                      two CTAs per SM, split rows merged by the last arriving CTA.
+ *                      Bandwidth-optimal for long streams (batched memories).
+ *   CXA_DECODE_ROWS    the latency shape: a cluster of C CTAs per (slot, layer,
+ *                      head) row (C = SMs / rows, at most 8), every warp issuing its
+ *                      own copies, the cluster's states merged over distributed
+ *                      shared memory; no workspace is touched. Taken only when the
+ *                      rows fit on the SMs (rows <= SM count).
+ *   CXA_DECODE_AUTO    (default) the latency shape when the rows fit and the stream
+ *                      is short (rows x ceil(T / 64) <= 8 x SM count: one or a few
+ *                      memories), the persistent kernel otherwise.
+ *
+ * Process-wide; returns CXA_EINVAL for an unknown value. Host only.
+ */
+#define CXA_DECODE_AUTO   0
+#define CXA_DECODE_STREAM 1
+#define CXA_DECODE_ROWS   2
+
+CXA_API int cxa_set_decode_policy(int policy);
+
+/*
  * Failure-detection self-test (no counterpart in the source pages). Enqueues on
  * `stream` one kernel whose single waiting thread waits, through the same bounded
  * wait every kernel of this library uses, on a barrier that nothing completes;

@@ -26,6 +26,26 @@ POPULATE_C_STORE = {"f32": 2.0 ** -24, "bf16": 2.0 ** -8}
 POPULATE_BLOCK = {"f32": 2e-3, "bf16": 5e-3}
 
 
+POLICIES = {"auto": cxa.CXA_DECODE_AUTO, "stream": cxa.CXA_DECODE_STREAM, "rows": cxa.CXA_DECODE_ROWS}
+
+
+class decode_policy:
+    """Context manager: run the enclosed decodes with one kernel shape (the
+    persistent stream kernel or the cluster-per-row latency kernel), then go back
+    to the automatic choice."""
+
+    def __init__(self, name: str):
+        self.code = POLICIES[name]
+
+    def __enter__(self):
+        assert cxa.cxa_set_decode_policy(self.code) == cxa.CXA_OK
+        return self
+
+    def __exit__(self, *exc):
+        cxa.cxa_set_decode_policy(cxa.CXA_DECODE_AUTO)
+        return False
+
+
 def dev(x, dtype=torch.float32):
     return torch.from_numpy(np.ascontiguousarray(x)).to(device="cuda", dtype=dtype)
 

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 from _gpu_common import (DECODE_BF16_MAX_ABS, DECODE_F32_MAX_ABS, cache_for, check_populate, check_populate_head,
-                         dev, host, inputs_on_device)
+                         decode_policy, dev, host, inputs_on_device)
 from encoder_decoder_speech_gb300 import cxa
 from encoder_decoder_speech_gb300 import workloads as W
 from oracle import cross_attention as O
@@ -121,10 +121,12 @@ DECODE_CASES = [
 ]
 
 
+@pytest.mark.parametrize("shape", ["stream", "rows"])
 @pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("T,key_len", DECODE_CASES, ids=[f"T{c[0]}" for c in DECODE_CASES])
-def test_decode_kernel_isolated(T, key_len, cache_dtype):
-    got, ref = _decode_case(T, key_len, cache_dtype, seed=T)
+def test_decode_kernel_isolated(T, key_len, cache_dtype, shape):
+    with decode_policy(shape):
+        got, ref = _decode_case(T, key_len, cache_dtype, seed=T)
     err = np.abs(got - ref).max()
     assert err <= DECODE_TOL[cache_dtype], err
     for b, n in enumerate(key_len):
@@ -149,19 +151,21 @@ def test_decode_repeated_calls_share_the_workspace():
         assert np.abs(out - O.decode(Q, K, V, kl)).max() <= DECODE_F32_MAX_ABS
 
 
+@pytest.mark.parametrize("shape", ["stream", "rows"])
 @pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
-def test_padding_rows_are_never_read(cache_dtype):
+def test_padding_rows_are_never_read(cache_dtype, shape):
     """NaN / Inf in cache rows t >= key_len[b] must not reach the output."""
     w = W.custom("poison", B=3, T=500, d=128, L=2, H=2, ragged=True, index=922)
     c, d, _ = _populate(w, cache_dtype)
     Q = dev(W.make_Q(w, 0))
-    clean = c.decode(Q, d["key_len"]).clone()
     kl = W.make_key_len(w)
-    for b in range(w.B):
-        c.Kc[b, :, :, int(kl[b]):] = float("nan")
-        c.Vc[b, :, :, int(kl[b]):] = float("inf")
-    poisoned = c.decode(Q, d["key_len"])
-    torch.cuda.synchronize()
+    with decode_policy(shape):
+        clean = c.decode(Q, d["key_len"]).clone()
+        for b in range(w.B):
+            c.Kc[b, :, :, int(kl[b]):] = float("nan")
+            c.Vc[b, :, :, int(kl[b]):] = float("inf")
+        poisoned = c.decode(Q, d["key_len"])
+        torch.cuda.synchronize()
     assert torch.equal(clean, poisoned)
 
 
@@ -296,11 +300,12 @@ def test_large_sampled_heads():
         assert np.abs(out[b, l, hh] - e2e).max() <= DECODE_BF16_MAX_ABS
 
 
+@pytest.mark.parametrize("shape", ["stream", "rows", "alternate"])
 @pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
-def test_back_to_back_steps_without_sync(cache_dtype):
+def test_back_to_back_steps_without_sync(cache_dtype, shape):
     """Consecutive decode launches on one stream overlap (the next grid starts
     streaming the cache while the previous one finishes); every step's output
-    must still be exact."""
+    must still be exact, with either kernel shape or the two alternating."""
     w = W.custom("b2b", B=5, T=900, d=384, L=2, H=6, ragged=True, index=926)
     c, d, h = _populate(w, cache_dtype)
     Kg, Vg = host(c.Kc), host(c.Vc)
@@ -308,14 +313,17 @@ def test_back_to_back_steps_without_sync(cache_dtype):
     Qd = [dev(q) for q in Qs]
     outs = [torch.empty_like(Qd[0]) for _ in Qs]
     torch.cuda.synchronize()
-    for q, o in zip(Qd, outs):
-        c.decode(q, d["key_len"], out=o)
+    for i, (q, o) in enumerate(zip(Qd, outs)):
+        pick = shape if shape != "alternate" else ("stream", "rows")[i % 2]
+        with decode_policy(pick):
+            c.decode(q, d["key_len"], out=o)
     torch.cuda.synchronize()
     for q, o in zip(Qs, outs):
         assert np.abs(host(o) - O.decode(q, Kg, Vg, h["key_len"])).max() <= DECODE_TOL[cache_dtype]
 
 
-def test_chained_queries_read_after_the_previous_step():
+@pytest.mark.parametrize("shape", ["stream", "rows", "alternate"])
+def test_chained_queries_read_after_the_previous_step(shape):
     """Step k+1's query buffer is step k's output buffer: the next launch must
     not read Q before the previous grid has written it."""
     w = W.custom("chain", B=3, T=1100, d=256, L=2, H=4, ragged=True, index=927)
@@ -325,7 +333,9 @@ def test_chained_queries_read_after_the_previous_step():
     bufs = [dev(q0), torch.empty_like(dev(q0))]
     torch.cuda.synchronize()
     for k in range(10):
-        c.decode(bufs[k % 2], d["key_len"], out=bufs[(k + 1) % 2])
+        pick = shape if shape != "alternate" else ("stream", "rows")[k % 2]
+        with decode_policy(pick):
+            c.decode(bufs[k % 2], d["key_len"], out=bufs[(k + 1) % 2])
     torch.cuda.synchronize()
     ref = q0.astype(np.float64)
     for k in range(10):
