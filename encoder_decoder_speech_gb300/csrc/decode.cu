@@ -19,7 +19,9 @@
 //  * In each CTA a producer warp keeps a kStages-deep ring of shared-memory
 //    stages full with cp.async.bulk copies per chunk (K rows, V rows and the
 //    row's query rows, all contiguous) completing on a "full" mbarrier; the
-//    consumer warps read a stage and release it on its "empty" mbarrier.
+//    consumer warps read a stage and release it on its "empty" mbarrier. The
+//    copies of a stage are issued from separate lanes (one thread's bulk copies
+//    are processed one after another).
 //  * Each consumer lane group (16 lanes per fp32 key row, 8 or 16 per bf16 row)
 //    runs its own online softmax per query (running max m, sum s, accumulators)
 //    over the keys it is given, in fp32 and base 2 (q is pre-multiplied by
@@ -282,7 +284,6 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend
   const bool active = total > 0 && blockIdx.x < ranges;
   const long long g0 = active ? blockIdx.x * total / ranges : 0;
   const long long g1 = active ? (blockIdx.x + 1) * total / ranges : 0;
-  const bool producer = warp == kProducerWarp && lane == 0;
 
   // The order in which the CTA works through its range: when the range ends inside a
   // row, that trailing segment [gA, g1) first, then [g0, gA). Both rows the CTA shares
@@ -313,42 +314,61 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend
   // own dependency wait, so everything written before it is complete.
   const uint64_t pol = policy_evict_first();
   Cursor pcur{0, 0, 0};
-  Cursor pc{0, 0, 0};                    // the next chunk to pre-issue
   long long npre = 0, nissued = 0;
-  auto issue_stage = [&](long long i, const Cursor& c) {
-    const int kl = min(max(__ldg(p.key_len + c.b) + p.key_len_add, 0), p.T);
-    const int n = min(R::kChunkKeys, kl - c.c * R::kChunkKeys);
-    const long long crow = static_cast<long long>(c.b) * p.LHc + p.lh0 + c.lh;   // cache row
-    const size_t off = (static_cast<size_t>(crow) * p.T + static_cast<size_t>(c.c) * R::kChunkKeys) * R::kRowBytes;
-    const uint32_t kv_bytes = static_cast<uint32_t>(n) * R::kRowBytes;
-    const uint32_t full = smem_u32(&bars[i]);
-    const uint32_t dst = smem_u32(stages + i * R::kStageBytes);
-    mbar_arrive_expect_tx(full, 2 * kv_bytes + static_cast<uint32_t>(nq) * kQRowBytes);
-    bulk_g2s_hint(dst, p.Kc + off, kv_bytes, full, pol);
-    bulk_g2s_hint(dst + R::kKVBytes, p.Vc + off, kv_bytes, full, pol);
-  };
-  if (active && producer) {
-    pcur = locate(seq_g(0), s_first, s_nch, p.B);
-    pc = pcur;
-    npre = nAll < kStages ? nAll : kStages;
-    for (; nissued < npre; ++nissued) {
-      if constexpr (kAppend) {
-        const int kl = min(max(__ldg(p.key_len + pc.b) + p.key_len_add, 0), p.T);
-        const int end = pc.c * R::kChunkKeys + min(R::kChunkKeys, kl - pc.c * R::kChunkKeys);
-        if (end > min(__ldg(p.key_len + pc.b), p.T) - 1) break;   // may hold the previous step's row
-      }
-      issue_stage(nissued, pc);
-      step(pc, nissued);
+  // Stages [i0, i1) (at most kStages) go out from lane pairs of the producer warp:
+  // lane 2(i - i0) arms stage i and copies its K rows, lane 2(i - i0) + 1 its V rows
+  // (one thread's bulk copies are processed one after another, so a ring fill from
+  // one thread would take a copy's turn per row block). c is the cursor of position
+  // i0. Called by the whole producer warp.
+  auto issue_stages = [&](long long i0, long long i1, Cursor c) {
+    const long long i = i0 + (lane >> 1);
+    const bool act = i < i1;
+    for (long long k = i0; k < i && k < i1; ++k) step(c, k);
+    uint32_t full = 0, dst = 0, kv_bytes = 0;
+    size_t off = 0;
+    if (act) {
+      const int kl = min(max(__ldg(p.key_len + c.b) + p.key_len_add, 0), p.T);
+      const int n = min(R::kChunkKeys, kl - c.c * R::kChunkKeys);
+      const long long crow = static_cast<long long>(c.b) * p.LHc + p.lh0 + c.lh;   // cache row
+      off = (static_cast<size_t>(crow) * p.T + static_cast<size_t>(c.c) * R::kChunkKeys) * R::kRowBytes;
+      kv_bytes = static_cast<uint32_t>(n) * R::kRowBytes;
+      full = smem_u32(&bars[i]);
+      dst = smem_u32(stages + i * R::kStageBytes);
+      if ((lane & 1) == 0) mbar_arrive_expect_tx(full, 2 * kv_bytes + static_cast<uint32_t>(nq) * kQRowBytes);
     }
+    __syncwarp();
+    if (act) {
+      if ((lane & 1) == 0)
+        bulk_g2s_hint(dst, p.Kc + off, kv_bytes, full, pol);
+      else
+        bulk_g2s_hint(dst + R::kKVBytes, p.Vc + off, kv_bytes, full, pol);
+    }
+  };
+  Cursor pc{0, 0, 0};                    // kAppend: the first stage held back until the wait
+  if (active && warp == kProducerWarp) {
+    pcur = locate(seq_g(0), s_first, s_nch, p.B);
+    npre = nAll < kStages ? nAll : kStages;
+    long long pre_n = npre;
+    if constexpr (kAppend) {
+      Cursor c = pcur;
+      for (pre_n = 0; pre_n < npre; ++pre_n) {
+        const int kl = min(max(__ldg(p.key_len + c.b) + p.key_len_add, 0), p.T);
+        const int end = c.c * R::kChunkKeys + min(R::kChunkKeys, kl - c.c * R::kChunkKeys);
+        if (end > min(__ldg(p.key_len + c.b), p.T) - 1) break;   // may hold the previous step's row
+        step(c, pre_n);
+      }
+      pc = c;
+    }
+    issue_stages(0, pre_n, pcur);
+    nissued = pre_n;
   }
   if constexpr (kAppend) {
     wait_prior_grid();
     allow_dependent_launch();
-    if (active && producer)
-      for (; nissued < npre; ++nissued) {
-        issue_stage(nissued, pc);
-        step(pc, nissued);
-      }
+    if (active && warp == kProducerWarp) {
+      issue_stages(nissued, npre, pc);
+      nissued = npre;
+    }
   }
   // Q, out and the workspace may belong to the previous grid: wait for it.
   wait_prior_grid();
@@ -395,46 +415,51 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      Cursor cur = pcur;
-      for (long long i = 0; i < npre; ++i) {   // the queries of the pre-issued stages
-        const uint32_t qdst = smem_u32(stages + i * R::kStageBytes) + 2 * R::kKVBytes;
-        for (int n = 0; n < nq; ++n)
-          bulk_g2s(qdst + n * kQRowBytes, p.Q + qrow(cur.b, cur.lh, n) * kDh, kQRowBytes, smem_u32(&bars[i]));
-        step(cur, i);
+    // The whole warp: lane 0 arms each stage, lanes 0 and 1 copy its K and V rows and
+    // lanes 2 .. nq + 1 its query rows, so a stage's copies go out in parallel.
+    Cursor cur = pcur;
+    for (long long i = 0; i < npre; ++i) {   // the queries of the pre-issued stages
+      const uint32_t qdst = smem_u32(stages + i * R::kStageBytes) + 2 * R::kKVBytes;
+      const int qn = lane - static_cast<int>(i) * nq;
+      if (qn >= 0 && qn < nq)
+        bulk_g2s(qdst + qn * kQRowBytes, p.Q + qrow(cur.b, cur.lh, qn) * kDh, kQRowBytes, smem_u32(&bars[i]));
+      step(cur, i);
+    }
+    uint32_t armed = static_cast<uint32_t>((1u << npre) - 1u), armed_parity = 0;
+    bool ok = true;
+    for (long long i = npre; i < nAll; ++i) {
+      const int s = static_cast<int>(i % kStages);
+      const uint32_t parity = static_cast<uint32_t>((i / kStages) & 1);
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars[kStages + s]), parity ^ 1u, s_flags))) {
+        ok = false;
+        break;
       }
-      uint32_t armed = static_cast<uint32_t>((1u << npre) - 1u), armed_parity = 0;
-      bool ok = true;
-      for (long long i = npre; i < nAll; ++i) {
-        const int s = static_cast<int>(i % kStages);
-        const uint32_t parity = static_cast<uint32_t>((i / kStages) & 1);
-        if (!mbar_wait(smem_u32(&bars[kStages + s]), parity ^ 1u, s_flags)) {
-          ok = false;
-          break;
-        }
-        const int kl = min(max(__ldg(p.key_len + cur.b) + p.key_len_add, 0), p.T);
-        const int t0 = cur.c * R::kChunkKeys;
-        const int n = min(R::kChunkKeys, kl - t0);
-        const long long crow = static_cast<long long>(cur.b) * p.LHc + p.lh0 + cur.lh;   // cache row
-        const size_t off = (static_cast<size_t>(crow) * p.T + t0) * R::kRowBytes;
-        const uint32_t kv_bytes = static_cast<uint32_t>(n) * R::kRowBytes;
-        const uint32_t full = smem_u32(&bars[s]);
-        const uint32_t dst = smem_u32(stages + s * R::kStageBytes);
-        mbar_arrive_expect_tx(full, 2 * kv_bytes + static_cast<uint32_t>(nq) * kQRowBytes);
+      const int kl = min(max(__ldg(p.key_len + cur.b) + p.key_len_add, 0), p.T);
+      const int t0 = cur.c * R::kChunkKeys;
+      const int n = min(R::kChunkKeys, kl - t0);
+      const long long crow = static_cast<long long>(cur.b) * p.LHc + p.lh0 + cur.lh;   // cache row
+      const size_t off = (static_cast<size_t>(crow) * p.T + t0) * R::kRowBytes;
+      const uint32_t kv_bytes = static_cast<uint32_t>(n) * R::kRowBytes;
+      const uint32_t full = smem_u32(&bars[s]);
+      const uint32_t dst = smem_u32(stages + s * R::kStageBytes);
+      if (lane == 0) mbar_arrive_expect_tx(full, 2 * kv_bytes + static_cast<uint32_t>(nq) * kQRowBytes);
+      __syncwarp();
+      if (lane == 0)
         bulk_g2s_hint(dst, p.Kc + off, kv_bytes, full, pol);
+      else if (lane == 1)
         bulk_g2s_hint(dst + R::kKVBytes, p.Vc + off, kv_bytes, full, pol);
-        for (int qn = 0; qn < nq; ++qn)
-          bulk_g2s(dst + 2 * R::kKVBytes + qn * kQRowBytes, p.Q + qrow(cur.b, cur.lh, qn) * kDh, kQRowBytes, full);
-        armed |= 1u << s;
-        armed_parity = (armed_parity & ~(1u << s)) | (parity << s);
-        step(cur, i);
-      }
-      if (!ok) {
-        s_flags[0] = 1;
-        atomicOr(p.status, 1u);
-        for (int s = 0; s < kStages; ++s)   // let issued copies land before exiting
-          if (armed & (1u << s)) mbar_wait(smem_u32(&bars[s]), (armed_parity >> s) & 1u);
-      }
+      else if (lane - 2 < nq)
+        bulk_g2s(dst + 2 * R::kKVBytes + (lane - 2) * kQRowBytes, p.Q + qrow(cur.b, cur.lh, lane - 2) * kDh, kQRowBytes,
+                 full);
+      armed |= 1u << s;
+      armed_parity = (armed_parity & ~(1u << s)) | (parity << s);
+      step(cur, i);
+    }
+    if (!ok && lane == 0) {
+      s_flags[0] = 1;
+      atomicOr(p.status, 1u);
+      for (int s = 0; s < kStages; ++s)   // let issued copies land before exiting
+        if (armed & (1u << s)) mbar_wait(smem_u32(&bars[s]), (armed_parity >> s) & 1u);
     }
     __syncwarp();
   } else if (warp == kMergeWarp) {
