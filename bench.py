@@ -46,7 +46,7 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     p.add_argument("--no-variants", action="store_true", help="skip the bf16-cache variant")
     p.add_argument("--profile", choices=["decode", "decode_bf16", "populate", "shared_bf16", "shared_bf16_16", "shared_f32",
-                                          "align", "block", "selfattn"],
+                                          "align", "block", "selfattn", "decode_single", "decode_single_bf16"],
                    default=None,
                    help="run a few launches of one kernel on the workload's inputs (for ncu), print nothing else")
     p.add_argument("--sweep", action="store_true",
@@ -68,12 +68,13 @@ def parse_args(argv=None):
                         "Whisper-large dims (16 heads)")
     p.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--oracle-subset", choices=["large", "sweep"], default=None, help=argparse.SUPPRESS)
+    p.add_argument("--oracle-small", choices=["tiny", "base"], default=None, help=argparse.SUPPRESS)
     p.add_argument("--save", default=None, help=argparse.SUPPRESS)
     p.add_argument("--budget-s", type=float, default=12.0, help=argparse.SUPPRESS)
     p.add_argument("--max-slots", type=int, default=16, help=argparse.SUPPRESS)
     p.add_argument("--procs", type=int, default=1, help=argparse.SUPPRESS)
     a = p.parse_args(argv)
-    if a.warmup < 3 and not (a.oracle_sample or a.oracle_subset):
+    if a.warmup < 3 and not (a.oracle_sample or a.oracle_subset or a.oracle_small):
         p.error("--warmup must be >= 3")
     return a
 
@@ -350,6 +351,27 @@ def cpu_model() -> str:
         pass
     import platform
     return platform.processor() or platform.machine()
+
+
+def oracle_small_window(name: str):
+    """The oracle on one whole window of a single-memory workload (Whisper-Tiny dims:
+    populate + 1 step; Whisper-Base dims: populate + 64 steps), single-threaded."""
+    from encoder_decoder_speech_gb300 import workloads as W
+    from oracle import cross_attention as O
+    w = W.WORKLOADS[name]
+    E = W.make_E_all(w)
+    WK, WV, bV = W.make_weights(w)
+    kl = W.make_key_len(w)
+    Qs = [W.make_Q(w, s) for s in range(w.steps)]
+    t0 = time.perf_counter()
+    Kc, Vc = O.populate(E, WK, WV, bV, w.H)
+    t1 = time.perf_counter()
+    for s in range(w.steps):
+        O.decode(Qs[s], Kc, Vc, kl)
+    t2 = time.perf_counter()
+    return {"kind": "oracle", "cores": 1, "workload": name, "window_s": t2 - t0, "populate_s": t1 - t0,
+            "decode_s_per_step": (t2 - t1) / w.steps, "tokens_per_s": w.B * w.steps / (t2 - t0),
+            "sample": f"one whole window: fp64 populate + {w.steps} decode step(s), single thread"}
 
 
 def _oracle_env():
@@ -774,6 +796,14 @@ def run_small(args):
     from weights packed once is timed back to back (20 calls) and cold (mean of 20,
     CUDA events, launch latency included)."""
     import numpy as np
+    # the oracle on one window of each workload, in its own process, before any GPU work
+    oracle = {}
+    if not args.no_cpu_baseline:
+        for name in ("tiny", "base"):
+            r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-small", name, "--warmup", "0"],
+                               capture_output=True, text=True, env=_oracle_env(), timeout=1800)
+            if r.returncode == 0:
+                oracle[name] = json.loads(r.stdout.strip().splitlines()[-1])
     import torch
     from encoder_decoder_speech_gb300 import _build, cxa
     from encoder_decoder_speech_gb300 import workloads as W
@@ -872,7 +902,8 @@ def run_small(args):
                               **res["auto"], "stream_kernel": res["stream"],
                               "populate_ms": round(pop_ms, 4),
                               "populate_TFLOPs": round(populate_flops(w.L, w.d, w.B, w.T) / (pop_ms * 1e-3) / 1e12, 1),
-                              "populate_ms_cold": round(float(np.mean(pop_cold)), 4)}),
+                              "populate_ms_cold": round(float(np.mean(pop_cold)), 4),
+                              "cpu_baseline": oracle.get(name)}),
                   flush=True)
             cache.close()
     assert cxa.cxa_device_status(1) == cxa.CXA_OK
@@ -1025,6 +1056,31 @@ def run_selfattn(args):
                 line["host_us_per_step"] = round((h1 - h0) * 1e6 / T, 2)
             print(json.dumps(line), flush=True)
         del graph
+        # per position: a graph of 50 steps that all append and decode at one position
+        per_pos = {}
+        for ps in (0, 64, 256, T - 1):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                for s in range(3):
+                    cache.self_attention_step(pos[ps], Qs[s], Ks[s], Vs[s], out=out, stream=side)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=side):
+                for s in range(50):
+                    cache.self_attention_step(pos[ps], Qs[s % 4], Ks[s % 4], Vs[s % 4], out=out, stream=side)
+            torch.cuda.synchronize()
+            g.replay()
+            torch.cuda.synchronize()
+            a.record()
+            for _ in range(4):
+                g.replay()
+            b_.record()
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b_) * 1000.0 / 200
+            kv = 2 * rows * (ps + 1) * 64 * esz
+            per_pos[str(ps)] = {"us": round(us, 2), "kv_MB": round(kv / 1e6, 1), "GBps": round(kv / (us * 1e-6) / 1e9, 1)}
+            del g
+        print(json.dumps({"self_attention_step_per_position": {"cache_dtype": cd, "B": B, "L": L, "H": H,
+                                                               "max_seq_len": T}, "positions": per_pos}), flush=True)
         cache.close()
     assert cxa.cxa_device_status(1) == cxa.CXA_OK
     return 0
@@ -1125,6 +1181,18 @@ def run_profile(args):
     _build.build_library()
     cxa.load()
     torch.cuda.set_device(0)
+    if args.profile in ("decode_single", "decode_single_bf16"):
+        # the single-memory Whisper-Base decode (the latency-shaped kernel): populate,
+        # then three decode steps
+        w = W.WORKLOADS["base"]
+        (E, WK, WV, bV, kl, Q, _), _ = device_inputs(torch, W, w, 0)
+        cache = cxa.CrossAttentionCache(w.B, w.T, w.L, w.H, w.dh, "bf16" if args.profile.endswith("bf16") else "f32")
+        cache.populate(E, WK, WV, bV)
+        for s in range(3):
+            cache.decode(Q[s], kl)
+        torch.cuda.synchronize()
+        assert cxa.cxa_device_status(1) == cxa.CXA_OK
+        return 0
     w = W.WORKLOADS[WORKLOAD]
     (E, WK, WV, bV, kl, Q, _), _ = device_inputs(torch, W, w, 0)
     bf16 = args.profile in ("decode_bf16", "shared_bf16", "shared_bf16_16")
@@ -1340,6 +1408,9 @@ def main(argv=None):
     args = parse_args(argv)
     if args.oracle_subset:
         print(json.dumps(oracle_subset(args.oracle_subset, args.budget_s)))
+        return 0
+    if args.oracle_small:
+        print(json.dumps(oracle_small_window(args.oracle_small)))
         return 0
     if args.oracle_sample:
         if args.procs > 1:

@@ -1,4 +1,7 @@
 """Shared helpers of the GPU parity tests (device copies of seeded inputs)."""
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -131,3 +134,15 @@ def check_populate_head(Kg, Vg, E_b, WK_l, WV_l, bV_l, h: int, in_dtype: str, ca
     worst = max(check_populate_block(Kg, Kr, Ka, in_dtype, cache_dtype, what + " K"),
                 check_populate_block(Vg, Vr, Va, in_dtype, cache_dtype, what + " V"))
     return fk, fv, worst, Kr, Vr
+
+
+def record_parity(config: str, variant: str, **metrics):
+    """Append one JSON line of measured errors for a (config, variant) to the file
+    named by CXA_PARITY_RECORD, when it is set (a record of the parity run)."""
+    path = os.environ.get("CXA_PARITY_RECORD")
+    if not path:
+        return
+    with open(path, "a") as f:
+        f.write(json.dumps({"config": config, "variant": variant,
+                            **{k: (float(v) if isinstance(v, (int, float, np.floating)) else v)
+                               for k, v in metrics.items()}}) + "\n")

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 from _gpu_common import (DECODE_BF16_MAX_ABS, DECODE_F32_MAX_ABS, cache_for, check_populate, check_populate_head,
-                         decode_policy, dev, host, inputs_on_device)
+                         decode_policy, dev, host, inputs_on_device, record_parity)
 from encoder_decoder_speech_gb300 import cxa
 from encoder_decoder_speech_gb300 import workloads as W
 from oracle import cross_attention as O
@@ -67,6 +67,8 @@ def test_populate_tiny_config(cache_dtype):
     ek, ev, blk = check_populate(host(c.Kc), host(c.Vc), h["E"], h["WK"], h["WV"], h["bV"], w.H, "f32", cache_dtype,
                                  "tiny")
     print(f"tiny populate rel-frob K {ek:.3e} V {ev:.3e}, worst block {blk:.3e} ({cache_dtype} cache)")
+    record_parity("tiny", f"{cache_dtype} cache", populate_rel_frob_K=ek, populate_rel_frob_V=ev,
+                  populate_worst_block_ratio=blk)
 
 
 def test_populate_partial_slots_leave_others_untouched():
@@ -234,7 +236,7 @@ def test_config_end_to_end(name):
     w = W.WORKLOADS[name]
     c, d, h = _populate(w, "f32")
     Kg, Vg = host(c.Kc), host(c.Vc)
-    check_populate(Kg, Vg, h["E"], h["WK"], h["WV"], h["bV"], w.H, "f32", "f32", name)
+    ek, ev, blk = check_populate(Kg, Vg, h["E"], h["WK"], h["WV"], h["bV"], w.H, "f32", "f32", name)
     Kr, Vr = O.populate(h["E"], h["WK"], h["WV"], h["bV"], w.H)
     worst_iso = worst_e2e = 0.0
     for s in range(w.steps):
@@ -244,6 +246,9 @@ def test_config_end_to_end(name):
         if s < 4:
             worst_e2e = max(worst_e2e, np.abs(out - O.decode(Q, Kr, Vr, h["key_len"])).max())
     print(f"{name}: decode max-abs kernel-isolated {worst_iso:.2e}, end-to-end {worst_e2e:.2e}")
+    record_parity(name, "f32 cache", populate_rel_frob_K=ek, populate_rel_frob_V=ev, populate_worst_block_ratio=blk,
+                  decode_max_abs_kernel_isolated=worst_iso, decode_max_abs_end_to_end=worst_e2e,
+                  decode_steps_checked=w.steps)
     assert worst_iso <= DECODE_F32_MAX_ABS
 
 
@@ -260,12 +265,13 @@ def test_batched_base(cache_dtype):
     Qs = {s: W.make_Q(w, s) for s in steps}
     outs = {s: host(c.decode(dev(Qs[s]), d["key_len"])) for s in steps}
     kl = h["key_len"]
-    worst_iso = worst_e2e = worst_blk = 0.0
+    worst_iso = worst_e2e = worst_blk = worst_frob = 0.0
     for b in range(w.B):
         Kg, Vg = host(c.Kc[b:b + 1]), host(c.Vc[b:b + 1])
-        _, _, blk = check_populate(Kg, Vg, h["E"][b:b + 1], h["WK"], h["WV"], h["bV"], w.H, "f32", cache_dtype,
-                                   f"batched slot {b}")
+        fk, fv, blk = check_populate(Kg, Vg, h["E"][b:b + 1], h["WK"], h["WV"], h["bV"], w.H, "f32", cache_dtype,
+                                     f"batched slot {b}")
         worst_blk = max(worst_blk, blk)
+        worst_frob = max(worst_frob, fk, fv)
         Kr, Vr = O.populate(h["E"][b:b + 1], h["WK"], h["WV"], h["bV"], w.H)
         for s in steps:
             iso = O.decode(Qs[s][b:b + 1], Kg, Vg, kl[b:b + 1])
@@ -274,6 +280,9 @@ def test_batched_base(cache_dtype):
             worst_e2e = max(worst_e2e, float(np.abs(outs[s][b:b + 1] - e2e).max()))
     print(f"batched base ({cache_dtype} cache): worst populate block {worst_blk:.3e}, decode max-abs "
           f"kernel-isolated {worst_iso:.2e}, end-to-end {worst_e2e:.2e}")
+    record_parity("batched_base", f"{cache_dtype} cache", populate_worst_slot_rel_frob=worst_frob,
+                  populate_worst_block_ratio=worst_blk, decode_max_abs_kernel_isolated=worst_iso,
+                  decode_max_abs_end_to_end=worst_e2e, slots=w.B, decode_steps_checked=len(steps))
     assert worst_iso <= DECODE_TOL[cache_dtype]
     if cache_dtype == "bf16":
         assert worst_e2e <= DECODE_BF16_MAX_ABS
@@ -290,14 +299,21 @@ def test_large_sampled_heads():
                    | {(0, 0, 0), (w.B - 1, w.L - 1, w.H - 1)})
     Q = W.make_Q(w, 0)
     out = host(c.decode(dev(Q), d["key_len"]))
+    worst = dict(frob=0.0, blk=0.0, iso=0.0, e2e=0.0)
     for (b, l, hh) in heads:
         Kg, Vg = host(c.Kc[b, l, hh]), host(c.Vc[b, l, hh])
-        _, _, _, Kr, Vr = check_populate_head(Kg, Vg, h["E"][b], h["WK"][l], h["WV"][l], h["bV"][l], hh, "bf16",
-                                              "bf16", f"large ({b}, {l}, {hh})")
+        fk, fv, blk, Kr, Vr = check_populate_head(Kg, Vg, h["E"][b], h["WK"][l], h["WV"][l], h["bV"][l], hh, "bf16",
+                                                  "bf16", f"large ({b}, {l}, {hh})")
         iso = O.attend_row(Q[b, l, hh], Kg, Vg, w.T, w.scale)
         e2e = O.attend_row(Q[b, l, hh], Kr, Vr, w.T, w.scale)
+        worst = dict(frob=max(worst["frob"], fk, fv), blk=max(worst["blk"], blk),
+                     iso=max(worst["iso"], np.abs(out[b, l, hh] - iso).max()),
+                     e2e=max(worst["e2e"], np.abs(out[b, l, hh] - e2e).max()))
         assert np.abs(out[b, l, hh] - iso).max() <= DECODE_BF16_MAX_ABS
         assert np.abs(out[b, l, hh] - e2e).max() <= DECODE_BF16_MAX_ABS
+    record_parity("large", "bf16 inputs, bf16 cache", sampled_heads=len(heads), populate_worst_rel_frob=worst["frob"],
+                  populate_worst_block_ratio=worst["blk"], decode_max_abs_kernel_isolated=worst["iso"],
+                  decode_max_abs_end_to_end=worst["e2e"])
 
 
 @pytest.mark.parametrize("shape", ["stream", "rows", "alternate"])

@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from _gpu_common import DECODE_BF16_MAX_ABS, DECODE_F32_MAX_ABS, check_populate_head, dev, host
+from _gpu_common import DECODE_BF16_MAX_ABS, DECODE_F32_MAX_ABS, check_populate_head, dev, host, record_parity
 from encoder_decoder_speech_gb300 import cxa
 from encoder_decoder_speech_gb300 import workloads as W
 from oracle import cross_attention as O
@@ -42,12 +42,16 @@ def test_sweep_point(T, B):
         c = cxa.CrossAttentionCache(B, T, w.L, w.H, 64, cache_dtype)
         c.populate(E, dev(WK), dev(WV), dev(bV))
         out = host(c.decode(dev(Q), dev(kl, torch.int32)))
+        wf = wb = wi = 0.0
         for (b, l, h) in picks:
             Kg, Vg = host(c.Kc[b, l, h]), host(c.Vc[b, l, h])
-            check_populate_head(Kg, Vg, W.make_E(w, b, kl), WK[l], WV[l], bV[l], h, "f32", cache_dtype,
-                                f"sweep T{T} B{B} ({b}, {l}, {h})")
+            fk, fv, blk, _, _ = check_populate_head(Kg, Vg, W.make_E(w, b, kl), WK[l], WV[l], bV[l], h, "f32",
+                                                    cache_dtype, f"sweep T{T} B{B} ({b}, {l}, {h})")
             iso = O.attend_row(Q[b, l, h], Kg, Vg, int(kl[b]), w.scale)
+            wf, wb, wi = max(wf, fk, fv), max(wb, blk), max(wi, np.abs(out[b, l, h] - iso).max())
             assert np.abs(out[b, l, h] - iso).max() <= TOL[cache_dtype]
+        record_parity(f"sweep T{T} B{B}", f"{cache_dtype} cache", sampled_heads=len(picks),
+                      populate_worst_rel_frob=wf, populate_worst_block_ratio=wb, decode_max_abs_kernel_isolated=wi)
         c.close()
         del c
         torch.cuda.empty_cache()
