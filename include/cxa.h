@@ -425,8 +425,9 @@ CXA_API int cxa_selftest_wait_timeout(unsigned int limit_us, void* stream);
  * that loads the library holds CXA_NOALLOC_SCRATCH_BYTES of it until the
  * process exits.
  *
- * Arguments and results are those of cxa_decode without the workspace. The
- * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * Arguments and results are those of cxa_decode without the workspace (a short
+ * stream that cxa_decode would run on the cluster-per-row kernel, which needs no
+ * scratch, runs there too and leaves the array alone). The call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  * routine. Geometry whose scratch, cxa_decode_workspace_bytes(B, T, L, H, dh),
  * exceeds CXA_NOALLOC_SCRATCH_BYTES is rejected with CXA_EINVAL (and a head_dim
  * other than 64 as unsupported geometry), launching nothing.
