@@ -1244,6 +1244,34 @@ def run_profile(args):
     return 0
 
 
+def library_tf32_tflops(torch, n=8192, reps=10):
+    """The TF32 denominator measured the way the bf16 one is: a library fp32 matmul
+    of n^3 with TF32 tensor cores allowed, best of `reps` (a reference figure only;
+    nothing on the product path calls it)."""
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        a = torch.randn(n, n, device="cuda")
+        b = torch.randn(n, n, device="cuda")
+        c = torch.empty(n, n, device="cuda")
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b, c
+        torch.cuda.empty_cache()
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
 def window_psnr(torch, cxa, w, dev_inputs, oracle_path):
     """Informational parity of one whole window: the GPU's 128 decode outputs of
     the memory the oracle leg ran (populate from the packed weights, then every
@@ -1319,6 +1347,7 @@ def run_cxa(args):
             "decode_launch_us": v["decode_launch_us"], "populate_ms": v["populate_ms"]}
     e2e_ms, h2d, d2h, e2e_reps = measure_e2e(torch, cxa, w, host_inputs, dev_inputs[1:4], K, Wu, dist)
     large = None if args.no_variants else measure_populate_large(torch, cxa, W, Wu)
+    tf32_lib = None if args.no_variants else library_tf32_tflops(torch)
     parity = None
     if oracle_out is not None:
         parity = window_psnr(torch, cxa, w, dev_inputs, oracle_out)
@@ -1357,6 +1386,8 @@ def run_cxa(args):
                      "frac": pop_tflops / tf32_peak, "frac_of_burst": pop_tflops / tf32_burst,
                      "flops_per_call": pflops, "ms": main["populate_ms"],
                      "pack_weights_ms": main["pack_weights_ms"],
+                     "library_tf32_tflops": tf32_lib,
+                     "frac_of_library_tf32": None if tf32_lib is None else pop_tflops / tf32_lib,
                      "pack_note": "K-major repack of WK/WV, once per model load (timed apart, 10 calls)"},
         "populate_large_bf16": None if large is None else {
             "bound": "tensor", "kernel": "populate_gemm_kernel<bf16> + pack_weights",
