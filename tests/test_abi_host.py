@@ -168,3 +168,31 @@ def test_populate_packed_validates_before_any_cuda_call(cxa_lib):
     assert cxa.cxa_populate_packed(h, 0, 2, FAKE, FAKE, n, FAKE, 1500, 512, 6, 4, cxa.CXA_F32, 0) == cxa.CXA_EINVAL
     assert cxa.cxa_is_ready(h, 0) == 0 and cxa.cxa_is_ready(h, 1) == 0
     cxa.cxa_cache_destroy(h)
+
+
+def test_decode_policy_values(cxa_lib):
+    for p in (cxa.CXA_DECODE_AUTO, cxa.CXA_DECODE_STREAM, cxa.CXA_DECODE_ROWS):
+        assert cxa.cxa_set_decode_policy(p) == cxa.CXA_OK
+    assert cxa.cxa_set_decode_policy(3) == cxa.CXA_EINVAL
+    assert cxa.cxa_set_decode_policy(-1) == cxa.CXA_EINVAL
+    assert cxa.cxa_set_decode_policy(cxa.CXA_DECODE_AUTO) == cxa.CXA_OK
+
+
+def test_convert_bf16_validates_before_any_cuda_call(cxa_lib):
+    assert cxa.cxa_convert_bf16(0, FAKE, 8, 0) == cxa.CXA_EINVAL            # NULL source
+    assert cxa.cxa_convert_bf16(FAKE, 0, 8, 0) == cxa.CXA_EINVAL            # NULL destination
+    assert cxa.cxa_convert_bf16(FAKE + 4, FAKE + BIG, 8, 0) == cxa.CXA_EINVAL   # misaligned source
+    assert cxa.cxa_convert_bf16(FAKE, FAKE + BIG + 2, 8, 0) == cxa.CXA_EINVAL   # misaligned destination
+    assert cxa.cxa_convert_bf16(FAKE, FAKE + 16, 64, 0) == cxa.CXA_EINVAL      # overlap
+    assert "overlap" in cxa.cxa_last_error_message()
+    assert cxa.cxa_convert_bf16(FAKE, FAKE + BIG, 0, 0) == cxa.CXA_OK           # nothing to do, no CUDA call
+
+
+def test_noalloc_rejects_unsupported_geometry_before_any_cuda_call(cxa_lib):
+    # a descriptor with dh = 64 but scratch beyond the fixed maximum is refused with a
+    # message naming the maximum; the check comes before any CUDA call
+    rc, h = make(B=64, T=32768, L=6, H=8)
+    assert rc == cxa.CXA_OK
+    assert cxa.cxa_decode_noalloc(h, FAKE, FAKE, FAKE + 4096, 0.0, 0) == cxa.CXA_EINVAL
+    assert "fixed maximum" in cxa.cxa_last_error_message()
+    cxa.cxa_cache_destroy(h)
