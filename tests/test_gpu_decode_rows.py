@@ -1,7 +1,8 @@
 """The latency shape of the one-query decode (a cluster of C CTAs per (slot,
 layer, head) row, C the largest size up to 8 whose clusters are all resident)
 against the oracle, kernel-isolated: 1 to 300 rows, which take clusters of 8
-down to 1 CTA and both warp counts, key lengths 0, 1, fewer keys than CTAs in
+down to 1 CTA and both warp counts; rows long enough that every warp refills its
+ring many times; key lengths 0, 1, fewer keys than CTAs in
 the cluster, share boundaries inside a sub-chunk, the whole cache, beyond T and
 negative; both cache dtypes; a layer range; and the automatic choice, which
 must take the stream kernel once the rows no longer fit or the stream is long,
@@ -113,3 +114,18 @@ def test_automatic_choice_gives_the_same_result(geom):
     ref = O.decode(Q, K, V, kl)
     assert np.abs(a - ref).max() <= DECODE_F32_MAX_ABS
     assert np.abs(s - ref).max() <= DECODE_F32_MAX_ABS
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [3000, 8192])
+def test_rows_kernel_long_rows_refill_the_rings(T, cache_dtype):
+    """A single memory of 3000 or 8192 keys forced onto the latency shape: each warp
+    works through many sub-chunks, refilling its two stages, and the result agrees
+    with the oracle."""
+    B, L, H = 1, 6, 8
+    c, K, V = _filled(B, T, L, H, cache_dtype, seed=T + 1)
+    kl = np.array([T - 37], dtype=np.int32)
+    Q = np.random.default_rng(T).standard_normal((B, L, H, 64)).astype(np.float32)
+    with decode_policy("rows"):
+        out = host(c.decode(dev(Q), dev(kl, torch.int32)))
+    assert np.abs(out - O.decode(Q, K, V, kl)).max() <= TOL[cache_dtype]
