@@ -573,23 +573,35 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend
   } else if constexpr (R::kKeyLanes) {
     // ------------------------------------------------------------ consumers, several
     // queries on an fp32 cache: warp w takes keys 32*(w & 1) .. +32 of each chunk and
-    // queries (w >> 1)*QPW .. +QPW. Scores: lane = key, a whole 64-channel dot
-    // product per query, the lane's 16-byte K slices read in an order rotated by
-    // lane & 7 (eight lanes of distinct rows then cover all banks) with each query
-    // slice read at the same rotation (eight distinct slices: one wavefront). The
-    // probabilities go to shared memory; P.V: lane = channels 2l, 2l + 1.
+    // queries (w >> 1)*QPW .. +QPW. Scores are register-tiled: lane (kq, cgh, cgl,
+    // kg_lo) = lane bits (4, 3, 2, 1..0) accumulates a 4-key x QPW-query tile over the
+    // 16 channels of channel group cg = 2 cgh + cgl, for the keys of key group
+    // kg = 4 kq + kg_lo, each 16-byte slice read once for four keys or QPW queries.
+    // The slices are visited in an order rotated by kg_lo, so the eight lanes of a
+    // quarter warp (two channel groups x four rotations) read eight distinct bank
+    // groups. A reduce-scatter over lane bits 2 and 3 then leaves each lane the QPW
+    // whole scores of one key, 4 kg + 2 cgl + cgh. The probabilities go to shared
+    // memory by key. P.V: lane (kp, cq) = lane bits (4, 3..0) takes the keys of parity
+    // kp and channels 4cq .. 4cq + 3 (one 16-byte V slice and one probability
+    // broadcast per key for 4 x QPW products); the two parities meet at the row end.
     constexpr int QPW = kNQ / 2;
     static_assert(kConsumerWarps == 4 && R::kChunkKeys == 64 && (QPW == 2 || QPW == 3 || QPW % 4 == 0),
                   "two key halves x two query halves of a 64-key chunk");
     const int kh = warp & 1, qh = warp >> 1;
+    const int kg_lo = lane & 3, cgl = (lane >> 2) & 1, cgh = (lane >> 3) & 1;
+    const int kg = (lane >> 4) * 4 + kg_lo;            // key group: keys 4kg .. 4kg + 3 of the half
+    const int cg = cgh * 2 + cgl;                      // channel group: channels 16cg .. 16cg + 15
+    const int my_key = kg * 4 + 2 * cgl + cgh;         // the key whose scores this lane ends with
     float* s_pw = s_p + warp * 32 * QPW;   // this warp's probabilities, [32 keys][QPW]
+    const int kpar = lane >> 4, cq = lane & 15;       // P.V: key parity, channel quad
     Cursor cur = locate(seq_g(0), s_first, s_nch, p.B);
-    float m[QPW], lsum[QPW], acc[QPW][2];
+    float m[QPW], lsum[QPW], acc[QPW][4];
 #pragma unroll
     for (int qi = 0; qi < QPW; ++qi) {
       m[qi] = -INFINITY;
       lsum[qi] = 0.f;
-      acc[qi][0] = acc[qi][1] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[qi][c] = 0.f;
     }
     bool ok = true;
     int re = 0;                          // row ends handed to the merge warp so far
@@ -605,25 +617,50 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend
         const int kl = min(max(__ldg(p.key_len + cur.b) + p.key_len_add, 0), p.T);
         const int n = min(R::kChunkKeys, kl - cur.c * R::kChunkKeys);
         const uint8_t* sK = stages + s * R::kStageBytes;
-        const float* kp = reinterpret_cast<const float*>(sK + (kh * 32 + lane) * R::kRowBytes);
-        const float* qp = reinterpret_cast<const float*>(sK + 2 * R::kKVBytes) + qh * QPW * kDh;
-        float sc[QPW];
+        const float* kp = reinterpret_cast<const float*>(sK + (kh * 32 + kg * 4) * R::kRowBytes) + cg * 16;
+        const float* qp = reinterpret_cast<const float*>(sK + 2 * R::kKVBytes) + qh * QPW * kDh + cg * 16;
+        float part[4][QPW];
 #pragma unroll
-        for (int qi = 0; qi < QPW; ++qi) sc[qi] = 0.f;
+        for (int jk = 0; jk < 4; ++jk)
 #pragma unroll
-        for (int j = 0; j < kDh / 4; ++j) {
-          const int c4 = ((j + (lane & 7)) & (kDh / 4 - 1)) * 4;
-          const float4 kv = *reinterpret_cast<const float4*>(kp + c4);
+          for (int qi = 0; qi < QPW; ++qi) part[jk][qi] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c4 = ((j + kg_lo) & 3) * 4;
+          float4 kv[4];
+#pragma unroll
+          for (int jk = 0; jk < 4; ++jk) kv[jk] = *reinterpret_cast<const float4*>(kp + jk * kDh + c4);
 #pragma unroll
           for (int qi = 0; qi < QPW; ++qi) {
             const float4 qv = *reinterpret_cast<const float4*>(qp + qi * kDh + c4);
-            sc[qi] = fmaf(qv.x, kv.x, sc[qi]);
-            sc[qi] = fmaf(qv.y, kv.y, sc[qi]);
-            sc[qi] = fmaf(qv.z, kv.z, sc[qi]);
-            sc[qi] = fmaf(qv.w, kv.w, sc[qi]);
+#pragma unroll
+            for (int jk = 0; jk < 4; ++jk) {
+              part[jk][qi] = fmaf(qv.x, kv[jk].x, part[jk][qi]);
+              part[jk][qi] = fmaf(qv.y, kv[jk].y, part[jk][qi]);
+              part[jk][qi] = fmaf(qv.z, kv[jk].z, part[jk][qi]);
+              part[jk][qi] = fmaf(qv.w, kv[jk].w, part[jk][qi]);
+            }
           }
         }
-        const bool valid = kh * 32 + lane < n;
+        // reduce-scatter over the channel groups: lane bit 2 (cgl) keeps keys 2 cgl,
+        // 2 cgl + 1 of the tile, then lane bit 3 (cgh) keeps key 2 cgl + cgh
+        float half[2][QPW];
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int qi = 0; qi < QPW; ++qi) {
+            const float send = cgl ? part[t][qi] : part[2 + t][qi];
+            const float keep = cgl ? part[2 + t][qi] : part[t][qi];
+            half[t][qi] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+          }
+        float sc[QPW];
+#pragma unroll
+        for (int qi = 0; qi < QPW; ++qi) {
+          const float send = cgh ? half[0][qi] : half[1][qi];
+          const float keep = cgh ? half[1][qi] : half[0][qi];
+          sc[qi] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+        const bool valid = kh * 32 + my_key < n;
         float pw[QPW];
 #pragma unroll
         for (int qi = 0; qi < QPW; ++qi) {
@@ -633,51 +670,50 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend
           m[qi] = mnew;
           pw[qi] = valid ? exp2f(sv - mnew) : 0.f;
           lsum[qi] = fmaf(lsum[qi], corr, pw[qi]);
-          acc[qi][0] *= corr;
-          acc[qi][1] *= corr;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[qi][c] *= corr;
         }
         if constexpr (QPW % 4 == 0) {
 #pragma unroll
           for (int q4 = 0; q4 < QPW / 4; ++q4)
-            *reinterpret_cast<float4*>(s_pw + lane * QPW + 4 * q4) =
+            *reinterpret_cast<float4*>(s_pw + my_key * QPW + 4 * q4) =
                 make_float4(pw[4 * q4], pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]);
         } else if constexpr (QPW == 2) {
-          *reinterpret_cast<float2*>(s_pw + lane * QPW) = make_float2(pw[0], pw[1]);
+          *reinterpret_cast<float2*>(s_pw + my_key * QPW) = make_float2(pw[0], pw[1]);
         } else {
 #pragma unroll
-          for (int qi = 0; qi < QPW; ++qi) s_pw[lane * QPW + qi] = pw[qi];
+          for (int qi = 0; qi < QPW; ++qi) s_pw[my_key * QPW + qi] = pw[qi];
         }
         __syncwarp();
         const int nk = min(32, n - kh * 32);   // valid keys of this warp's half
-        const float* vp = reinterpret_cast<const float*>(sK + R::kKVBytes + kh * 32 * R::kRowBytes) + 2 * lane;
+        const float* vp = reinterpret_cast<const float*>(sK + R::kKVBytes + kh * 32 * R::kRowBytes) + 4 * cq;
 #pragma unroll 4
-        for (int k = 0; k < nk; ++k) {
-          const float2 v2 = *reinterpret_cast<const float2*>(vp + k * kDh);
-          if constexpr (QPW == 2) {
-            const float2 pk = *reinterpret_cast<const float2*>(s_pw + k * QPW);
-            acc[0][0] = fmaf(pk.x, v2.x, acc[0][0]);
-            acc[0][1] = fmaf(pk.x, v2.y, acc[0][1]);
-            acc[1][0] = fmaf(pk.y, v2.x, acc[1][0]);
-            acc[1][1] = fmaf(pk.y, v2.y, acc[1][1]);
-          } else if constexpr (QPW == 3) {
+        for (int k = kpar; k < nk; k += 2) {
+          const float4 v4 = *reinterpret_cast<const float4*>(vp + k * kDh);
+          float pk[QPW];
+          if constexpr (QPW % 4 == 0) {
 #pragma unroll
-            for (int qi = 0; qi < 3; ++qi) {
-              const float pk = s_pw[k * QPW + qi];
-              acc[qi][0] = fmaf(pk, v2.x, acc[qi][0]);
-              acc[qi][1] = fmaf(pk, v2.y, acc[qi][1]);
+            for (int q4 = 0; q4 < QPW / 4; ++q4) {
+              const float4 t = *reinterpret_cast<const float4*>(s_pw + k * QPW + 4 * q4);
+              pk[4 * q4] = t.x;
+              pk[4 * q4 + 1] = t.y;
+              pk[4 * q4 + 2] = t.z;
+              pk[4 * q4 + 3] = t.w;
             }
+          } else if constexpr (QPW == 2) {
+            const float2 t = *reinterpret_cast<const float2*>(s_pw + k * QPW);
+            pk[0] = t.x;
+            pk[1] = t.y;
+          } else {
+#pragma unroll
+            for (int qi = 0; qi < QPW; ++qi) pk[qi] = s_pw[k * QPW + qi];
           }
 #pragma unroll
-          for (int q4 = 0; q4 < QPW / 4; ++q4) {
-            const float4 pk = *reinterpret_cast<const float4*>(s_pw + k * QPW + 4 * q4);
-            acc[4 * q4 + 0][0] = fmaf(pk.x, v2.x, acc[4 * q4 + 0][0]);
-            acc[4 * q4 + 0][1] = fmaf(pk.x, v2.y, acc[4 * q4 + 0][1]);
-            acc[4 * q4 + 1][0] = fmaf(pk.y, v2.x, acc[4 * q4 + 1][0]);
-            acc[4 * q4 + 1][1] = fmaf(pk.y, v2.y, acc[4 * q4 + 1][1]);
-            acc[4 * q4 + 2][0] = fmaf(pk.z, v2.x, acc[4 * q4 + 2][0]);
-            acc[4 * q4 + 2][1] = fmaf(pk.z, v2.y, acc[4 * q4 + 2][1]);
-            acc[4 * q4 + 3][0] = fmaf(pk.w, v2.x, acc[4 * q4 + 3][0]);
-            acc[4 * q4 + 3][1] = fmaf(pk.w, v2.y, acc[4 * q4 + 3][1]);
+          for (int qi = 0; qi < QPW; ++qi) {
+            acc[qi][0] = fmaf(pk[qi], v4.x, acc[qi][0]);
+            acc[qi][1] = fmaf(pk[qi], v4.y, acc[qi][1]);
+            acc[qi][2] = fmaf(pk[qi], v4.z, acc[qi][2]);
+            acc[qi][3] = fmaf(pk[qi], v4.w, acc[qi][3]);
           }
         }
       }
@@ -703,7 +739,14 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend
           float S = lsum[qi];
 #pragma unroll
           for (int off = 16; off >= 1; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
-          *reinterpret_cast<float2*>(sl_red + (q * kSlotWarps + kh) * kDh + 2 * lane) = make_float2(acc[qi][0], acc[qi][1]);
+          float a4[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) a4[c] = acc[qi][c] + __shfl_xor_sync(0xffffffffu, acc[qi][c], 16);
+          if (kpar == 0) {   // the slots are 8-byte aligned: two 8-byte stores
+            float* dst = sl_red + (q * kSlotWarps + kh) * kDh + 4 * cq;
+            *reinterpret_cast<float2*>(dst) = make_float2(a4[0], a4[1]);
+            *reinterpret_cast<float2*>(dst + 2) = make_float2(a4[2], a4[3]);
+          }
           if (lane == 0) {
             sl_m[q * kSlotWarps + kh] = m[qi];
             sl_s[q * kSlotWarps + kh] = S;
@@ -717,7 +760,8 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend
         for (int qi = 0; qi < QPW; ++qi) {
           m[qi] = -INFINITY;
           lsum[qi] = 0.f;
-          acc[qi][0] = acc[qi][1] = 0.f;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[qi][c] = 0.f;
         }
       }
       step(cur, i);
