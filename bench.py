@@ -682,7 +682,7 @@ def measure_populate_large(torch, cxa, W, Wu, reps=10):
     cache.close()
     return {"ms": ms, "flops_per_call": populate_flops(w.L, w.d, w.B, w.T), "decode_us": dec_us,
             "decode_bytes": decode_bytes(w.L, w.H, w.dh, 2, kl_h, w.B), "B": w.B, "convert_ms": conv_ms,
-            "convert_bytes": E32.numel() * 6, "steps": steps}
+            "convert_bytes": E32.numel() * 6, "steps": steps, "T": w.T, "d": w.d, "L": w.L}
 
 
 def run_sweep(args):
@@ -1248,26 +1248,36 @@ def library_tf32_tflops(torch, n=8192, reps=10):
     """The TF32 denominator measured the way the bf16 one is: a library fp32 matmul
     of n^3 with TF32 tensor cores allowed, best of `reps` (a reference figure only;
     nothing on the product path calls it)."""
+    ms = library_matmul_ms(torch, n, n, n, torch.float32, reps, best=True)
+    return 2.0 * n ** 3 / (ms * 1e-3) / 1e12
+
+
+def library_matmul_ms(torch, M, K, N, dtype, reps=20, best=False):
+    """A library matmul [M, K] x [K, N] -> [M, N] in `dtype` (fp32 with TF32 tensor
+    cores allowed), median (or best) of `reps` CUDA-event timings: the same
+    contraction as a populate, without its head-major layout or bias, as a
+    reference figure only (nothing on the product path calls it)."""
     prev = torch.backends.cuda.matmul.allow_tf32
     torch.backends.cuda.matmul.allow_tf32 = True
     try:
-        a = torch.randn(n, n, device="cuda")
-        b = torch.randn(n, n, device="cuda")
-        c = torch.empty(n, n, device="cuda")
+        a = torch.randn(M, K, device="cuda", dtype=dtype)
+        b = torch.randn(K, N, device="cuda", dtype=dtype)
+        c = torch.empty(M, N, device="cuda", dtype=dtype)
         for _ in range(3):
             torch.matmul(a, b, out=c)
         torch.cuda.synchronize()
-        best = float("inf")
+        ts = []
         for _ in range(reps):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             torch.matmul(a, b, out=c)
             e1.record()
             torch.cuda.synchronize()
-            best = min(best, e0.elapsed_time(e1))
+            ts.append(e0.elapsed_time(e1))
         del a, b, c
         torch.cuda.empty_cache()
-        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+        ts.sort()
+        return ts[0] if best else ts[len(ts) // 2]
     finally:
         torch.backends.cuda.matmul.allow_tf32 = prev
 
@@ -1348,6 +1358,11 @@ def run_cxa(args):
     e2e_ms, h2d, d2h, e2e_reps = measure_e2e(torch, cxa, w, host_inputs, dev_inputs[1:4], K, Wu, dist)
     large = None if args.no_variants else measure_populate_large(torch, cxa, W, Wu)
     tf32_lib = None if args.no_variants else library_tf32_tflops(torch)
+    # the library on the populates' own contractions ([B*T, d] x [d, 2*L*d])
+    lib_base_ms = None if args.no_variants else library_matmul_ms(torch, w.B * w.T, w.d, 2 * w.L * w.d,
+                                                                  torch.float32)
+    lib_large_ms = None if large is None else library_matmul_ms(torch, large["B"] * large["T"], large["d"],
+                                                                2 * large["L"] * large["d"], torch.bfloat16)
     parity = None
     if oracle_out is not None:
         parity = window_psnr(torch, cxa, w, dev_inputs, oracle_out)
@@ -1388,6 +1403,10 @@ def run_cxa(args):
                      "pack_weights_ms": main["pack_weights_ms"],
                      "library_tf32_tflops": tf32_lib,
                      "frac_of_library_tf32": None if tf32_lib is None else pop_tflops / tf32_lib,
+                     "library_same_shape_ms": lib_base_ms,
+                     "library_same_shape_note": "torch.matmul fp32 (TF32 allowed) of the same [B*T, d] x "
+                                               "[d, 2*L*d] contraction, row-major output, no bias, median of 20",
+                     "speed_vs_library_same_shape": None if lib_base_ms is None else lib_base_ms / main["populate_ms"],
                      "pack_note": "K-major repack of WK/WV, once per model load (timed apart, 10 calls)"},
         "populate_large_bf16": None if large is None else {
             "bound": "tensor", "kernel": "populate_gemm_kernel<bf16> + pack_weights",
@@ -1395,7 +1414,9 @@ def run_cxa(args):
             "achieved": large["flops_per_call"] / (large["ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
             "peak": peaks["bf16_tflops"], "peak_note": f"{peaks['source']} bf16 burst",
             "frac": large["flops_per_call"] / (large["ms"] * 1e-3) / 1e12 / peaks["bf16_tflops"],
-            "ms": large["ms"], "convert_e_ms": large["convert_ms"],
+            "ms": large["ms"], "library_same_shape_ms": lib_large_ms,
+            "speed_vs_library_same_shape": None if lib_large_ms is None else lib_large_ms / large["ms"],
+            "convert_e_ms": large["convert_ms"],
             "convert_e_GBps": large["convert_bytes"] / (large["convert_ms"] * 1e-3) / 1e9,
             "convert_note": "E arrives in fp32: cxa_convert_bf16 (round to nearest even) before each populate, "
                             "timed apart; weights converted and packed once"},
