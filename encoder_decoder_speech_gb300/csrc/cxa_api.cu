@@ -41,6 +41,7 @@ thread_local std::string g_last_msg;
 std::atomic<unsigned long long> g_launches{0};
 std::atomic<unsigned long long> g_timeouts_seen{0};
 std::atomic<int> g_decode_policy{CXA_DECODE_AUTO};
+std::atomic<int> g_populate_policy{CXA_POPULATE_AUTO};
 
 int fail(int code, const std::string& msg) {
   g_last_msg = msg;
@@ -109,6 +110,7 @@ void set_last_error(const std::string& msg) { g_last_msg = msg; }
 unsigned long long timeout_epoch() { return g_timeouts_seen.load(std::memory_order_acquire); }
 
 int decode_policy() { return g_decode_policy.load(std::memory_order_relaxed); }
+int populate_policy() { return g_populate_policy.load(std::memory_order_relaxed); }
 
 bool cache_geometry(const cxa_cache* c, int* B, int* T, int* L, int* H, int* dh) {
   if (c == nullptr) return false;
@@ -592,6 +594,13 @@ int cxa_set_decode_policy(int policy) {
   if (policy != CXA_DECODE_AUTO && policy != CXA_DECODE_STREAM && policy != CXA_DECODE_ROWS)
     return fail(CXA_EINVAL, "cxa_set_decode_policy: unknown policy");
   g_decode_policy.store(policy, std::memory_order_relaxed);
+  return CXA_OK;
+}
+
+int cxa_set_populate_policy(int policy) {
+  if (policy != CXA_POPULATE_AUTO && policy != CXA_POPULATE_PAIR && policy != CXA_POPULATE_SINGLE)
+    return fail(CXA_EINVAL, "cxa_set_populate_policy: unknown policy");
+  g_populate_policy.store(policy, std::memory_order_relaxed);
   return CXA_OK;
 }
 

@@ -155,6 +155,8 @@ unsigned long long timeout_epoch();
 
 // The process-wide decode shape policy (cxa_set_decode_policy).
 int decode_policy();
+// The process-wide populate shape policy (cxa_set_populate_policy).
+int populate_policy();
 
 // Records the calling thread's last failure text (cxa_last_error_message).
 void set_last_error(const std::string& msg);

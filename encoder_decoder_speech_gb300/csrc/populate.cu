@@ -35,29 +35,42 @@
 #include <string>
 #include <type_traits>
 
+#include "cxa.h"
 #include "internal.h"
 #include "chunk_stream.cuh"
+#include "cluster.cuh"
 #include "ptx.cuh"
 
 namespace cxa {
 namespace {
 
-constexpr int kBM = 128;                       // rows (tokens) per tile = TMEM lanes
+constexpr int kBM = 128;                       // rows (tokens) per CTA and tile = TMEM lanes
 constexpr int kBN = 256;                       // columns per tile = 4 heads of 64
-constexpr int kStages = 4;
 constexpr uint32_t kRowBytes = 128;            // one k-block row: 32 fp32 / 64 bf16
 constexpr uint32_t kABytes = kBM * kRowBytes;  // 16 KB
-constexpr uint32_t kBBytes = kBN * kRowBytes;  // 32 KB
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kTmemCols = 2 * kBN;        // two accumulators
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
 constexpr uint32_t kBoxBytes = kBM * 128;      // one store box: the tile's 128 rows x 128 bytes
 constexpr uint32_t kStagingBytes = 2 * kBoxBytes;   // double-buffered, shared by the epilogue warps
 constexpr int kEpiBarrier = 1;                 // named barrier of the 4 epilogue warps
-constexpr int kNumBarriers = 2 * kStages + 4 + 1;
-constexpr size_t kSmemBytes =
-    1024 + size_t(kStages) * kStageBytes + kStagingBytes + 8 * kNumBarriers + 16;
+
+// One CTA per tile (kPair false: a 128 x 256 tile, 4-stage ring of 48 KB stages), or
+// a CTA pair per tile (kPair true: cta_group::2, a 256 x 256 tile whose A rows and B
+// rows are split between the two CTAs, so each stage holds 16 KB of A and 16 KB of
+// B and the ring is 6 deep).
+template <bool kPair>
+struct Shape {
+  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kTileM = kPair ? 2 * kBM : kBM;          // rows per tile
+  static constexpr uint32_t kBRows = kPair ? kBN / 2 : kBN;     // B rows one CTA loads
+  static constexpr uint32_t kBBytes = kBRows * kRowBytes;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr int kNumBarriers = 2 * kStages + 4 + 1;
+  static constexpr size_t kSmemBytes =
+      1024 + size_t(kStages) * kStageBytes + kStagingBytes + 8 * kNumBarriers + 16;
+  static_assert(kSmemBytes + 16 <= 227 * 1024, "dynamic + static shared memory fits one CTA");
+};
 
 struct GemmParams {
   void* Kc;
@@ -83,11 +96,16 @@ __device__ __forceinline__ void report_timeout(unsigned int* status, volatile in
   atomicOr(status, 1u);
 }
 
-template <bool kBF16In>
+template <bool kBF16In, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     populate_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB,
                          const GemmParams p) {
+  using S = Shape<kPair>;
+  constexpr int kStages = S::kStages;
+  constexpr int kNumBarriers = S::kNumBarriers;
+  constexpr uint32_t kBBytes = S::kBBytes;
+  constexpr uint32_t kStageBytes = S::kStageBytes;
   constexpr int kKElems = kBF16In ? 64 : 32;   // elements per 128-byte k-block row
   constexpr int kKStep = kBF16In ? 16 : 8;     // K of one MMA instruction
   constexpr int kMmasPerBlock = kKElems / kKStep;
@@ -112,6 +130,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // A pair: rank 0 (the even CTA) issues the MMAs and owns the full and accumulator-
+  // empty barriers both CTAs count on; rank 1 loads and drains its halves.
+  const uint32_t rank = kPair ? cluster_rank() : 0u;
+  const bool even = rank == 0;
+  const int tile0 = kPair ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+  const int tile_step = kPair ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -120,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);   // one arrival per epilogue warp
+      mbar_init(tempty_bar(a), kPair ? 2 * kEpiWarps : kEpiWarps);   // one arrival per epilogue warp
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -129,11 +153,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair)
+    cluster_sync();   // both CTAs' barriers are initialised before any cross-CTA arrival
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -144,19 +176,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int tile = tile0; ok && tile < p.num_tiles; tile += tile_step) {
         const int mtg = p.raster_n ? tile / (p.num_tiles / p.num_m_tiles) : tile % p.num_m_tiles;
         const int nt = p.raster_n ? tile % (p.num_tiles / p.num_m_tiles) : tile / p.num_m_tiles;
         const int slot = mtg / p.mt_per_slot;
         const int mt = mtg - slot * p.mt_per_slot;
+        const int row0 = mt * S::kTileM + static_cast<int>(rank) * kBM;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
-          tma_load_3d(sA + stage * kABytes, &tmA, full_bar(stage), kb * kKElems, mt * kBM, slot);
-          tma_load_2d(sB + stage * kBBytes, &tmB, full_bar(stage), kb * kKElems, nt * kBN);
+          if constexpr (kPair) {
+            // both halves complete on the even CTA's full barrier, which expects them both
+            if (even) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytes);
+            const uint32_t fb = mapa_shared(full_bar(stage), 0);
+            tma_load_3d_pair(sA + stage * kABytes, &tmA, fb, kb * kKElems, row0, slot);
+            tma_load_2d_pair(sB + stage * kBBytes, &tmB, fb, kb * kKElems,
+                             nt * kBN + static_cast<int>(rank * S::kBRows));
+          } else {
+            mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
+            tma_load_3d(sA + stage * kABytes, &tmA, full_bar(stage), kb * kKElems, row0, slot);
+            tma_load_2d(sB + stage * kBBytes, &tmB, full_bar(stage), kb * kKElems, nt * kBN);
+          }
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -167,22 +209,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) {
         report_timeout(p.status, abort_flag);
-        // Let every copy already issued land before the CTA can exit.
-        for (int s = 0; s < kStages; ++s)
-          if (armed & (1u << s)) mbar_wait(full_bar(s), (armed_parity >> s) & 1u);
+        // Let every copy already issued land before the CTA can exit (a pair's copies
+        // complete on the even CTA's barriers; the odd CTA then stays until the final
+        // cluster barrier, which the even CTA reaches after these waits).
+        if (!kPair || even)
+          for (int s = 0; s < kStages; ++s)
+            if (armed & (1u << s)) mbar_wait(full_bar(s), (armed_parity >> s) & 1u);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(kBF16In ? 1u : 2u, kBM, kBN);
+    if (lane == 0 && even) {
+      constexpr uint32_t idesc = make_idesc(kBF16In ? 1u : 2u, S::kTileM, kBN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int tile = tile0; ok && tile < p.num_tiles; tile += tile_step) {
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -202,25 +247,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t ad = smem_desc_k_sw128(a0 + k * kStepBytes);
             const uint64_t bd = smem_desc_k_sw128(b0 + k * kStepBytes);
             const uint32_t accumulate = (kb | k) != 0 ? 1u : 0u;
-            if constexpr (kBF16In)
-              mma_bf16(d_tmem, ad, bd, idesc, accumulate);
-            else
-              mma_tf32(d_tmem, ad, bd, idesc, accumulate);
+            if constexpr (kPair) {
+              if constexpr (kBF16In)
+                mma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
+              else
+                mma_tf32_pair(d_tmem, ad, bd, idesc, accumulate);
+            } else {
+              if constexpr (kBF16In)
+                mma_bf16(d_tmem, ad, bd, idesc, accumulate);
+              else
+                mma_tf32(d_tmem, ad, bd, idesc, accumulate);
+            }
           }
-          tc_commit(empty_bar(stage));   // frees the smem stage once these MMAs finish
+          // frees the smem stage (of both CTAs) once these MMAs finish
+          if constexpr (kPair)
+            tc_commit_pair(empty_bar(stage), 0x3);
+          else
+            tc_commit(empty_bar(stage));
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(tfull_bar(acc));       // accumulator ready for the epilogue
+        // accumulator ready for the epilogue (of both CTAs)
+        if constexpr (kPair)
+          tc_commit_pair(tfull_bar(acc), 0x3);
+        else
+          tc_commit(tfull_bar(acc));
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
       if (!ok) report_timeout(p.status, abort_flag);
       // Every MMA issued must complete before TMEM is released.
-      tc_commit(drain_bar);
+      if constexpr (kPair)
+        tc_commit_pair(drain_bar, 0x1);
+      else
+        tc_commit(drain_bar);
       if (!mbar_wait(drain_bar, 0)) report_timeout(p.status, abort_flag);
     }
     __syncwarp();
@@ -270,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       sbuf ^= 1;
     };
     __shared__ int s_epi_stop;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    for (int tile = tile0; tile < p.num_tiles; tile += tile_step) {
       // The four warps must take the same path through the tile (named barriers):
       // each reports its own wait's timeout, then one thread reads the abort flag
       // once for all of them.
@@ -285,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nt = p.raster_n ? tile % (p.num_tiles / p.num_m_tiles) : tile / p.num_m_tiles;
       const int slot = mtg / p.mt_per_slot;
       const int mt = mtg - slot * p.mt_per_slot;
-      const int t0 = mt * kBM;                  // first token of the tile
+      const int t0 = mt * S::kTileM + static_cast<int>(rank) * kBM;   // first token of this CTA's rows
       const int b = p.b0 + slot;
 #pragma unroll 1
       for (int g = 0; g < kBN / 64; ++g) {
@@ -346,7 +409,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (lane == 0) {
+        if constexpr (kPair)
+          mbar_arrive_cluster(tempty_bar(acc), 0);   // the even CTA's MMA waits for both CTAs
+        else
+          mbar_arrive(tempty_bar(acc));
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -354,10 +422,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair)
+    cluster_sync();   // neither CTA leaves while the pair's MMAs or arrivals may still touch it
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -458,17 +532,49 @@ EncodeTiledFn tensor_map_encoder(std::string* msg) {
   return fn;
 }
 
-template <bool kBF16In>
+template <bool kBF16In, bool kPair>
 cudaError_t set_smem_attr_once(int device) {
   static std::mutex mu;
   static bool done[128] = {};
   std::lock_guard<std::mutex> lock(mu);
   if (device >= 0 && device < 128 && done[device]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(populate_gemm_kernel<kBF16In>,
+  cudaError_t e = cudaFuncSetAttribute(populate_gemm_kernel<kBF16In, kPair>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
+                                       static_cast<int>(Shape<kPair>::kSmemBytes));
   if (e == cudaSuccess && device >= 0 && device < 128) done[device] = true;
   return e;
+}
+
+// CTA pairs of the pair kernel resident on the device at once (queried once per
+// device and input dtype), or -1 when pairs cannot be launched.
+template <bool kBF16In>
+int pair_clusters(const DeviceInfo& dev) {
+  static std::mutex mu;
+  static int cache[128] = {};
+  const int dv = dev.device >= 0 && dev.device < 128 ? dev.device : 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dv] != 0) return cache[dv];
+  }
+  int n = 0;
+  if (set_smem_attr_once<kBF16In, true>(dev.device) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Shape<true>::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, populate_gemm_kernel<kBF16In, true>, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  std::lock_guard<std::mutex> lock(mu);
+  cache[dv] = n > 0 ? n : -1;
+  return cache[dv];
 }
 
 template <bool kBF16In>
@@ -482,6 +588,17 @@ cudaError_t run(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t str
   EncodeTiledFn encode = tensor_map_encoder(msg);
   if (encode == nullptr) return cudaErrorInvalidValue;
   const CUtensorMapDataType dt = kBF16In ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  // CTA pairs (cta_group::2) wherever pairs can be resident and the policy allows
+  // them; one CTA per tile otherwise
+  const int policy = populate_policy();
+  const int pairs = policy == CXA_POPULATE_SINGLE ? 0 : pair_clusters<kBF16In>(dev);
+  if (policy == CXA_POPULATE_PAIR && pairs <= 0) {
+    *msg = "CTA pairs of the populate kernel cannot be resident on this device (policy CXA_POPULATE_PAIR)";
+    return cudaErrorInvalidValue;
+  }
+  const bool pair = pairs > 0;
+  const int tile_m = pair ? Shape<true>::kTileM : Shape<false>::kTileM;
+  const uint32_t b_rows = pair ? Shape<true>::kBRows : Shape<false>::kBRows;
   CUtensorMap tmA, tmB;
   {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.d), static_cast<cuuint64_t>(a.T), static_cast<cuuint64_t>(a.nb)};
@@ -498,7 +615,7 @@ cudaError_t run(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t str
   {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.d), static_cast<cuuint64_t>(N)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.d) * esz};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kKElems), static_cast<cuuint32_t>(kBN)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kKElems), static_cast<cuuint32_t>(b_rows)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = encode(&tmB, dt, 2, const_cast<void*>(a.wpack), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -508,7 +625,7 @@ cudaError_t run(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t str
     }
   }
 
-  cudaError_t e = set_smem_attr_once<kBF16In>(dev.device);
+  cudaError_t e = pair ? set_smem_attr_once<kBF16In, true>(dev.device) : set_smem_attr_once<kBF16In, false>(dev.device);
   if (e != cudaSuccess) return e;
 
   // 2. the persistent GEMM over the packed weights
@@ -522,7 +639,7 @@ cudaError_t run(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t str
   p.d = a.d;
   p.L = a.L;
   p.H = a.H;
-  p.mt_per_slot = (a.T + kBM - 1) / kBM;
+  p.mt_per_slot = (a.T + tile_m - 1) / tile_m;
   p.num_m_tiles = a.nb * p.mt_per_slot;
   const int num_n_tiles = (N + kBN - 1) / kBN;
   p.num_tiles = p.num_m_tiles * num_n_tiles;
@@ -535,9 +652,26 @@ cudaError_t run(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t str
   p.num_heads_total = 2 * a.L * a.H;
   p.cache_bf16 = a.cache_bf16 ? 1 : 0;
 
-  const int grid = p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms;
-  populate_gemm_kernel<kBF16In><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, p);
-  e = cudaGetLastError();
+  if (pair) {
+    const int clusters = p.num_tiles < pairs ? p.num_tiles : pairs;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Shape<true>::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, populate_gemm_kernel<kBF16In, true>, tmA, tmB, p);
+  } else {
+    const int grid = p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms;
+    populate_gemm_kernel<kBF16In, false><<<grid, kThreads, Shape<false>::kSmemBytes, stream>>>(tmA, tmB, p);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaSuccess;

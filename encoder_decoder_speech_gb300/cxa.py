@@ -18,6 +18,7 @@ from . import _build
 CXA_OK, CXA_EINVAL, CXA_ENOTREADY, CXA_ECUDA, CXA_ETIMEOUT = 0, -1, -2, -3, -4
 CXA_F32, CXA_BF16 = 0, 1
 CXA_DECODE_AUTO, CXA_DECODE_STREAM, CXA_DECODE_ROWS = 0, 1, 2
+CXA_POPULATE_AUTO, CXA_POPULATE_PAIR, CXA_POPULATE_SINGLE = 0, 1, 2
 
 # every symbol include/cxa.h declares: name -> (restype, argtypes)
 _c_void_pp = ctypes.POINTER(ctypes.c_void_p)
@@ -46,6 +47,7 @@ SIGNATURES = {
     "cxa_device_status": (ctypes.c_int, [ctypes.c_int]),
     "cxa_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint, ctypes.c_void_p]),
     "cxa_set_decode_policy": (ctypes.c_int, [ctypes.c_int]),
+    "cxa_set_populate_policy": (ctypes.c_int, [ctypes.c_int]),
     "cxa_decode_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                           ctypes.c_float, ctypes.c_void_p]),
     "cxa_decode_shared_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 6),
@@ -275,6 +277,11 @@ def cxa_device_status(clear=0) -> int:
 def cxa_set_decode_policy(policy: int) -> int:
     """Process-wide choice of the one-query decode kernel shape (CXA_DECODE_*)."""
     return load().cxa_set_decode_policy(policy)
+
+
+def cxa_set_populate_policy(policy: int) -> int:
+    """Process-wide choice of the populate GEMM shape (CXA_POPULATE_*)."""
+    return load().cxa_set_populate_policy(policy)
 
 
 def cxa_selftest_wait_timeout(limit_us: int, stream=None) -> int:

@@ -401,6 +401,28 @@ CXA_API int cxa_device_status(int clear);
 CXA_API int cxa_set_decode_policy(int policy);
 
 /*
+ * Which kernel shape runs the populate GEMM (cxa_populate, cxa_populate_packed).
+ * Both write bit-identical caches; they differ in speed:
+ *
+ *   CXA_POPULATE_PAIR    a cluster of two CTAs per 256 x 256 output tile sharing one
+ *                        tensor-core MMA (tcgen05 cta_group::2): each CTA holds 128
+ *                        rows of E and 128 columns of the packed weights per k-block,
+ *                        so an SM loads a third less operand data per product than
+ *                        with one CTA per tile. A populate returns CXA_EINVAL when
+ *                        pairs cannot be resident on the device.
+ *   CXA_POPULATE_SINGLE  one CTA per 128 x 256 output tile.
+ *   CXA_POPULATE_AUTO    (default) pairs when the device can hold them, one CTA per
+ *                        tile otherwise.
+ *
+ * Process-wide; returns CXA_EINVAL for an unknown value. Host only.
+ */
+#define CXA_POPULATE_AUTO   0
+#define CXA_POPULATE_PAIR   1
+#define CXA_POPULATE_SINGLE 2
+
+CXA_API int cxa_set_populate_policy(int policy);
+
+/*
  * Failure-detection self-test (no counterpart in the source pages). Enqueues on
  * `stream` one kernel whose single waiting thread waits, through the same bounded
  * wait every kernel of this library uses, on a barrier that nothing completes;

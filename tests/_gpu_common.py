@@ -32,6 +32,26 @@ POPULATE_BLOCK = {"f32": 2e-3, "bf16": 5e-3}
 POLICIES = {"auto": cxa.CXA_DECODE_AUTO, "stream": cxa.CXA_DECODE_STREAM, "rows": cxa.CXA_DECODE_ROWS}
 
 
+POPULATE_POLICIES = {"auto": cxa.CXA_POPULATE_AUTO, "pair": cxa.CXA_POPULATE_PAIR,
+                     "single": cxa.CXA_POPULATE_SINGLE}
+
+
+class populate_policy:
+    """Context manager: run the enclosed populates with one GEMM shape (CTA pairs
+    or one CTA per tile), then go back to the automatic choice."""
+
+    def __init__(self, name: str):
+        self.code = POPULATE_POLICIES[name]
+
+    def __enter__(self):
+        assert cxa.cxa_set_populate_policy(self.code) == cxa.CXA_OK
+        return self
+
+    def __exit__(self, *exc):
+        cxa.cxa_set_populate_policy(cxa.CXA_POPULATE_AUTO)
+        return False
+
+
 class decode_policy:
     """Context manager: run the enclosed decodes with one kernel shape (the
     persistent stream kernel or the cluster-per-row latency kernel), then go back

@@ -170,6 +170,15 @@ def test_populate_packed_validates_before_any_cuda_call(cxa_lib):
     cxa.cxa_cache_destroy(h)
 
 
+def test_populate_policy_values(cxa_lib):
+    for p in (cxa.CXA_POPULATE_AUTO, cxa.CXA_POPULATE_PAIR, cxa.CXA_POPULATE_SINGLE):
+        assert cxa.cxa_set_populate_policy(p) == cxa.CXA_OK
+    assert cxa.cxa_set_populate_policy(3) == cxa.CXA_EINVAL
+    assert "unknown policy" in cxa.cxa_last_error_message()
+    assert cxa.cxa_set_populate_policy(-1) == cxa.CXA_EINVAL
+    assert cxa.cxa_set_populate_policy(cxa.CXA_POPULATE_AUTO) == cxa.CXA_OK
+
+
 def test_decode_policy_values(cxa_lib):
     for p in (cxa.CXA_DECODE_AUTO, cxa.CXA_DECODE_STREAM, cxa.CXA_DECODE_ROWS):
         assert cxa.cxa_set_decode_policy(p) == cxa.CXA_OK

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 from _gpu_common import (DECODE_BF16_MAX_ABS, DECODE_F32_MAX_ABS, cache_for, check_populate, check_populate_head,
-                         decode_policy, dev, host, inputs_on_device, record_parity)
+                         decode_policy, dev, host, inputs_on_device, populate_policy, record_parity)
 from encoder_decoder_speech_gb300 import cxa
 from encoder_decoder_speech_gb300 import workloads as W
 from oracle import cross_attention as O
@@ -400,6 +400,37 @@ def test_populate_from_weights_packed_once(in_dtype, cache_dtype):
         assert torch.equal(a.Kc, b.Kc) and torch.equal(a.Vc, b.Vc)
         check_populate(host(b.Kc), host(b.Vc), Eh, h["WK"], h["WV"], h["bV"], w.H, in_dtype, cache_dtype,
                        f"packed window {window}")
+
+
+# (name, B, T, d, L, H, input dtype, cache dtype) for the two GEMM shapes
+POP_SHAPE_GEOMS = [
+    ("ragged_T", 3, 700, 256, 2, 4, "f32", "f32"),      # T not a multiple of the pair's 256-row tile
+    ("short_T", 2, 100, 128, 3, 2, "bf16", "bf16"),     # T <= 128: the odd CTA's rows all lie past T
+    ("half_n_tile", 2, 333, 192, 3, 3, "f32", "bf16"),  # 18 heads: the last 256-column tile is half empty
+]
+
+
+@pytest.mark.parametrize("geom", POP_SHAPE_GEOMS, ids=[g[0] for g in POP_SHAPE_GEOMS])
+def test_populate_pair_and_single_shapes_agree(geom):
+    """The CTA-pair GEMM (cta_group::2, forced with CXA_POPULATE_PAIR, which fails
+    rather than fall back) and the one-CTA GEMM write bit-identical caches that
+    pass the oracle gates, on edges of the pair's 256 x 256 tile."""
+    name, B, T, dm, L, H, in_dtype, cache_dtype = geom
+    w = W.custom(name, B=B, T=T, d=dm, L=L, H=H, ragged=True, in_dtype=in_dtype, index=942)
+    d, h = inputs_on_device(w)
+    caches = {}
+    for shape in ("single", "pair"):
+        c = cache_for(w, cache_dtype)
+        packed = c.pack_weights(d["WK"], d["WV"])
+        with populate_policy(shape):
+            c.populate_packed(d["E"], packed, d["bV"])
+        torch.cuda.synchronize()
+        caches[shape] = c
+    assert torch.equal(caches["single"].Kc, caches["pair"].Kc)
+    assert torch.equal(caches["single"].Vc, caches["pair"].Vc)
+    check_populate(host(caches["pair"].Kc), host(caches["pair"].Vc), h["E"], h["WK"], h["WV"], h["bV"], w.H,
+                   in_dtype, cache_dtype, name)
+    assert cxa.cxa_device_status(1) == cxa.CXA_OK
 
 
 def test_populate_packed_refuses_a_short_buffer():
