@@ -588,10 +588,16 @@ cudaError_t run(const PopulateLaunch& a, const DeviceInfo& dev, cudaStream_t str
   EncodeTiledFn encode = tensor_map_encoder(msg);
   if (encode == nullptr) return cudaErrorInvalidValue;
   const CUtensorMapDataType dt = kBF16In ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  // CTA pairs (cta_group::2) wherever pairs can be resident and the policy allows
-  // them; one CTA per tile otherwise
+  // CTA pairs (cta_group::2) when the policy asks for them, or under the automatic
+  // choice when pairs can be resident and the GEMM spans at least four waves of
+  // one-CTA tiles (measured on GB300: below that the pairs' 256-row tiles leave more
+  // SMs idle in the last wave than the halved operand loads save); one CTA per tile
+  // otherwise
   const int policy = populate_policy();
-  const int pairs = policy == CXA_POPULATE_SINGLE ? 0 : pair_clusters<kBF16In>(dev);
+  const long long single_tiles = static_cast<long long>(a.nb) * ((a.T + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+  const bool want_pair = policy == CXA_POPULATE_PAIR ||
+                         (policy == CXA_POPULATE_AUTO && single_tiles >= 4LL * dev.num_sms);
+  const int pairs = want_pair ? pair_clusters<kBF16In>(dev) : 0;
   if (policy == CXA_POPULATE_PAIR && pairs <= 0) {
     *msg = "CTA pairs of the populate kernel cannot be resident on this device (policy CXA_POPULATE_PAIR)";
     return cudaErrorInvalidValue;

@@ -411,8 +411,10 @@ CXA_API int cxa_set_decode_policy(int policy);
  *                        with one CTA per tile. A populate returns CXA_EINVAL when
  *                        pairs cannot be resident on the device.
  *   CXA_POPULATE_SINGLE  one CTA per 128 x 256 output tile.
- *   CXA_POPULATE_AUTO    (default) pairs when the device can hold them, one CTA per
- *                        tile otherwise.
+ *   CXA_POPULATE_AUTO    (default) pairs when the device can hold them and the GEMM
+ *                        has at least 4 x (SM count) one-CTA tiles (nb x ceil(T / 128)
+ *                        x ceil(2 L d / 256)); one CTA per tile for smaller GEMMs,
+ *                        where the pairs' larger tiles leave more SMs idle.
  *
  * Process-wide; returns CXA_EINVAL for an unknown value. Host only.
  */
