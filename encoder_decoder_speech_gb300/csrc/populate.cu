@@ -24,6 +24,11 @@
 //                   optionally round to bf16, stage 128-row boxes in shared
 //                   memory and write them with coalesced 16-byte stores to
 //                   Kc/Vc[b][l][h][t][:].
+//      For large GEMMs the same kernel runs on CTA pairs (clusters of two,
+//      tcgen05 cta_group::2): a 256 x 256 tile per pair, each CTA loading its 128
+//      rows of E and 128 of the tile's 256 weight rows per k-block (6-stage ring
+//      of 32 KB stages), the even CTA issuing the MMAs for both and signalling
+//      both CTAs' barriers, each CTA draining its own 128 accumulator rows.
 //      Tiles never straddle two encoder memories (M tiles are per slot; rows
 //      t >= T are zero-filled by TMA and never stored).
 #include <cuda.h>
