@@ -433,6 +433,30 @@ def test_populate_pair_and_single_shapes_agree(geom):
     assert cxa.cxa_device_status(1) == cxa.CXA_OK
 
 
+def test_populate_pair_partial_slots():
+    """A populate of slots [1, 3) of a 4-slot cache on CTA pairs writes those slots
+    exactly as one CTA per tile does and leaves slots 0 and 3 as they were."""
+    w = W.custom("pair_partial", B=4, T=600, d=256, L=2, H=4, ragged=True, index=943)
+    d, h = inputs_on_device(w)
+    E = d["E"][1:3].contiguous()
+    out = {}
+    for shape in ("single", "pair"):
+        c = cache_for(w, "f32")
+        c.Kc.fill_(7.0)
+        c.Vc.fill_(-7.0)
+        packed = c.pack_weights(d["WK"], d["WV"])
+        with populate_policy(shape):
+            c.populate_packed(E, packed, d["bV"], b0=1)
+        torch.cuda.synchronize()
+        assert [c.is_ready(b) for b in range(w.B)] == [False, True, True, False]
+        for b in (0, 3):
+            assert bool((c.Kc[b] == 7.0).all()) and bool((c.Vc[b] == -7.0).all())
+        out[shape] = c
+    assert torch.equal(out["single"].Kc, out["pair"].Kc) and torch.equal(out["single"].Vc, out["pair"].Vc)
+    check_populate(host(out["pair"].Kc[1:3]), host(out["pair"].Vc[1:3]), h["E"][1:3], h["WK"], h["WV"], h["bV"],
+                   w.H, "f32", "f32", "pair partial")
+
+
 def test_populate_packed_refuses_a_short_buffer():
     w = W.custom("packed_short", B=1, T=64, d=128, L=2, H=2, index=941)
     d, _ = inputs_on_device(w)
