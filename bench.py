@@ -427,7 +427,8 @@ def run_reference(args):
         "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * res["seconds"] / max(res["slots"], 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy, Whisper-Base shapes)",
-        "config": workload_config(w, "f64 (oracle)"),
+        "config": dict(workload_config(w, "f64 (oracle)"), populate_inputs="fp32 inputs, fp64 arithmetic (oracle)",
+                       l2="host memory (the oracle runs on the CPU)"),
         "cpu_baseline": cpu_baseline_obj(res),
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
