@@ -407,6 +407,7 @@ POP_SHAPE_GEOMS = [
     ("ragged_T", 3, 700, 256, 2, 4, "f32", "f32"),      # T not a multiple of the pair's 256-row tile
     ("short_T", 2, 100, 128, 3, 2, "bf16", "bf16"),     # T <= 128: the odd CTA's rows all lie past T
     ("half_n_tile", 2, 333, 192, 3, 3, "f32", "bf16"),  # 18 heads: the last 256-column tile is half empty
+    ("bf16_in_f32_cache", 3, 520, 128, 2, 2, "bf16", "f32"),  # the fourth dtype combination
 ]
 
 
