@@ -1,0 +1,99 @@
+"""Decode with extreme logits, checked against the oracle on the very cache the
+GPU holds: in every (slot, layer, head) row one key is planted along that row's
+query, so its score is about +200 and the softmax row is one-hot up to e^-190.
+The planted key sits first in the row, last among its valid keys, or in between,
+so the running maximum moves at the start, at the very end or in the middle of a
+row (and of a row split across CTAs, whose segments then merge with maxima
+hundreds apart). Every other key keeps its ordinary score. A kernel that lets a
+stale maximum through, drops a rescale or mis-weights a segment returns a mix of
+V rows instead of the planted key's row."""
+import numpy as np
+import pytest
+import torch
+
+from _gpu_common import DECODE_BF16_MAX_ABS, DECODE_F32_MAX_ABS, cache_for, decode_policy, dev, host, inputs_on_device
+from encoder_decoder_speech_gb300 import cxa
+from encoder_decoder_speech_gb300 import workloads as W
+from oracle import cross_attention as O
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": DECODE_F32_MAX_ABS, "bf16": DECODE_BF16_MAX_ABS}
+SPIKE_SCORE = 200.0   # scale * q.k of the planted key (natural-log units)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cxa_lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    yield
+    torch.cuda.synchronize()
+    assert cxa.cxa_device_status(1) == cxa.CXA_OK
+
+
+def _plant(c, q_rows, key_len):
+    """Set one key per (slot, layer, head) row of the cache to a multiple of that
+    row's query q_rows [B, L, H, 64], scaled so that 0.125 * q.k = SPIKE_SCORE.
+    Returns the planted positions [B, L, H] (-1 for an empty slot)."""
+    B, L, H = q_rows.shape[:3]
+    pos = np.full((B, L, H), -1, dtype=np.int64)
+    Kc = c.Kc
+    for b in range(B):
+        n = int(min(max(key_len[b], 0), c.T))
+        if n == 0:
+            continue
+        for l in range(L):
+            for h in range(H):
+                choice = (l * H + h) % 3
+                t = 0 if choice == 0 else (n - 1 if choice == 1 else (b * 31 + l * 7 + h * 3) % n)
+                q = q_rows[b, l, h].astype(np.float64)
+                alpha = SPIKE_SCORE / (0.125 * float(q @ q))
+                Kc[b, l, h, t] = torch.from_numpy((alpha * q).astype(np.float32)).to(Kc.device, Kc.dtype)
+                pos[b, l, h] = t
+    return pos
+
+
+def _workload(index):
+    return W.custom("large_logits", B=5, T=900, d=256, L=2, H=4, ragged=True, index=index)
+
+
+@pytest.mark.parametrize("shape", ["stream", "rows"])
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+def test_decode_one_hot_rows(shape, cache_dtype):
+    w = _workload(950)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, cache_dtype)
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    Qh = W.make_Q(w, 0)
+    pos = _plant(c, Qh, h["key_len"])
+    torch.cuda.synchronize()
+    K, V = host(c.Kc), host(c.Vc)
+    with decode_policy(shape):
+        out = host(c.decode(dev(Qh), d["key_len"]))
+    ref = O.decode(Qh, K, V, h["key_len"])
+    # precondition: the oracle's rows are the planted keys' V rows
+    for b in range(w.B):
+        for l in range(w.L):
+            for hh in range(w.H):
+                if pos[b, l, hh] >= 0:
+                    assert np.abs(ref[b, l, hh] - V[b, l, hh, pos[b, l, hh]]).max() < 1e-9
+    assert np.isfinite(out).all()
+    assert np.abs(out - ref).max() <= TOL[cache_dtype]
+
+
+@pytest.mark.parametrize("cache_dtype,nq", [("f32", 2), ("f32", 5), ("f32", 8), ("bf16", 2), ("bf16", 8)])
+def test_shared_decode_one_hot_rows(cache_dtype, nq):
+    """The key of each row is planted along its first hypothesis' query; the other
+    hypotheses see that key at a large score of either sign."""
+    w = _workload(951)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, cache_dtype)
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    rng = np.random.default_rng(952 + nq)
+    Q = rng.standard_normal((w.B, nq, w.L, w.H, 64)).astype(np.float32)
+    _plant(c, Q[:, 0], h["key_len"])
+    torch.cuda.synchronize()
+    K, V = host(c.Kc), host(c.Vc)
+    out = host(c.decode_shared(dev(Q), d["key_len"]))
+    ref = O.decode_shared(Q, K, V, h["key_len"])
+    assert np.isfinite(out).all()
+    assert np.abs(out - ref).max() <= TOL[cache_dtype]
