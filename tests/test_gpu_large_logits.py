@@ -97,3 +97,28 @@ def test_shared_decode_one_hot_rows(cache_dtype, nq):
     ref = O.decode_shared(Q, K, V, h["key_len"])
     assert np.isfinite(out).all()
     assert np.abs(out - ref).max() <= TOL[cache_dtype]
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+def test_alignment_weights_one_hot_rows(cache_dtype):
+    """The alignment-head rows of planted keys are one-hot at the planted position
+    (the clusters' partial maxima then differ by hundreds between CTAs), and their
+    head mean is the mean of those one-hot rows."""
+    w = W.custom("large_logits_align", B=16, T=1500, d=512, L=6, H=8, ragged=True, index=953)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, cache_dtype)
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    Qh = W.make_Q(w, 0)
+    pos = _plant(c, Qh, h["key_len"])
+    torch.cuda.synchronize()
+    heads = [(0, 0), (1, 5), (2, 2), (3, 7), (4, 1), (5, 4)]
+    wt, mean = c.alignment_weights(dev(Qh), d["key_len"], heads)
+    wt, mean = host(wt), host(mean)
+    ref_w, ref_m = O.attention_weights(Qh, host(c.Kc), h["key_len"], heads)
+    for b in range(w.B):
+        for k, (l, hh) in enumerate(heads):
+            if pos[b, l, hh] >= 0:
+                assert abs(ref_w[b, k, pos[b, l, hh]] - 1.0) < 1e-9
+    assert np.isfinite(wt).all() and np.isfinite(mean).all()
+    assert np.abs(wt - ref_w).max() <= 1e-5
+    assert np.abs(mean - ref_m).max() <= 1e-5
