@@ -30,10 +30,11 @@ def _lib(cxa_lib):
     assert cxa.cxa_device_status(1) == cxa.CXA_OK
 
 
-def _plant(c, q_rows, key_len):
-    """Set one key per (slot, layer, head) row of the cache to a multiple of that
-    row's query q_rows [B, L, H, 64], scaled so that 0.125 * q.k = SPIKE_SCORE.
-    Returns the planted positions [B, L, H] (-1 for an empty slot)."""
+def _plant(c, q_rows, key_len, layers=None):
+    """Set one key per (slot, layer, head) row of the cache (of the given layers,
+    all by default) to a multiple of that row's query q_rows [B, L, H, 64], scaled
+    so that 0.125 * q.k = SPIKE_SCORE. Returns the planted positions [B, L, H]
+    (-1 where nothing was planted)."""
     B, L, H = q_rows.shape[:3]
     pos = np.full((B, L, H), -1, dtype=np.int64)
     Kc = c.Kc
@@ -41,7 +42,7 @@ def _plant(c, q_rows, key_len):
         n = int(min(max(key_len[b], 0), c.T))
         if n == 0:
             continue
-        for l in range(L):
+        for l in range(L) if layers is None else layers:
             for h in range(H):
                 choice = (l * H + h) % 3
                 t = 0 if choice == 0 else (n - 1 if choice == 1 else (b * 31 + l * 7 + h * 3) % n)
@@ -122,3 +123,77 @@ def test_alignment_weights_one_hot_rows(cache_dtype):
     assert np.isfinite(wt).all() and np.isfinite(mean).all()
     assert np.abs(wt - ref_w).max() <= 1e-5
     assert np.abs(mean - ref_m).max() <= 1e-5
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B,H", [(16, 8), (5, 4)])
+def test_cross_block_one_hot_rows(cache_dtype, B, H):
+    """The block's attention (LayerNorm, query projection, attention, out projection):
+    keys planted along the projected queries LayerNorm(x) WQ + bQ. Batched-Base
+    width takes the two-launch form (its clusters do not all fit), the small width
+    the one-launch form."""
+    d_model = 64 * H
+    w = W.custom("large_logits_block", B=B, T=1500 if B == 16 else 400, d=d_model, L=2, H=H, ragged=True,
+                 index=954)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, cache_dtype)
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    rng = np.random.default_rng(955)
+    p = {"WQ": rng.standard_normal((d_model, d_model)) * d_model ** -0.5,
+         "WO": rng.standard_normal((d_model, d_model)) * d_model ** -0.5,
+         "gamma": 1.0 + 0.1 * rng.standard_normal(d_model), "beta": 0.1 * rng.standard_normal(d_model),
+         "bQ": 0.02 * rng.standard_normal(d_model), "bO": 0.02 * rng.standard_normal(d_model)}
+    p = {k: v.astype(np.float32) for k, v in p.items()}
+    x0 = rng.standard_normal((B, d_model)).astype(np.float32)
+    layer = 1
+    q = (O.layer_norm(x0, p["gamma"], p["beta"], 1e-5) @ p["WQ"].astype(np.float64) + p["bQ"]).reshape(B, H, 64)
+    q_rows = np.zeros((B, w.L, H, 64), np.float32)
+    q_rows[:, layer] = q
+    pos = _plant(c, q_rows, h["key_len"], layers=[layer])
+    torch.cuda.synchronize()
+    x = dev(x0)
+    dp = {k: dev(v) for k, v in p.items()}
+    c.cross_block(layer, x, dp["WQ"], dp["WO"], d["key_len"], ln_gamma=dp["gamma"], ln_beta=dp["beta"],
+                  bQ=dp["bQ"], bO=dp["bO"])
+    ref = O.cross_block(x0, layer, host(c.Kc), host(c.Vc), h["key_len"], p["WQ"], p["WO"], p["gamma"], p["beta"],
+                        1e-5, p["bQ"], p["bO"])
+    assert (pos[:, layer] >= 0).any()
+    got = host(x)
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= {"f32": 2e-4, "bf16": 2e-2}[cache_dtype]
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+def test_self_attention_step_new_key_dominates(cache_dtype):
+    """At two steps the appended key is planted along that step's query, so the
+    step's output is the appended V row, which the kernel takes from its inputs
+    rather than from the cache row it streams; later steps see that key at large
+    scores of either sign."""
+    B, L, H, T, S = 4, 2, 3, 448, 40
+    c = cxa.CrossAttentionCache(B, T, L, H, 64, cache_dtype)
+    rng = np.random.default_rng(956)
+    Qs = rng.standard_normal((S, B, L, H, 64)).astype(np.float32)
+    Ks = rng.standard_normal((S, B, L, H, 64)).astype(np.float32)
+    Vs = rng.standard_normal((S, B, L, H, 64)).astype(np.float32)
+    for s in (0, 23):
+        q = Qs[s].astype(np.float64)
+        alpha = SPIKE_SCORE / (0.125 * np.einsum("blhc,blhc->blh", q, q))
+        Ks[s] = (alpha[..., None] * q).astype(np.float32)
+    if cache_dtype == "bf16":
+        Ks, Vs = W.bf16_round(Ks), W.bf16_round(Vs)
+    outs = [torch.empty((B, L, H, 64), device="cuda") for _ in range(S)]
+    Qd, Kd, Vd = [dev(x) for x in Qs], [dev(x) for x in Ks], [dev(x) for x in Vs]
+    pos = [dev(np.full(B, s, np.int32), torch.int32) for s in range(S)]
+    torch.cuda.synchronize()
+    for s in range(S):
+        c.self_attention_step(pos[s], Qd[s], Kd[s], Vd[s], out=outs[s])
+    torch.cuda.synchronize()
+    got = np.stack([host(o) for o in outs])
+    assert np.isfinite(got).all()
+    for s in (0, 23):
+        assert np.abs(got[s] - Vs[s]).max() <= TOL[cache_dtype]
+    for b in range(B):
+        for l in range(L):
+            for hh in range(H):
+                ref = O.self_attention_steps(Qs[:, b, l, hh], Ks[:, b, l, hh], Vs[:, b, l, hh])
+                assert np.abs(got[:, b, l, hh] - ref).max() <= TOL[cache_dtype]
