@@ -602,12 +602,82 @@ def _mut_round_truncate(monkeypatch):
     monkeypatch.setattr(O, "round_bf16", round_bf16)
 
 
+def _mut_layer_norm_unbiased(monkeypatch):
+    def layer_norm(x, gamma=None, beta=None, eps=1e-5):
+        x = np.asarray(x, np.float64)
+        mean = x.mean(axis=-1, keepdims=True)
+        var = ((x - mean) ** 2).sum(axis=-1, keepdims=True) / (x.shape[-1] - 1)
+        y = (x - mean) / np.sqrt(var + eps)
+        return y * (1.0 if gamma is None else np.asarray(gamma)) + (0.0 if beta is None else np.asarray(beta))
+    monkeypatch.setattr(O, "layer_norm", layer_norm)
+
+
+def _mut_layer_norm_eps_outside_root(monkeypatch):
+    def layer_norm(x, gamma=None, beta=None, eps=1e-5):
+        x = np.asarray(x, np.float64)
+        mean = x.mean(axis=-1, keepdims=True)
+        y = (x - mean) / (np.sqrt(((x - mean) ** 2).mean(axis=-1, keepdims=True)) + eps)
+        return y * (1.0 if gamma is None else np.asarray(gamma)) + (0.0 if beta is None else np.asarray(beta))
+    monkeypatch.setattr(O, "layer_norm", layer_norm)
+
+
+def _mut_block_without_residual(monkeypatch):
+    orig = O.cross_block
+
+    def cross_block(x, *args, **kw):
+        return orig(x, *args, **kw) - np.asarray(x, np.float64)
+    monkeypatch.setattr(O, "cross_block", cross_block)
+
+
+def _mut_causal_window_excludes_self(monkeypatch):
+    def self_attention_steps(Qs, Ks, Vs, scale=None):
+        Qs, Ks, Vs = (np.asarray(a, np.float64) for a in (Qs, Ks, Vs))
+        S, dh = Qs.shape
+        scale = 1.0 / np.sqrt(dh) if scale is None else scale
+        return np.stack([O.attend_row(Qs[i], Ks, Vs, i, scale) for i in range(S)])
+    monkeypatch.setattr(O, "self_attention_steps", self_attention_steps)
+
+
+def _mut_alignment_unmasked(monkeypatch):
+    def attention_weights(Q, Kc, key_len, heads, scale=None):
+        Q, Kc = np.asarray(Q, np.float64), np.asarray(Kc, np.float64)
+        B, T = Kc.shape[0], Kc.shape[3]
+        w = np.zeros((B, len(heads), T))
+        for b in range(B):
+            for k, (l, h) in enumerate(heads):
+                s = 0.125 * (Kc[b, l, h] @ Q[b, l, h])
+                e = np.exp(s - s.max())
+                w[b, k] = e / e.sum()
+        return w, w.mean(axis=1)
+    monkeypatch.setattr(O, "attention_weights", attention_weights)
+
+
+def _mut_alignment_mean_drops_a_head(monkeypatch):
+    orig = O.attention_weights
+
+    def attention_weights(*args, **kw):
+        w, _ = orig(*args, **kw)
+        return w, w[:, :-1].mean(axis=1)
+    monkeypatch.setattr(O, "attention_weights", attention_weights)
+
+
+def _mut_shared_decode_first_query(monkeypatch):
+    orig = O.decode_shared
+
+    def decode_shared(Q, Kc, Vc, key_len, scale=None):
+        Q = np.asarray(Q, np.float64)
+        return orig(np.repeat(Q[:, :1], Q.shape[1], axis=1), Kc, Vc, key_len, scale)
+    monkeypatch.setattr(O, "decode_shared", decode_shared)
+
+
 def _all_pins_pass():
     try:
         return (pin_populate_bruteforce() < 1e-12 and pin_decode_bruteforce() < 1e-12
                 and pin_closed_forms() < 1e-12 and pin_full_window() < 1e-13 and pin_shared_decode() < 1e-12
                 and pin_layout_offset() == 0 and pin_scale_on_scores() < 1e-13
-                and pin_populate_head() < 1e-12 and pin_rel_frobenius() < 1e-12 and pin_round_bf16() == 0)
+                and pin_populate_head() < 1e-12 and pin_rel_frobenius() < 1e-12 and pin_round_bf16() == 0
+                and pin_cross_block() < 1e-11 and pin_self_attention() < 1e-12
+                and pin_attention_weights() < 1e-12)
     except (ValueError, IndexError, TypeError):   # a broken shape is a failed pin too
         return False
 
@@ -617,6 +687,9 @@ def _all_pins_pass():
     _mut_sign_flip, _mut_mask_off_by_one, _mut_no_normalisation, _mut_missing_scale,
     _mut_head_without_bias, _mut_head_neighbouring_block, _mut_frobenius_without_sqrt,
     _mut_frobenius_squared_denominator, _mut_round_half_away, _mut_round_truncate,
+    _mut_layer_norm_unbiased, _mut_layer_norm_eps_outside_root, _mut_block_without_residual,
+    _mut_causal_window_excludes_self, _mut_alignment_unmasked, _mut_alignment_mean_drops_a_head,
+    _mut_shared_decode_first_query,
 ])
 def test_planted_mistake_is_caught(monkeypatch, mutation):
     mutation(monkeypatch)
