@@ -316,6 +316,26 @@ def test_large_sampled_heads():
                   decode_max_abs_end_to_end=worst["e2e"])
 
 
+def test_large_dims_tf32_sampled_heads():
+    """Whisper-large widths with fp32 inputs (TF32 operands, 40 k-blocks per tile,
+    320 column tiles: the CTA-pair GEMM) into an fp32 cache, two memories: 24
+    sampled (slot, layer, head) blocks element by element, and their decode rows."""
+    w = W.custom("large_tf32", B=2, T=1500, d=1280, L=32, H=20, ragged=True, index=945)
+    c, d, h = _populate(w, "f32")
+    rng = np.random.default_rng(78)
+    heads = sorted({(int(rng.integers(w.B)), int(rng.integers(w.L)), int(rng.integers(w.H))) for _ in range(24)}
+                   | {(0, 0, 0), (w.B - 1, w.L - 1, w.H - 1)})
+    Q = W.make_Q(w, 0)
+    out = host(c.decode(dev(Q), d["key_len"]))
+    for (b, l, hh) in heads:
+        Kg, Vg = host(c.Kc[b, l, hh]), host(c.Vc[b, l, hh])
+        check_populate_head(Kg, Vg, h["E"][b], h["WK"][l], h["WV"][l], h["bV"][l], hh, "f32", "f32",
+                            f"large tf32 ({b}, {l}, {hh})")
+        n = int(min(max(h["key_len"][b], 0), w.T))
+        iso = O.attend_row(Q[b, l, hh], Kg, Vg, n, 0.125)
+        assert np.abs(out[b, l, hh] - iso).max() <= DECODE_F32_MAX_ABS
+
+
 @pytest.mark.parametrize("shape", ["stream", "rows", "alternate"])
 @pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
 def test_back_to_back_steps_without_sync(cache_dtype, shape):
