@@ -377,7 +377,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // Each chunk's P.V once its P^T and V tile are ready: A = the V tile (as V^T),
     // B = P^T, D = the row segment's O^T buffer (accumulating from its first chunk).
     if (lane == 0) {
-      constexpr uint32_t idesc_o = make_idesc(1u, kDh, kNPad) | (1u << 15);   // A (V^T) MN-major
+      // A (V^T) and B (P^T, stored as P [key][query]) both MN-major
+      constexpr uint32_t idesc_o = make_idesc(1u, kDh, kNPad) | (1u << 15) | (1u << 16);
       Cursor cur = locate(g0, s_first, s_nch, p.B);
       int prev_b = -1, prev_lh = -1, seg = -1;
       bool ok = true;
@@ -398,12 +399,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         tc_fence_after();
         const int rb = seg & 1;
         const uint64_t vd = smem_desc_mn_sw128(stage_base + st * kStageBytes + kTileBytes);
-        const uint64_t pd = smem_desc_k_sw128(p_base + b * kPBytes);
+        const uint64_t pd = smem_desc_mn_sw32(p_base + b * kPBytes);
         const uint32_t d_tmem = tmem_base + kOCol + static_cast<uint32_t>(rb * kNPad);
 #pragma unroll
-        for (int kb = 0; kb < kChunk / 16; ++kb)   // 16 keys: 2048 bytes of V, 32 bytes of a P^T row
-          mma_bf16(d_tmem, vd + kb * (2048 >> 4), pd + (kb >> 2) * (2048 >> 4) + (kb & 3) * 2, idesc_o,
-                   (first && kb == 0) ? 0u : 1u);
+        for (int kb = 0; kb < kChunk / 16; ++kb)   // 16 keys: 2048 bytes of V, 512 bytes of P
+          mma_bf16(d_tmem, vd + kb * (2048 >> 4), pd + kb * (512 >> 4), idesc_o, (first && kb == 0) ? 0u : 1u);
         tc_commit(pempty_bar(b));
         tc_commit(vempty_bar(st));
         if (last) tc_commit(ofull_bar(rb));
@@ -419,10 +419,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // ------------------------------------------------------------ consumers
     const int tid = threadIdx.x;                   // 0..127: key of the chunk for the softmax
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    // P^T byte offset of (query 0, key tid) in buffer 0: key half, swizzled 16-byte chunk
-    const int kk = tid & 63;
-    const uint32_t p_key = static_cast<uint32_t>((tid >> 6) * 2048 + (kk & 7) * 2);
-    const uint32_t p_chunk = static_cast<uint32_t>(kk >> 3);
+    // this key's row of P [key][16 queries] (32 bytes) in buffer 0, and its swizzle:
+    // queries 8j .. 8j + 7 go to 16-byte chunk j ^ ((tid >> 2) & 1)
+    const uint32_t p_row = p_base + static_cast<uint32_t>(tid) * 32u;
+    const uint32_t p_sw = static_cast<uint32_t>((tid >> 2) & 1);
     Cursor cur = locate(g0, s_first, s_nch, p.B);
     int seg_c0 = cur.c;
     // m_ref: the reference max the probabilities are taken against (log2 units); it
@@ -588,14 +588,31 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
       // the P^T buffer is free once the P.V of chunk i-2 has finished
       if (ok && !mbar_wait(pempty_bar(a), acc_parity ^ 1u, s_flags)) fail();
-      const uint32_t p_off = static_cast<uint32_t>(a * kPBytes) + p_key;
+      {
+        // the probabilities, rounded to bf16, eight queries to a 16-byte store
+        uint32_t pw[(kNQT + 7) / 8 * 4];
 #pragma unroll
-      for (int q = 0; q < kNQT; ++q) {
-        const __nv_bfloat16 pb = __float2bfloat16_rn(valid_key ? ex2(sc[q] - m_ref[q]) : 0.f);
-        s_run[q] += __bfloat162float(pb);
-        const int r = q & 7;
-        *reinterpret_cast<uint16_t*>(bp + p_off + (q >> 3) * 1024 + r * 128 +
-                                     ((p_chunk ^ static_cast<uint32_t>(r)) << 4)) = __bfloat16_as_ushort(pb);
+        for (int q2 = 0; q2 < (kNQT + 7) / 8 * 4; ++q2) {
+          float pr[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int q = 2 * q2 + e;
+            float v = 0.f;
+            if (q < kNQT) {
+              const __nv_bfloat16 pb = __float2bfloat16_rn(valid_key ? ex2(sc[q] - m_ref[q]) : 0.f);
+              v = __bfloat162float(pb);
+              s_run[q] += v;
+            }
+            pr[e] = v;
+          }
+          __nv_bfloat162 pp = __floats2bfloat162_rn(pr[0], pr[1]);   // exact: both are bf16 values
+          pw[q2] = *reinterpret_cast<uint32_t*>(&pp);
+        }
+        const uint32_t row = p_row + static_cast<uint32_t>(a * kPBytes);
+#pragma unroll
+        for (int j = 0; j < (kNQT + 7) / 8; ++j)
+          st_shared_v4(row + ((static_cast<uint32_t>(j) ^ p_sw) << 4), pw[4 * j], pw[4 * j + 1], pw[4 * j + 2],
+                       pw[4 * j + 3]);
       }
       if (n < kChunk) {
         // tail chunk: zero the V rows of keys >= n (their P is 0; the rows may hold any bits)

@@ -363,6 +363,22 @@ __device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory descriptor for an MN-major 16-bit operand tile of exactly 16
+// elements (one 32-byte row) along M or N, stored with 32-byte swizzling: each K
+// index is one 32-byte row, whose 16-byte chunk j sits at chunk j ^ ((row >> 2) & 1),
+// and 8-row K groups are 256 bytes apart (the stride-dimension offset). The tile
+// base is 256-byte aligned. The leading-dimension offset steps between 16-element MN
+// blocks, of which such a tile has one.
+__device__ __forceinline__ uint64_t smem_desc_mn_sw32(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(256 >> 4) << 16;
+  d |= static_cast<uint64_t>(256 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(6) << 61;
+  return d;
+}
+
 // Instruction descriptor for kind::f16 / kind::tf32 with fp32 accumulation and
 // both operands K-major. ab_format: 1 = bf16, 2 = tf32.
 // Bits: [4,6) D format (1 = f32), [7,10) A format, [10,13) B format,
