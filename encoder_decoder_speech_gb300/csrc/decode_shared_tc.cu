@@ -21,12 +21,14 @@
 //    rescale of the O accumulator in TMEM before the chunk's P.V is issued.
 //    The MMA warp only builds Q tiles and issues the score MMAs; K and V stream
 //    through separate rings (a K stage returns once its score MMA has run).
-//    Probabilities (<= 256) are written, rounded to bf16, as P^T[query][key] in
-//    the 128-byte-swizzled K-major layout; the running sums add the same
-//    rounded values, so the weights of the final average sum to one exactly.
+//    Probabilities (<= 256) are written, rounded to bf16, as P[key][query]: one
+//    32-byte row per key, eight queries to a 16-byte store, the row's two chunks
+//    swapped every four keys (the 32-byte swizzle of an MN-major operand); the
+//    running sums add the same rounded values, so the weights of the final
+//    average sum to one exactly.
 //  * values: O^T[64 channels x 16 queries] += V_chunk^T[64 x 128 keys] P[128 x 16]
-//    (M = 64, N = 16): A is V MN-major straight from its TMA tile, B is P^T as
-//    written (K-major), accumulated over the row segment's chunks in TMEM (two
+//    (M = 64, N = 16): A is V MN-major straight from its TMA tile, B is P^T read
+//    MN-major from P as written, accumulated over the row segment's chunks in TMEM (two
 //    buffers, alternate segments). With M = 64 the accumulator rows sit in
 //    lanes 0..15 of each warp's 32-lane quarter: channel 16w + l in lane
 //    32w + l. One consumer thread issues the chunk's P.V right after the
@@ -65,7 +67,7 @@ constexpr int kBoxBytes = kBoxRows * kRowBytes;
 constexpr int kTileBytes = kChunk * kRowBytes; // K or V of one chunk: 16 KB
 constexpr int kStageBytes = 2 * kTileBytes;
 constexpr int kStages = 3;
-constexpr int kPBytes = 4096;                  // P^T of a chunk: 2 key halves x 16 rows x 128 B
+constexpr int kPBytes = 4096;                  // P of a chunk: 128 keys x 16 queries x 2 B
 constexpr int kQTileBytes = kSCols * kRowBytes; // 4 KB
 constexpr int kConsumerWarps = 4;              // one key per consumer thread
 constexpr int kThreads = (kConsumerWarps + 3) * 32;   // + producer, score-MMA and P.V-MMA warps
