@@ -53,7 +53,7 @@ constexpr int kThreads = kConsumers;
 #define CXA_BLOCK_CHUNK_F32 24
 #endif
 #ifndef CXA_BLOCK_CHUNK_BF16
-#define CXA_BLOCK_CHUNK_BF16 48
+#define CXA_BLOCK_CHUNK_BF16 32
 #endif
 constexpr int kStages = CXA_BLOCK_STAGES;
 static_assert(kStages % kConsumerWarps == 0, "each warp owns kStages / 8 stages");
