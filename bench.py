@@ -54,7 +54,8 @@ def parse_args(argv=None):
                         "(T_enc x batch, d=512, 6 layers, 8x64 heads); one JSON line per point")
     p.add_argument("--shared", action="store_true",
                    help="time shared-cache decode (nq hypotheses per memory) on the batched Whisper-Base "
-                        "workload for nq = 1, 2, 4, 5, 8; one JSON line per (nq, cache dtype)")
+                        "workload for nq = 1, 2, 4, 5, 8 (and 12, 16 with a bf16 cache); one JSON line per "
+                        "(nq, cache dtype)")
     p.add_argument("--small", action="store_true",
                    help="Whisper-Tiny / Whisper-Base single-memory decode, warm-L2 and cold, and populate")
     p.add_argument("--block", action="store_true",
@@ -769,7 +770,7 @@ def run_shared(args):
     for cd, esz in (("f32", 4), ("bf16", 2)):
         cache = cxa.CrossAttentionCache(w.B, w.T, w.L, w.H, w.dh, cd)
         cache.populate(E, WK, WV, bV)
-        for nq in (1, 2, 4, 5, 8) + ((16,) if cd == "bf16" else ()):
+        for nq in (1, 2, 4, 5, 8) + ((12, 16) if cd == "bf16" else ()):
             Q = torch.from_numpy(np.random.default_rng(nq).standard_normal(
                 (w.B, nq, w.L, w.H, w.dh)).astype(np.float32)).to("cuda")
             out = torch.empty_like(Q)

@@ -543,24 +543,54 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend
           }
           if (__shfl_sync(0xffffffffu, last, 0)) {
             __threadfence();
-            for (int q = 0; q < nq; ++q) {
-              const float* P0 = p.part + (row * nq + q) * p.part_stride * kPartFloats;
-              float MM = -INFINITY, SS = 0.f, A0 = 0.f, A1 = 0.f;   // one pass, rescaling as the max grows
-              for (int k = 0; k < nseg; ++k) {
-                const float mk = __ldcg(P0 + k * kPartFloats);
-                const float sk = __ldcg(P0 + k * kPartFloats + 1);
-                const float a0 = __ldcg(P0 + k * kPartFloats + 4 + lane);
-                const float a1 = __ldcg(P0 + k * kPartFloats + 4 + lane + 32);
-                const float M2 = fmaxf(MM, mk);
-                const float f0 = rescale(MM, M2), f1 = rescale(mk, M2);
-                SS = SS * f0 + sk * f1;
-                A0 = A0 * f0 + a0 * f1;
-                A1 = A1 * f0 + a1 * f1;
-                MM = M2;
+            // the segments' states in segment order, rescaling as the max grows; four
+            // queries by four segments of loads in flight at a time
+            constexpr int kQB = kNQ >= 6 ? 4 : (kNQ >= 2 ? 2 : 1);
+            for (int q0 = 0; q0 < nq; q0 += kQB) {
+              float MM[kQB], SS[kQB], A0[kQB], A1[kQB];
+#pragma unroll
+              for (int u = 0; u < kQB; ++u) {
+                MM[u] = -INFINITY;
+                SS[u] = 0.f;
+                A0[u] = 0.f;
+                A1[u] = 0.f;
               }
-              float* o = p.out + qrow(cur.b, cur.lh, q) * kDh;
-              o[lane] = SS > 0.f ? A0 / SS : 0.f;
-              o[lane + 32] = SS > 0.f ? A1 / SS : 0.f;
+              for (int k0 = 0; k0 < nseg; k0 += 4) {
+                float mk[kQB][4], sk[kQB][4], a0k[kQB][4], a1k[kQB][4];
+#pragma unroll
+                for (int u = 0; u < kQB; ++u) {
+                  const float* P0 = p.part + (row * nq + (q0 + u < nq ? q0 + u : 0)) * p.part_stride * kPartFloats;
+#pragma unroll
+                  for (int v = 0; v < 4; ++v) {
+                    const bool in = q0 + u < nq && k0 + v < nseg;
+                    const float* Pk = P0 + (k0 + v) * kPartFloats;
+                    mk[u][v] = in ? __ldcg(Pk) : -INFINITY;
+                    sk[u][v] = in ? __ldcg(Pk + 1) : 0.f;
+                    a0k[u][v] = in ? __ldcg(Pk + 4 + lane) : 0.f;
+                    a1k[u][v] = in ? __ldcg(Pk + 4 + lane + 32) : 0.f;
+                  }
+                }
+#pragma unroll
+                for (int u = 0; u < kQB; ++u) {
+#pragma unroll
+                  for (int v = 0; v < 4; ++v) {
+                    const float M2 = fmaxf(MM[u], mk[u][v]);
+                    const float f0 = rescale(MM[u], M2), f1 = rescale(mk[u][v], M2);
+                    SS[u] = SS[u] * f0 + sk[u][v] * f1;
+                    A0[u] = A0[u] * f0 + a0k[u][v] * f1;
+                    A1[u] = A1[u] * f0 + a1k[u][v] * f1;
+                    MM[u] = M2;
+                  }
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < kQB; ++u) {
+                if (q0 + u < nq) {
+                  float* o = p.out + qrow(cur.b, cur.lh, q0 + u) * kDh;
+                  o[lane] = SS[u] > 0.f ? A0[u] / SS[u] : 0.f;
+                  o[lane + 32] = SS[u] > 0.f ? A1[u] / SS[u] : 0.f;
+                }
+              }
             }
             if (lane == 0) p.counters[row] = 0u;
           }

@@ -2,8 +2,14 @@
 // (slot, layer, head) attend the slot's one bf16 cache, the batch-N-over-one-
 // shared-cache case of SharedSplitKVCached ("Caso de estudio: WhisperKit", §3).
 //
-// The work split, the segment flush and the last-arriver merge are those of the
-// stream decode kernel (decode.cu). A 128-key chunk goes through two tcgen05
+// The work split and the segment flush are those of the stream decode kernel
+// (decode.cu). A row cut by a range boundary leaves one partial state per CTA that
+// works on it, and no CTA publishes a partial state (device fence, arrival
+// counter) or merges a row while its K/V stream is running: with eight or more
+// query columns a second, small kernel (decode_shared_merge_kernel, chained by
+// programmatic dependent launch) merges the cut rows after the grid; with four,
+// each CTA publishes its (at most two) cut rows at the end of its range and the
+// last arriver of a row merges it. A 128-key chunk goes through two tcgen05
 // products with fp32 accumulators in tensor memory:
 //
 //  * scores: S^T[128 keys x 32] = K_chunk[128 x 64] [Q_hi; Q_lo]^T (kind::f16,
@@ -87,7 +93,7 @@ struct TcParams {
   const int* key_len;
   float* out;
   float* part;
-  unsigned int* counters;
+  unsigned int* counters;   // arrival counters (the four-column instance)
   unsigned int* status;
   int B, T, LH, LHc, lh0, nq, part_stride;
   float qscale;
@@ -135,6 +141,39 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
       : "memory");
 }
 
+// The dense chunk numbering from key_len, by one warp: s_nch[b] chunks per row of
+// slot b, s_first[b] the number of slot b's first chunk (s_first[B] = total) and,
+// if s_kl is given, the key lengths clamped to [0, T]. Every CTA of both kernels
+// computes the same numbering.
+__device__ __forceinline__ void number_chunks(const int* key_len, int B, int T, int LH, int lane, long long* s_first,
+                                              int* s_nch, int* s_kl) {
+  long long run = 0;
+  for (int base_b = 0; base_b < B; base_b += 32) {
+    const int b = base_b + lane;
+    int nch = 0;
+    if (b < B) {
+      const int kl = min(max(__ldg(key_len + b), 0), T);
+      nch = (kl + kChunk - 1) / kChunk;
+      s_nch[b] = nch;
+      if (s_kl != nullptr) s_kl[b] = kl;
+    }
+    long long v = static_cast<long long>(nch) * LH;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const long long o = __shfl_up_sync(0xffffffffu, v, off);
+      if (lane >= off) v += o;
+    }
+    if (b < B) s_first[b] = run + v - static_cast<long long>(nch) * LH;
+    run += __shfl_sync(0xffffffffu, v, 31);
+  }
+  if (lane == 0) s_first[B] = run;
+}
+
+// Cut rows merged in the kernel, at the end of each CTA's range (four query
+// columns), or by the merge kernel (more).
+template <int kNQT>
+__host__ __device__ constexpr bool merge_in_kernel() { return kNQT <= 4; }
+
 template <int kNQT>   // query columns the softmax handles (4, 8, 12 or 16 >= nq)
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     decode_shared_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -171,27 +210,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0) {   // chunk numbering from key_len (every CTA computes the same prefix)
-    long long run = 0;
-    for (int base_b = 0; base_b < p.B; base_b += 32) {
-      const int b = base_b + lane;
-      int nch = 0;
-      if (b < p.B) {
-        const int kl = min(max(__ldg(p.key_len + b), 0), p.T);
-        nch = (kl + kChunk - 1) / kChunk;
-        s_nch[b] = nch;
-        s_kl[b] = kl;
-      }
-      long long v = static_cast<long long>(nch) * LH;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const long long o = __shfl_up_sync(0xffffffffu, v, off);
-        if (lane >= off) v += o;
-      }
-      if (b < p.B) s_first[b] = run + v - static_cast<long long>(nch) * LH;
-      run += __shfl_sync(0xffffffffu, v, 31);
-    }
+    number_chunks(p.key_len, p.B, p.T, LH, lane, s_first, s_nch, s_kl);
     if (lane == 0) {
-      s_first[p.B] = run;
       s_flags[0] = 0;
       s_flags[1] = 0;
     }
@@ -441,6 +461,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // last P.V has run by then).
     bool f_pending = false, f_whole = false;
     int f_seg = 0, f_b = 0, f_lh = 0, f_pseg = 0, f_nseg = 1;
+    // cut rows of this range, published at its end (in-kernel merge): slot, row, segments
+    int n_cut = 0, cb0 = 0, clh0 = 0, cn0 = 0, cb1 = 0, clh1 = 0, cn1 = 0;
     long long f_row = 0;
     auto fail = [&]() {
       ok = false;
@@ -448,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       atomicOr(p.status, 1u);
     };
     // Write the finished segment f_seg: O^T from TMEM through a free P^T buffer
-    // (as [query][channel] floats) to the output rows or the segment's partial
-    // slots; the last segment of a split row merges all of them.
+    // (as [query][channel] floats) to the output rows, or, for a part of a cut
+    // row, to the segment's partial slots.
     auto flush = [&](int free_pbuf) {
       const int rb = f_seg & 1;
       if (ok && !mbar_wait(ofull_bar(rb), static_cast<uint32_t>((f_seg >> 1) & 1), s_flags)) fail();
@@ -478,53 +500,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                                      4 * c4) = ok ? v : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-      if (!f_whole) {
-        if (tid < nq) {
-          float* P = p.part + ((f_row * nq + tid) * p.part_stride + f_pseg) * kPartFloats;
-          P[0] = ok ? s_m[rb * kNPad + tid] : -INFINITY;
-          P[1] = ok ? sum[tid] + sum[kNPad + tid] + sum[2 * kNPad + tid] + sum[3 * kNPad + tid] : 0.f;
-        }
-        // the barrier orders every thread's partial writes before thread 0's
-        // device-scope fence and the counter update that publishes them
-        named_barrier(1, kConsumerWarps * 32);
-        if (tid == 0) {
-          __threadfence();
-          const unsigned int prev = atomicAdd(p.counters + f_row, 1u);
-          s_flags[1] = (prev == static_cast<unsigned int>(f_nseg - 1)) ? 1 : 0;
-          __threadfence();
-        }
-        named_barrier(1, kConsumerWarps * 32);
-        if (s_flags[1]) {
-#pragma unroll 2
-          for (int e = tid; e < nq * kDh; e += kConsumerWarps * 32) {   // (query, channel)
-            const int q = e / kDh, c = e % kDh;
-            const float* P0 = p.part + (f_row * nq + q) * p.part_stride * kPartFloats;
-            float MM = -INFINITY, SS = 0.f, AA = 0.f;
-            for (int k0 = 0; k0 < f_nseg; k0 += 4) {
-              float mk[4], sk[4], ak[4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const bool in = k0 + u < f_nseg;
-                const float* Pk = P0 + (k0 + u) * kPartFloats;
-                mk[u] = in ? __ldcg(Pk) : -INFINITY;
-                sk[u] = in ? __ldcg(Pk + 1) : 0.f;
-                ak[u] = in ? __ldcg(Pk + 4 + c) : 0.f;
-              }
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const float M2 = fmaxf(MM, mk[u]);
-                const float f0 = rescale(MM, M2), f1 = rescale(mk[u], M2);
-                SS = SS * f0 + sk[u] * f1;
-                AA = AA * f0 + ak[u] * f1;
-                MM = M2;
-              }
-            }
-            p.out[qrow(f_b, f_lh, q) * kDh + c] = SS > 0.f ? AA / SS : 0.f;
-          }
-          if (tid == 0) p.counters[f_row] = 0u;
-        }
+      if (!f_whole && tid < nq) {
+        float* P = p.part + ((f_row * nq + tid) * p.part_stride + f_pseg) * kPartFloats;
+        P[0] = ok ? s_m[rb * kNPad + tid] : -INFINITY;
+        P[1] = ok ? sum[tid] + sum[kNPad + tid] + sum[2 * kNPad + tid] + sum[3 * kNPad + tid] : 0.f;
       }
-      named_barrier(1, kConsumerWarps * 32);   // the staging buffer and the flags are free again
+      if (merge_in_kernel<kNQT>() && !f_whole) {   // only a range's first and last segments are cut
+        if (n_cut == 0) {
+          cb0 = f_b;
+          clh0 = f_lh;
+          cn0 = f_nseg;
+        } else {
+          cb1 = f_b;
+          clh1 = f_lh;
+          cn1 = f_nseg;
+        }
+        ++n_cut;
+      }
+      named_barrier(1, kConsumerWarps * 32);   // the staging buffer is free again
       f_pending = false;
     };
 
@@ -672,13 +665,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         f_lh = cur.lh;
         f_row = static_cast<long long>(cur.b) * LH + cur.lh;
         f_whole = seg_c0 == 0 && cur.c == nch - 1;
-        f_nseg = 1;
         f_pseg = 0;
-        if (!f_whole) {
+        f_nseg = 1;
+        if (!f_whole) {   // this CTA's segment index among the row's owners, and their number
           const long long grow = s_first[cur.b] + static_cast<long long>(cur.lh) * nch;
           const long long first_owner = owner_of(grow, total, ranges);
-          f_nseg = static_cast<int>(owner_of(grow + nch - 1, total, ranges) - first_owner + 1);
           f_pseg = static_cast<int>(blockIdx.x - first_owner);
+          f_nseg = static_cast<int>(owner_of(grow + nch - 1, total, ranges) - first_owner + 1);
         }
         ++seg;
 #pragma unroll
@@ -691,12 +684,140 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       advance(cur, s_nch, p.B, LH);
       if (cur.b != pb || cur.lh != plh) seg_c0 = cur.c;
     }
+    if (merge_in_kernel<kNQT>() && n_cut > 0) {
+      // Publish the cut rows (their partial writes are ordered before this point by
+      // the flushes' barriers): one device-scope fence, then the arrival counters;
+      // the last arriver of a row merges its segments' states in segment order.
+      if (tid == 0) {
+        __threadfence();
+        const unsigned int prev0 = atomicAdd(p.counters + static_cast<long long>(cb0) * LH + clh0, 1u);
+        const unsigned int prev1 =
+            n_cut > 1 ? atomicAdd(p.counters + static_cast<long long>(cb1) * LH + clh1, 1u) : 0u;
+        int last = prev0 == static_cast<unsigned int>(cn0 - 1) ? 1 : 0;
+        if (n_cut > 1 && prev1 == static_cast<unsigned int>(cn1 - 1)) last |= 2;
+        __threadfence();
+        s_flags[1] = last;
+      }
+      named_barrier(1, kConsumerWarps * 32);
+      const int last = s_flags[1];
+      for (int k = 0; k < 2; ++k) {
+        if (!(last & (1 << k))) continue;
+        const int mb = k ? cb1 : cb0, mlh = k ? clh1 : clh0, nseg = k ? cn1 : cn0;
+        const long long row = static_cast<long long>(mb) * LH + mlh;
+#pragma unroll 2
+        for (int e = tid; e < nq * kDh; e += kConsumerWarps * 32) {   // (query, channel)
+          const int q = e / kDh, c = e % kDh;
+          const float* P0 = p.part + (row * nq + q) * p.part_stride * kPartFloats;
+          float MM = -INFINITY, SS = 0.f, AA = 0.f;
+          for (int k0 = 0; k0 < nseg; k0 += 4) {
+            float mk[4], sk[4], ak[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const bool in = k0 + u < nseg;
+              const float* Pk = P0 + (k0 + u) * kPartFloats;
+              mk[u] = in ? __ldcg(Pk) : -INFINITY;
+              sk[u] = in ? __ldcg(Pk + 1) : 0.f;
+              ak[u] = in ? __ldcg(Pk + 4 + c) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float M2 = fmaxf(MM, mk[u]);
+              const float f0 = rescale(MM, M2), f1 = rescale(mk[u], M2);
+              SS = SS * f0 + sk[u] * f1;
+              AA = AA * f0 + ak[u] * f1;
+              MM = M2;
+            }
+          }
+          p.out[qrow(mb, mlh, q) * kDh + c] = SS > 0.f ? AA / SS : 0.f;
+        }
+        if (tid == 0) p.counters[row] = 0u;
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// Rows cut by the boundaries of the main grid's ranges: the segment states that the
+// CTAs sharing such a row left in its partial slots ((max, sum) and the unnormalised
+// accumulator per query), merged in segment order into the output rows. One CTA per
+// boundary; a row cut by several boundaries is merged at its first.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeElems = 4;   // (query, channel) outputs per thread per pass: nq x 64 <= 1024 in one pass
+
+__global__ void __launch_bounds__(kMergeThreads) decode_shared_merge_kernel(const TcParams p, int main_grid) {
+  extern __shared__ uint8_t merge_smem[];
+  long long* s_first = reinterpret_cast<long long*>(merge_smem);   // [B + 1]
+  int* s_nch = reinterpret_cast<int*>(s_first + p.B + 1);           // [B]
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int LH = p.LH, nq = p.nq;
+  if (threadIdx.x < 32) number_chunks(p.key_len, p.B, p.T, LH, lane, s_first, s_nch, nullptr);
+  // Every CTA waits for the main grid, whether or not it has a row to merge: the
+  // next grid's dependency wait, which covers this grid, then covers that one too.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __syncthreads();
+  const long long total = s_first[p.B];
+  const long long ranges = total < main_grid ? total : static_cast<long long>(main_grid);
+  for (long long j = 1 + blockIdx.x; j < ranges; j += gridDim.x) {
+    const long long g = j * total / ranges;   // first chunk of range j
+    const Cursor cur = locate(g, s_first, s_nch, p.B);
+    if (cur.c == 0) continue;                 // the boundary falls between rows
+    const long long grow = g - cur.c;         // the row's first chunk
+    if ((j - 1) * total / ranges > grow) continue;   // cut before, inside the row too
+    const int nch = s_nch[cur.b];
+    const long long first_owner = owner_of(grow, total, ranges);
+    const int nseg = static_cast<int>(owner_of(grow + nch - 1, total, ranges) - first_owner + 1);
+    const long long row = static_cast<long long>(cur.b) * LH + cur.lh;
+    for (int e0 = threadIdx.x; e0 < nq * kDh; e0 += kMergeElems * kMergeThreads) {
+      float MM[kMergeElems], SS[kMergeElems], AA[kMergeElems];
+#pragma unroll
+      for (int u = 0; u < kMergeElems; ++u) {
+        MM[u] = -INFINITY;
+        SS[u] = 0.f;
+        AA[u] = 0.f;
+      }
+      for (int k0 = 0; k0 < nseg; k0 += 4) {
+        float mk[kMergeElems][4], sk[kMergeElems][4], ak[kMergeElems][4];
+#pragma unroll
+        for (int u = 0; u < kMergeElems; ++u) {
+          const int e = e0 + u * kMergeThreads;
+          const int q = e / kDh, c = e % kDh;
+          const float* P0 = p.part + (row * nq + q) * p.part_stride * kPartFloats;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const bool in = e < nq * kDh && k0 + v < nseg;
+            const float* Pk = P0 + (k0 + v) * kPartFloats;
+            mk[u][v] = in ? __ldcg(Pk) : -INFINITY;
+            sk[u][v] = in ? __ldcg(Pk + 1) : 0.f;
+            ak[u][v] = in ? __ldcg(Pk + 4 + c) : 0.f;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeElems; ++u) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const float M2 = fmaxf(MM[u], mk[u][v]);
+            const float f0 = rescale(MM[u], M2), f1 = rescale(mk[u][v], M2);
+            SS[u] = SS[u] * f0 + sk[u][v] * f1;
+            AA[u] = AA[u] * f0 + ak[u][v] * f1;
+            MM[u] = M2;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kMergeElems; ++u) {
+        const int e = e0 + u * kMergeThreads;
+        if (e < nq * kDh) {
+          const int q = e / kDh, c = e % kDh;
+          p.out[((static_cast<long long>(cur.b) * nq + q) * LH + cur.lh) * kDh + c] = SS[u] > 0.f ? AA[u] / SS[u] : 0.f;
+        }
+      }
+    }
   }
 }
 
@@ -747,7 +868,7 @@ bool encode_cache_map(EncodeTiledFn encode, CUtensorMap* map, const void* cache,
 
 template <int kNQT>
 cudaError_t launch_tc(const TcParams& prm, const void* Kc, const void* Vc, const DeviceInfo& dev,
-                      cudaStream_t stream, std::string* msg) {
+                      cudaStream_t stream, std::string* msg, int* grid) {
   EncodeTiledFn encode = encoder();
   if (encode == nullptr) {
     *msg = "cuTensorMapEncodeTiled is not available from the CUDA driver";
@@ -812,7 +933,8 @@ cudaError_t launch_tc(const TcParams& prm, const void* Kc, const void* Vc, const
     if (fits[d] > per_sm) per_sm = fits[d];
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(dev.num_sms * (per_sm < kCtasPerSm ? per_sm : kCtasPerSm));
+  *grid = dev.num_sms * (per_sm < kCtasPerSm ? per_sm : kCtasPerSm);
+  cfg.gridDim = dim3(*grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -822,6 +944,23 @@ cudaError_t launch_tc(const TcParams& prm, const void* Kc, const void* Vc, const
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_shared_tc_kernel<kNQT>, tmK, tmV, prm);
+}
+
+// The merge kernel after a main grid of main_grid CTAs: one CTA per range boundary
+// (main_grid - 1 of them at most), started by programmatic dependent launch so that
+// its chunk numbering overlaps the main grid's tail.
+cudaError_t launch_merge(const TcParams& prm, int main_grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(main_grid > 1 ? main_grid - 1 : 1);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(prm.B + 1) * 8 + static_cast<size_t>(prm.B) * 4;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_shared_merge_kernel, prm, main_grid);
 }
 
 size_t counters_bytes(int B, int L, int H) {
@@ -852,11 +991,19 @@ cudaError_t launch_decode_shared_tc(const DecodeLaunch& a, const DeviceInfo& dev
   prm.nq = a.nq;
   prm.part_stride = (a.T + kPartChunk - 1) / kPartChunk;
   prm.qscale = a.scale * 1.4426950408889634f;
-  cudaError_t e = a.nq <= 4   ? launch_tc<4>(prm, a.Kc, a.Vc, dev, stream, msg)
-                  : a.nq <= 8 ? launch_tc<8>(prm, a.Kc, a.Vc, dev, stream, msg)
-                  : a.nq <= 12 ? launch_tc<12>(prm, a.Kc, a.Vc, dev, stream, msg)
-                              : launch_tc<16>(prm, a.Kc, a.Vc, dev, stream, msg);
-  if (e == cudaSuccess) count_launches(1);
+  // the workspace has the stream kernel's layout: arrival counters (used by the
+  // four-column instance, which leaves them at zero), then the partial slots
+  int grid = 0;
+  cudaError_t e = a.nq <= 4   ? launch_tc<4>(prm, a.Kc, a.Vc, dev, stream, msg, &grid)
+                  : a.nq <= 8 ? launch_tc<8>(prm, a.Kc, a.Vc, dev, stream, msg, &grid)
+                  : a.nq <= 12 ? launch_tc<12>(prm, a.Kc, a.Vc, dev, stream, msg, &grid)
+                              : launch_tc<16>(prm, a.Kc, a.Vc, dev, stream, msg, &grid);
+  if (e != cudaSuccess) return e;
+  count_launches(1);
+  if (!merge_in_kernel<4>() || a.nq > 4) {
+    e = launch_merge(prm, grid, stream);
+    if (e == cudaSuccess) count_launches(1);
+  }
   return e;
 }
 

@@ -164,3 +164,28 @@ def test_shared_decode_clamps_key_lengths():
     ref = O.decode_shared(Q, host(c.Kc), host(c.Vc), np.clip(kl, 0, w.T))
     assert np.abs(out - ref).max() <= DECODE_BF16_MAX_ABS
     assert np.all(out[0] == 0.0) and np.all(out[1] == 0.0)
+
+
+@pytest.mark.parametrize("nq", [2, 4, 8, 16])
+@pytest.mark.parametrize("geom", ["one_long_memory", "mixed_lengths"])
+def test_shared_decode_rows_cut_many_times(nq, geom):
+    """Rows far longer than a CTA's share of the chunks, so that range boundaries cut
+    each row tens of times (about 76 segments per row for one 32768-key memory of
+    4 rows): every cut row is merged once, from all of its segments in order
+    (in the kernel for up to four queries, by the merge kernel for more)."""
+    if geom == "one_long_memory":
+        w = W.custom("shared_cut", B=1, T=32768, d=128, L=2, H=2, ragged=False, index=947)
+        kl = np.array([32763], dtype=np.int32)
+    else:
+        w = W.custom("shared_cut_mixed", B=3, T=4096, d=128, L=2, H=2, ragged=False, index=948)
+        kl = np.array([4096, 1, 2500], dtype=np.int32)
+    d, h = inputs_on_device(w)
+    c = cache_for(w, "bf16")
+    c.populate(d["E"], d["WK"], d["WV"], d["bV"])
+    Q = _queries(w, nq, 110 + nq)
+    kld = dev(kl, torch.int32)
+    outs = [c.decode_shared(dev(Q), kld) for _ in range(2)]
+    out = host(outs[1])
+    ref = O.decode_shared(Q, host(c.Kc), host(c.Vc), kl)
+    assert np.abs(out - ref).max() <= DECODE_BF16_MAX_ABS
+    assert torch.equal(outs[0], outs[1])
