@@ -745,9 +745,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 // Rows cut by the boundaries of the main grid's ranges: the segment states that the
 // CTAs sharing such a row left in its partial slots ((max, sum) and the unnormalised
 // accumulator per query), merged in segment order into the output rows. One CTA per
-// boundary; a row cut by several boundaries is merged at its first.
+// boundary; a row cut by several boundaries is merged at its first. Thread layout:
+// the queries (padded to a power of two) split the CTA's threads; each thread takes
+// one query and 1, 2 or 4 adjacent channels (one vector load per segment), so a
+// segment's weight is one exp2 per query and thread, and its accumulator one fma
+// per channel.
 constexpr int kMergeThreads = 256;
-constexpr int kMergeElems = 4;   // (query, channel) outputs per thread per pass: nq x 64 <= 1024 in one pass
 
 __global__ void __launch_bounds__(kMergeThreads) decode_shared_merge_kernel(const TcParams p, int main_grid) {
   extern __shared__ uint8_t merge_smem[];
@@ -763,61 +766,75 @@ __global__ void __launch_bounds__(kMergeThreads) decode_shared_merge_kernel(cons
   __syncthreads();
   const long long total = s_first[p.B];
   const long long ranges = total < main_grid ? total : static_cast<long long>(main_grid);
+  const int nqp = nq <= 1 ? 1 : nq <= 2 ? 2 : nq <= 4 ? 4 : nq <= 8 ? 8 : 16;
+  const int tq = kMergeThreads / nqp;                 // threads per query
+  const int q = threadIdx.x / tq, t = threadIdx.x % tq;
+  const int cpt = tq >= kDh ? 1 : kDh / tq;           // channels t * cpt .. + cpt (<= 4)
   for (long long j = 1 + blockIdx.x; j < ranges; j += gridDim.x) {
     const long long g = j * total / ranges;   // first chunk of range j
     const Cursor cur = locate(g, s_first, s_nch, p.B);
     if (cur.c == 0) continue;                 // the boundary falls between rows
     const long long grow = g - cur.c;         // the row's first chunk
     if ((j - 1) * total / ranges > grow) continue;   // cut before, inside the row too
+    if (q >= nq || t >= kDh) continue;
     const int nch = s_nch[cur.b];
     const long long first_owner = owner_of(grow, total, ranges);
     const int nseg = static_cast<int>(owner_of(grow + nch - 1, total, ranges) - first_owner + 1);
     const long long row = static_cast<long long>(cur.b) * LH + cur.lh;
-    for (int e0 = threadIdx.x; e0 < nq * kDh; e0 += kMergeElems * kMergeThreads) {
-      float MM[kMergeElems], SS[kMergeElems], AA[kMergeElems];
+    const float* P0 = p.part + (row * nq + q) * p.part_stride * kPartFloats;
+    float MM = -INFINITY, SS = 0.f, AA[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k0 = 0; k0 < nseg; k0 += 4) {   // four segments' loads in flight at a time
+      float mk[4], sk[4], ak[4][4];
 #pragma unroll
-      for (int u = 0; u < kMergeElems; ++u) {
-        MM[u] = -INFINITY;
-        SS[u] = 0.f;
-        AA[u] = 0.f;
-      }
-      for (int k0 = 0; k0 < nseg; k0 += 4) {
-        float mk[kMergeElems][4], sk[kMergeElems][4], ak[kMergeElems][4];
-#pragma unroll
-        for (int u = 0; u < kMergeElems; ++u) {
-          const int e = e0 + u * kMergeThreads;
-          const int q = e / kDh, c = e % kDh;
-          const float* P0 = p.part + (row * nq + q) * p.part_stride * kPartFloats;
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const bool in = e < nq * kDh && k0 + v < nseg;
-            const float* Pk = P0 + (k0 + v) * kPartFloats;
-            mk[u][v] = in ? __ldcg(Pk) : -INFINITY;
-            sk[u][v] = in ? __ldcg(Pk + 1) : 0.f;
-            ak[u][v] = in ? __ldcg(Pk + 4 + c) : 0.f;
+      for (int v = 0; v < 4; ++v) {
+        const bool in = k0 + v < nseg;
+        const float* Pk = P0 + (k0 + v) * kPartFloats;
+        mk[v] = in ? __ldcg(Pk) : -INFINITY;
+        sk[v] = in ? __ldcg(Pk + 1) : 0.f;
+        const float* a = Pk + 4 + t * cpt;   // 16-byte aligned for 4 channels, 8 for 2
+        float4 av = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (in) {
+          if (cpt == 4) {
+            av = __ldcg(reinterpret_cast<const float4*>(a));
+          } else if (cpt == 2) {
+            const float2 a2 = __ldcg(reinterpret_cast<const float2*>(a));
+            av.x = a2.x;
+            av.y = a2.y;
+          } else {
+            av.x = __ldcg(a);
           }
         }
-#pragma unroll
-        for (int u = 0; u < kMergeElems; ++u) {
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const float M2 = fmaxf(MM[u], mk[u][v]);
-            const float f0 = rescale(MM[u], M2), f1 = rescale(mk[u][v], M2);
-            SS[u] = SS[u] * f0 + sk[u][v] * f1;
-            AA[u] = AA[u] * f0 + ak[u][v] * f1;
-            MM[u] = M2;
-          }
-        }
+        ak[v][0] = av.x;
+        ak[v][1] = av.y;
+        ak[v][2] = av.z;
+        ak[v][3] = av.w;
       }
+      float M = MM;
 #pragma unroll
-      for (int u = 0; u < kMergeElems; ++u) {
-        const int e = e0 + u * kMergeThreads;
-        if (e < nq * kDh) {
-          const int q = e / kDh, c = e % kDh;
-          p.out[((static_cast<long long>(cur.b) * nq + q) * LH + cur.lh) * kDh + c] = SS[u] > 0.f ? AA[u] / SS[u] : 0.f;
-        }
+      for (int v = 0; v < 4; ++v) M = fmaxf(M, mk[v]);
+      const float f0 = MM == -INFINITY ? 0.f : ex2(MM - M);
+      float w[4];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) w[v] = mk[v] == -INFINITY ? 0.f : ex2(mk[v] - M);
+      SS *= f0;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) SS = fmaf(sk[v], w[v], SS);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        AA[c] *= f0;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) AA[c] = fmaf(ak[v][c], w[v], AA[c]);
       }
+      MM = M;
     }
+    const float inv = SS > 0.f ? 1.f / SS : 0.f;
+    float* o = p.out + ((static_cast<long long>(cur.b) * nq + q) * LH + cur.lh) * kDh + t * cpt;
+    if (cpt == 4)
+      *reinterpret_cast<float4*>(o) = make_float4(AA[0] * inv, AA[1] * inv, AA[2] * inv, AA[3] * inv);
+    else if (cpt == 2)
+      *reinterpret_cast<float2*>(o) = make_float2(AA[0] * inv, AA[1] * inv);
+    else
+      o[0] = AA[0] * inv;
   }
 }
 
