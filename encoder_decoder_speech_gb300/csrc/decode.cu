@@ -544,7 +544,9 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend
           if (__shfl_sync(0xffffffffu, last, 0)) {
             __threadfence();
             // the segments' states in segment order, rescaling as the max grows; four
-            // queries by four segments of loads in flight at a time
+            // queries by four segments of loads in flight at a time, and per query and
+            // four segments one max and five exponentials (the old max's factor and the
+            // segments' weights)
             constexpr int kQB = kNQ >= 6 ? 4 : (kNQ >= 2 ? 2 : 1);
             for (int q0 = 0; q0 < nq; q0 += kQB) {
               float MM[kQB], SS[kQB], A0[kQB], A1[kQB];
@@ -572,23 +574,30 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend
                 }
 #pragma unroll
                 for (int u = 0; u < kQB; ++u) {
+                  float M = MM[u];
+#pragma unroll
+                  for (int v = 0; v < 4; ++v) M = fmaxf(M, mk[u][v]);
+                  const float f0 = rescale(MM[u], M);
+                  SS[u] *= f0;
+                  A0[u] *= f0;
+                  A1[u] *= f0;
 #pragma unroll
                   for (int v = 0; v < 4; ++v) {
-                    const float M2 = fmaxf(MM[u], mk[u][v]);
-                    const float f0 = rescale(MM[u], M2), f1 = rescale(mk[u][v], M2);
-                    SS[u] = SS[u] * f0 + sk[u][v] * f1;
-                    A0[u] = A0[u] * f0 + a0k[u][v] * f1;
-                    A1[u] = A1[u] * f0 + a1k[u][v] * f1;
-                    MM[u] = M2;
+                    const float w = rescale(mk[u][v], M);
+                    SS[u] = fmaf(sk[u][v], w, SS[u]);
+                    A0[u] = fmaf(a0k[u][v], w, A0[u]);
+                    A1[u] = fmaf(a1k[u][v], w, A1[u]);
                   }
+                  MM[u] = M;
                 }
               }
 #pragma unroll
               for (int u = 0; u < kQB; ++u) {
                 if (q0 + u < nq) {
                   float* o = p.out + qrow(cur.b, cur.lh, q0 + u) * kDh;
-                  o[lane] = SS[u] > 0.f ? A0[u] / SS[u] : 0.f;
-                  o[lane + 32] = SS[u] > 0.f ? A1[u] / SS[u] : 0.f;
+                  const float inv = SS[u] > 0.f ? 1.f / SS[u] : 0.f;
+                  o[lane] = A0[u] * inv;
+                  o[lane + 32] = A1[u] * inv;
                 }
               }
             }
