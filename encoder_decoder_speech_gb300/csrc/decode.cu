@@ -534,15 +534,14 @@ __global__ void __launch_bounds__(kThreads, (min_ctas_per_sm<kBF16, kNQ, kAppend
               P[1] = okr ? Sq[q] : 0.f;
             }
           }
-          __syncwarp();
+          __syncwarp();   // orders every lane's partial writes before lane 0's release
           unsigned int last = 0u;
           if (lane == 0) {
-            __threadfence();
-            const unsigned int prev = atomicAdd(p.counters + row, 1u);
+            const unsigned int prev = atomic_add_acq_rel_gpu(p.counters + row, 1u);
             last = prev == static_cast<unsigned int>(nseg - 1) ? 1u : 0u;
           }
           if (__shfl_sync(0xffffffffu, last, 0)) {
-            __threadfence();
+            __syncwarp();   // lane 0's acquire before every lane's reads of the partials
             // the segments' states in segment order, rescaling as the max grows; four
             // queries by four segments of loads in flight at a time, and per query and
             // four segments one max and five exponentials (the old max's factor and the

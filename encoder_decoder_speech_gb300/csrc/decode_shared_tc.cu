@@ -686,16 +686,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     if (merge_in_kernel<kNQT>() && n_cut > 0) {
       // Publish the cut rows (their partial writes are ordered before this point by
-      // the flushes' barriers): one device-scope fence, then the arrival counters;
-      // the last arriver of a row merges its segments' states in segment order.
+      // the flushes' barriers) with acquire-release arrival counters; the last
+      // arriver of a row merges its segments' states in segment order, after the
+      // barrier that orders thread 0's acquire before every thread's reads.
       if (tid == 0) {
-        __threadfence();
-        const unsigned int prev0 = atomicAdd(p.counters + static_cast<long long>(cb0) * LH + clh0, 1u);
+        const unsigned int prev0 = atomic_add_acq_rel_gpu(p.counters + static_cast<long long>(cb0) * LH + clh0, 1u);
         const unsigned int prev1 =
-            n_cut > 1 ? atomicAdd(p.counters + static_cast<long long>(cb1) * LH + clh1, 1u) : 0u;
+            n_cut > 1 ? atomic_add_acq_rel_gpu(p.counters + static_cast<long long>(cb1) * LH + clh1, 1u) : 0u;
         int last = prev0 == static_cast<unsigned int>(cn0 - 1) ? 1 : 0;
         if (n_cut > 1 && prev1 == static_cast<unsigned int>(cn1 - 1)) last |= 2;
-        __threadfence();
         s_flags[1] = last;
       }
       named_barrier(1, kConsumerWarps * 32);

@@ -227,6 +227,16 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t local, uint32_t rank) {
 }
 
 // Arrive (release, cluster scope) on the mbarrier at local offset `bar` of CTA `rank`.
+// Atomic add with acquire-release semantics at GPU scope: the writes this thread
+// has made or observed (through a barrier) before it are visible to a thread that
+// reads the new value with acquire semantics, and the reads this thread (or, after a
+// barrier, its CTA) makes after it see what the earlier adders published.
+__device__ __forceinline__ unsigned int atomic_add_acq_rel_gpu(unsigned int* p, unsigned int v) {
+  unsigned int r;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(r) : "l"(p), "r"(v) : "memory");
+  return r;
+}
+
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar, uint32_t rank) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mapa_shared(bar, rank))
                : "memory");
