@@ -592,16 +592,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int q = 2 * q2 + e;
-            float v = 0.f;
-            if (q < kNQT) {
-              const __nv_bfloat16 pb = __float2bfloat16_rn(valid_key ? ex2(sc[q] - m_ref[q]) : 0.f);
-              v = __bfloat162float(pb);
-              s_run[q] += v;
-            }
-            pr[e] = v;
+            pr[e] = q < kNQT && valid_key ? ex2(sc[q] - m_ref[q]) : 0.f;
           }
-          __nv_bfloat162 pp = __floats2bfloat162_rn(pr[0], pr[1]);   // exact: both are bf16 values
-          pw[q2] = *reinterpret_cast<uint32_t*>(&pp);
+          // one conversion rounds both (queries 2 q2 in the low half, 2 q2 + 1 in the
+          // high half); the sums add the rounded values, read back from the halves
+          __nv_bfloat162 pp = __floats2bfloat162_rn(pr[0], pr[1]);
+          const uint32_t u = *reinterpret_cast<uint32_t*>(&pp);
+          if (2 * q2 < kNQT) s_run[2 * q2] += __uint_as_float(u << 16);
+          if (2 * q2 + 1 < kNQT) s_run[2 * q2 + 1] += __uint_as_float(u & 0xFFFF0000u);
+          pw[q2] = u;
         }
         const uint32_t row = p_row + static_cast<uint32_t>(a * kPBytes);
 #pragma unroll
