@@ -169,6 +169,42 @@ __device__ __forceinline__ void number_chunks(const int* key_len, int B, int T, 
   if (lane == 0) s_first[B] = run;
 }
 
+// The smallest power of two >= n (n <= 32).
+template <int n>
+__host__ __device__ constexpr int pow2_at_least() {
+  return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : n <= 8 ? 8 : n <= 16 ? 16 : 32;
+}
+
+// Warp sums of v[0..N) (padded with zeros to a power of two P), reduce-scattered:
+// at each halving a lane keeps the half of its values that its lane bit selects and
+// adds its partner's copy of that half, so P - 1 shuffles leave each lane one
+// query's sum over the lanes differing in the top log2(P) bits (query *q), and
+// 5 - log2(P) more add the rest. Lanes whose low 5 - log2(P) bits are zero hold the
+// P distinct totals.
+template <int N>
+__device__ __forceinline__ float warp_sum_scatter(const float (&v)[N], int lane, int* q) {
+  constexpr int P = pow2_at_least<N>();
+  float cur[P];
+#pragma unroll
+  for (int j = 0; j < P; ++j) cur[j] = j < N ? v[j] : 0.f;
+  int qi = 0;
+#pragma unroll
+  for (int n = P, off = 16; n > 1; n >>= 1, off >>= 1) {
+    const bool hi = (lane & off) != 0;
+#pragma unroll
+    for (int j = 0; j < n / 2; ++j) {
+      const float keep = hi ? cur[j + n / 2] : cur[j];
+      const float send = hi ? cur[j] : cur[j + n / 2];
+      cur[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+    if (hi) qi += n / 2;
+  }
+#pragma unroll
+  for (int off = 32 / P / 2; off >= 1; off >>= 1) cur[0] += __shfl_xor_sync(0xffffffffu, cur[0], off);
+  *q = qi;
+  return cur[0];
+}
+
 // Cut rows merged in the kernel, at the end of each CTA's range (four query
 // columns), or by the merge kernel (more).
 template <int kNQT>
@@ -641,18 +677,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
       if (seg_ends) {
         // ---- the segment ends: per-warp sums over the keys, references; written out next chunk
+        if constexpr (kNQT < 16) {   // reduce-scattered (measured faster up to twelve columns)
+          int qs;
+          const float tot = warp_sum_scatter(s_run, lane, &qs);
+          constexpr int kLanesPerQ = 32 / pow2_at_least<kNQT>();
+          if ((lane & (kLanesPerQ - 1)) == 0 && qs < kNQT) s_sum[(rb * kConsumerWarps + warp) * kNPad + qs] = tot;
+        } else {                     // a butterfly per query (faster at sixteen)
 #pragma unroll
-        for (int q = 0; q < kNQT; ++q) {
-          float sq = s_run[q];
+          for (int q = 0; q < kNQT; ++q) {
+            float sq = s_run[q];
 #pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-          s_run[q] = sq;
-        }
-        if (lane == 0) {
+            for (int off = 16; off >= 1; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+            s_run[q] = sq;
+          }
+          if (lane == 0) {
 #pragma unroll
-          for (int q4 = 0; q4 < kNQT / 4; ++q4)
-            *reinterpret_cast<float4*>(s_sum + (rb * kConsumerWarps + warp) * kNPad + 4 * q4) =
-                make_float4(s_run[4 * q4], s_run[4 * q4 + 1], s_run[4 * q4 + 2], s_run[4 * q4 + 3]);
+            for (int q4 = 0; q4 < kNQT / 4; ++q4)
+              *reinterpret_cast<float4*>(s_sum + (rb * kConsumerWarps + warp) * kNPad + 4 * q4) =
+                  make_float4(s_run[4 * q4], s_run[4 * q4 + 1], s_run[4 * q4 + 2], s_run[4 * q4 + 3]);
+          }
         }
         if (tid == 0) {   // the references are the same in every thread
 #pragma unroll
