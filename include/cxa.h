@@ -226,6 +226,13 @@ CXA_API int cxa_decode(const cxa_cache* c, const float* Q, const int* key_len, f
  *            L, H, dh, nq) bytes, 256-byte aligned, with the same counter rules
  *            as cxa_decode's workspace.
  *
+ * Launches: one kernel, or, with a bf16 cache and nq >= 5, two: the decode and a
+ * small kernel that merges the rows whose keys were split between the decode's
+ * CTAs (from the workspace's partial states, in segment order). Both use
+ * programmatic dependent launch with the overlap rules of cxa_decode; the merge
+ * kernel reads key_len early and everything else only after the decode grid has
+ * finished, so the pair behaves like one decode towards the kernels around it.
+ *
  * With nq = 1 this is exactly cxa_decode. Errors as for cxa_decode, and
  * CXA_EINVAL for nq outside those ranges.
  */
