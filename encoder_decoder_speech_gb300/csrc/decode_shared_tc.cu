@@ -26,7 +26,8 @@
 //    redux.sync and a 4-entry shared-memory max, plus, inside a row segment, a
 //    rescale of the O accumulator in TMEM before the chunk's P.V is issued.
 //    The MMA warp only builds Q tiles and issues the score MMAs; K and V stream
-//    through separate rings (a K stage returns once its score MMA has run).
+//    through separate rings of six tiles in all (a K stage returns once its score
+//    MMA has run; two K and four V stages, three and three at sixteen columns).
 //    Probabilities (<= 256) are written, rounded to bf16, as P[key][query]: one
 //    32-byte row per key, eight queries to a 16-byte store, the row's two chunks
 //    swapped every four keys (the 32-byte swizzle of an MN-major operand); the
@@ -71,8 +72,14 @@ constexpr int kRowBytes = kDh * 2;             // one bf16 row of 64 channels
 constexpr int kBoxRows = 32;                   // keys per TMA box
 constexpr int kBoxBytes = kBoxRows * kRowBytes;
 constexpr int kTileBytes = kChunk * kRowBytes; // K or V of one chunk: 16 KB
-constexpr int kStageBytes = 2 * kTileBytes;
-constexpr int kStages = 3;
+// K and V stream through separate rings sharing six 16 KB tiles: a K stage returns
+// as soon as its score MMA has run, a V stage only after the chunk's P.V. Measured
+// on batched Whisper-Base, two K and four V stages are fastest up to twelve query
+// columns and three and three at sixteen.
+constexpr int kRingTiles = 6;
+template <int kNQT>
+__host__ __device__ constexpr int k_stages() { return kNQT >= 16 ? 3 : 2; }
+constexpr int kRingBytes = kRingTiles * kTileBytes;
 constexpr int kPBytes = 4096;                  // P of a chunk: 128 keys x 16 queries x 2 B
 constexpr int kQTileBytes = kSCols * kRowBytes; // 4 KB
 constexpr int kConsumerWarps = 4;              // one key per consumer thread
@@ -84,8 +91,9 @@ constexpr int kCtasPerSm = 2;
 constexpr uint32_t kTmemCols = 128;            // S: 2 x 32 at 0; O^T: 2 x 16 (row segments) at 64
 constexpr uint32_t kOCol = 64;
 constexpr float kRescaleLog2 = 8.f;            // a reference max moves only past this margin (x256)
-// K full/empty, V full/empty [kStages]; tfull, tempty, pfull, pempty, ofull [2]
-constexpr int kBars = 4 * kStages + 10;
+// K full/empty [K stages], V full/empty [V stages]; tfull, tempty, pempty, ofull, pfull [2]
+constexpr int kRingBars = 2 * kRingTiles;
+constexpr int kBars = kRingBars + 10;
 constexpr int kPRegion = 2 * kPBytes;
 
 struct TcParams {
@@ -218,11 +226,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* bp = smem_raw + (base - raw);
-  // layout: P^T x 2 | stages [K tile | V tile] x kStages | Q tile | small arrays
+  constexpr int kKStages = k_stages<kNQT>();
+  constexpr int kVStages = kRingTiles - kKStages;
+  // layout: P^T x 2 | K tiles x kKStages | V tiles x kVStages | Q tile | small arrays
   const uint32_t p_base = base;
-  const uint32_t stage_base = base + kPRegion;
-  const uint32_t q_base = stage_base + kStages * kStageBytes;
-  float* s_red = reinterpret_cast<float*>(bp + kPRegion + kStages * kStageBytes + kQTileBytes);  // [4][16]
+  const uint32_t k_base = base + kPRegion;
+  const uint32_t v_base = k_base + kKStages * kTileBytes;
+  const uint32_t q_base = base + kPRegion + kRingBytes;
+  float* s_red = reinterpret_cast<float*>(bp + kPRegion + kRingBytes + kQTileBytes);  // [4][16]
   float* s_corr = s_red + kConsumerWarps * kNPad;                     // [16] factors of the last max update
   float* s_sum = s_corr + kNPad;                                      // [2][4][16] per-warp sums of a segment
   float* s_m = s_sum + 2 * kConsumerWarps * kNPad;                    // [2][16] references of a segment
@@ -232,14 +243,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   int* s_kl = s_nch + p.B + (p.B & 1);                                 // key lengths, clamped to [0, T]
   volatile int* s_flags = reinterpret_cast<volatile int*>(s_kl + p.B + (p.B & 1));   // abort, last, tmem base
   auto kfull_bar = [&](int s) { return smem_u32(&bars[s]); };
-  auto kempty_bar = [&](int s) { return smem_u32(&bars[kStages + s]); };
-  auto vfull_bar = [&](int s) { return smem_u32(&bars[2 * kStages + s]); };
-  auto vempty_bar = [&](int s) { return smem_u32(&bars[3 * kStages + s]); };
-  auto tfull_bar = [&](int a) { return smem_u32(&bars[4 * kStages + a]); };
-  auto tempty_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 2 + a]); };
-  auto pempty_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 4 + a]); };
-  auto ofull_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 6 + a]); };
-  auto pfull_bar = [&](int a) { return smem_u32(&bars[4 * kStages + 8 + a]); };
+  auto kempty_bar = [&](int s) { return smem_u32(&bars[kKStages + s]); };
+  auto vfull_bar = [&](int s) { return smem_u32(&bars[2 * kKStages + s]); };
+  auto vempty_bar = [&](int s) { return smem_u32(&bars[2 * kKStages + kVStages + s]); };
+  auto tfull_bar = [&](int a) { return smem_u32(&bars[kRingBars + a]); };
+  auto tempty_bar = [&](int a) { return smem_u32(&bars[kRingBars + 2 + a]); };
+  auto pempty_bar = [&](int a) { return smem_u32(&bars[kRingBars + 4 + a]); };
+  auto ofull_bar = [&](int a) { return smem_u32(&bars[kRingBars + 6 + a]); };
+  auto pfull_bar = [&](int a) { return smem_u32(&bars[kRingBars + 8 + a]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int LH = p.LH, nq = p.nq;
@@ -253,9 +264,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
   }
   if (threadIdx.x == 32) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(kfull_bar(s), 1);
       mbar_init(kempty_bar(s), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(vfull_bar(s), 1);
       mbar_init(vempty_bar(s), 1);
     }
@@ -308,9 +321,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       Cursor cur = locate(g0, s_first, s_nch, p.B);
       uint32_t armed = 0, armed_parity = 0;
       bool ok = true;
+      const int nst = v_ring ? kVStages : kKStages;
       for (long long g = g0, i = 0; g < g1; ++g, ++i) {
-        const int s = static_cast<int>(i % kStages);
-        const uint32_t parity = static_cast<uint32_t>((i / kStages) & 1);
+        const int s = static_cast<int>(i % nst);
+        const uint32_t parity = static_cast<uint32_t>((i / nst) & 1);
         if (!mbar_wait(v_ring ? vempty_bar(s) : kempty_bar(s), parity ^ 1u, s_flags)) {
           ok = false;
           break;
@@ -320,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int nbox = (min(kChunk, kl - t0) + kBoxRows - 1) / kBoxRows;   // rows past them stay stale
         const int crow = cur.b * p.LHc + p.lh0 + cur.lh;
         const uint32_t fb = v_ring ? vfull_bar(s) : kfull_bar(s);
-        const uint32_t dst = stage_base + s * kStageBytes + (v_ring ? kTileBytes : 0);
+        const uint32_t dst = (v_ring ? v_base : k_base) + s * kTileBytes;
         mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nbox * kBoxBytes));
         for (int j = 0; j < nbox; ++j) tma_load_3d(dst + j * kBoxBytes, tm, fb, 0, t0 + j * kBoxRows, crow);
         armed |= 1u << s;
@@ -330,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (!ok) {
         s_flags[0] = 1;
         atomicOr(p.status, 1u);
-        for (int s = 0; s < kStages; ++s)
+        for (int s = 0; s < nst; ++s)
           if (armed & (1u << s)) mbar_wait(v_ring ? vfull_bar(s) : kfull_bar(s), (armed_parity >> s) & 1u);
       }
     }
@@ -365,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     };
     load_q(cur.b, cur.lh);
     for (long long g = g0, i = 0; g < g1; ++g, ++i) {
-      const int s = static_cast<int>(i % kStages);
+      const int s = static_cast<int>(i % kKStages);
       const int a = static_cast<int>(i & 1);
       if (!mbar_wait(tempty_bar(a), static_cast<uint32_t>(((i >> 1) & 1) ^ 1), s_flags)) {
         ok = false;
@@ -408,13 +422,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         prev_lh = cur.lh;
         load_next_segment(cur.b, cur.lh, g - cur.c);
       }
-      if (!mbar_wait(kfull_bar(s), static_cast<uint32_t>((i / kStages) & 1), s_flags)) {
+      if (!mbar_wait(kfull_bar(s), static_cast<uint32_t>((i / kKStages) & 1), s_flags)) {
         ok = false;
         break;
       }
       tc_fence_after();
       if (lane == 0) {
-        const uint64_t kd = smem_desc_k_sw128(stage_base + s * kStageBytes);
+        const uint64_t kd = smem_desc_k_sw128(k_base + s * kTileBytes);
         const uint64_t qd = smem_desc_k_sw128(q_base);
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * kSCols);
 #pragma unroll
@@ -441,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       int prev_b = -1, prev_lh = -1, seg = -1;
       bool ok = true;
       for (long long g = g0, i = 0; g < g1; ++g, ++i) {
-        const int b = static_cast<int>(i & 1), st = static_cast<int>(i % kStages);
+        const int b = static_cast<int>(i & 1), st = static_cast<int>(i % kVStages);
         const bool first = cur.b != prev_b || cur.lh != prev_lh;
         if (first) {
           ++seg;
@@ -450,13 +464,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         const bool last = (cur.c == s_nch[cur.b] - 1) || (g + 1 == g1);
         if (!mbar_wait(pfull_bar(b), static_cast<uint32_t>((i >> 1) & 1), s_flags) ||
-            !mbar_wait(vfull_bar(st), static_cast<uint32_t>((i / kStages) & 1), s_flags)) {
+            !mbar_wait(vfull_bar(st), static_cast<uint32_t>((i / kVStages) & 1), s_flags)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const int rb = seg & 1;
-        const uint64_t vd = smem_desc_mn_sw128(stage_base + st * kStageBytes + kTileBytes);
+        const uint64_t vd = smem_desc_mn_sw128(v_base + st * kTileBytes);
         const uint64_t pd = smem_desc_mn_sw32(p_base + b * kPBytes);
         const uint32_t d_tmem = tmem_base + kOCol + static_cast<uint32_t>(rb * kNPad);
 #pragma unroll
@@ -562,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     long long i = 0;
     for (long long g = g0;; ++g, ++i) {
       const bool tail = g == g1;
-      const int s = static_cast<int>(i % kStages);
+      const int s = static_cast<int>(i % kVStages);
       const int a = static_cast<int>(i & 1);
       const uint32_t acc_parity = static_cast<uint32_t>((i >> 1) & 1);
       const int nch = tail ? 1 : s_nch[cur.b];
@@ -646,8 +660,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
       if (n < kChunk) {
         // tail chunk: zero the V rows of keys >= n (their P is 0; the rows may hold any bits)
-        if (ok && !mbar_wait(vfull_bar(s), static_cast<uint32_t>((i / kStages) & 1), s_flags)) fail();
-        const uint32_t vt = stage_base + s * kStageBytes + kTileBytes;
+        if (ok && !mbar_wait(vfull_bar(s), static_cast<uint32_t>((i / kVStages) & 1), s_flags)) fail();
+        const uint32_t vt = v_base + s * kTileBytes;
         for (int u = n * (kRowBytes / 16) + tid; u < kTileBytes / 16; u += kConsumerWarps * 32)
           st_shared_v4(vt + u * 16, 0u, 0u, 0u, 0u);
       }
@@ -898,7 +912,7 @@ EncodeTiledFn encoder() {
 }
 
 size_t smem_bytes(int B) {
-  size_t n = 1024 + kPRegion + static_cast<size_t>(kStages) * kStageBytes + kQTileBytes;
+  size_t n = 1024 + kPRegion + kRingBytes + kQTileBytes;
   n += (kConsumerWarps * kNPad + kNPad + 2 * kConsumerWarps * kNPad + 2 * kNPad) * 4 + kBars * 8;
   n += static_cast<size_t>(B + 1) * 8 + 2 * static_cast<size_t>(B + (B & 1)) * 4 + 16;
   return n;
