@@ -1,4 +1,4 @@
-// Shared-cache multi-query decode on the tensor cores: nq (3..16) query rows per
+// Shared-cache multi-query decode on the tensor cores: nq (2..16) query rows per
 // (slot, layer, head) attend the slot's one bf16 cache, the batch-N-over-one-
 // shared-cache case of SharedSplitKVCached ("Caso de estudio: WhisperKit", §3).
 //
@@ -7,8 +7,8 @@
 // works on it, and no CTA publishes a partial state (device fence, arrival
 // counter) or merges a row while its K/V stream is running: with eight or more
 // query columns a second, small kernel (decode_shared_merge_kernel, chained by
-// programmatic dependent launch) merges the cut rows after the grid; with four,
-// each CTA publishes its (at most two) cut rows at the end of its range and the
+// programmatic dependent launch) merges the cut rows after the grid; with four
+// (two to four queries), each CTA publishes its (at most two) cut rows at the end of its range and the
 // last arriver of a row merges it. A 128-key chunk goes through two tcgen05
 // products with fp32 accumulators in tensor memory:
 //
@@ -20,7 +20,7 @@
 //    carried to about 16 mantissa bits (K is exact: the cache is bf16).
 //    Double-buffered in TMEM.
 //  * softmax on the CUDA cores: each of the 128 consumer threads owns one key
-//    and reads its scores with one tcgen05.ld. Probabilities are taken against
+//    and reads its scores with two tcgen05.ld (the hi and lo columns). Probabilities are taken against
 //    a per-query reference max that moves only when some score passes it by
 //    more than 2^8 (one bar.red.or per chunk tells); a move costs a warp
 //    redux.sync and a 4-entry shared-memory max, plus, inside a row segment, a
@@ -38,9 +38,10 @@
 //    MN-major from P as written, accumulated over the row segment's chunks in TMEM (two
 //    buffers, alternate segments). With M = 64 the accumulator rows sit in
 //    lanes 0..15 of each warp's 32-lane quarter: channel 16w + l in lane
-//    32w + l. One consumer thread issues the chunk's P.V right after the
-//    barrier that completes P^T; an O rescale (rare) waits for the previous
-//    P.V's commit and runs before it.
+//    32w + l. A dedicated warp issues the chunk's P.V once the barrier that
+//    completes P^T has let one consumer thread arrive on its mbarrier (and the
+//    V tile has landed); an O rescale (rare) waits for the previous P.V's
+//    commit and runs before it.
 //  * at the end of a segment each consumer warp reads its 16 channels of O^T
 //    and writes them for every query (result or the segment's partial slot).
 //
