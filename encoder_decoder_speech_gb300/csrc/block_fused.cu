@@ -10,7 +10,7 @@
 // A thread-block cluster of H CTAs per slot b, CTA h of the cluster owning head h
 // (H <= 8: a portable cluster). Each CTA
 //   * streams its (b, layer, h) K/V row through a 16-stage bulk-copy ring (24 fp32 /
-//     48 bf16 keys of K and V per stage) from its first instruction (no earlier
+//     32 bf16 keys of K and V per stage) from its first instruction (no earlier
 //     kernel writes the cache); chunk i belongs to warp i % 8 alone, which waits
 //     for it, runs it through its lane groups' softmax states and refills the
 //     stage with chunk i + 16, so no warp waits for another within the loop;

@@ -26,9 +26,9 @@
 //    runs its own online softmax per query (running max m, sum s, accumulators)
 //    over the keys it is given, in fp32 and base 2 (q is pre-multiplied by
 //    scale * log2(e)). With an fp32 cache and four or more queries a warp
-//    instead takes 32 keys and half of the queries: one key per lane for the
-//    scores, the probabilities through shared memory, two channels per lane for
-//    P.V.
+//    instead takes 32 keys and half of the queries: register-tiled scores (a
+//    4-key x query x 16-channel tile per lane, reduced to one key per lane),
+//    the probabilities through shared memory, four channels per lane for P.V.
 //  * When a row's run of chunks in this CTA ends, the groups' states are merged
 //    (warp shuffles, then shared memory). A CTA that owned the whole row writes
 //    out directly; otherwise it stores its partials (m, s, acc[64]), one per
