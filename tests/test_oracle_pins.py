@@ -670,6 +670,25 @@ def _mut_shared_decode_first_query(monkeypatch):
     monkeypatch.setattr(O, "decode_shared", decode_shared)
 
 
+def _mut_decode_layers_next_layer(monkeypatch):
+    def decode_layers(Q, Kc, Vc, key_len, l0, scale=None):
+        Q = np.asarray(Q, np.float64)
+        nl = Q.shape[1]
+        return O.decode(Q, np.asarray(Kc)[:, l0 + 1:l0 + 1 + nl], np.asarray(Vc)[:, l0 + 1:l0 + 1 + nl], key_len,
+                        scale)
+    monkeypatch.setattr(O, "decode_layers", decode_layers)
+
+
+def _mut_masked_blend_next_row(monkeypatch):
+    def masked_blend_update(cache, new_row, pos):
+        cache = np.asarray(cache, np.float64)
+        mask = np.zeros((cache.shape[0], 1))
+        if 0 <= pos + 1 < cache.shape[0]:
+            mask[pos + 1, 0] = 1.0
+        return cache * (1.0 - mask) + np.asarray(new_row, np.float64)[None, :] * mask
+    monkeypatch.setattr(O, "masked_blend_update", masked_blend_update)
+
+
 def _all_pins_pass():
     try:
         return (pin_populate_bruteforce() < 1e-12 and pin_decode_bruteforce() < 1e-12
@@ -689,7 +708,7 @@ def _all_pins_pass():
     _mut_frobenius_squared_denominator, _mut_round_half_away, _mut_round_truncate,
     _mut_layer_norm_unbiased, _mut_layer_norm_eps_outside_root, _mut_block_without_residual,
     _mut_causal_window_excludes_self, _mut_alignment_unmasked, _mut_alignment_mean_drops_a_head,
-    _mut_shared_decode_first_query,
+    _mut_shared_decode_first_query, _mut_decode_layers_next_layer, _mut_masked_blend_next_row,
 ])
 def test_planted_mistake_is_caught(monkeypatch, mutation):
     mutation(monkeypatch)
